@@ -1,0 +1,222 @@
+"""The pages' index maps, restated step by step on the CPU.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).
+
+* ``flatten`` / ``unflatten`` / ``plan``: the TileLang tutorial "loop_mapping.py"
+  (Chapter 08, section 6, module docstring): the nest is flattened row-major,
+  ``access_idx = flat // vector_size``, ``thread = access_idx % num_thread``,
+  ``local_idx = (access_idx // num_thread) * vector_size + flat % vector_size``.
+* ``gmem_smem_partition`` / ``gmem_smem_replay``: Apache TVM docs
+  "copy -> gmem_smem", section "Algorithm" steps 1-3 and section "How inputs
+  change the algorithm" (the ``[outer, threads, vec]`` split, the widest-first
+  vector width, the serial loop of vector copies).
+* ``permute_align`` / ``permute_replay``: Apache TVM docs "permute_layout",
+  section "Algorithm" steps 1 and 3 (the aligned ``extent``/``src_str``/
+  ``dst_str``, ``P = prod(extent) / 32``, and the two register-staged phases
+  with ``j = r ^ ((lane >> shift) & mask)``).
+
+Pure-Python loops: these are meant for the small cases the pages show.
+"""
+from __future__ import annotations
+
+from .definition import as_layout, paired_modes
+
+WARP = 32
+
+
+# ---------------------------------------------------------------------------
+# TileLang loop partition ("loop_mapping.py")
+# ---------------------------------------------------------------------------
+
+def flatten(index, extents) -> int:
+    """Row-major position of ``index`` in a nest with ``extents`` (last fastest)."""
+    flat = 0
+    for k in range(len(extents)):
+        flat = flat * extents[k] + index[k]
+    return flat
+
+
+def unflatten(flat: int, extents) -> tuple:
+    """Inverse of ``flatten``: peel the last (fastest) coordinate first."""
+    coords = []
+    for e in reversed(extents):
+        flat, c = divmod(flat, e)
+        coords.append(c)
+    return tuple(reversed(coords))
+
+
+def plan(extents, num_thread: int, vector_size: int) -> dict:
+    """{iteration point: (thread, per-thread slot)} of the default loop partition.
+
+    Levels, fastest first: the ``vector_size`` innermost iterations share one
+    thread's consecutive slots, consecutive groups rotate over the threads,
+    and the remainder becomes a per-thread serial loop.
+    """
+    total = 1
+    for e in extents:
+        total *= e
+    out = {}
+    for flat in range(total):
+        group, lane_in_vec = divmod(flat, vector_size)
+        rnd, thread = divmod(group, num_thread)
+        out[unflatten(flat, extents)] = (thread, rnd * vector_size + lane_in_vec)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# copy -> gmem_smem: [outer, threads, vec]
+# ---------------------------------------------------------------------------
+
+class Decline(Exception):
+    """The variant does not accept this input (the page's "declines")."""
+
+
+def _coalesce(modes):
+    """Merge neighbours (outer, inner) that are row-major contiguous on both sides."""
+    out = []
+    for m in modes:
+        if out:
+            e0, *s0 = out[-1]
+            e1, *s1 = m
+            if all(a == b * e1 for a, b in zip(s0, s1)):
+                out[-1] = (e0 * e1, *s1)
+                continue
+        out.append(tuple(m))
+    return out
+
+
+def gmem_smem_partition(shape, g_stride, s_stride, elem_bytes: int,
+                        num_threads: int, g_offset: int = 0, s_offset: int = 0):
+    """The synthesized partition of one global<->shared copy.
+
+    Step 1: the region's modes (unit modes dropped) are put in the GLOBAL
+    side's canonical order, stride descending, and neighbours contiguous on
+    both sides are merged; the innermost mode is the contiguous tail.
+    Step 2: vector widths of 128, 64, 32, 16, 8 bits are tried widest first;
+    ``vec`` elements are accepted when the tail is contiguous on both sides
+    and its extent is a multiple of ``vec``, and every other stride on both
+    sides and both base offsets are multiples of ``vec`` (so each per-thread,
+    per-round vector pointer is aligned).  Reading of the page: the split must
+    also be exact, ``threads * vec`` dividing the element count.
+    The variant declines when the element count is not a multiple of the
+    thread count ("What it accepts", row "divisibility").
+
+    Returns dict(modes=[(extent, g_stride, s_stride)], vec, outer, total).
+    """
+    modes = [(e, g, s) for e, g, s in zip(shape, g_stride, s_stride) if e != 1]
+    modes.sort(key=lambda m: -m[1])  # stable: ties keep their logical order
+    modes = _coalesce(modes)
+    total = 1
+    for e, _, _ in modes:
+        total *= e
+    if total % num_threads:
+        raise Decline("element count %d not divisible by %d threads" % (total, num_threads))
+    bits_per_elem = 8 * elem_bytes
+    for bits in (128, 64, 32, 16, 8):
+        if bits < bits_per_elem or bits % bits_per_elem:
+            continue
+        vec = bits // bits_per_elem
+        if vec > 1:
+            if not modes:
+                continue
+            te, tg, ts = modes[-1]
+            if tg != 1 or ts != 1 or te % vec:
+                continue
+            others = [x for e, g, s in modes[:-1] for x in (g, s)]
+            if any(x % vec for x in others) or g_offset % vec or s_offset % vec:
+                continue
+        if total % (num_threads * vec):
+            continue
+        return dict(modes=modes, vec=vec, outer=total // (num_threads * vec),
+                    total=total)
+    raise Decline("no vector width")
+
+
+def gmem_smem_replay(part, num_threads: int, g_offset: int = 0, s_offset: int = 0):
+    """The emitted serial loop: round f, thread tid moves elements
+    ``[(f * threads + tid) * vec, +vec)`` of the canonical order.
+
+    Yields (f, tid, g_lin, s_lin, [(g_off, s_off) per vector element]); g_lin
+    and s_lin are the offsets of the vector's first element, the quantities
+    the page's generated IR names.
+    """
+    extents = [m[0] for m in part["modes"]]
+    vec = part["vec"]
+    for f in range(part["outer"]):
+        for tid in range(num_threads):
+            elems = []
+            for v in range(vec):
+                idx = unflatten((f * num_threads + tid) * vec + v, extents)
+                g = g_offset + sum(i * m[1] for i, m in zip(idx, part["modes"]))
+                s = s_offset + sum(i * m[2] for i, m in zip(idx, part["modes"]))
+                elems.append((g, s))
+            yield f, tid, elems[0][0], elems[0][1], elems
+
+
+def gmem_smem_copy(src_words, dst_words, part, num_threads, g_is_src: bool,
+                   g_offset: int = 0, s_offset: int = 0):
+    """Run the replayed loop on two Python lists of words (global, shared)."""
+    for _f, _tid, _g, _s, elems in gmem_smem_replay(part, num_threads, g_offset, s_offset):
+        for g, s in elems:
+            if g_is_src:
+                dst_words[s] = src_words[g]
+            else:
+                dst_words[g] = src_words[s]
+
+
+# ---------------------------------------------------------------------------
+# permute_layout: warp register-staged XOR swizzle
+# ---------------------------------------------------------------------------
+
+def permute_align(src_layout, dst_layout):
+    """Step 1: sliced and canonicalized shards, source regrouped to the
+    destination's shape.
+
+    Reading of the page: unit modes are dropped, the non-unit modes are paired
+    in logical order, and neighbours are merged only where BOTH sides are
+    row-major contiguous; a linear source therefore collapses as far as the
+    destination allows and ends up with the destination's shape.  Returns
+    (extent, src_str, dst_str, P) with P = prod(extent) / 32; raises Decline
+    when the element count is not a whole number of warp lanes.
+    """
+    modes = _coalesce(paired_modes(as_layout(src_layout), as_layout(dst_layout)))
+    extent = tuple(m[0] for m in modes)
+    total = 1
+    for e in extent:
+        total *= e
+    if total % WARP:
+        raise Decline("%d elements are not a multiple of the warp size" % total)
+    return extent, tuple(m[1] for m in modes), tuple(m[2] for m in modes), total // WARP
+
+
+def swizzled_iteration(lane: int, r: int, k: int, shift: int) -> int:
+    """j = r ^ ((lane >> shift) & mask) with mask = 2**k - 1."""
+    return r ^ ((lane >> shift) & ((1 << k) - 1))
+
+
+def project(idx, strides) -> int:
+    return sum(i * s for i, s in zip(idx, strides))
+
+
+def permute_replay(src_words, dst_words, extent, src_str, dst_str, P: int,
+                   k: int, shift: int, src_base: int = 0, dst_base: int = 0):
+    """Step 3: phase 1 stages each lane's P words in registers through the
+    source layout, a warp barrier follows, phase 2 writes them through the
+    destination layout.  Because every read finishes before any write, the
+    result is right even when the two buffers are the same list.
+
+    Returns the access record [(lane, r, j, src_off, dst_off)].
+    """
+    regs = [[None] * P for _ in range(WARP)]
+    record = []
+    for lane in range(WARP):
+        for r in range(P):
+            j = swizzled_iteration(lane, r, k, shift)
+            idx = unflatten(lane + j * WARP, extent)
+            so = src_base + project(idx, src_str)
+            regs[lane][r] = src_words[so]
+            record.append((lane, r, j, so, dst_base + project(idx, dst_str)))
+    # ---- warp barrier: every read above completes before any write below ----
+    for lane, r, _j, _so, do in record:
+        dst_words[do] = regs[lane][r]
+    return record
