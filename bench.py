@@ -1,0 +1,454 @@
+"""Benchmark of the strided tile layout copy on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload 1..5] [--elem-bytes W4] [--kernel auto|...]
+
+A step is one lc_layout_copy over the whole workload (one kernel launch);
+inputs are synthetic, seeded, resident in HBM and larger than L2 (no flush
+needed).  Prints ONE JSON line on rank 0.  The default workload is the
+scale-factor transpose batch: 2^20 tiles of (pipe=2, high=1, 4, 32) fp32,
+strides (128,128,32,1) -> (128,128,1,4).
+
+--impl reference times the CPU oracle (the plain C word loop) on the host
+cores over a bounded sample of the same workload; it never touches a GPU.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from concurrent.futures import ThreadPoolExecutor
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "effective GB/s (read+write) and % of GB300 HBM peak per layout permute"
+UNIT = "GB/s"
+DEFAULT_WORKLOAD = 2
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD)
+    p.add_argument("--elem-bytes", type=int, default=None)
+    p.add_argument("--kernel", default="auto")
+    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# helpers shared with the tests (rank aggregation, peaks, workload description)
+# ---------------------------------------------------------------------------
+
+def rank_info():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """Largest value over all ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def workload_bytes(cfg) -> int:
+    """Algorithmic bytes of one step: every logical word read once, written once."""
+    return 2 * workloads.logical_elems(cfg) * cfg["elem_bytes"]
+
+
+def describe(cfg) -> str:
+    s, d = cfg["src"], cfg["dst"]
+    return "%s: %d tile(s) of shape %s, %d-byte words, strides %s -> %s" % (
+        cfg["name"], cfg["n_tiles"], s["shape"], cfg["elem_bytes"], s["stride"], d["stride"])
+
+
+def kernel_sources_sha(kernel_name: str) -> str:
+    files = {"warp_permute": ["k_warp.cu"], "tile_transpose": ["k_tile.cu"],
+             "vec_copy": ["k_vec.cu"]}.get(kernel_name, [])
+    h = hashlib.sha256()
+    for f in files + ["ptx.cuh", "device_common.cuh"]:
+        with open(os.path.join(ROOT, "movement_primitives_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_name: str, workload_name: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    summary is missing or the kernel's sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "%s_%s.md" % (kernel_name, workload_name))
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_per_launch_bytes:\s*(\d+)", text)
+    h = re.search(r"source_sha256:\s*([0-9a-f]+)", text)
+    if not m or not h or h.group(1) != kernel_sources_sha(kernel_name):
+        return None
+    return int(m.group(1))
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-i", self.gpu_id, "-lms", "50"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def snapshot(self):
+        try:
+            out = subprocess.run(["nvidia-smi", "--query-gpu=" + self.FIELDS,
+                                  "--format=csv,noheader,nounits", "-i", self.gpu_id],
+                                 capture_output=True, text=True, timeout=10).stdout
+            self.lines += [l.strip() for l in out.splitlines() if l.strip()]
+        except (OSError, subprocess.TimeoutExpired):
+            pass
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, flag in zip(self.REASONS, parts[3:]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_id_for(device_index: int) -> str:
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(device_index).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        return vis.split(",")[device_index] if vis else str(device_index)
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def sampled(cfg, fraction: float):
+    """The same workload restricted to a leading fraction of its tiles, or of
+    its outermost non-unit mode when it has a single tile."""
+    c = dict(cfg)
+    if cfg["n_tiles"] > 1:
+        c["n_tiles"] = max(1, int(cfg["n_tiles"] * fraction))
+        return c
+    shape = list(cfg["src"]["shape"])
+    k = next(i for i, e in enumerate(shape) if e > 1)
+    shape[k] = max(1, int(shape[k] * fraction))
+    c["src"] = dict(cfg["src"], shape=tuple(shape))
+    c["dst"] = dict(cfg["dst"], shape=tuple(shape))
+    return c
+
+
+def run_oracle(cfg, src_np, dst_np, cores: int) -> float:
+    """One oracle pass over `cfg` split across `cores` threads; returns seconds."""
+    import oracle
+    tasks = []
+    if cfg["n_tiles"] >= cores:
+        step = -(-cfg["n_tiles"] // cores)
+        for b in range(0, cfg["n_tiles"], step):
+            tasks.append((cfg, (b, min(cfg["n_tiles"], b + step))))
+    else:
+        # split the outermost non-unit mode into slabs, each its own copy
+        shape = list(cfg["src"]["shape"])
+        k = next((i for i, e in enumerate(shape) if e > 1), 0)
+        n = shape[k]
+        step = max(1, -(-n // cores))
+        for b in range(0, n, step):
+            sub = dict(cfg)
+            sh = list(shape)
+            sh[k] = min(n, b + step) - b
+            sub["src"] = dict(cfg["src"], shape=tuple(sh),
+                              offset=cfg["src"]["offset"] + b * cfg["src"]["stride"][k],
+                              tile_stride=cfg["src"]["tile_stride"] or workloads.footprint_elems(cfg["src"], 1))
+            sub["dst"] = dict(cfg["dst"], shape=tuple(sh),
+                              offset=cfg["dst"]["offset"] + b * cfg["dst"]["stride"][k],
+                              tile_stride=cfg["dst"]["tile_stride"] or workloads.footprint_elems(cfg["dst"], 1))
+            tasks.append((sub, None))
+
+    def one(task):
+        c, rng = task
+        oracle.copy(src_np, c["src"], dst_np, c["dst"], c["elem_bytes"], c["n_tiles"], tile_range=rng)
+
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=cores) as ex:
+        list(ex.map(one, tasks))
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(cfg, src_np, seconds: float):
+    """The oracle, as it stands, on this host's cores over a bounded sample."""
+    import numpy as np
+    import oracle  # noqa: F401  (builds the C loop on first use)
+    cores = host_cores()
+    probe = sampled(cfg, 1.0 / 4096)
+    dst = np.empty(workloads.footprint_elems(cfg["dst"], cfg["n_tiles"]) * cfg["elem_bytes"], np.uint8)
+    t = run_oracle(probe, src_np, dst, cores)
+    frac = min(1.0, max(1.0 / 4096, seconds / max(t, 1e-6) / 4096))
+    sample = sampled(cfg, frac)
+    t = run_oracle(sample, src_np, dst, cores)
+    gbs = workload_bytes(sample) / t / 1e9
+    return dict(value=round(gbs, 3), unit=UNIT, cores=cores, kind="oracle",
+                sample="%.4f of the workload (%d logical words, %.1f s on %d threads)"
+                       % (frac, workloads.logical_elems(sample), t, cores))
+
+
+def run_reference(args):
+    rank, world, _ = rank_info()
+    if rank != 0:
+        return 0
+    import numpy as np
+    cfg = workloads.config(args.workload, args.elem_bytes)
+    src = workloads.make_src(cfg).numpy()
+    dst = np.empty(workloads.footprint_elems(cfg["dst"], cfg["n_tiles"]) * cfg["elem_bytes"], np.uint8)
+    cores = host_cores()
+    probe = sampled(cfg, 1.0 / 4096)
+    t = run_oracle(probe, src, dst, cores)
+    budget = 120.0 / max(1, args.steps + args.warmup)  # whole run within a few minutes
+    frac = min(1.0, max(1.0 / 4096, budget / max(t, 1e-6) / 4096))
+    sample = sampled(cfg, frac)
+    for _ in range(args.warmup):
+        run_oracle(sample, src, dst, cores)
+    times = [run_oracle(sample, src, dst, cores) for _ in range(args.steps)]
+    total = sum(times)
+    value = workload_bytes(sample) * args.steps / total / 1e9
+    desc = "%.5f of the workload per step (%d logical words) on %d threads" % (
+        frac, workloads.logical_elems(sample), cores)
+    line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "impl": "reference",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * total / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": dtype_name(cfg), "data": "synthetic",
+            "config": {"workload": describe(cfg), "sample": desc},
+            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores,
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def dtype_name(cfg) -> str:
+    return {"uniform_f32": "f32", "normal_bf16": "bf16"}.get(
+        cfg["kind"], {1: "u8", 2: "u16", 4: "u32", 8: "u64", 16: "u128"}[cfg["elem_bytes"]])
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    rank, world, local = rank_info()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    __graft_entry__.build()
+    import movement_primitives_gb300 as lc
+
+    cfg = workloads.config(args.workload, args.elem_bytes)
+    step_bytes = workload_bytes(cfg)
+    src_h = workloads.make_src(cfg)
+    src = src_h.to(dev)
+    dst = workloads.make_dst(cfg, device=dev)
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    plan = lc.plan(cfg["src"], cfg["dst"], cfg["elem_bytes"], cfg["n_tiles"], args.kernel)
+
+    def step():
+        lc.layout_copy_ptr(src.data_ptr(), cfg["src"], dst.data_ptr(), cfg["dst"], cfg["elem_bytes"],
+                           cfg["n_tiles"], kernel=args.kernel, stream=sh)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    st, detail = lc.last_device_error(sh)
+    if st != 0:
+        raise RuntimeError("device error word %#x during warm-up" % detail)
+    # spot check against the oracle's offsets (the tests do the full parity)
+    import oracle
+    n = workloads.logical_elems(cfg)
+    pts = np.random.default_rng(0).integers(0, n, 4096)
+    so, do = oracle.offsets_of(cfg["src"], cfg["dst"], cfg["n_tiles"], pts)
+    w = cfg["elem_bytes"]
+    sv = src.view(-1, w)
+    dv = dst.view(-1, w)
+    if not torch.equal(sv[torch.from_numpy(so).to(dev)], dv[torch.from_numpy(do).to(dev)]):
+        raise RuntimeError("spot check against the oracle failed")
+
+    sampler = ClockSampler(gpu_id_for(dev.index)) if rank == 0 else None
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    t0.record(stream)
+    for k in range(args.steps):
+        ev[k][0].record(stream)
+        step()
+        ev[k][1].record(stream)
+    t1.record(stream)
+    if sampler:
+        sampler.snapshot()  # while the queued launches run
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop() if sampler else None
+    st, detail = lc.last_device_error(sh)
+    if st != 0:
+        raise RuntimeError("device error word %#x in the timed region" % detail)
+    elapsed_ms = max_over_ranks(t0.elapsed_time(t1), dev)
+    launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    # end to end through the public API with host buffers (pinned), H2D + copy + D2H
+    src_pin = src_h.pin_memory()
+    dst_pin = torch.empty(dst.numel(), dtype=torch.uint8).pin_memory()
+    e2e_steps = max(1, args.e2e_steps)
+    for it in range(e2e_steps + 2):
+        if it == 2:
+            barrier()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        src.copy_(src_pin, non_blocking=True)
+        lc.layout_copy(src, cfg["src"], dst, cfg["dst"], n_tiles=cfg["n_tiles"],
+                       elem_bytes=cfg["elem_bytes"], kernel=args.kernel, stream=stream)
+        dst_pin.copy_(dst, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
+
+    peak, peak_kind = measured_peak()
+    achieved = step_bytes / (launch_ms / 1e3) / 1e9
+    traffic = profiled_traffic(plan["kernel_name"], cfg["name"])
+    if rank == 0:
+        cpu = None if args.no_cpu_baseline else cpu_baseline(cfg, src_h.numpy(), args.cpu_seconds)
+        value = world * step_bytes * args.steps / (elapsed_ms / 1e3) / 1e9
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(elapsed_ms / args.steps, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": dtype_name(cfg), "data": "synthetic",
+            "config": {"workload": describe(cfg), "kernel": plan["kernel_name"],
+                       "bytes_per_step": step_bytes,
+                       "l2": "inputs larger than L2 (%d MiB per side), no flush" % (step_bytes // 2 >> 20),
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "pct_of_peak": round(100.0 * value / world / peak, 2),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "peak_kind": peak_kind + " (MEASURED_PEAKS.json hbm_gbs, copy burst)"
+                         if peak_kind == "measured" else peak_kind},
+            "clocks": clocks,
+            "gpu_launches": args.steps,
+            "e2e": {"value": round(world * step_bytes / (e2e_ms / 1e3) / 1e9, 2), "unit": UNIT,
+                    "h2d_bytes_per_step": src.numel() * src.element_size(),
+                    "d2h_bytes_per_step": dst.numel() * dst.element_size()},
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,225 @@
+/*
+ * layout_copy.h -- C ABI of the GB300 (sm_103a) strided tile layout copy.
+ *
+ * A TileLayout S[shape : stride] maps a logical index (i_0 .. i_{r-1}) to the
+ * element offset  offset + sum_k i_k * stride_k  (Apache TVM docs
+ * "permute_layout", section "Algorithm", step 3, `project`; "copy ->
+ * gmem_smem", section "Demonstration program", `TileLayout(S[shape])`).
+ * lc_layout_copy moves, for every tile t in [0, n_tiles) and every logical
+ * index i, the elem_bytes-byte word at
+ *     src + (src.offset + t * src.tile_stride + sum_k i_k * src.stride_k) * elem_bytes
+ * to
+ *     dst + (dst.offset + t * dst.tile_stride + sum_k i_k * dst.stride_k) * elem_bytes.
+ * Both layouts are indexed by the same logical index: their non-unit extents
+ * must be equal, in order ("copy -> gmem_smem", section "What it accepts",
+ * row "dtype / shape"; "permute_layout", section "What it accepts", row
+ * "operands").  Words are moved as raw bits; nothing is converted.  Bytes of
+ * dst outside the destination image are never written.
+ *
+ * Conventions for every entry point
+ *   - Strides and offsets count ELEMENTS of elem_bytes bytes, not bytes.
+ *   - Layout structs are read during the call and not retained.
+ *   - Device pointers are plain CUDA device addresses owned by the caller;
+ *     the library never allocates, frees or retains user buffers.
+ *   - `stream` is a cudaStream_t (the type below is the same pointer type);
+ *     NULL is the legacy default stream.  Launches are asynchronous on it.
+ *   - Every function returns an lc_status (0 = LC_OK); nothing throws or
+ *     aborts across the ABI.  On an error nothing has been launched, except
+ *     LC_ERR_CUDA, which reports the CUDA runtime's launch error.
+ *   - One process, one GPU: the current CUDA device of the calling thread.
+ */
+#ifndef LAYOUT_COPY_H_
+#define LAYOUT_COPY_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LC_MAX_RANK 8
+
+/* Same pointer type as cudaStream_t (struct CUstream_st *). */
+typedef struct CUstream_st *lc_stream_t;
+
+/* A TileLayout plus this library's batching fields.
+ *   rank         1..LC_MAX_RANK
+ *   shape[k]     >= 0; unit modes (extent 1) are ignored when pairing modes
+ *   stride[k]    elements; >= 0 on the source (0 = broadcast read),
+ *                > 0 on the destination for every non-unit mode
+ *   offset       >= 0, element offset of tile 0
+ *   tile_stride  >= 0, elements between consecutive tiles; 0 means the
+ *                layout's cosize, 1 + sum_k (shape_k - 1) * stride_k, i.e.
+ *                tiles packed back to back.  The pages show a single tile
+ *                or a serial `pipe` loop ("permute_layout", section
+ *                "Demonstration program"); tiles are that loop, batched. */
+typedef struct {
+    int32_t rank;
+    int64_t shape[LC_MAX_RANK];
+    int64_t stride[LC_MAX_RANK];
+    int64_t offset;
+    int64_t tile_stride;
+} lc_tile_layout;
+
+typedef enum {
+    LC_OK = 0,
+    LC_ERR_NULL = 1,            /* a required pointer is NULL */
+    LC_ERR_RANK = 2,            /* rank outside 1..LC_MAX_RANK */
+    LC_ERR_SHAPE = 3,           /* negative extent or n_tiles, or P not whole */
+    LC_ERR_EXTENT_MISMATCH = 4, /* non-unit extents differ ("extent mismatch") */
+    LC_ERR_ELEM_BYTES = 5,      /* elem_bytes not in {1,2,4,8,16} */
+    LC_ERR_BAD_STRIDE = 6,      /* negative stride/offset, or 0 on dst */
+    LC_ERR_NOT_INJECTIVE = 7,   /* two logical indices share a dst offset */
+    LC_ERR_OVERLAP = 8,         /* src and dst byte ranges overlap */
+    LC_ERR_ALIGN = 9,           /* pointer not aligned to elem_bytes */
+    LC_ERR_NO_SWIZZLE = 10,     /* no conflict-free XOR swizzle ("fail") */
+    LC_ERR_CUDA = 11,           /* CUDA runtime error at launch */
+    LC_ERR_TIMEOUT = 12,        /* a bounded device wait gave up */
+    LC_ERR_UNSUPPORTED = 13,    /* a forced kernel class cannot take this copy */
+    LC_ERR_OVERFLOW = 14        /* an offset does not fit in 63 bits */
+} lc_status;
+
+/* Kernel classes (the planner picks one; lc_layout_copy_ex can force one). */
+typedef enum {
+    LC_KERNEL_AUTO = 0,
+    /* [outer, threads, vec] vector copy: the destination-ordered logical
+     * index is split into vectors of the widest of 16/8/4/2/1 bytes that keep
+     * every per-thread pointer aligned ("copy -> gmem_smem", sections
+     * "Algorithm" steps 1-3; TileLang "loop_mapping.py" partition).  Takes
+     * every valid copy; the fast path for copies whose innermost mode is
+     * contiguous on both sides (identity copies, row gathers, axis permutes
+     * that keep the last axis). */
+    LC_KERNEL_VEC_COPY = 1,
+    /* Warp register-staged permute: units of 32*P elements are bulk-copied
+     * global -> shared, each warp permutes one unit in shared memory through
+     * registers with the per-lane XOR swizzle j = r ^ ((lane >> shift) & mask)
+     * chosen by the bank simulator, and the units are bulk-copied back
+     * ("permute_layout", section "Algorithm").  Small transposed units. */
+    LC_KERNEL_WARP_PERMUTE = 2,
+    /* Tile transpose: TMA tensor loads of 128-byte x R-row tiles into a
+     * shared-memory ring (mbarrier pipelined), 16-byte shared reads, an
+     * in-register transpose of the sub-16-byte elements, 16-byte coalesced
+     * global stores.  Large 2-D transposes with batch modes. */
+    LC_KERNEL_TILE_TRANSPOSE = 3
+} lc_kernel;
+
+/* What the planner decided for one copy (filled by lc_plan). */
+typedef struct {
+    int32_t kernel;            /* lc_kernel */
+    int32_t elem_bytes;        /* word size moved (after fusing a contiguous
+                                  inner run into wider words) */
+    int32_t n_modes;           /* canonical modes, outermost first */
+    int64_t extent[LC_MAX_RANK + 1];
+    int64_t src_stride[LC_MAX_RANK + 1];
+    int64_t dst_stride[LC_MAX_RANK + 1];
+    int64_t total;             /* logical words moved (all tiles) */
+    /* vector copy */
+    int32_t vec;               /* words per vector */
+    int64_t run;               /* words in the contiguous inner run (1 if none) */
+    /* warp permute */
+    int32_t unit_modes;        /* number of modes in one unit (innermost) */
+    int32_t P;                 /* words per lane per unit */
+    int32_t k, shift, mask;    /* XOR swizzle */
+    int32_t conflicts_read, conflicts_write;
+    int64_t units_per_chunk;
+    /* tile transpose */
+    int32_t tile_rows;         /* R: source rows per tile */
+    int32_t tile_cols;         /* words per 128-byte tile row */
+    int32_t stages;
+    /* launch */
+    int32_t grid, block, smem_bytes;
+} lc_plan_info;
+
+/* The copy.  Validates, plans (host only, microseconds), launches one
+ * kernel on `stream`.  n_tiles >= 0; a copy of zero words returns LC_OK
+ * without launching (and then src/dst may be NULL).
+ * Errors: LC_ERR_NULL, _RANK, _SHAPE, _EXTENT_MISMATCH, _ELEM_BYTES,
+ * _BAD_STRIDE, _NOT_INJECTIVE, _OVERLAP, _ALIGN, _OVERFLOW (before any
+ * launch); LC_ERR_CUDA (launch failed).  Device-side wait timeouts are
+ * reported later by lc_last_device_error. */
+int lc_layout_copy(const void *src, const lc_tile_layout *src_layout,
+                   void *dst, const lc_tile_layout *dst_layout,
+                   int32_t elem_bytes, int64_t n_tiles, lc_stream_t stream);
+
+/* As lc_layout_copy, with the kernel class forced (LC_KERNEL_AUTO = let the
+ * planner choose).  LC_ERR_UNSUPPORTED when the forced class cannot take the
+ * copy.  Meant for tests and benchmarks that compare classes. */
+int lc_layout_copy_ex(const void *src, const lc_tile_layout *src_layout,
+                      void *dst, const lc_tile_layout *dst_layout,
+                      int32_t elem_bytes, int64_t n_tiles, int32_t kernel,
+                      lc_stream_t stream);
+
+/* The planner alone: validation and the plan lc_layout_copy_ex would launch
+ * for (layouts, elem_bytes, n_tiles, kernel), without touching the GPU.
+ * Pointer checks (NULL, alignment, overlap) are skipped.  `out` must not be
+ * NULL. */
+int lc_plan(const lc_tile_layout *src_layout, const lc_tile_layout *dst_layout,
+            int32_t elem_bytes, int64_t n_tiles, int32_t kernel,
+            lc_plan_info *out);
+
+/* XOR swizzle of the warp permute ("permute_layout", section "Algorithm",
+ * steps 1-2; section "What it accepts", row "bank-freedom").  Both layouts
+ * describe ONE warp's shard: unit modes are dropped, the non-unit modes are
+ * paired in order and neighbours contiguous on both sides are merged, giving
+ * extent / src_str / dst_str with P = prod(extent) / 32 words per lane.  The
+ * bank simulator (32 banks of 4-byte words; 128-byte wavefronts, i.e. 32
+ * lanes for words up to 4 bytes, 16 lanes for 8, 8 lanes for 16; a bank's
+ * degree is the number of distinct 4-byte words it serves) tries k = 0 ..
+ * log2(P) (k = 0 only when P is not a power of two) and, for each k, shift =
+ * 0 .. 5-k, and returns the first pair whose read phase and write phase both
+ * have degree 1; mask = 2^k - 1.  Offsets of the layouts are ignored
+ * (addresses are relative to a 128-byte-aligned base).
+ * Outputs (all must be non-NULL): k, shift, mask, and the worst bank degree
+ * of each phase at that choice.  LC_ERR_NO_SWIZZLE when no pair is
+ * conflict-free (outputs then hold the pair with the lowest worst degree);
+ * LC_ERR_SHAPE when prod(extent) is not a multiple of 32. */
+int lc_choose_swizzle(const lc_tile_layout *src_layout,
+                      const lc_tile_layout *dst_layout, int32_t elem_bytes,
+                      int32_t *k, int32_t *shift, int32_t *mask,
+                      int32_t *conflicts_read, int32_t *conflicts_write);
+
+/* The bank simulator itself for one given (k, shift), same model and
+ * alignment as lc_choose_swizzle: worst degree of each phase. */
+int lc_swizzle_conflicts(const lc_tile_layout *src_layout,
+                         const lc_tile_layout *dst_layout, int32_t elem_bytes,
+                         int32_t k, int32_t shift, int32_t *conflicts_read,
+                         int32_t *conflicts_write);
+
+/* The synthesized [outer, threads, vec] partition of one global <-> shared
+ * copy executed by `threads` threads ("copy -> gmem_smem", section
+ * "Algorithm" steps 1-2, section "How inputs change the algorithm"): the
+ * global layout drives the canonical (stride-descending) order, vector
+ * widths of 16, 8, 4, 2, 1 bytes are tried widest first, and a width of vec
+ * words is accepted when the innermost mode is contiguous on both sides with
+ * an extent that is a multiple of vec, every other stride on both sides and
+ * both offsets are multiples of vec, and threads * vec divides the element
+ * count.  Outputs: vec (words) and outer = count / (threads * vec).
+ * LC_ERR_SHAPE ("declines") when the element count is not a multiple of
+ * `threads`. */
+int lc_gmem_smem_partition(const lc_tile_layout *global_layout,
+                           const lc_tile_layout *shared_layout,
+                           int32_t elem_bytes, int32_t threads,
+                           int32_t *vec, int64_t *outer);
+
+/* Synchronises `stream`, then reads and clears this device's error word,
+ * which kernels set when a bounded wait gives up (LC_ERR_TIMEOUT).
+ * Returns LC_OK when the word was clear; LC_ERR_CUDA if the stream reported
+ * an error.  `detail` (may be NULL) receives the raw word. */
+int lc_last_device_error(lc_stream_t stream, uint64_t *detail);
+
+/* Failure-path check: launches one tiny kernel that waits on a shared-memory
+ * barrier nothing ever arrives at, giving up after timeout_ns nanoseconds
+ * (clamped to 1 us .. 1 s), so that the bounded-wait error path can be
+ * tested without hanging anything.  lc_last_device_error then reports
+ * LC_ERR_TIMEOUT. */
+int lc_debug_wait_timeout(int64_t timeout_ns, lc_stream_t stream);
+
+/* Human-readable name of a status / kernel class (static strings). */
+const char *lc_status_string(int32_t status);
+const char *lc_kernel_name(int32_t kernel);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LAYOUT_COPY_H_ */

@@ -1,0 +1,188 @@
+"""GB300-native strided tile layout copy / permute.
+
+A TileLayout ``S[shape : stride]`` maps a logical index to the element offset
+``offset + sum_k i_k * stride_k``; ``layout_copy`` moves every logical index's
+word from the source layout to the destination layout on the GPU (Apache TVM
+docs "copy -> gmem_smem" and "permute_layout").  Everything runs in the C-ABI
+library ``liblayoutcopy.so`` (``include/layout_copy.h``); this module only
+marshals arguments.  PyTorch provides device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass, field
+from typing import Sequence
+
+from . import _lib
+from ._lib import KERNELS, STATUS, STATUS_NAMES
+
+__all__ = ["TileLayout", "LayoutCopyError", "layout_copy", "layout_copy_ptr", "plan",
+           "choose_swizzle", "swizzle_conflicts", "gmem_smem_partition",
+           "last_device_error", "debug_wait_timeout", "KERNELS", "STATUS"]
+
+
+@dataclass(frozen=True)
+class TileLayout:
+    """shape : stride (elements), base offset of tile 0, elements between tiles
+    (0 = the layout's cosize, tiles packed back to back)."""
+    shape: Sequence[int]
+    stride: Sequence[int] = field(default=None)
+    offset: int = 0
+    tile_stride: int = 0
+
+    def __post_init__(self):
+        shape = tuple(int(e) for e in self.shape)
+        object.__setattr__(self, "shape", shape)
+        if self.stride is None:  # S[shape] alone is row-major
+            st, acc = [], 1
+            for e in reversed(shape):
+                st.append(acc)
+                acc *= max(e, 1)
+            object.__setattr__(self, "stride", tuple(reversed(st)))
+        else:
+            object.__setattr__(self, "stride", tuple(int(s) for s in self.stride))
+
+    @classmethod
+    def of(cls, obj) -> "TileLayout":
+        if isinstance(obj, TileLayout):
+            return obj
+        if isinstance(obj, dict):
+            return cls(obj["shape"], obj.get("stride"), obj.get("offset", 0), obj.get("tile_stride", 0))
+        return cls(*obj)
+
+    def to_c(self) -> _lib.CTileLayout:
+        if len(self.shape) != len(self.stride):
+            raise ValueError("shape and stride lengths differ")
+        c = _lib.CTileLayout()
+        c.rank = len(self.shape)
+        for k, (e, s) in enumerate(zip(self.shape[:_lib.MAX_RANK], self.stride[:_lib.MAX_RANK])):
+            c.shape[k] = e
+            c.stride[k] = s
+        c.offset = self.offset
+        c.tile_stride = self.tile_stride
+        return c
+
+    def footprint(self, n_tiles: int) -> int:
+        """Elements a buffer needs to hold n_tiles tiles (bounds check only)."""
+        if n_tiles <= 0 or any(e == 0 for e in self.shape):
+            return 0
+        span = 1 + sum((e - 1) * s for e, s in zip(self.shape, self.stride))
+        return self.offset + (n_tiles - 1) * (self.tile_stride or span) + span
+
+
+class LayoutCopyError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        msg = _lib.lib().lc_status_string(status).decode()
+        super().__init__("%s (%s)%s" % (STATUS_NAMES.get(status, status), msg,
+                                        ": " + what if what else ""))
+
+
+def _check(status: int, what: str = "") -> None:
+    if status != 0:
+        raise LayoutCopyError(status, what)
+
+
+def _kernel_id(kernel) -> int:
+    return KERNELS[kernel] if isinstance(kernel, str) else int(kernel)
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def layout_copy_ptr(src_ptr: int, src_layout, dst_ptr: int, dst_layout, elem_bytes: int,
+                    n_tiles: int = 1, kernel="auto", stream=0) -> None:
+    """Raw-pointer form: device addresses, layouts in elements, stream handle."""
+    sl, dl = TileLayout.of(src_layout).to_c(), TileLayout.of(dst_layout).to_c()
+    st = _lib.lib().lc_layout_copy_ex(ctypes.c_void_p(src_ptr), ctypes.byref(sl),
+                                      ctypes.c_void_p(dst_ptr), ctypes.byref(dl),
+                                      int(elem_bytes), int(n_tiles), _kernel_id(kernel),
+                                      ctypes.c_void_p(_stream_handle(stream)))
+    _check(st, "layout_copy")
+
+
+def layout_copy(src, src_layout, dst, dst_layout, n_tiles: int = 1, elem_bytes: int | None = None,
+                kernel="auto", stream=None) -> None:
+    """Copy between two CUDA tensors viewed through TileLayouts.
+
+    Layout strides and offsets count elements of ``elem_bytes`` bytes (default:
+    the tensors' element size) from each tensor's first byte.  Launches on
+    ``stream`` (default: the current torch stream) and returns at once.
+    """
+    if not (src.is_cuda and dst.is_cuda):
+        raise ValueError("layout_copy needs CUDA tensors (there is no CPU path)")
+    if not (src.is_contiguous() and dst.is_contiguous()):
+        raise ValueError("pass contiguous tensors; express strides through the layouts")
+    w = int(elem_bytes) if elem_bytes is not None else src.element_size()
+    if elem_bytes is None and dst.element_size() != w:
+        raise ValueError("source and destination element sizes differ; pass elem_bytes")
+    sl, dl = TileLayout.of(src_layout), TileLayout.of(dst_layout)
+    for name, t, l in (("source", src, sl), ("destination", dst, dl)):
+        need = l.footprint(n_tiles) * w
+        have = t.numel() * t.element_size()
+        if need > have:
+            raise ValueError("%s layout reaches %d bytes; the tensor holds %d" % (name, need, have))
+    layout_copy_ptr(src.data_ptr(), sl, dst.data_ptr(), dl, w, n_tiles, kernel, _stream_handle(stream))
+
+
+def plan(src_layout, dst_layout, elem_bytes: int, n_tiles: int = 1, kernel="auto") -> dict:
+    """What the planner would launch (host only; pointers assumed aligned)."""
+    sl, dl = TileLayout.of(src_layout).to_c(), TileLayout.of(dst_layout).to_c()
+    info = _lib.CPlanInfo()
+    _check(_lib.lib().lc_plan(ctypes.byref(sl), ctypes.byref(dl), int(elem_bytes), int(n_tiles),
+                              _kernel_id(kernel), ctypes.byref(info)), "plan")
+    n = info.n_modes
+    out = {f: getattr(info, f) for f, _ in _lib.CPlanInfo._fields_
+           if f not in ("extent", "src_stride", "dst_stride")}
+    out["kernel_name"] = _lib.lib().lc_kernel_name(info.kernel).decode()
+    out["modes"] = [(info.extent[i], info.src_stride[i], info.dst_stride[i]) for i in range(n)]
+    return out
+
+
+def choose_swizzle(src_layout, dst_layout, elem_bytes: int) -> dict:
+    """The warp permute's XOR swizzle for one warp shard (see lc_choose_swizzle)."""
+    sl, dl = TileLayout.of(src_layout).to_c(), TileLayout.of(dst_layout).to_c()
+    v = [ctypes.c_int32() for _ in range(5)]
+    st = _lib.lib().lc_choose_swizzle(ctypes.byref(sl), ctypes.byref(dl), int(elem_bytes),
+                                      *[ctypes.byref(x) for x in v])
+    if st not in (0, STATUS["LC_ERR_NO_SWIZZLE"]):
+        _check(st, "choose_swizzle")
+    k, shift, mask, cr, cw = (x.value for x in v)
+    return dict(ok=st == 0, k=k, shift=shift, mask=mask, conflicts_read=cr, conflicts_write=cw)
+
+
+def swizzle_conflicts(src_layout, dst_layout, elem_bytes: int, k: int, shift: int):
+    sl, dl = TileLayout.of(src_layout).to_c(), TileLayout.of(dst_layout).to_c()
+    cr, cw = ctypes.c_int32(), ctypes.c_int32()
+    _check(_lib.lib().lc_swizzle_conflicts(ctypes.byref(sl), ctypes.byref(dl), int(elem_bytes),
+                                           int(k), int(shift), ctypes.byref(cr), ctypes.byref(cw)),
+           "swizzle_conflicts")
+    return cr.value, cw.value
+
+
+def gmem_smem_partition(global_layout, shared_layout, elem_bytes: int, threads: int):
+    """(vec, outer) of one global <-> shared copy by ``threads`` threads."""
+    gl, sl = TileLayout.of(global_layout).to_c(), TileLayout.of(shared_layout).to_c()
+    vec, outer = ctypes.c_int32(), ctypes.c_int64()
+    _check(_lib.lib().lc_gmem_smem_partition(ctypes.byref(gl), ctypes.byref(sl), int(elem_bytes),
+                                             int(threads), ctypes.byref(vec), ctypes.byref(outer)),
+           "gmem_smem_partition")
+    return vec.value, outer.value
+
+
+def last_device_error(stream=None):
+    """(status, raw word): synchronises the stream, reads and clears the error word."""
+    detail = ctypes.c_uint64()
+    st = _lib.lib().lc_last_device_error(ctypes.c_void_p(_stream_handle(stream)), ctypes.byref(detail))
+    return st, detail.value
+
+
+def debug_wait_timeout(timeout_ns: int, stream=None) -> None:
+    _check(_lib.lib().lc_debug_wait_timeout(int(timeout_ns), ctypes.c_void_p(_stream_handle(stream))),
+           "debug_wait_timeout")

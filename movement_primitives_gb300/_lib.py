@@ -1,0 +1,96 @@
+"""ctypes view of liblayoutcopy.so: struct mirrors and function prototypes.
+
+Argument marshalling only.  The library must have been built (``build.py``,
+or ``__graft_entry__.build()``); importing this module without it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "liblayoutcopy.so")
+MAX_RANK = 8
+
+OK = 0
+STATUS_NAMES = {
+    0: "LC_OK", 1: "LC_ERR_NULL", 2: "LC_ERR_RANK", 3: "LC_ERR_SHAPE",
+    4: "LC_ERR_EXTENT_MISMATCH", 5: "LC_ERR_ELEM_BYTES", 6: "LC_ERR_BAD_STRIDE",
+    7: "LC_ERR_NOT_INJECTIVE", 8: "LC_ERR_OVERLAP", 9: "LC_ERR_ALIGN",
+    10: "LC_ERR_NO_SWIZZLE", 11: "LC_ERR_CUDA", 12: "LC_ERR_TIMEOUT",
+    13: "LC_ERR_UNSUPPORTED", 14: "LC_ERR_OVERFLOW",
+}
+STATUS = {v: k for k, v in STATUS_NAMES.items()}
+KERNELS = {"auto": 0, "vec_copy": 1, "warp_permute": 2, "tile_transpose": 3}
+
+
+class CTileLayout(ctypes.Structure):
+    _fields_ = [("rank", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * MAX_RANK),
+                ("stride", ctypes.c_int64 * MAX_RANK),
+                ("offset", ctypes.c_int64),
+                ("tile_stride", ctypes.c_int64)]
+
+
+_M = MAX_RANK + 1
+
+
+class CPlanInfo(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("elem_bytes", ctypes.c_int32),
+                ("n_modes", ctypes.c_int32),
+                ("extent", ctypes.c_int64 * _M), ("src_stride", ctypes.c_int64 * _M),
+                ("dst_stride", ctypes.c_int64 * _M), ("total", ctypes.c_int64),
+                ("vec", ctypes.c_int32), ("run", ctypes.c_int64),
+                ("unit_modes", ctypes.c_int32), ("P", ctypes.c_int32),
+                ("k", ctypes.c_int32), ("shift", ctypes.c_int32), ("mask", ctypes.c_int32),
+                ("conflicts_read", ctypes.c_int32), ("conflicts_write", ctypes.c_int32),
+                ("units_per_chunk", ctypes.c_int64),
+                ("tile_rows", ctypes.c_int32), ("tile_cols", ctypes.c_int32),
+                ("stages", ctypes.c_int32),
+                ("grid", ctypes.c_int32), ("block", ctypes.c_int32), ("smem_bytes", ctypes.c_int32)]
+
+
+_P_LAYOUT = ctypes.POINTER(CTileLayout)
+_P_I32 = ctypes.POINTER(ctypes.c_int32)
+_P_I64 = ctypes.POINTER(ctypes.c_int64)
+
+# name -> (restype, argtypes); every symbol declared in include/layout_copy.h
+PROTOTYPES = {
+    "lc_layout_copy": (ctypes.c_int, [ctypes.c_void_p, _P_LAYOUT, ctypes.c_void_p, _P_LAYOUT,
+                                      ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p]),
+    "lc_layout_copy_ex": (ctypes.c_int, [ctypes.c_void_p, _P_LAYOUT, ctypes.c_void_p, _P_LAYOUT,
+                                         ctypes.c_int32, ctypes.c_int64, ctypes.c_int32,
+                                         ctypes.c_void_p]),
+    "lc_plan": (ctypes.c_int, [_P_LAYOUT, _P_LAYOUT, ctypes.c_int32, ctypes.c_int64,
+                               ctypes.c_int32, ctypes.POINTER(CPlanInfo)]),
+    "lc_choose_swizzle": (ctypes.c_int, [_P_LAYOUT, _P_LAYOUT, ctypes.c_int32, _P_I32, _P_I32,
+                                         _P_I32, _P_I32, _P_I32]),
+    "lc_swizzle_conflicts": (ctypes.c_int, [_P_LAYOUT, _P_LAYOUT, ctypes.c_int32, ctypes.c_int32,
+                                            ctypes.c_int32, _P_I32, _P_I32]),
+    "lc_gmem_smem_partition": (ctypes.c_int, [_P_LAYOUT, _P_LAYOUT, ctypes.c_int32,
+                                              ctypes.c_int32, _P_I32, _P_I64]),
+    "lc_last_device_error": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint64)]),
+    "lc_debug_wait_timeout": (ctypes.c_int, [ctypes.c_int64, ctypes.c_void_p]),
+    "lc_status_string": (ctypes.c_char_p, [ctypes.c_int32]),
+    "lc_kernel_name": (ctypes.c_char_p, [ctypes.c_int32]),
+}
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library with prototypes set; raises if it was not built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                "movement_primitives_gb300: %s is missing; build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'` "
+                "(there is no fallback implementation)" % LIB_PATH)
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in PROTOTYPES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib

@@ -1,0 +1,298 @@
+// TMA tile transpose: tensor tiles in a shared-memory ring (mbarrier
+// pipelined), 16-byte shared reads, in-register transpose of the sub-16-byte
+// words, 16-byte coalesced global stores.
+//
+// X is the mode contiguous in the destination, Y the one contiguous in the
+// source; up to three batch modes ride along as extra tensor dimensions.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "device_common.cuh"
+#include "launch.h"
+
+namespace lc {
+
+template <int W> struct TileCfg {
+    static constexpr int V = 16 / W;              // words per 16-byte chunk
+    static constexpr int TY = 128 / W;            // words per 128-byte tile row
+    static constexpr int R = W <= 2 ? 256 : 128;  // source rows per tile (planner agrees)
+    static constexpr int NT = W == 1 ? 128 : 256; // threads
+    static constexpr int S = 4;                   // ring stages
+    static constexpr int TILE_BYTES = 128 * R;
+    static constexpr int MB = 8 * R / V;          // V-row x 16-byte micro-blocks
+    static constexpr int SMEM = 128 + S * TILE_BYTES;
+};
+
+struct TileArgs {
+    uint8_t *dst;    // address of destination word offset 0
+    int64_t eX, eY;  // X contiguous in dst, Y contiguous in src (words)
+    int64_t dY;      // destination stride of Y (bytes)
+    int32_t nb;      // batch modes (<= 3), outermost first
+    int64_t be[3], bd[3];
+    int64_t tiles_x, tiles_y, n_tiles;
+    uint64_t timeout_ns;
+};
+
+// V rows of one 16-byte column chunk -> V destination chunks: out[q] holds
+// word q of every input row (a V x V transpose of W-byte words in registers;
+// the 2-byte and 1-byte cases use byte permutes).
+template <int W>
+__device__ __forceinline__ void transpose_chunk(const uint32_t (&in)[16 / W][4], uint32_t (&out)[16 / W][4]) {
+    if constexpr (W == 16) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) out[0][k] = in[0][k];
+    } else if constexpr (W == 8) {
+        out[0][0] = in[0][0]; out[0][1] = in[0][1]; out[0][2] = in[1][0]; out[0][3] = in[1][1];
+        out[1][0] = in[0][2]; out[1][1] = in[0][3]; out[1][2] = in[1][2]; out[1][3] = in[1][3];
+    } else if constexpr (W == 4) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) out[q][i] = in[i][q];
+    } else if constexpr (W == 2) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+#pragma unroll
+            for (int p = 0; p < 4; ++p)
+                out[q][p] = __byte_perm(in[2 * p][q >> 1], in[2 * p + 1][q >> 1], (q & 1) ? 0x7632 : 0x5410);
+    } else {
+        // 4 x 4 byte blocks: rows 4p..4p+3, word t -> outputs 4t..4t+3, word p
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const uint32_t A = in[4 * p][t], B = in[4 * p + 1][t];
+                const uint32_t C = in[4 * p + 2][t], D = in[4 * p + 3][t];
+                const uint32_t ab_lo = __byte_perm(A, B, 0x5140), ab_hi = __byte_perm(A, B, 0x7362);
+                const uint32_t cd_lo = __byte_perm(C, D, 0x5140), cd_hi = __byte_perm(C, D, 0x7362);
+                out[4 * t + 0][p] = __byte_perm(ab_lo, cd_lo, 0x5410);
+                out[4 * t + 1][p] = __byte_perm(ab_lo, cd_lo, 0x7632);
+                out[4 * t + 2][p] = __byte_perm(ab_hi, cd_hi, 0x5410);
+                out[4 * t + 3][p] = __byte_perm(ab_hi, cd_hi, 0x7632);
+            }
+    }
+}
+
+// Stores words [0, n) of a 16-byte chunk (the ragged right edge); the word
+// index is a compile-time constant in every unrolled step, so the chunk stays
+// in registers.
+template <int W>
+__device__ __forceinline__ void store_partial(uint8_t *p, const uint32_t (&v)[4], int n) {
+    constexpr int V = 16 / W;
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+        if (k >= n) break;
+        if constexpr (W == 1) p[k] = static_cast<uint8_t>(v[k >> 2] >> (8 * (k & 3)));
+        else if constexpr (W == 2) reinterpret_cast<uint16_t *>(p)[k] = static_cast<uint16_t>(v[k >> 1] >> (16 * (k & 1)));
+        else if constexpr (W == 4) reinterpret_cast<uint32_t *>(p)[k] = v[k];
+        else if constexpr (W == 8) reinterpret_cast<uint2 *>(p)[k] = make_uint2(v[2 * k], v[2 * k + 1]);
+    }
+}
+
+template <int W>
+__device__ __forceinline__ void tile_issue_load(const CUtensorMap *tmap, const TileArgs &a, int64_t t,
+                                                uint32_t dst, uint32_t bar) {
+    using C = TileCfg<W>;
+    const int64_t tx = t % a.tiles_x, rest = t / a.tiles_x;
+    const int64_t ty = rest % a.tiles_y;
+    int64_t b = rest / a.tiles_y;
+    int32_t b0 = 0, b1 = 0, b2 = 0;  // batch coordinates, outermost first
+    if (a.nb == 3) { b2 = static_cast<int32_t>(b % a.be[2]); b /= a.be[2]; }
+    if (a.nb >= 2) { b1 = static_cast<int32_t>(b % a.be[1]); b /= a.be[1]; }
+    if (a.nb >= 1) { b0 = static_cast<int32_t>(b % a.be[0]); }
+    const int32_t c0 = static_cast<int32_t>(ty * C::TY * (W == 16 ? 2 : 1));
+    const int32_t c1 = static_cast<int32_t>(tx * C::R);
+    ptx::mbar_arrive_expect_tx(bar, C::TILE_BYTES);
+    // tensor dims: (Y, X, batch innermost .. outermost)
+    switch (a.nb) {
+        case 0: ptx::tma_load_2d(dst, tmap, c0, c1, bar); break;
+        case 1: ptx::tma_load_3d(dst, tmap, c0, c1, b0, bar); break;
+        case 2: ptx::tma_load_4d(dst, tmap, c0, c1, b1, b0, bar); break;
+        default: ptx::tma_load_5d(dst, tmap, c0, c1, b2, b1, b0, bar); break;
+    }
+}
+
+// Tile t = (batch, ty, tx), tx fastest: TMA brings source rows
+// [tx*R, tx*R + R) x words [ty*TY, ty*TY + TY) (128 bytes per row) into a
+// stage.  Micro-block mb = (row group mr = mb / 8, 16-byte chunk c = mb % 8):
+// V rows x 16 bytes, transposed in registers into V destination chunks,
+// destination rows ty*TY + c*V + q, words tx*R + mr*V .. + V.  The 8 lanes of
+// a 16-byte shared-memory wavefront read the 8 chunks of one 128-byte row,
+// i.e. all 32 banks once: conflict-free with no swizzle.
+template <int W>
+__global__ void __launch_bounds__(TileCfg<W>::NT)
+    k_tile_transpose(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ TileArgs a) {
+    using C = TileCfg<W>;
+    constexpr int V = C::V;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
+    const uint8_t *tiles = smem + 128;
+    const int tid = threadIdx.x;
+    const int64_t n_local = a.n_tiles > blockIdx.x ? (a.n_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const uint32_t bar0 = ptx::smem_addr(bars), tile0 = ptx::smem_addr(tiles);
+    if (tid == 0) {
+        ptx::prefetch_tensormap(&tmap);
+        for (int s = 0; s < C::S; ++s) ptx::mbar_init(bar0 + 8 * s, 1);
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0)
+        for (int64_t i = 0; i < lmin(C::S, n_local); ++i)
+            tile_issue_load<W>(&tmap, a, blockIdx.x + i * gridDim.x, tile0 + i * C::TILE_BYTES, bar0 + 8 * i);
+
+    for (int64_t i = 0; i < n_local; ++i) {
+        const int s = static_cast<int>(i % C::S);
+        const uint32_t parity = static_cast<uint32_t>((i / C::S) & 1);
+        const int64_t t = blockIdx.x + i * gridDim.x;
+        const bool ok = ptx::mbar_wait_bounded(bar0 + 8 * s, parity, a.timeout_ns);
+        if (ok) {
+            const int64_t tx = t % a.tiles_x, rest = t / a.tiles_x;
+            const int64_t ty = rest % a.tiles_y;
+            int64_t b = rest / a.tiles_y;
+            uint8_t *dbase = a.dst;
+            for (int k = a.nb - 1; k >= 0; --k) {
+                dbase += (b % a.be[k]) * a.bd[k];
+                b /= a.be[k];
+            }
+            const uint8_t *st = tiles + static_cast<size_t>(s) * C::TILE_BYTES;
+            for (int mb = tid; mb < C::MB; mb += C::NT) {
+                const int c = mb & 7, mr = mb >> 3;
+                const int64_t x0 = tx * C::R + int64_t(mr) * V;
+                if (x0 >= a.eX) continue;  // rows past the tensor (TMA filled them)
+                uint32_t in[V][4], out[V][4];
+#pragma unroll
+                for (int r = 0; r < V; ++r) {
+                    const uint4 q = *reinterpret_cast<const uint4 *>(st + (mr * V + r) * 128 + c * 16);
+                    in[r][0] = q.x; in[r][1] = q.y; in[r][2] = q.z; in[r][3] = q.w;
+                }
+                transpose_chunk<W>(in, out);
+                const int64_t y0 = ty * C::TY + int64_t(c) * V;
+                const int nx = static_cast<int>(lmin(V, a.eX - x0));
+#pragma unroll
+                for (int q = 0; q < V; ++q) {
+                    if (y0 + q < a.eY) {
+                        uint8_t *p = dbase + (y0 + q) * a.dY + x0 * W;
+                        if (nx == V)
+                            *reinterpret_cast<uint4 *>(p) = make_uint4(out[q][0], out[q][1], out[q][2], out[q][3]);
+                        else
+                            store_partial<W>(p, out[q], nx);
+                    }
+                }
+            }
+        }
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                report_error(LC_ERR_TIMEOUT, LC_KERNEL_TILE_TRANSPOSE);
+                for (int64_t q = i; q < lmin(i + C::S, n_local); ++q)
+                    ptx::mbar_wait_bounded(bar0 + 8 * (q % C::S), static_cast<uint32_t>((q / C::S) & 1),
+                                           a.timeout_ns);
+            }
+            return;
+        }
+        if (tid == 0 && i + C::S < n_local)
+            tile_issue_load<W>(&tmap, a, blockIdx.x + (i + C::S) * gridDim.x, tile0 + s * C::TILE_BYTES,
+                               bar0 + 8 * s);
+    }
+}
+
+namespace {
+
+// cuTensorMapEncodeTiled, fetched from the driver at run time so that the
+// library links against the CUDA runtime only.
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+template <int W>
+int launch_tile_t(const CUtensorMap &tmap, const TileArgs &a, cudaStream_t stream) {
+    using C = TileCfg<W>;
+    const void *fn = reinterpret_cast<const void *>(&k_tile_transpose<W>);
+    int sms, per;
+    if (prepare(fn, C::NT, C::SMEM, C::SMEM, &sms, &per) != cudaSuccess) return LC_ERR_CUDA;
+    const int64_t grid = lmin(a.n_tiles, int64_t(sms) * per);
+    k_tile_transpose<W><<<static_cast<unsigned>(grid), C::NT, C::SMEM, stream>>>(tmap, a);
+    return finish_launch();
+}
+
+}  // namespace
+
+int launch_tile(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream) {
+    const TilePlan &tp = p.tile;
+    const int w = p.w;
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return LC_ERR_CUDA;
+    const int rank = 2 + tp.batch.n;
+    const int mult = w == 16 ? 2 : 1;  // 16-byte words travel as two 8-byte TMA elements
+    cuuint64_t dims[5], strides[4];
+    cuuint32_t box[5], estr[5];
+    dims[0] = static_cast<cuuint64_t>(tp.Y.e * mult);
+    dims[1] = static_cast<cuuint64_t>(tp.X.e);
+    strides[0] = static_cast<cuuint64_t>(tp.X.s * w);
+    for (int i = 0; i < tp.batch.n; ++i) {  // innermost batch mode first
+        const Mode &b = tp.batch.m[tp.batch.n - 1 - i];
+        dims[2 + i] = static_cast<cuuint64_t>(b.e);
+        strides[1 + i] = static_cast<cuuint64_t>(b.s * w);
+    }
+    box[0] = static_cast<cuuint32_t>(128 / (w / mult));
+    box[1] = static_cast<cuuint32_t>(tp.R);
+    for (int i = 2; i < 5; ++i) box[i] = 1;
+    for (int i = 0; i < 5; ++i) estr[i] = 1;
+    CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    if (w == 2) dt = CU_TENSOR_MAP_DATA_TYPE_UINT16;
+    else if (w == 4) dt = CU_TENSOR_MAP_DATA_TYPE_UINT32;
+    else if (w >= 8) dt = CU_TENSOR_MAP_DATA_TYPE_UINT64;
+    CUtensorMap tmap;
+    std::memset(&tmap, 0, sizeof(tmap));
+    void *base = const_cast<uint8_t *>(src + p.src_off * w);
+    if (enc(&tmap, dt, static_cast<cuuint32_t>(rank), base, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return LC_ERR_UNSUPPORTED;  // the driver refused this tensor shape
+
+    TileArgs a{};
+    a.dst = dst + p.dst_off * w;
+    a.eX = tp.X.e;
+    a.eY = tp.Y.e;
+    a.dY = tp.Y.d * w;
+    a.nb = tp.batch.n;
+    int64_t nbatch = 1;
+    for (int i = 0; i < tp.batch.n; ++i) {
+        a.be[i] = tp.batch.m[i].e;
+        a.bd[i] = tp.batch.m[i].d * w;
+        nbatch *= tp.batch.m[i].e;
+    }
+    a.tiles_x = (tp.X.e + tp.R - 1) / tp.R;
+    a.tiles_y = (tp.Y.e + tp.TY - 1) / tp.TY;
+    a.n_tiles = a.tiles_x * a.tiles_y * nbatch;
+    a.timeout_ns = wait_limit_ns();
+    switch (w) {
+        case 1: return launch_tile_t<1>(tmap, a, stream);
+        case 2: return launch_tile_t<2>(tmap, a, stream);
+        case 4: return launch_tile_t<4>(tmap, a, stream);
+        case 8: return launch_tile_t<8>(tmap, a, stream);
+        case 16: return launch_tile_t<16>(tmap, a, stream);
+    }
+    return LC_ERR_UNSUPPORTED;
+}
+
+cudaError_t take_error_tile(unsigned long long *v) { return take_module_error(v); }
+
+}  // namespace lc

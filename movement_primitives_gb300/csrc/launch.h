@@ -1,0 +1,29 @@
+// Host-side launch interface between the ABI (api.cu) and the kernel
+// translation units.  Not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "lc_internal.h"
+
+namespace lc {
+
+// Limit of every bounded device wait (LC_WAIT_TIMEOUT_NS overrides 2 s).
+uint64_t wait_limit_ns();
+
+// Opts `fn` into `attr_smem` bytes of dynamic shared memory on the current
+// device (once) and reports the SM count and resident blocks per SM.
+cudaError_t prepare(const void *fn, int threads, int smem, int attr_smem, int *sms, int *per_sm);
+
+inline int finish_launch() { return cudaGetLastError() == cudaSuccess ? LC_OK : LC_ERR_CUDA; }
+
+int launch_vec(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream);
+int launch_warp(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream);
+int launch_tile(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream);
+
+cudaError_t take_error_warp(unsigned long long *v);
+cudaError_t take_error_tile(unsigned long long *v);
+
+}  // namespace lc

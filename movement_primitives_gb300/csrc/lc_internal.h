@@ -1,0 +1,91 @@
+// Internal planner structures shared by the host planner (plan.cpp) and the
+// kernel launchers (kernels.cu).  Not part of the ABI.
+#pragma once
+
+#include <cstdint>
+
+#include "layout_copy.h"
+
+namespace lc {
+
+constexpr int kMaxModes = LC_MAX_RANK + 1;  // the tile mode rides along
+
+// One mode of the aligned iteration: extent and the element stride on each
+// side (the "extent / src_str / dst_str" of the permute_layout page).
+struct Mode {
+    int64_t e, s, d;
+};
+
+struct ModeList {
+    int n = 0;
+    Mode m[kMaxModes];
+};
+
+// [outer, threads, vec] vector copy over the destination-ordered modes.
+struct VecPlan {
+    ModeList outer;   // every mode but the contiguous run, outermost first
+    int64_t run = 1;  // words in the run contiguous on both sides
+    int vec = 1;      // words per vector (vec * w in {1,2,4,8,16} bytes)
+};
+
+// Warp register-staged permute of dense units of U = 32 * P words.
+struct WarpPlan {
+    ModeList unit;    // unit modes, logical order (the page's extent order)
+    ModeList batch;   // modes enumerating the units, outermost first
+    int64_t U = 0;
+    int P = 0, k = 0, shift = 0, mask = 0, cr = 0, cw = 0;
+    int64_t units_per_stage = 1;
+    int64_t n_units = 0;
+};
+
+// TMA tile transpose: X is contiguous in dst, Y contiguous in src.
+struct TilePlan {
+    Mode X{}, Y{};
+    ModeList batch;   // at most 3 (TMA tensors have at most 5 dims)
+    int R = 0;        // source rows (X) per tile
+    int TY = 0;       // words (Y) per 128-byte tile row
+    int S = 0;        // pipeline stages
+    int threads = 0;
+};
+
+struct Plan {
+    int kernel = LC_KERNEL_AUTO;
+    int w = 0;                 // word bytes moved (after fusion)
+    int fused = 1;             // inner-run words fused into one word
+    int64_t src_off = 0, dst_off = 0;  // base offsets, in words of w bytes
+    int64_t total = 0;         // words moved
+    ModeList logical;          // logical order, jointly coalesced (original w)
+    ModeList sorted;           // destination-stride order (fused w)
+    VecPlan vec;
+    WarpPlan warp;
+    TilePlan tile;
+};
+
+// Pointer facts the planner needs (alignment of the two base addresses).
+struct PtrInfo {
+    uintptr_t src = 0, dst = 0;
+    bool check = false;  // false for lc_plan: pointers assumed 256-byte aligned
+};
+
+int make_plan(const lc_tile_layout *src, const lc_tile_layout *dst, int32_t w,
+              int64_t n_tiles, int32_t kernel, const PtrInfo &ptr, Plan *out);
+void fill_info(const Plan &p, lc_plan_info *info);
+
+// Bank simulator ("permute_layout", section "Algorithm", step 2).
+void phase_degrees(const ModeList &unit, int w, int k, int shift, int *rd, int *wd);
+// Returns 0 when conflict-free (k, shift) found; 1 otherwise (best returned).
+int choose_xor(const ModeList &unit, int w, int *k, int *shift, int *rd, int *wd);
+
+// Joint coalescing and shard alignment, exposed for the swizzle queries.
+int align_shards(const lc_tile_layout *src, const lc_tile_layout *dst, ModeList *out);
+
+// Fast unsigned 32-bit division by an invariant divisor: q = n / d for every
+// 32-bit n (Granlund & Montgomery, "Division by invariant integers using
+// multiplication", PLDI 1994, the round-up multiplier with the extra add).
+struct FastDiv {
+    uint32_t d = 1, m = 1;
+    int32_t s = 0;
+};
+FastDiv make_fastdiv(uint32_t d);
+
+}  // namespace lc

@@ -1,0 +1,597 @@
+// Host planner of the strided tile layout copy: validation, canonical forms,
+// the kernel-class decision, the [outer, threads, vec] vector width and the
+// shared-memory bank simulator that picks the warp permute's XOR swizzle.
+//
+// Everything here is integer host code run once per call (microseconds).
+#include <algorithm>
+#include <cstring>
+#include <vector>
+
+#include "lc_internal.h"
+
+namespace lc {
+
+namespace {
+
+constexpr int kWarp = 32;
+constexpr int64_t kMaxOffset = int64_t(1) << 62;  // byte offsets stay in int64
+constexpr int64_t kBruteInjective = int64_t(1) << 24;
+
+bool mul_ok(int64_t a, int64_t b, int64_t *r) { return !__builtin_mul_overflow(a, b, r); }
+bool add_ok(int64_t a, int64_t b, int64_t *r) { return !__builtin_add_overflow(a, b, r); }
+
+bool valid_width(int w) { return w == 1 || w == 2 || w == 4 || w == 8 || w == 16; }
+
+// Neighbouring modes (outer, inner) merge when they are row-major contiguous
+// on BOTH sides: s_outer == s_inner * e_inner and d_outer == d_inner * e_inner.
+void coalesce(ModeList *ml) {
+    int n = 0;
+    for (int i = 0; i < ml->n; ++i) {
+        const Mode &c = ml->m[i];
+        if (n > 0) {
+            Mode &o = ml->m[n - 1];
+            if (o.s == c.s * c.e && o.d == c.d * c.e) {
+                o.e *= c.e;
+                o.s = c.s;
+                o.d = c.d;
+                continue;
+            }
+        }
+        ml->m[n++] = c;
+    }
+    ml->n = n;
+}
+
+// Modes of a set are "dense" on one side when their offsets tile [0, prod e)
+// exactly: sorted by that side's stride they read 1, e_a, e_a * e_b, ...
+bool dense(const ModeList &ml, int first, bool src_side) {
+    std::vector<std::pair<int64_t, int64_t>> v;  // (stride, extent)
+    for (int i = first; i < ml.n; ++i)
+        v.push_back({src_side ? ml.m[i].s : ml.m[i].d, ml.m[i].e});
+    std::sort(v.begin(), v.end());
+    int64_t expect = 1;
+    for (auto &p : v) {
+        if (p.first != expect) return false;
+        expect *= p.second;
+    }
+    return true;
+}
+
+// Is  i -> sum_k i_k d_k  one-to-one over the modes?  Sorted by stride, a
+// stride larger than everything the smaller modes reach proves it; otherwise
+// small cases are settled by enumeration and large ones are refused.
+int dst_injective(const ModeList &ml, int64_t total) {
+    std::vector<std::pair<int64_t, int64_t>> v;
+    for (int i = 0; i < ml.n; ++i) v.push_back({ml.m[i].d, ml.m[i].e});
+    std::sort(v.begin(), v.end());
+    int64_t reach = 0;
+    bool nested = true;
+    for (auto &p : v) {
+        if (p.first <= reach) { nested = false; break; }
+        reach += (p.second - 1) * p.first;
+    }
+    if (nested) return LC_OK;
+    if (total > kBruteInjective) return LC_ERR_NOT_INJECTIVE;
+    std::vector<int64_t> offs;
+    offs.reserve(size_t(total));
+    std::vector<int64_t> idx(ml.n, 0);
+    for (int64_t t = 0; t < total; ++t) {
+        int64_t o = 0;
+        for (int i = 0; i < ml.n; ++i) o += idx[i] * ml.m[i].d;
+        offs.push_back(o);
+        for (int i = ml.n - 1; i >= 0; --i) {
+            if (++idx[i] < ml.m[i].e) break;
+            idx[i] = 0;
+        }
+    }
+    std::sort(offs.begin(), offs.end());
+    return std::adjacent_find(offs.begin(), offs.end()) == offs.end() ? LC_OK
+                                                                      : LC_ERR_NOT_INJECTIVE;
+}
+
+int check_layout(const lc_tile_layout *l) {
+    if (l->rank < 1 || l->rank > LC_MAX_RANK) return LC_ERR_RANK;
+    for (int k = 0; k < l->rank; ++k)
+        if (l->shape[k] < 0) return LC_ERR_SHAPE;
+    if (l->offset < 0 || l->tile_stride < 0) return LC_ERR_BAD_STRIDE;
+    return LC_OK;
+}
+
+// 1 + sum (e - 1) * stride, with overflow reported.
+int cosize(const lc_tile_layout *l, int64_t *out) {
+    int64_t c = 1;
+    for (int k = 0; k < l->rank; ++k) {
+        if (l->shape[k] == 0) { *out = 0; return LC_OK; }
+        int64_t t;
+        if (!mul_ok(l->shape[k] - 1, l->stride[k], &t) || !add_ok(c, t, &c)) return LC_ERR_OVERFLOW;
+    }
+    *out = c;
+    return LC_OK;
+}
+
+// Byte address alignment of a base (pointer + offset * w).
+uintptr_t base_addr(uintptr_t p, int64_t off, int w) { return p + uintptr_t(off) * uintptr_t(w); }
+
+// --------------------------------------------------------------------------
+// bank simulator
+// --------------------------------------------------------------------------
+
+// Worst degree of one warp-wide access: 128-byte wavefronts (32 lanes for
+// words up to 4 bytes, 16 lanes for 8, 8 lanes for 16); per bank, the number
+// of distinct 4-byte words it must deliver.
+int access_degree(const int64_t *byte_addr, int w) {
+    const int per = w <= 4 ? kWarp : 128 / w;
+    int worst = 0;
+    for (int g = 0; g < kWarp; g += per) {
+        int64_t words[kWarp * 4];
+        int nw = 0;
+        for (int l = g; l < g + per; ++l) {
+            int64_t first = byte_addr[l] >> 2, last = (byte_addr[l] + w - 1) >> 2;
+            for (int64_t x = first; x <= last; ++x) words[nw++] = x;
+        }
+        std::sort(words, words + nw);
+        nw = int(std::unique(words, words + nw) - words);
+        int per_bank[32] = {0};
+        for (int i = 0; i < nw; ++i) {
+            int b = int(words[i] & 31);
+            worst = std::max(worst, ++per_bank[b]);
+        }
+    }
+    return worst;
+}
+
+int64_t unit_size(const ModeList &u) {
+    int64_t t = 1;
+    for (int i = 0; i < u.n; ++i) t *= u.m[i].e;
+    return t;
+}
+
+}  // namespace
+
+FastDiv make_fastdiv(uint32_t d) {
+    FastDiv f;
+    f.d = d ? d : 1;
+    int s = 0;
+    while ((uint64_t(1) << s) < f.d) ++s;
+    f.s = s;
+    f.m = uint32_t(((uint64_t(1) << 32) * ((uint64_t(1) << s) - f.d)) / f.d + 1);
+    return f;
+}
+
+void phase_degrees(const ModeList &unit, int w, int k, int shift, int *rd, int *wd) {
+    const int64_t total = unit_size(unit);
+    const int P = int(total / kWarp);
+    const int mask = (1 << k) - 1;
+    int r_worst = 0, w_worst = 0;
+    for (int r = 0; r < P; ++r) {
+        int64_t ra[kWarp], wa[kWarp];
+        for (int lane = 0; lane < kWarp; ++lane) {
+            const int j = r ^ ((lane >> shift) & mask);
+            int64_t flat = lane + int64_t(kWarp) * j, so = 0, dof = 0;
+            for (int i = unit.n - 1; i >= 0; --i) {
+                const int64_t c = flat % unit.m[i].e;
+                flat /= unit.m[i].e;
+                so += c * unit.m[i].s;
+                dof += c * unit.m[i].d;
+            }
+            ra[lane] = so * w;
+            wa[lane] = dof * w;
+        }
+        r_worst = std::max(r_worst, access_degree(ra, w));
+        w_worst = std::max(w_worst, access_degree(wa, w));
+    }
+    *rd = r_worst;
+    *wd = w_worst;
+}
+
+int choose_xor(const ModeList &unit, int w, int *k_out, int *shift_out, int *rd_out, int *wd_out) {
+    const int64_t P = unit_size(unit) / kWarp;
+    int kmax = 0;
+    if (P > 0 && (P & (P - 1)) == 0)
+        while ((int64_t(1) << (kmax + 1)) <= P) ++kmax;
+    int best = 1 << 30, bk = 0, bs = 0, brd = 0, bwd = 0;
+    for (int k = 0; k <= kmax; ++k) {
+        const int smax = k ? 5 - k : 0;
+        for (int shift = 0; shift <= smax; ++shift) {
+            int rd, wd;
+            phase_degrees(unit, w, k, shift, &rd, &wd);
+            if (rd <= 1 && wd <= 1) {
+                *k_out = k; *shift_out = shift; *rd_out = rd; *wd_out = wd;
+                return 0;
+            }
+            if (std::max(rd, wd) < best) {
+                best = std::max(rd, wd); bk = k; bs = shift; brd = rd; bwd = wd;
+            }
+        }
+    }
+    *k_out = bk; *shift_out = bs; *rd_out = brd; *wd_out = bwd;
+    return 1;
+}
+
+int align_shards(const lc_tile_layout *src, const lc_tile_layout *dst, ModeList *out) {
+    int st;
+    if ((st = check_layout(src)) || (st = check_layout(dst))) return st;
+    int ns = 0, nd = 0;
+    Mode tmp[LC_MAX_RANK];
+    int64_t de[LC_MAX_RANK], dd[LC_MAX_RANK];
+    for (int k = 0; k < dst->rank; ++k)
+        if (dst->shape[k] != 1) { de[nd] = dst->shape[k]; dd[nd] = dst->stride[k]; ++nd; }
+    for (int k = 0; k < src->rank; ++k)
+        if (src->shape[k] != 1) { tmp[ns] = Mode{src->shape[k], src->stride[k], 0}; ++ns; }
+    if (ns != nd) return LC_ERR_EXTENT_MISMATCH;
+    out->n = 0;
+    for (int i = 0; i < ns; ++i) {
+        if (tmp[i].e != de[i]) return LC_ERR_EXTENT_MISMATCH;
+        out->m[out->n++] = Mode{tmp[i].e, tmp[i].s, dd[i]};
+    }
+    coalesce(out);
+    return LC_OK;
+}
+
+// --------------------------------------------------------------------------
+// the plan
+// --------------------------------------------------------------------------
+
+namespace {
+
+// Widest vector (16, 8, 4, 2, 1 bytes, at least one word) whose per-thread
+// pointers all stay aligned ("copy -> gmem_smem", section "Algorithm",
+// step 2): the run length is a multiple of it, so are every other stride on
+// both sides and both base offsets, and so are the two base addresses.
+int choose_vec(const Plan &p, const PtrInfo &ptr) {
+    for (int bytes = 16; bytes >= p.w; bytes >>= 1) {
+        if (bytes % p.w) continue;
+        const int v = bytes / p.w;
+        if (v == 1) return 1;
+        if (p.vec.run % v) continue;
+        bool ok = p.src_off % v == 0 && p.dst_off % v == 0;
+        for (int i = 0; ok && i < p.vec.outer.n; ++i)
+            ok = p.vec.outer.m[i].s % v == 0 && p.vec.outer.m[i].d % v == 0;
+        if (ok && ptr.check)
+            ok = base_addr(ptr.src, p.src_off, p.w) % bytes == 0 &&
+                 base_addr(ptr.dst, p.dst_off, p.w) % bytes == 0;
+        if (ok) return v;
+    }
+    return 1;
+}
+
+void plan_vec(Plan *p, const PtrInfo &ptr) {
+    p->vec = VecPlan{};
+    const ModeList &sl = p->sorted;
+    int n = sl.n;
+    if (n > 0 && sl.m[n - 1].s == 1 && sl.m[n - 1].d == 1) {
+        p->vec.run = sl.m[n - 1].e;
+        --n;
+    }
+    for (int i = 0; i < n; ++i) p->vec.outer.m[i] = sl.m[i];
+    p->vec.outer.n = n;
+    p->vec.vec = choose_vec(*p, ptr);
+}
+
+constexpr int64_t kStageTarget = 16 * 1024;  // bytes of units staged at once
+
+// Warp permute: the smallest innermost (logical-order) mode suffix that is a
+// dense block on both sides and a whole number of warp lanes (32 * P words,
+// P <= 32); the rest of the modes enumerate units.  Units move whole with
+// bulk copies, so their bytes and every unit base must be 16-byte aligned.
+bool plan_warp(Plan *p, const PtrInfo &ptr, bool need_conflict_free) {
+    const ModeList &lg = p->logical;
+    const int w = p->w;  // unfused (caller guarantees p->fused == 1)
+    int first = -1;
+    int64_t U = 1;
+    for (int i = lg.n - 1; i >= 0; --i) {
+        U *= lg.m[i].e;
+        if (U > 32 * kWarp) break;
+        if (U % kWarp == 0 && dense(lg, i, true) && dense(lg, i, false)) { first = i; break; }
+    }
+    if (first < 0) return false;
+    if ((U * w) % 16) return false;
+    for (int i = 0; i < first; ++i)
+        if ((lg.m[i].s * w) % 16 || (lg.m[i].d * w) % 16) return false;
+    if ((p->src_off * w) % 16 || (p->dst_off * w) % 16) return false;
+    if (ptr.check && (ptr.src % 16 || ptr.dst % 16)) return false;
+
+    WarpPlan &wp = p->warp;
+    wp = WarpPlan{};
+    for (int i = first; i < lg.n; ++i) wp.unit.m[wp.unit.n++] = lg.m[i];
+    for (int i = 0; i < first; ++i) wp.batch.m[wp.batch.n++] = lg.m[i];
+    wp.U = U;
+    wp.P = int(U / kWarp);
+    const int bad = choose_xor(wp.unit, w, &wp.k, &wp.shift, &wp.cr, &wp.cw);
+    if (bad && need_conflict_free) return false;
+    wp.mask = (1 << wp.k) - 1;
+    wp.n_units = p->total / U;
+    wp.units_per_stage = std::max<int64_t>(1, std::min<int64_t>(wp.n_units, kStageTarget / (U * w)));
+    return true;
+}
+
+// Tile transpose: a mode contiguous in dst (X) and another contiguous in src
+// (Y); at most three other (batch) modes; TMA needs 16-byte aligned bases
+// and 16-byte multiple strides, stores need the same on the destination.
+bool plan_tile(Plan *p, const PtrInfo &ptr) {
+    const ModeList &sl = p->sorted;
+    int xi = -1, yi = -1;
+    for (int i = 0; i < sl.n; ++i) {
+        if (sl.m[i].d == 1) xi = i;
+        if (sl.m[i].s == 1) yi = i;
+    }
+    if (xi < 0 || yi < 0 || xi == yi) return false;
+    TilePlan &tp = p->tile;
+    tp = TilePlan{};
+    tp.X = sl.m[xi];
+    tp.Y = sl.m[yi];
+    for (int i = 0; i < sl.n; ++i)
+        if (i != xi && i != yi) tp.batch.m[tp.batch.n++] = sl.m[i];
+    if (tp.batch.n > 3) return false;
+    const int w = p->w;
+    auto a16 = [](int64_t x) { return x % 16 == 0; };
+    if (!a16(tp.X.s * w) || !a16(tp.Y.d * w)) return false;
+    if (tp.X.s * w >= (int64_t(1) << 40)) return false;
+    for (int i = 0; i < tp.batch.n; ++i) {
+        const Mode &b = tp.batch.m[i];
+        if (b.s <= 0 || !a16(b.s * w) || !a16(b.d * w)) return false;
+        if (b.s * w >= (int64_t(1) << 40) || b.e > (int64_t(1) << 31)) return false;
+    }
+    if (tp.X.e > (int64_t(1) << 31) || tp.Y.e * (w == 16 ? 2 : 1) > (int64_t(1) << 31)) return false;
+    if (!a16(p->src_off * w) || !a16(p->dst_off * w)) return false;
+    if (ptr.check && (ptr.src % 16 || ptr.dst % 16)) return false;
+    tp.TY = 128 / w;
+    tp.R = w <= 2 ? 256 : 128;  // must match TileCfg in kernels.cu
+    tp.S = 4;
+    tp.threads = w == 1 ? 128 : 256;
+    return true;
+}
+
+// A contiguous run of L words with L * w <= 16 bytes (a power of two) moves
+// as one wider word when every other stride, both offsets and both base
+// addresses allow it: the copy is then a permute of (L * w)-byte words.
+void fuse_inner_run(Plan *p, const PtrInfo &ptr) {
+    ModeList &sl = p->sorted;
+    if (sl.n == 0) return;
+    const Mode r = sl.m[sl.n - 1];
+    if (r.s != 1 || r.d != 1) return;
+    const int64_t L = r.e;
+    const int64_t nb = L * p->w;
+    if (nb > 16 || (nb & (nb - 1))) return;
+    if (p->src_off % L || p->dst_off % L) return;
+    for (int i = 0; i + 1 < sl.n; ++i)
+        if (sl.m[i].s % L || sl.m[i].d % L) return;
+    if (ptr.check && (base_addr(ptr.src, p->src_off, p->w) % nb ||
+                      base_addr(ptr.dst, p->dst_off, p->w) % nb))
+        return;
+    --sl.n;
+    for (int i = 0; i < sl.n; ++i) { sl.m[i].s /= L; sl.m[i].d /= L; }
+    p->src_off /= L;
+    p->dst_off /= L;
+    p->w = int(nb);
+    p->fused = int(L);
+}
+
+}  // namespace
+
+int make_plan(const lc_tile_layout *src, const lc_tile_layout *dst, int32_t w,
+              int64_t n_tiles, int32_t kernel, const PtrInfo &ptr, Plan *out) {
+    if (!src || !dst || !out) return LC_ERR_NULL;
+    int st;
+    if ((st = check_layout(src)) || (st = check_layout(dst))) return st;
+    if (!valid_width(w)) return LC_ERR_ELEM_BYTES;
+    if (n_tiles < 0) return LC_ERR_SHAPE;
+    if (kernel < LC_KERNEL_AUTO || kernel > LC_KERNEL_TILE_TRANSPOSE) return LC_ERR_UNSUPPORTED;
+
+    Plan p;
+    p.w = w;
+    // pair the non-unit modes ("equal non-unit extents")
+    ModeList paired;
+    if ((st = align_shards(src, dst, &paired))) return st;
+    // align_shards already coalesced; recount the total from the raw extents
+    int64_t total = n_tiles;
+    for (int k = 0; k < src->rank; ++k)
+        if (!mul_ok(total, src->shape[k], &total)) return LC_ERR_OVERFLOW;
+    p.total = total;
+    if (total == 0) { p.kernel = kernel ? kernel : LC_KERNEL_VEC_COPY; *out = p; return LC_OK; }
+
+    for (int k = 0; k < src->rank; ++k)
+        if (src->shape[k] != 1 && src->stride[k] < 0) return LC_ERR_BAD_STRIDE;
+    for (int k = 0; k < dst->rank; ++k)
+        if (dst->shape[k] != 1 && dst->stride[k] <= 0) return LC_ERR_BAD_STRIDE;
+
+    int64_t cs, cd;
+    if ((st = cosize(src, &cs)) || (st = cosize(dst, &cd))) return st;
+    const int64_t sts = src->tile_stride ? src->tile_stride : cs;
+    const int64_t dts = dst->tile_stride ? dst->tile_stride : cd;
+
+    // largest offsets reached, which must stay addressable in bytes
+    int64_t smax, dmax, t;
+    if (!mul_ok(n_tiles - 1, sts, &t) || !add_ok(t, src->offset + cs - 1, &smax)) return LC_ERR_OVERFLOW;
+    if (!mul_ok(n_tiles - 1, dts, &t) || !add_ok(t, dst->offset + cd - 1, &dmax)) return LC_ERR_OVERFLOW;
+    if (smax >= kMaxOffset / 16 || dmax >= kMaxOffset / 16) return LC_ERR_OVERFLOW;
+
+    // logical order: the tile mode outermost, then the paired modes, merged
+    ModeList lg;
+    if (n_tiles > 1) lg.m[lg.n++] = Mode{n_tiles, sts, dts};
+    for (int i = 0; i < paired.n; ++i) lg.m[lg.n++] = paired.m[i];
+    coalesce(&lg);
+    if ((st = dst_injective(lg, total))) return st;
+
+    if (ptr.check) {
+        if (!ptr.src || !ptr.dst) return LC_ERR_NULL;
+        if (ptr.src % w || ptr.dst % w) return LC_ERR_ALIGN;
+        const uintptr_t s0 = base_addr(ptr.src, src->offset, w), s1 = base_addr(ptr.src, smax + 1, w);
+        const uintptr_t d0 = base_addr(ptr.dst, dst->offset, w), d1 = base_addr(ptr.dst, dmax + 1, w);
+        if (s0 < d1 && d0 < s1) return LC_ERR_OVERLAP;
+    }
+
+    p.logical = lg;
+    p.src_off = src->offset;
+    p.dst_off = dst->offset;
+    // destination order: stride descending (stable), merged again
+    p.sorted = lg;
+    std::stable_sort(p.sorted.m, p.sorted.m + p.sorted.n,
+                     [](const Mode &a, const Mode &b) { return a.d > b.d; });
+    coalesce(&p.sorted);
+
+    if (kernel == LC_KERNEL_WARP_PERMUTE) {
+        plan_vec(&p, ptr);
+        if (!plan_warp(&p, ptr, false)) return LC_ERR_UNSUPPORTED;
+        p.kernel = kernel;
+        *out = p;
+        return LC_OK;
+    }
+    fuse_inner_run(&p, ptr);
+    plan_vec(&p, ptr);  // always available: the fallback of every other class
+    if (kernel == LC_KERNEL_TILE_TRANSPOSE) {
+        if (!plan_tile(&p, ptr)) return LC_ERR_UNSUPPORTED;
+        p.kernel = kernel;
+        *out = p;
+        return LC_OK;
+    }
+    if (kernel == LC_KERNEL_VEC_COPY) {
+        p.kernel = kernel;
+        *out = p;
+        return LC_OK;
+    }
+
+    // automatic choice
+    const ModeList &sl = p.sorted;
+    const bool run = sl.n > 0 && sl.m[sl.n - 1].s == 1 && sl.m[sl.n - 1].d == 1;
+    bool has_x = false, has_y = false;
+    for (int i = 0; i < sl.n; ++i) { has_x |= sl.m[i].d == 1; has_y |= sl.m[i].s == 1; }
+    if (!run && has_x && has_y) {
+        if (p.fused == 1) {
+            Plan q = p;
+            if (plan_warp(&q, ptr, true)) { q.kernel = LC_KERNEL_WARP_PERMUTE; *out = q; return LC_OK; }
+        }
+        if (plan_tile(&p, ptr)) { p.kernel = LC_KERNEL_TILE_TRANSPOSE; *out = p; return LC_OK; }
+    }
+    p.kernel = LC_KERNEL_VEC_COPY;
+    *out = p;
+    return LC_OK;
+}
+
+void fill_info(const Plan &p, lc_plan_info *info) {
+    std::memset(info, 0, sizeof(*info));
+    info->kernel = p.kernel;
+    info->elem_bytes = p.w;
+    info->total = p.total;
+    const ModeList &ml = p.kernel == LC_KERNEL_WARP_PERMUTE ? p.logical : p.sorted;
+    info->n_modes = ml.n;
+    for (int i = 0; i < ml.n; ++i) {
+        info->extent[i] = ml.m[i].e;
+        info->src_stride[i] = ml.m[i].s;
+        info->dst_stride[i] = ml.m[i].d;
+    }
+    info->vec = p.vec.vec;
+    info->run = p.vec.run;
+    info->unit_modes = p.warp.unit.n;
+    info->P = p.warp.P;
+    info->k = p.warp.k;
+    info->shift = p.warp.shift;
+    info->mask = p.warp.mask;
+    info->conflicts_read = p.warp.cr;
+    info->conflicts_write = p.warp.cw;
+    info->units_per_chunk = p.warp.units_per_stage;
+    info->tile_rows = p.tile.R;
+    info->tile_cols = p.tile.TY;
+    info->stages = p.tile.S;
+}
+
+}  // namespace lc
+
+// ----------------------------------------------------------------------------
+// host-only ABI entry points
+// ----------------------------------------------------------------------------
+
+extern "C" int lc_plan(const lc_tile_layout *src_layout, const lc_tile_layout *dst_layout,
+                       int32_t elem_bytes, int64_t n_tiles, int32_t kernel, lc_plan_info *out) {
+    if (!out) return LC_ERR_NULL;
+    lc::Plan p;
+    lc::PtrInfo ptr;
+    const int st = lc::make_plan(src_layout, dst_layout, elem_bytes, n_tiles, kernel, ptr, &p);
+    if (st) return st;
+    lc::fill_info(p, out);
+    return LC_OK;
+}
+
+extern "C" int lc_choose_swizzle(const lc_tile_layout *src_layout, const lc_tile_layout *dst_layout,
+                                 int32_t elem_bytes, int32_t *k, int32_t *shift, int32_t *mask,
+                                 int32_t *conflicts_read, int32_t *conflicts_write) {
+    if (!src_layout || !dst_layout || !k || !shift || !mask || !conflicts_read || !conflicts_write)
+        return LC_ERR_NULL;
+    if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8 && elem_bytes != 16)
+        return LC_ERR_ELEM_BYTES;
+    lc::ModeList unit;
+    const int st = lc::align_shards(src_layout, dst_layout, &unit);
+    if (st) return st;
+    int64_t total = 1;
+    for (int i = 0; i < unit.n; ++i) total *= unit.m[i].e;
+    if (total == 0 || total % 32) return LC_ERR_SHAPE;
+    int kk, ss, rd, wd;
+    const int bad = lc::choose_xor(unit, elem_bytes, &kk, &ss, &rd, &wd);
+    *k = kk; *shift = ss; *mask = (1 << kk) - 1; *conflicts_read = rd; *conflicts_write = wd;
+    return bad ? LC_ERR_NO_SWIZZLE : LC_OK;
+}
+
+extern "C" int lc_swizzle_conflicts(const lc_tile_layout *src_layout, const lc_tile_layout *dst_layout,
+                                    int32_t elem_bytes, int32_t k, int32_t shift,
+                                    int32_t *conflicts_read, int32_t *conflicts_write) {
+    if (!src_layout || !dst_layout || !conflicts_read || !conflicts_write) return LC_ERR_NULL;
+    if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8 && elem_bytes != 16)
+        return LC_ERR_ELEM_BYTES;
+    if (k < 0 || k > 5 || shift < 0 || shift > 31) return LC_ERR_SHAPE;
+    lc::ModeList unit;
+    const int st = lc::align_shards(src_layout, dst_layout, &unit);
+    if (st) return st;
+    int64_t total = 1;
+    for (int i = 0; i < unit.n; ++i) total *= unit.m[i].e;
+    if (total == 0 || total % 32) return LC_ERR_SHAPE;
+    int rd, wd;
+    lc::phase_degrees(unit, elem_bytes, k, shift, &rd, &wd);
+    *conflicts_read = rd;
+    *conflicts_write = wd;
+    return LC_OK;
+}
+
+extern "C" int lc_gmem_smem_partition(const lc_tile_layout *global_layout,
+                                      const lc_tile_layout *shared_layout, int32_t elem_bytes,
+                                      int32_t threads, int32_t *vec, int64_t *outer) {
+    if (!global_layout || !shared_layout || !vec || !outer) return LC_ERR_NULL;
+    if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8 && elem_bytes != 16)
+        return LC_ERR_ELEM_BYTES;
+    if (threads < 1) return LC_ERR_SHAPE;
+    lc::ModeList ml;
+    int st = lc::align_shards(global_layout, shared_layout, &ml);
+    if (st) return st;
+    // the global side drives the canonical (stride-descending) order
+    std::stable_sort(ml.m, ml.m + ml.n, [](const lc::Mode &a, const lc::Mode &b) { return a.s > b.s; });
+    // merge neighbours contiguous on both sides
+    int n = 0;
+    for (int i = 0; i < ml.n; ++i) {
+        if (n && ml.m[n - 1].s == ml.m[i].s * ml.m[i].e && ml.m[n - 1].d == ml.m[i].d * ml.m[i].e) {
+            ml.m[n - 1].e *= ml.m[i].e;
+            ml.m[n - 1].s = ml.m[i].s;
+            ml.m[n - 1].d = ml.m[i].d;
+        } else {
+            ml.m[n++] = ml.m[i];
+        }
+    }
+    ml.n = n;
+    int64_t total = 1;
+    for (int i = 0; i < ml.n; ++i) total *= ml.m[i].e;
+    if (total % threads) return LC_ERR_SHAPE;
+    for (int bytes = 16; bytes >= elem_bytes; bytes >>= 1) {
+        if (bytes % elem_bytes) continue;
+        const int v = bytes / elem_bytes;
+        bool ok = total % (int64_t(threads) * v) == 0;
+        if (ok && v > 1) {
+            ok = ml.n > 0 && ml.m[ml.n - 1].s == 1 && ml.m[ml.n - 1].d == 1 && ml.m[ml.n - 1].e % v == 0 &&
+                 global_layout->offset % v == 0 && shared_layout->offset % v == 0;
+            for (int i = 0; ok && i + 1 < ml.n; ++i) ok = ml.m[i].s % v == 0 && ml.m[i].d % v == 0;
+        }
+        if (ok) {
+            *vec = v;
+            *outer = total / (int64_t(threads) * v);
+            return LC_OK;
+        }
+    }
+    return LC_ERR_SHAPE;
+}

@@ -1,0 +1,250 @@
+"""The C-ABI library on the host (no GPU): symbols, planner, bank simulator,
+[outer, threads, vec] partition and validation, against the oracle."""
+import itertools
+import os
+import random
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import banks, index_maps
+from oracle.definition import Layout
+
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def M():
+    import __graft_entry__
+    __graft_entry__.build()
+    import movement_primitives_gb300
+    return movement_primitives_gb300
+
+
+def _declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^[A-Za-z_][\w \*]*?\b(lc_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol(M):
+    import ctypes
+    names = _declared_functions()
+    assert len(names) >= 10
+    handle = ctypes.CDLL(M._lib.LIB_PATH)
+    for n in names:
+        assert hasattr(handle, n), n
+    assert set(names) == set(M._lib.PROTOTYPES), "binding and header disagree"
+
+
+def test_status_and_kernel_names(M):
+    lib = M._lib.lib()
+    for code in range(15):
+        assert lib.lc_status_string(code) and lib.lc_status_string(code) != b"unknown status"
+    assert lib.lc_kernel_name(2) == b"warp_permute"
+
+
+# ---------------------------------------------------------------------------
+# planner on the workloads and the pages' worked examples
+# ---------------------------------------------------------------------------
+
+def test_plan_scale_factor_transpose(M):
+    """'permute_layout' demonstration: P = 4, shift = 3, mask = 3 (k = 2)."""
+    import workloads
+    c = workloads.config(2)
+    p = M.plan(c["src"], c["dst"], 4, c["n_tiles"])
+    assert p["kernel_name"] == "warp_permute"
+    assert (p["P"], p["k"], p["shift"], p["mask"]) == (4, 2, 3, 3)
+    assert (p["conflicts_read"], p["conflicts_write"]) == (1, 1)
+    assert p["modes"][-2:] == [(4, 32, 1), (32, 1, 4)]
+
+
+def test_plan_workloads(M):
+    import workloads
+    expect = {1: "warp_permute", 3: "tile_transpose", 5: "vec_copy"}
+    for cfg, kname in expect.items():
+        c = workloads.config(cfg)
+        assert M.plan(c["src"], c["dst"], c["elem_bytes"], c["n_tiles"])["kernel_name"] == kname
+    for w in (1, 2, 4, 8, 16):
+        c = workloads.config(4, w)
+        p = M.plan(c["src"], c["dst"], w, 1)
+        assert p["kernel_name"] == "tile_transpose" and p["tile_cols"] * w == 128
+    p = M.plan(workloads.config(5)["src"], workloads.config(5)["dst"], 2)
+    assert (p["vec"], p["run"]) == (8, 128)  # 16-byte vectors over 256-byte runs
+
+
+def test_gmem_smem_partition_table(M):
+    """'copy -> gmem_smem' dtype table: fp32 vec 4 / outer 8, fp16 8 / 4, u8 16 / 2."""
+    for w, vec, outer in [(4, 4, 8), (2, 8, 4), (1, 16, 2)]:
+        assert M.gmem_smem_partition(M.TileLayout((32, 32)), M.TileLayout((32, 32)), w, 32) == (vec, outer)
+
+
+def test_gmem_smem_partition_matches_oracle(M):
+    rng = random.Random(3)
+    for _ in range(300):
+        rank = rng.randint(1, 3)
+        ext = tuple(rng.choice([1, 2, 4, 8, 16]) for _ in range(rank))
+        go = list(range(rank)); rng.shuffle(go)
+        so = list(range(rank)); rng.shuffle(so)
+
+        def st(order):
+            s, acc = [0] * rank, 1
+            for m in reversed(order):
+                s[m] = acc
+                acc *= ext[m]
+            return tuple(s)
+        g, s = st(go), st(so)
+        w = rng.choice([1, 2, 4, 8, 16])
+        T = rng.choice([1, 2, 4, 8, 32])
+        goff, soff = rng.choice([0, 0, 2, 4]), rng.choice([0, 0, 8])
+        try:
+            want = index_maps.gmem_smem_partition(ext, g, s, w, T, goff, soff)
+        except index_maps.Decline:
+            with pytest.raises(M.LayoutCopyError):
+                M.gmem_smem_partition(M.TileLayout(ext, g, goff), M.TileLayout(ext, s, soff), w, T)
+            continue
+        got = M.gmem_smem_partition(M.TileLayout(ext, g, goff), M.TileLayout(ext, s, soff), w, T)
+        assert got == (want["vec"], want["outer"]), (ext, g, s, w, T)
+
+
+# ---------------------------------------------------------------------------
+# bank simulator / XOR choice against the oracle's
+# ---------------------------------------------------------------------------
+
+def _swizzle_cases():
+    cases = []
+    for rank in (1, 2, 3):
+        for ext in itertools.product((1, 2, 4, 8, 16, 32), repeat=rank):
+            total = int(np.prod(ext))
+            if total % 32 or total > 256:
+                continue
+            for so in itertools.permutations(range(rank)):
+                for do in itertools.permutations(range(rank)):
+                    def st(order):
+                        s, acc = [0] * rank, 1
+                        for m in reversed(order):
+                            s[m] = acc
+                            acc *= ext[m]
+                        return tuple(s)
+                    cases.append((ext, st(so), st(do)))
+    return cases
+
+
+def test_choose_swizzle_matches_oracle(M):
+    cases = _swizzle_cases()
+    for i, (ext, ss, ds) in enumerate(cases[::5]):
+        for w in ((1, 2, 4, 8, 16) if i % 7 == 0 else (4,)):
+            got = M.choose_swizzle(M.TileLayout(ext, ss), M.TileLayout(ext, ds), w)
+            e, s_str, d_str, _P = index_maps.permute_align(Layout(ext, ss), Layout(ext, ds))
+            want = banks.choose_xor_k(e, s_str, d_str, w)
+            if want is None:
+                assert not got["ok"]
+            else:
+                assert got["ok"]
+                assert (got["k"], got["shift"], got["mask"], got["conflicts_read"],
+                        got["conflicts_write"]) == want, (ext, ss, ds, w)
+
+
+def test_swizzle_conflicts_match_oracle(M):
+    rng = random.Random(9)
+    cases = _swizzle_cases()
+    for _ in range(150):
+        ext, ss, ds = rng.choice(cases)
+        w = rng.choice([1, 2, 4, 8, 16])
+        e, s_str, d_str, P = index_maps.permute_align(Layout(ext, ss), Layout(ext, ds))
+        kmax = P.bit_length() - 1 if P & (P - 1) == 0 else 0
+        k = rng.randint(0, kmax)
+        shift = rng.randint(0, 5 - k) if k else 0
+        got = M.swizzle_conflicts(M.TileLayout(ext, ss), M.TileLayout(ext, ds), w, k, shift)
+        assert got == banks.phase_degrees(e, s_str, d_str, w, k, shift)
+
+
+def test_choose_swizzle_worked_example(M):
+    sl = M.TileLayout((1, 1, 4, 32), (128, 128, 32, 1))
+    dl = M.TileLayout((1, 1, 4, 32), (128, 128, 1, 4))
+    assert M.choose_swizzle(sl, dl, 4) == dict(ok=True, k=2, shift=3, mask=3,
+                                               conflicts_read=1, conflicts_write=1)
+    assert M.swizzle_conflicts(sl, dl, 4, 0, 0) == (1, 4)
+
+
+# ---------------------------------------------------------------------------
+# validation (host-side status codes; no launch happens on these paths)
+# ---------------------------------------------------------------------------
+
+def test_validation_codes(M):
+    S = M.STATUS
+    T = M.TileLayout
+
+    def code(src, dst, w=4, n=1):
+        try:
+            M.plan(src, dst, w, n)
+            return 0
+        except M.LayoutCopyError as e:
+            return e.status
+
+    assert code(T((4, 5), (5, 1)), T((5, 4), (4, 1))) == S["LC_ERR_EXTENT_MISMATCH"]
+    assert code(T((4, 4), (4, 1)), T((4, 4), (1, 4)), w=3) == S["LC_ERR_ELEM_BYTES"]
+    assert code(T((4, 4), (4, -1)), T((4, 4), (1, 4))) == S["LC_ERR_BAD_STRIDE"]
+    assert code(T((4, 4), (4, 1)), T((4, 4), (0, 4))) == S["LC_ERR_BAD_STRIDE"]
+    assert code(T((4, 4), (4, 1)), T((4, 4), (1, 1))) == S["LC_ERR_NOT_INJECTIVE"]
+    assert code(T((4, 4), (4, 1)), T((4, 4), (2, 1))) == S["LC_ERR_NOT_INJECTIVE"]
+    assert code(T((4, 4), (4, 1)), T((4, 4), (4, 1)), n=-1) == S["LC_ERR_SHAPE"]
+    assert code(T((-1, 4), (4, 1)), T((-1, 4), (4, 1))) == S["LC_ERR_SHAPE"]
+    assert code(T((2,) * 9, (1,) * 9), T((2,) * 9, (1,) * 9)) == S["LC_ERR_RANK"]
+    assert code(T((4, 4), (4, 1), -1), T((4, 4), (1, 4))) == S["LC_ERR_BAD_STRIDE"]
+    assert code(T((1 << 40, 1 << 30), (1 << 30, 1)), T((1 << 40, 1 << 30), (1, 1 << 40))) \
+        == S["LC_ERR_OVERFLOW"]
+    # injective but not nested: proved by enumeration
+    assert code(T((2, 3), (3, 2)), T((2, 3), (3, 2))) == 0
+    # tiles that overlap on the destination
+    assert code(T((4,), (1,)), T((4,), (1,), 0, 2), n=3) == S["LC_ERR_NOT_INJECTIVE"]
+    # zero-size copies are fine
+    assert code(T((0, 4), (4, 1)), T((0, 4), (1, 4))) == 0
+    assert code(T((4, 4), (4, 1)), T((4, 4), (1, 4)), n=0) == 0
+
+
+def test_forced_kernel_unsupported(M):
+    T = M.TileLayout
+    with pytest.raises(M.LayoutCopyError) as e:
+        M.plan(T((100,), (1,)), T((100,), (1,)), 4, 1, kernel="tile_transpose")
+    assert e.value.status == M.STATUS["LC_ERR_UNSUPPORTED"]
+    with pytest.raises(M.LayoutCopyError):
+        M.plan(T((40, 40), (40, 1)), T((40, 40), (1, 40)), 4, 1, kernel="warp_permute")
+
+
+def test_pointer_checks_before_launch(M):
+    """NULL / misaligned / overlapping pointers are refused before any CUDA call."""
+    T = M.TileLayout
+    lay = T((16, 16), (16, 1))
+    for args, status in [((0, lay, 4096, lay, 4), "LC_ERR_NULL"),
+                         ((4098, lay, 1 << 20, lay, 4), "LC_ERR_ALIGN"),
+                         ((4096, lay, 4096 + 512, lay, 4), "LC_ERR_OVERLAP")]:
+        with pytest.raises(M.LayoutCopyError) as e:
+            M.layout_copy_ptr(*args, stream=0)
+        assert e.value.status == M.STATUS[status]
+
+
+def test_fastdiv_host_mirror():
+    """The invariant-divisor division used by the vector copy, re-derived here
+    from the published method and checked against integer division."""
+    def make(d):
+        s = 0
+        while (1 << s) < d:
+            s += 1
+        m = ((1 << 32) * ((1 << s) - d)) // d + 1
+        return m & 0xFFFFFFFF, s
+    rng = random.Random(1)
+    ds = [1, 2, 3, 5, 7, 31, 32, 33, 128, 1000, 65535, 65536, (1 << 31) - 1, 1 << 31, (1 << 32) - 1]
+    ds += [rng.randrange(1, 1 << 32) for _ in range(200)]
+    for d in ds:
+        m, s = make(d)
+        for n in [0, 1, d - 1, d, d + 1, (1 << 32) - 1, (1 << 31)] + [rng.randrange(1 << 32) for _ in range(50)]:
+            n &= 0xFFFFFFFF
+            q = (((n * m) >> 32) + n) >> s
+            assert q == n // d, (n, d)

@@ -1,0 +1,301 @@
+"""GPU parity: the CUDA path against the oracle, bit for bit (raw words).
+
+Every case builds seeded host bytes, prefills the destination with the
+sentinel 0xA5, runs the oracle on the host and the library on cuda:0 through
+the C ABI, and compares the WHOLE destination buffer byte for byte (so
+untouched bytes are checked too), then checks the device error word.
+"""
+import random
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+def lc():
+    import movement_primitives_gb300
+    return movement_primitives_gb300
+
+
+def _footprint(layout, n_tiles):
+    return workloads.footprint_elems(layout, n_tiles)
+
+
+def run_case(src_l, dst_l, w, n_tiles=1, kernel="auto", seed=0, src_pad=0, dst_pad=0,
+             src_shift=0, dst_shift=0):
+    """Oracle vs GPU on one copy; returns the planner's kernel name.
+
+    ``*_shift`` moves the base pointer by that many bytes (alignment cases);
+    ``*_pad`` adds slack bytes after the footprint.
+    """
+    ns = _footprint(src_l, n_tiles) * w + src_pad + src_shift
+    nd = _footprint(dst_l, n_tiles) * w + dst_pad + dst_shift
+    g = torch.Generator().manual_seed(seed)
+    src_h = torch.randint(0, 256, (max(ns, 1),), generator=g, dtype=torch.uint8)
+    dst_h = torch.full((max(nd, 1),), workloads.SENTINEL, dtype=torch.uint8)
+    want = dst_h.numpy().copy()
+    oracle.copy(src_h.numpy()[src_shift:].copy(), src_l, want[dst_shift:], dst_l, w, n_tiles)
+    src_d = src_h.cuda()
+    dst_d = dst_h.cuda()
+    lc().layout_copy_ptr(src_d.data_ptr() + src_shift, src_l, dst_d.data_ptr() + dst_shift, dst_l,
+                         w, n_tiles, kernel=kernel, stream=torch.cuda.current_stream().cuda_stream)
+    st, detail = lc().last_device_error()
+    assert st == 0, "device error word %#x" % detail
+    got = dst_d.cpu().numpy()
+    if not np.array_equal(got, want):
+        bad = np.flatnonzero(got != want)
+        raise AssertionError("%d bytes differ, first at %d (got %d want %d); kernel %s"
+                             % (bad.size, bad[0], got[bad[0]], want[bad[0]], kernel))
+    return lc().plan(src_l, dst_l, w, n_tiles, kernel)["kernel_name"]
+
+
+def L(shape, stride, offset=0, tile_stride=0):
+    return dict(shape=tuple(shape), stride=tuple(stride), offset=offset, tile_stride=tile_stride)
+
+
+def row_major(shape):
+    st, acc = [], 1
+    for e in reversed(shape):
+        st.append(acc)
+        acc *= e
+    return tuple(reversed(st))
+
+
+def permuted(shape, perm):
+    """Strides of a row-major tensor of shape[perm] seen through the axes of `shape`."""
+    out_shape = [shape[p] for p in perm]
+    ost = row_major(out_shape)
+    st = [0] * len(shape)
+    for j, p in enumerate(perm):
+        st[p] = ost[j]
+    return tuple(st)
+
+
+# ---------------------------------------------------------------------------
+# the five workloads, reduced (several tiles and a ragged tail), every class
+# ---------------------------------------------------------------------------
+
+SMALL = [(1, None), (2, None), (3, None), (4, 1), (4, 2), (4, 4), (4, 8), (4, 16), (5, None)]
+
+
+@pytest.mark.parametrize("cfg,w", SMALL)
+def test_workload_small_auto(cfg, w):
+    c = workloads.config(cfg, w, scale="small")
+    name = run_case(c["src"], c["dst"], c["elem_bytes"], c["n_tiles"], seed=cfg)
+    expect = {1: "warp_permute", 2: "warp_permute", 3: "tile_transpose", 4: "tile_transpose",
+              5: "vec_copy"}[cfg]
+    assert name == expect
+
+
+@pytest.mark.parametrize("cfg,w", SMALL)
+def test_workload_small_vec_copy(cfg, w):
+    c = workloads.config(cfg, w, scale="small")
+    run_case(c["src"], c["dst"], c["elem_bytes"], c["n_tiles"], kernel="vec_copy", seed=10 + cfg)
+
+
+@pytest.mark.parametrize("cfg", [1, 2])
+def test_workload_warp_permute_forced(cfg):
+    c = workloads.config(cfg, scale="small")
+    run_case(c["src"], c["dst"], c["elem_bytes"], c["n_tiles"], kernel="warp_permute", seed=cfg)
+
+
+@pytest.mark.parametrize("w", [1, 2, 4, 8, 16])
+def test_tile_transpose_ragged(w):
+    # row strides of 16-byte multiples (TMA), extents off the tile grid
+    for r, c in [(1008, 1104), (48, 560), (272, 144), (256, 128), (16, 16)]:
+        assert run_case(L((r, c), (c, 1)), L((r, c), (1, r)), w, kernel="tile_transpose",
+                        seed=r + c) == "tile_transpose"
+    # strides TMA cannot take: the automatic choice still gets it right
+    for r, c in [(37, 555), (257, 129), (3, 1000)]:
+        run_case(L((r, c), (c, 1)), L((r, c), (1, r)), w, seed=r * c)
+
+
+# ---------------------------------------------------------------------------
+# layouts beyond the workloads
+# ---------------------------------------------------------------------------
+
+def test_batched_transposes_with_batch_modes():
+    # (B, M, N) -> (B, N, M): one batch mode on the tile path
+    for w in (1, 2, 4, 8, 16):
+        sh = (3, 70, 130)
+        assert run_case(L(sh, row_major(sh)), L(sh, permuted(sh, (0, 2, 1))), w, seed=w) \
+            in ("tile_transpose", "warp_permute")
+    # three batch modes (rank 5)
+    sh = (2, 3, 2, 40, 72)
+    run_case(L(sh, row_major(sh)), L(sh, permuted(sh, (0, 1, 2, 4, 3))), 2, kernel="tile_transpose")
+    # batch modes in swapped order on the destination
+    sh = (4, 5, 64, 48)
+    run_case(L(sh, row_major(sh)), L(sh, permuted(sh, (1, 0, 3, 2))), 4, kernel="tile_transpose")
+
+
+def test_warp_permute_units_with_gaps_and_tiles():
+    # 4x32 units, tiles spaced apart (tile_stride > cosize) on both sides
+    sh = (4, 32)
+    run_case(L(sh, (32, 1), 16, 256), L(sh, (1, 4), 32, 160), 4, n_tiles=37, kernel="warp_permute")
+    # units whose destination order is a 3-D permutation
+    sh = (2, 4, 16)
+    for w in (1, 2, 4, 8, 16):
+        run_case(L(sh, row_major(sh)), L(sh, permuted(sh, (2, 0, 1))), w, n_tiles=9,
+                 kernel="warp_permute", seed=w)
+
+
+def test_axis_permutes_auto():
+    rng = random.Random(5)
+    for _ in range(25):
+        rank = rng.randint(2, 5)
+        sh = tuple(rng.choice([1, 2, 3, 5, 8, 16, 33]) for _ in range(rank))
+        perm = list(range(rank))
+        rng.shuffle(perm)
+        w = rng.choice([1, 2, 4, 8, 16])
+        run_case(L(sh, row_major(sh)), L(sh, permuted(sh, perm)), w, seed=rng.randrange(1000))
+
+
+def _random_layout_pair(rng):
+    rank = rng.randint(1, 4)
+    ext = [rng.choice([1, 2, 3, 4, 7, 8, 16, 32, 33]) for _ in range(rank)]
+    so = list(range(rank)); rng.shuffle(so)
+    do = list(range(rank)); rng.shuffle(do)
+
+    def strides(order, gap_p):
+        st = [0] * rank
+        acc = 1
+        for m in reversed(order):
+            acc *= rng.choice([1, 2]) if rng.random() < gap_p else 1
+            st[m] = acc
+            acc *= ext[m]
+        return st
+
+    ss = strides(so, 0.3)
+    if rng.random() < 0.15:
+        ss[rng.randrange(rank)] = 0  # broadcast read
+    ds = strides(do, 0.3)
+    n_tiles = rng.choice([1, 1, 2, 5])
+    src = L(ext, ss, rng.randint(0, 9), 0)
+    dst = L(ext, ds, rng.randint(0, 9), rng.choice([0, 0, None]) or 0)
+    return src, dst, rng.choice([1, 2, 4, 8, 16]), n_tiles
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_layouts(seed):
+    rng = random.Random(1000 + seed)
+    for i in range(40):
+        src, dst, w, n_tiles = _random_layout_pair(rng)
+        run_case(src, dst, w, n_tiles, seed=i)
+        run_case(src, dst, w, n_tiles, kernel="vec_copy", seed=i)
+
+
+def test_edge_cases():
+    # empty copies launch nothing and touch nothing
+    run_case(L((0, 4), (4, 1)), L((0, 4), (1, 4)), 4)
+    run_case(L((4, 4), (4, 1)), L((4, 4), (1, 4)), 4, n_tiles=0)
+    # one word
+    run_case(L((1,), (1,)), L((1,), (1,)), 16)
+    # unit modes ignored when pairing, different ranks
+    run_case(L((1, 5, 1, 7), (99, 7, 3, 1)), L((5, 7), (1, 5)), 2)
+    # rank 8
+    sh = (2, 2, 2, 2, 2, 2, 2, 3)
+    run_case(L(sh, row_major(sh)), L(sh, permuted(sh, (7, 6, 5, 4, 3, 2, 1, 0))), 4)
+    # broadcast source (stride 0 everywhere)
+    run_case(L((6, 9), (0, 0), 3), L((6, 9), (9, 1)), 8)
+    # identity copies of every width, odd sizes
+    for w in (1, 2, 4, 8, 16):
+        for n in (1, 15, 4097):
+            run_case(L((n,), (1,)), L((n,), (1,)), w, seed=n)
+
+
+def test_misaligned_bases_still_exact():
+    # base pointers off the 16-byte grid: the planner must pick narrower paths
+    for w, shift in [(1, 1), (2, 2), (4, 4), (8, 8)]:
+        run_case(L((64, 96), (96, 1)), L((64, 96), (1, 64)), w, src_shift=shift)
+        run_case(L((64, 96), (96, 1)), L((64, 96), (1, 64)), w, dst_shift=shift)
+        run_case(L((4, 32), (32, 1)), L((4, 32), (1, 4)), w, n_tiles=11, src_shift=shift)
+        run_case(L((8, 256), (256, 1)), L((8, 256), (256, 1)), w, dst_shift=shift)
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads, in the launch configuration the benchmark times
+# ---------------------------------------------------------------------------
+
+FULL = [(1, None), (2, None), (3, None), (4, 1), (4, 2), (4, 4), (4, 8), (4, 16), (5, None)]
+
+
+@pytest.mark.parametrize("cfg,w", FULL)
+def test_workload_full_size_sampled(cfg, w):
+    c = workloads.config(cfg, w)
+    src_h = workloads.make_src(c)
+    src_d = src_h.cuda()
+    dst_d = workloads.make_dst(c, device="cuda")
+    lc().layout_copy(src_d, c["src"], dst_d, c["dst"], n_tiles=c["n_tiles"], elem_bytes=c["elem_bytes"])
+    st, detail = lc().last_device_error()
+    assert st == 0, "device error word %#x" % detail
+    wbytes = c["elem_bytes"]
+    n = workloads.logical_elems(c)
+    rng = np.random.default_rng(cfg * 100 + wbytes)
+    pts = rng.integers(0, n, size=min(n, 1 << 20), dtype=np.int64)
+    pts[:2] = [0, n - 1]
+    so, do = oracle.offsets_of(c["src"], c["dst"], c["n_tiles"], pts)
+    words = {1: torch.uint8, 2: torch.int16, 4: torch.int32, 8: torch.int64}
+    if wbytes == 16:
+        sv, dv = src_d.view(torch.int64).view(-1, 2), dst_d.view(torch.int64).view(-1, 2)
+    else:
+        sv, dv = src_d.view(words[wbytes]), dst_d.view(words[wbytes])
+    so_t, do_t = torch.from_numpy(so).cuda(), torch.from_numpy(do).cuda()
+    assert torch.equal(sv[so_t], dv[do_t])
+    # The destination image is the whole buffer in these workloads, so the
+    # destination must hold a permutation of the source's 4-byte words (whole
+    # words move together for every width): order-free sums must agree.
+    assert src_d.numel() == dst_d.numel()
+    for part in range(0, src_d.numel() // 4, 1 << 26):
+        s = src_d.view(torch.int32)[part:part + (1 << 26)].to(torch.int64)
+        d = dst_d.view(torch.int32)[part:part + (1 << 26)].to(torch.int64)
+        if c["cfg"] in (2,):  # units are contiguous on both sides: per-slab permutation
+            assert int(s.sum()) == int(d.sum()) and int((s * s).sum()) == int((d * d).sum())
+    s = src_d.view(torch.int32).to(torch.int64)
+    d = dst_d.view(torch.int32).to(torch.int64)
+    assert int(s.sum()) == int(d.sum())
+    assert int((s * s).sum()) == int((d * d).sum())
+    del src_d, dst_d, s, d
+
+
+# ---------------------------------------------------------------------------
+# errors and the bounded-wait failure path
+# ---------------------------------------------------------------------------
+
+def test_bounded_wait_reports_timeout_and_recovers():
+    lc().debug_wait_timeout(200_000)  # 0.2 ms on a barrier nothing arrives at
+    st, detail = lc().last_device_error()
+    assert st == 12 and (detail & 0xff) == 12
+    assert lc().last_device_error() == (0, 0)  # cleared; the context still works
+    run_case(L((32, 32), (32, 1)), L((32, 32), (1, 32)), 4)
+
+
+def test_pointer_errors():
+    M = lc()
+    buf = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
+    p = buf.data_ptr()
+    l4 = L((16, 16), (16, 1))
+    with pytest.raises(M.LayoutCopyError) as e:
+        M.layout_copy_ptr(p, l4, p + 512, l4, 4)  # ranges [0,1024) and [512,1536)
+    assert e.value.status == M.STATUS["LC_ERR_OVERLAP"]
+    with pytest.raises(M.LayoutCopyError) as e:
+        M.layout_copy_ptr(p + 2, l4, p + 4096, l4, 4)
+    assert e.value.status == M.STATUS["LC_ERR_ALIGN"]
+    with pytest.raises(M.LayoutCopyError) as e:
+        M.layout_copy_ptr(0, l4, p, l4, 4)
+    assert e.value.status == M.STATUS["LC_ERR_NULL"]
+    with pytest.raises(ValueError):
+        M.layout_copy(buf[:100], l4, buf[1000:], l4, elem_bytes=4)  # tensor too small
