@@ -49,6 +49,8 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--n-tiles", type=int, default=None,
+                   help="override the tile count (a smaller case of the same kernel, e.g. for ncu)")
     return p.parse_args(argv)
 
 
@@ -260,20 +262,29 @@ def run_oracle(cfg, src_np, dst_np, cores: int) -> float:
     return time.perf_counter() - t0
 
 
+def calibrate(cfg, src_np, dst_np, cores, seconds):
+    """Fraction of the workload the oracle moves in about `seconds` here:
+    probe with growing samples until one takes a measurable time."""
+    frac = 1.0 / 4096
+    while True:
+        t = run_oracle(sampled(cfg, frac), src_np, dst_np, cores)
+        if t >= 0.25 or frac >= 1.0:
+            break
+        frac = min(1.0, frac * 8)
+    return min(1.0, frac * seconds / max(t, 1e-6))
+
+
 def cpu_baseline(cfg, src_np, seconds: float):
     """The oracle, as it stands, on this host's cores over a bounded sample."""
     import numpy as np
-    import oracle  # noqa: F401  (builds the C loop on first use)
     cores = host_cores()
-    probe = sampled(cfg, 1.0 / 4096)
     dst = np.empty(workloads.footprint_elems(cfg["dst"], cfg["n_tiles"]) * cfg["elem_bytes"], np.uint8)
-    t = run_oracle(probe, src_np, dst, cores)
-    frac = min(1.0, max(1.0 / 4096, seconds / max(t, 1e-6) / 4096))
+    frac = calibrate(cfg, src_np, dst, cores, seconds)
     sample = sampled(cfg, frac)
     t = run_oracle(sample, src_np, dst, cores)
     gbs = workload_bytes(sample) / t / 1e9
     return dict(value=round(gbs, 3), unit=UNIT, cores=cores, kind="oracle",
-                sample="%.4f of the workload (%d logical words, %.1f s on %d threads)"
+                sample="%.4f of the workload (%d logical words), %.2f s on %d threads"
                        % (frac, workloads.logical_elems(sample), t, cores))
 
 
@@ -286,10 +297,8 @@ def run_reference(args):
     src = workloads.make_src(cfg).numpy()
     dst = np.empty(workloads.footprint_elems(cfg["dst"], cfg["n_tiles"]) * cfg["elem_bytes"], np.uint8)
     cores = host_cores()
-    probe = sampled(cfg, 1.0 / 4096)
-    t = run_oracle(probe, src, dst, cores)
     budget = 120.0 / max(1, args.steps + args.warmup)  # whole run within a few minutes
-    frac = min(1.0, max(1.0 / 4096, budget / max(t, 1e-6) / 4096))
+    frac = calibrate(cfg, src, dst, cores, budget)
     sample = sampled(cfg, frac)
     for _ in range(args.warmup):
         run_oracle(sample, src, dst, cores)
@@ -337,6 +346,8 @@ def run_ours(args):
     import movement_primitives_gb300 as lc
 
     cfg = workloads.config(args.workload, args.elem_bytes)
+    if args.n_tiles:
+        cfg["n_tiles"] = args.n_tiles
     step_bytes = workload_bytes(cfg)
     src_h = workloads.make_src(cfg)
     src = src_h.to(dev)
@@ -391,23 +402,27 @@ def run_ours(args):
     launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
 
     # end to end through the public API with host buffers (pinned), H2D + copy + D2H
-    src_pin = src_h.pin_memory()
-    dst_pin = torch.empty(dst.numel(), dtype=torch.uint8).pin_memory()
-    e2e_steps = max(1, args.e2e_steps)
-    for it in range(e2e_steps + 2):
-        if it == 2:
-            barrier()
-            torch.cuda.synchronize()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-        src.copy_(src_pin, non_blocking=True)
-        lc.layout_copy(src, cfg["src"], dst, cfg["dst"], n_tiles=cfg["n_tiles"],
-                       elem_bytes=cfg["elem_bytes"], kernel=args.kernel, stream=stream)
-        dst_pin.copy_(dst, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
+    e2e = None
+    if args.e2e_steps > 0:
+        src_pin = src_h.pin_memory()
+        dst_pin = torch.empty(dst.numel(), dtype=torch.uint8).pin_memory()
+        for it in range(args.e2e_steps + 2):
+            if it == 2:
+                barrier()
+                torch.cuda.synchronize()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            src.copy_(src_pin, non_blocking=True)
+            lc.layout_copy(src, cfg["src"], dst, cfg["dst"], n_tiles=cfg["n_tiles"],
+                           elem_bytes=cfg["elem_bytes"], kernel=args.kernel, stream=stream)
+            dst_pin.copy_(dst, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, dev)
+        e2e = {"value": round(world * step_bytes / (e2e_ms / 1e3) / 1e9, 2), "unit": UNIT,
+               "h2d_bytes_per_step": src.numel() * src.element_size(),
+               "d2h_bytes_per_step": dst.numel() * dst.element_size()}
 
     peak, peak_kind = measured_peak()
     achieved = step_bytes / (launch_ms / 1e3) / 1e9
@@ -431,9 +446,7 @@ def run_ours(args):
                          if peak_kind == "measured" else peak_kind},
             "clocks": clocks,
             "gpu_launches": args.steps,
-            "e2e": {"value": round(world * step_bytes / (e2e_ms / 1e3) / 1e9, 2), "unit": UNIT,
-                    "h2d_bytes_per_step": src.numel() * src.element_size(),
-                    "d2h_bytes_per_step": dst.numel() * dst.element_size()},
+            "e2e": e2e,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)

@@ -9,7 +9,9 @@ import ctypes
 import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "liblayoutcopy.so")
+# LC_LIBRARY_PATH points at another build of the same library (e.g. one
+# compiled with different tuning knobs); by default the in-tree build is used.
+LIB_PATH = os.environ.get("LC_LIBRARY_PATH") or os.path.join(HERE, "liblayoutcopy.so")
 MAX_RANK = 8
 
 OK = 0

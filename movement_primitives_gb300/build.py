@@ -49,16 +49,25 @@ def _stale(target: str) -> bool:
     return any(os.path.getmtime(f) > t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile and link if any input changed; returns the library path."""
-    if not force and not _stale(LIB_PATH):
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          out: str | None = None, defines=()) -> str:
+    """Compile and link if any input changed; returns the library path.
+
+    ``out`` / ``defines`` build a variant (compile-time knobs such as
+    LC_TILE_STAGES_NARROW) into another file; the in-tree library is the
+    default build.
+    """
+    lib_path = out or LIB_PATH
+    build_dir = BUILD_DIR if out is None else out + ".objs"
+    if not force and not _stale(lib_path):
+        return lib_path
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
+    extra = ["-D" + d for d in defines]
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
-        cmd = [cc, "-c", os.path.join(CSRC, src), "-o", obj] + ARCH + COMMON
+        obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
+        cmd = [cc, "-c", os.path.join(CSRC, src), "-o", obj] + ARCH + COMMON + extra
         if ptxas_info and src.endswith(".cu"):
             cmd += ["-Xptxas", "-v"]
         res = subprocess.run(cmd, capture_output=True, text=True)
@@ -70,13 +79,13 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB_PATH + ".%d.tmp" % os.getpid()
+    tmp = lib_path + ".%d.tmp" % os.getpid()
     cmd = [cc, "-shared", "-o", tmp] + objs + ARCH + ["-Xcompiler", "-fPIC"]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (" ".join(cmd), res.stderr))
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -15,12 +15,26 @@
 
 namespace lc {
 
+// Ring depth per word width (1- and 2-byte words use 32 KiB tiles, wider
+// words 16 KiB); compile-time knobs so that variants can be measured.  On
+// GB300, 1-byte words run best at two CTAs per SM (3 stages) and 2-byte
+// words at one CTA with 4 stages.
+#ifndef LC_TILE_STAGES_W1
+#define LC_TILE_STAGES_W1 3
+#endif
+#ifndef LC_TILE_STAGES_W2
+#define LC_TILE_STAGES_W2 4
+#endif
+#ifndef LC_TILE_STAGES_WIDE
+#define LC_TILE_STAGES_WIDE 4
+#endif
+
 template <int W> struct TileCfg {
     static constexpr int V = 16 / W;              // words per 16-byte chunk
     static constexpr int TY = 128 / W;            // words per 128-byte tile row
     static constexpr int R = W <= 2 ? 256 : 128;  // source rows per tile (planner agrees)
     static constexpr int NT = W == 1 ? 128 : 256; // threads
-    static constexpr int S = 4;                   // ring stages
+    static constexpr int S = W == 1 ? LC_TILE_STAGES_W1 : W == 2 ? LC_TILE_STAGES_W2 : LC_TILE_STAGES_WIDE;
     static constexpr int TILE_BYTES = 128 * R;
     static constexpr int MB = 8 * R / V;          // V-row x 16-byte micro-blocks
     static constexpr int SMEM = 128 + S * TILE_BYTES;

@@ -13,7 +13,7 @@
 namespace lc {
 
 constexpr int kVecThreads = 256;
-constexpr int kVecUnroll = 4;  // vectors in flight per thread
+constexpr int kVecUnroll = 8;  // vectors in flight per thread
 
 struct VecArgs {
     const uint8_t *src;  // address of source word offset 0

@@ -54,6 +54,8 @@ struct Plan {
     int fused = 1;             // inner-run words fused into one word
     int64_t src_off = 0, dst_off = 0;  // base offsets, in words of w bytes
     int64_t total = 0;         // words moved
+    // byte ranges [lo, hi) each side reaches, relative to its pointer
+    int64_t src_lo = 0, src_hi = 0, dst_lo = 0, dst_hi = 0;
     ModeList logical;          // logical order, jointly coalesced (original w)
     ModeList sorted;           // destination-stride order (fused w)
     VecPlan vec;

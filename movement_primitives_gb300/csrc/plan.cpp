@@ -5,6 +5,9 @@
 // Everything here is integer host code run once per call (microseconds).
 #include <algorithm>
 #include <cstring>
+#include <mutex>
+#include <string>
+#include <unordered_map>
 #include <vector>
 
 #include "lc_internal.h"
@@ -337,7 +340,7 @@ bool plan_tile(Plan *p, const PtrInfo &ptr) {
     if (ptr.check && (ptr.src % 16 || ptr.dst % 16)) return false;
     tp.TY = 128 / w;
     tp.R = w <= 2 ? 256 : 128;  // must match TileCfg in kernels.cu
-    tp.S = 4;
+    tp.S = 4;  // ring depth reported for information (kernels.cu's TileCfg decides)
     tp.threads = w == 1 ? 128 : 256;
     return true;
 }
@@ -369,8 +372,13 @@ void fuse_inner_run(Plan *p, const PtrInfo &ptr) {
 
 }  // namespace
 
-int make_plan(const lc_tile_layout *src, const lc_tile_layout *dst, int32_t w,
-              int64_t n_tiles, int32_t kernel, const PtrInfo &ptr, Plan *out) {
+namespace {
+
+// Validation and planning.  `ptr` carries only the two base addresses modulo
+// 16 (every alignment decision depends on nothing more); NULL, alignment and
+// overlap of the real pointers are checked by make_plan.
+int make_plan_core(const lc_tile_layout *src, const lc_tile_layout *dst, int32_t w,
+                   int64_t n_tiles, int32_t kernel, const PtrInfo &ptr, Plan *out) {
     if (!src || !dst || !out) return LC_ERR_NULL;
     int st;
     if ((st = check_layout(src)) || (st = check_layout(dst))) return st;
@@ -413,14 +421,10 @@ int make_plan(const lc_tile_layout *src, const lc_tile_layout *dst, int32_t w,
     coalesce(&lg);
     if ((st = dst_injective(lg, total))) return st;
 
-    if (ptr.check) {
-        if (!ptr.src || !ptr.dst) return LC_ERR_NULL;
-        if (ptr.src % w || ptr.dst % w) return LC_ERR_ALIGN;
-        const uintptr_t s0 = base_addr(ptr.src, src->offset, w), s1 = base_addr(ptr.src, smax + 1, w);
-        const uintptr_t d0 = base_addr(ptr.dst, dst->offset, w), d1 = base_addr(ptr.dst, dmax + 1, w);
-        if (s0 < d1 && d0 < s1) return LC_ERR_OVERLAP;
-    }
-
+    p.src_lo = src->offset * w;
+    p.src_hi = (smax + 1) * w;
+    p.dst_lo = dst->offset * w;
+    p.dst_hi = (dmax + 1) * w;
     p.logical = lg;
     p.src_off = src->offset;
     p.dst_off = dst->offset;
@@ -465,6 +469,63 @@ int make_plan(const lc_tile_layout *src, const lc_tile_layout *dst, int32_t w,
     }
     p.kernel = LC_KERNEL_VEC_COPY;
     *out = p;
+    return LC_OK;
+}
+
+// Plans are pure functions of (layouts, width, tiles, kernel, base addresses
+// mod 16); a small cache keeps the bank simulator off the per-call path.
+std::mutex g_cache_mu;
+std::unordered_map<std::string, Plan> g_cache;
+constexpr size_t kCacheMax = 512;
+
+void append(std::string &k, const void *p, size_t n) { k.append(static_cast<const char *>(p), n); }
+
+std::string cache_key(const lc_tile_layout *src, const lc_tile_layout *dst, int32_t w, int64_t n_tiles,
+                      int32_t kernel, const PtrInfo &ptr) {
+    std::string k;
+    for (const lc_tile_layout *l : {src, dst}) {
+        append(k, &l->rank, sizeof(l->rank));
+        append(k, l->shape, sizeof(int64_t) * size_t(l->rank));
+        append(k, l->stride, sizeof(int64_t) * size_t(l->rank));
+        append(k, &l->offset, sizeof(l->offset));
+        append(k, &l->tile_stride, sizeof(l->tile_stride));
+    }
+    const int64_t tail[4] = {w, n_tiles, kernel, int64_t((ptr.src & 15) | ((ptr.dst & 15) << 4))};
+    append(k, tail, sizeof(tail));
+    return k;
+}
+
+}  // namespace
+
+int make_plan(const lc_tile_layout *src, const lc_tile_layout *dst, int32_t w,
+              int64_t n_tiles, int32_t kernel, const PtrInfo &ptr, Plan *out) {
+    if (!src || !dst || !out) return LC_ERR_NULL;
+    if (src->rank < 1 || src->rank > LC_MAX_RANK || dst->rank < 1 || dst->rank > LC_MAX_RANK)
+        return LC_ERR_RANK;
+    PtrInfo mod;
+    mod.src = ptr.check ? (ptr.src & 15) : 0;
+    mod.dst = ptr.check ? (ptr.dst & 15) : 0;
+    mod.check = true;
+    const std::string key = cache_key(src, dst, w, n_tiles, kernel, mod);
+    bool hit = false;
+    {
+        std::lock_guard<std::mutex> lk(g_cache_mu);
+        auto it = g_cache.find(key);
+        if (it != g_cache.end()) { *out = it->second; hit = true; }
+    }
+    if (!hit) {
+        const int st = make_plan_core(src, dst, w, n_tiles, kernel, mod, out);
+        if (st) return st;
+        std::lock_guard<std::mutex> lk(g_cache_mu);
+        if (g_cache.size() >= kCacheMax) g_cache.clear();
+        g_cache.emplace(key, *out);
+    }
+    if (!ptr.check || out->total == 0) return LC_OK;
+    if (!ptr.src || !ptr.dst) return LC_ERR_NULL;
+    if (ptr.src % uintptr_t(w) || ptr.dst % uintptr_t(w)) return LC_ERR_ALIGN;
+    const uintptr_t s0 = ptr.src + uintptr_t(out->src_lo), s1 = ptr.src + uintptr_t(out->src_hi);
+    const uintptr_t d0 = ptr.dst + uintptr_t(out->dst_lo), d1 = ptr.dst + uintptr_t(out->dst_hi);
+    if (s0 < d1 && d0 < s1) return LC_ERR_OVERLAP;
     return LC_OK;
 }
 

@@ -131,9 +131,11 @@ def test_tile_transpose_ragged(w):
 def test_batched_transposes_with_batch_modes():
     # (B, M, N) -> (B, N, M): one batch mode on the tile path
     for w in (1, 2, 4, 8, 16):
-        sh = (3, 70, 130)
+        sh = (3, 80, 144)  # 16-byte row strides for every width
         assert run_case(L(sh, row_major(sh)), L(sh, permuted(sh, (0, 2, 1))), w, seed=w) \
-            in ("tile_transpose", "warp_permute")
+            == "tile_transpose"
+        sh = (3, 70, 130)  # unaligned rows: correctness only
+        run_case(L(sh, row_major(sh)), L(sh, permuted(sh, (0, 2, 1))), w, seed=w)
     # three batch modes (rank 5)
     sh = (2, 3, 2, 40, 72)
     run_case(L(sh, row_major(sh)), L(sh, permuted(sh, (0, 1, 2, 4, 3))), 2, kernel="tile_transpose")
@@ -256,19 +258,26 @@ def test_workload_full_size_sampled(cfg, w):
     so_t, do_t = torch.from_numpy(so).cuda(), torch.from_numpy(do).cuda()
     assert torch.equal(sv[so_t], dv[do_t])
     # The destination image is the whole buffer in these workloads, so the
-    # destination must hold a permutation of the source's 4-byte words (whole
-    # words move together for every width): order-free sums must agree.
+    # destination must hold a permutation of the source's words: order-free
+    # sums over w-byte words (16-byte words as two 8-byte halves) must agree.
     assert src_d.numel() == dst_d.numel()
-    for part in range(0, src_d.numel() // 4, 1 << 26):
-        s = src_d.view(torch.int32)[part:part + (1 << 26)].to(torch.int64)
-        d = dst_d.view(torch.int32)[part:part + (1 << 26)].to(torch.int64)
-        if c["cfg"] in (2,):  # units are contiguous on both sides: per-slab permutation
-            assert int(s.sum()) == int(d.sum()) and int((s * s).sum()) == int((d * d).sum())
-    s = src_d.view(torch.int32).to(torch.int64)
-    d = dst_d.view(torch.int32).to(torch.int64)
-    assert int(s.sum()) == int(d.sum())
-    assert int((s * s).sum()) == int((d * d).sum())
-    del src_d, dst_d, s, d
+    as_words = {1: torch.uint8, 2: torch.int16, 4: torch.int32, 8: torch.int64, 16: torch.int64}
+    sw = src_d.view(as_words[wbytes]).view(-1, max(1, wbytes // 8))
+    dw = dst_d.view(as_words[wbytes]).view(-1, max(1, wbytes // 8))
+    chunk = 1 << 25
+    s_sum = d_sum = s_sq = d_sq = 0
+    for lo in range(0, sw.shape[0], chunk):
+        # weight the halves of a 16-byte word differently so that swapping
+        # halves between words would show
+        s = sw[lo:lo + chunk].to(torch.int64)
+        d = dw[lo:lo + chunk].to(torch.int64)
+        if s.shape[1] == 2:
+            s = s[:, 0] * 3 + s[:, 1]
+            d = d[:, 0] * 3 + d[:, 1]
+        s_sum += int(s.sum()); d_sum += int(d.sum())
+        s_sq += int((s * s).sum()); d_sq += int((d * d).sum())
+    assert (s_sum - d_sum) % (1 << 64) == 0 and (s_sq - d_sq) % (1 << 64) == 0
+    del src_d, dst_d, sw, dw
 
 
 # ---------------------------------------------------------------------------

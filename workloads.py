@@ -48,13 +48,13 @@ def config(cfg: int, elem_bytes: int | None = None, scale: str = "full") -> dict
                     elem_bytes=4, n_tiles=(1 << 12) + 3 if small else 1 << 20,
                     kind="uniform_f32", seed=2)
     if cfg == 3:
-        r, c = (1000, 1100) if small else (16384, 16384)
+        r, c = (1000, 1104) if small else (16384, 16384)
         return dict(name="transpose2d_bf16", cfg=3,
                     src=_layout((r, c), (c, 1)), dst=_layout((r, c), (1, r)),
                     elem_bytes=2, n_tiles=1, kind="normal_bf16", seed=3)
     if cfg == 4:
         w = 4 if elem_bytes is None else int(elem_bytes)
-        r, c = (520, 700) if small else (8192, 8192)
+        r, c = (528, 704) if small else (8192, 8192)
         return dict(name="transpose2d_w%d" % w, cfg=4,
                     src=_layout((r, c), (c, 1)), dst=_layout((r, c), (1, r)),
                     elem_bytes=w, n_tiles=1, kind="bytes", seed=40 + w)
