@@ -90,11 +90,13 @@ typedef enum {
      * contiguous on both sides (identity copies, row gathers, axis permutes
      * that keep the last axis). */
     LC_KERNEL_VEC_COPY = 1,
-    /* Warp register-staged permute: units of 32*P elements are bulk-copied
-     * global -> shared, each warp permutes one unit in shared memory through
-     * registers with the per-lane XOR swizzle j = r ^ ((lane >> shift) & mask)
-     * chosen by the bank simulator, and the units are bulk-copied back
-     * ("permute_layout", section "Algorithm").  Small transposed units. */
+    /* Warp register-staged permute: units of 32*P elements, dense on both
+     * sides, are staged in a per-warp shared-memory slot with 16-byte
+     * coalesced loads ("copy -> gmem_smem" [outer, threads, vec] split), each
+     * unit is permuted in place through registers with the per-lane XOR
+     * swizzle j = r ^ ((lane >> shift) & mask) chosen by the bank simulator
+     * ("permute_layout", section "Algorithm"), and the slot leaves with
+     * 16-byte stores.  Small transposed units. */
     LC_KERNEL_WARP_PERMUTE = 2,
     /* Tile transpose: TMA tensor loads of 128-byte x R-row tiles into a
      * shared-memory ring (mbarrier pipelined), 16-byte shared reads, an

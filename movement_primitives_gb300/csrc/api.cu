@@ -108,9 +108,8 @@ extern "C" int lc_layout_copy(const void *src, const lc_tile_layout *src_layout,
 
 extern "C" int lc_last_device_error(lc_stream_t stream, uint64_t *detail) {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return LC_ERR_CUDA;
-    unsigned long long words[3] = {0, 0, 0};
-    if (lc::take_module_error(&words[0]) != cudaSuccess || lc::take_error_warp(&words[1]) != cudaSuccess ||
-        lc::take_error_tile(&words[2]) != cudaSuccess)
+    unsigned long long words[2] = {0, 0};
+    if (lc::take_module_error(&words[0]) != cudaSuccess || lc::take_error_tile(&words[1]) != cudaSuccess)
         return LC_ERR_CUDA;
     unsigned long long v = 0;
     for (unsigned long long w : words)

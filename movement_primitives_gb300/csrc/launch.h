@@ -23,7 +23,6 @@ int launch_vec(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t str
 int launch_warp(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream);
 int launch_tile(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream);
 
-cudaError_t take_error_warp(unsigned long long *v);
 cudaError_t take_error_tile(unsigned long long *v);
 
 }  // namespace lc

@@ -271,7 +271,7 @@ void plan_vec(Plan *p, const PtrInfo &ptr) {
     p->vec.vec = choose_vec(*p, ptr);
 }
 
-constexpr int64_t kStageTarget = 16 * 1024;  // bytes of units staged at once
+constexpr int64_t kStageTarget = 4 * 1024;  // bytes of units one warp stages at once
 
 // Warp permute: the smallest innermost (logical-order) mode suffix that is a
 // dense block on both sides and a whole number of warp lanes (32 * P words,

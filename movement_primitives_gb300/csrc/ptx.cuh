@@ -1,8 +1,7 @@
-// Thin inline-PTX wrappers for sm_90+ asynchronous copies on sm_103a:
-// shared-memory mbarriers, bulk (non-tensor) copies, TMA tensor loads, proxy
-// fences and the global nanosecond timer used to bound every wait.
-// Instruction forms follow the public PTX ISA (sections on mbarrier,
-// cp.async.bulk, cp.async.bulk.tensor and fence.proxy).
+// Thin inline-PTX wrappers for the sm_90+ asynchronous-copy machinery used on
+// sm_103a: shared-memory mbarriers, TMA tensor loads, tensor-map prefetch and
+// the global nanosecond timer that bounds every wait.  Instruction forms
+// follow the public PTX ISA (sections on mbarrier and cp.async.bulk.tensor).
 #pragma once
 
 #include <cstdint>
@@ -61,119 +60,9 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     return false;
 }
 
-// Bulk global -> shared copy completing on an mbarrier (bytes % 16 == 0,
-// both addresses 16-byte aligned).
-__device__ __forceinline__ void bulk_g2s(uint32_t dst_smem, const void *src, uint32_t bytes,
-                                         uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            dst_smem),
-        "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
-
-// Bulk shared -> global copy tracked by bulk async-groups.
-__device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src_smem, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src_smem),
-                 "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-
-// All but the newest N bulk groups have finished READING shared memory.
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
-// Every committed bulk group has completed.
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-// Orders this thread's generic-proxy shared-memory writes before later
-// async-proxy (bulk copy) reads of the same memory.
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 __device__ __forceinline__ void prefetch_tensormap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
-
-// Shared-memory loads and stores at 32-bit shared-window addresses, so that
-// the accesses are never emitted as generic ones.
-__device__ __forceinline__ uint4 lds128(uint32_t a) {
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(a)
-                 : "memory");
-    return v;
-}
-__device__ __forceinline__ void sts128(uint32_t a, const uint4 &v) {
-    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                 : "memory");
-}
-__device__ __forceinline__ uint2 lds64(uint32_t a) {
-    uint2 v;
-    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a) : "memory");
-    return v;
-}
-__device__ __forceinline__ void sts64(uint32_t a, const uint2 &v) {
-    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(a), "r"(v.x), "r"(v.y) : "memory");
-}
-__device__ __forceinline__ uint32_t lds32(uint32_t a) {
-    uint32_t v;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
-    return v;
-}
-__device__ __forceinline__ void sts32(uint32_t a, uint32_t v) {
-    asm volatile("st.shared.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
-}
-__device__ __forceinline__ uint16_t lds16(uint32_t a) {
-    uint16_t v;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a) : "memory");
-    return v;
-}
-__device__ __forceinline__ void sts16(uint32_t a, uint16_t v) {
-    asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "h"(v) : "memory");
-}
-__device__ __forceinline__ uint8_t lds8(uint32_t a) {
-    uint16_t v;
-    asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(a) : "memory");
-    return static_cast<uint8_t>(v);
-}
-__device__ __forceinline__ void sts8(uint32_t a, uint8_t v) {
-    asm volatile("st.shared.u8 [%0], %1;" ::"r"(a), "h"(static_cast<uint16_t>(v)) : "memory");
-}
-
-// One W-byte word (W in {1, 2, 4, 8, 16}) through shared memory.
-template <int W> struct Smem;
-template <> struct Smem<1> {
-    using T = uint8_t;
-    static __device__ __forceinline__ T ld(uint32_t a) { return lds8(a); }
-    static __device__ __forceinline__ void st(uint32_t a, T v) { sts8(a, v); }
-};
-template <> struct Smem<2> {
-    using T = uint16_t;
-    static __device__ __forceinline__ T ld(uint32_t a) { return lds16(a); }
-    static __device__ __forceinline__ void st(uint32_t a, T v) { sts16(a, v); }
-};
-template <> struct Smem<4> {
-    using T = uint32_t;
-    static __device__ __forceinline__ T ld(uint32_t a) { return lds32(a); }
-    static __device__ __forceinline__ void st(uint32_t a, T v) { sts32(a, v); }
-};
-template <> struct Smem<8> {
-    using T = uint2;
-    static __device__ __forceinline__ T ld(uint32_t a) { return lds64(a); }
-    static __device__ __forceinline__ void st(uint32_t a, T v) { sts64(a, v); }
-};
-template <> struct Smem<16> {
-    using T = uint4;
-    static __device__ __forceinline__ T ld(uint32_t a) { return lds128(a); }
-    static __device__ __forceinline__ void st(uint32_t a, T v) { sts128(a, v); }
-};
 
 // TMA tiled tensor loads (box given by the tensor map) completing on an mbarrier.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int32_t c0, int32_t c1,
