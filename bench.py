@@ -49,6 +49,8 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--copy-ceiling", action="store_true",
+                   help="also time a plain device copy of the same byte count (same L2 policy)")
     p.add_argument("--graph", action="store_true",
                    help="replay the K timed launches from one CUDA graph (launch-bound copies)")
     p.add_argument("--n-tiles", type=int, default=None,
@@ -456,6 +458,29 @@ def run_ours(args):
                "h2d_bytes_per_step": src.numel() * src.element_size(),
                "d2h_bytes_per_step": dst.numel() * dst.element_size()}
 
+    copy_ceiling = None
+    if args.copy_ceiling:
+        # a contiguous device-to-device copy of the same bytes: the practical
+        # ceiling for a workload of this size (launch and ramp costs included)
+        nbytes = step_bytes // 2
+        a_buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        b_buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        for _ in range(5):
+            b_buf.copy_(a_buf)
+        cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(min(args.steps, 200))]
+        torch.cuda.synchronize()
+        for k, (e0c, e1c) in enumerate(cev):
+            if flush:
+                flush_buf.fill_(k & 0xFF)
+            e0c.record(stream)
+            b_buf.copy_(a_buf)
+            e1c.record(stream)
+        torch.cuda.synchronize()
+        cms = statistics.mean(x.elapsed_time(y) for x, y in cev)
+        copy_ceiling = round(step_bytes / (cms / 1e3) / 1e9, 2)
+        del a_buf, b_buf
+
     peak, peak_kind = measured_peak()
     achieved = step_bytes / (launch_ms / 1e3) / 1e9
     traffic = profiled_traffic(plan["kernel_name"], cfg["name"])
@@ -482,6 +507,7 @@ def run_ours(args):
                          if peak_kind == "measured" else peak_kind},
             "clocks": clocks,
             "gpu_launches": args.steps,
+            "copy_ceiling_gbs": copy_ceiling,
             "e2e": e2e,
             "cpu_baseline": cpu,
         }

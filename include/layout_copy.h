@@ -70,7 +70,8 @@ typedef enum {
     LC_ERR_ELEM_BYTES = 5,      /* elem_bytes not in {1,2,4,8,16} */
     LC_ERR_BAD_STRIDE = 6,      /* negative stride/offset, or 0 on dst */
     LC_ERR_NOT_INJECTIVE = 7,   /* two logical indices share a dst offset */
-    LC_ERR_OVERLAP = 8,         /* src and dst byte ranges overlap */
+    LC_ERR_OVERLAP = 8,         /* src and dst byte ranges overlap (other than
+                                   an exact in-place unit permute) */
     LC_ERR_ALIGN = 9,           /* pointer not aligned to elem_bytes */
     LC_ERR_NO_SWIZZLE = 10,     /* no conflict-free XOR swizzle ("fail") */
     LC_ERR_CUDA = 11,           /* CUDA runtime error at launch */
@@ -135,6 +136,12 @@ typedef struct {
 /* The copy.  Validates, plans (host only, microseconds), launches one
  * kernel on `stream`.  n_tiles >= 0; a copy of zero words returns LC_OK
  * without launching (and then src/dst may be NULL).
+ * In place: src and dst may be the same memory when every dense unit of the
+ * warp-permute class is read and written at the same bytes (same base
+ * address, equal batch and tile strides) -- the aliasing case of
+ * "permute_layout" ("safe even when source and destination alias"); each
+ * warp stages whole units before writing them back.  Any other overlap of
+ * the two byte ranges is refused with LC_ERR_OVERLAP.
  * Errors: LC_ERR_NULL, _RANK, _SHAPE, _EXTENT_MISMATCH, _ELEM_BYTES,
  * _BAD_STRIDE, _NOT_INJECTIVE, _OVERLAP, _ALIGN, _OVERFLOW (before any
  * launch); LC_ERR_CUDA (launch failed).  Device-side wait timeouts are

@@ -15,29 +15,48 @@
 
 namespace lc {
 
-// Ring depth per word width (1- and 2-byte words use 32 KiB tiles, wider
-// words 16 KiB); compile-time knobs so that variants can be measured.  On
-// GB300, 1-byte words run best at two CTAs per SM (3 stages) and 2-byte
-// words at one CTA with 4 stages.
-#ifndef LC_TILE_STAGES_W1
-#define LC_TILE_STAGES_W1 3
+// Per-width tile geometry, measured on GB300 (A/B on one box, L2 flushed
+// between launches): rows per TMA box, ring depth, and the visiting order.
+// Every value is a compile-time knob so that variants can be measured.
+#ifndef LC_TILE_ROWS_W1
+#define LC_TILE_ROWS_W1 256
 #endif
-#ifndef LC_TILE_STAGES_W2
-#define LC_TILE_STAGES_W2 4
+#ifndef LC_TILE_ROWS_W2
+#define LC_TILE_ROWS_W2 256
+#endif
+#ifndef LC_TILE_ROWS_W4
+#define LC_TILE_ROWS_W4 256
+#endif
+#ifndef LC_TILE_ROWS_W8
+#define LC_TILE_ROWS_W8 128
+#endif
+#ifndef LC_TILE_ROWS_W16
+#define LC_TILE_ROWS_W16 128
+#endif
+#ifndef LC_TILE_STAGES_W1
+#define LC_TILE_STAGES_W1 2
 #endif
 #ifndef LC_TILE_STAGES_WIDE
 #define LC_TILE_STAGES_WIDE 4
 #endif
+// 1: tiles visited Y-block (source column block) fastest, so CTAs running at
+// the same time read neighbouring 128-byte segments of the same source rows;
+// 0: X-block fastest.
+#ifndef LC_TILE_Y_FASTEST
+#define LC_TILE_Y_FASTEST 1
+#endif
 
 template <int W> struct TileCfg {
-    static constexpr int V = 16 / W;              // words per 16-byte chunk
-    static constexpr int TY = 128 / W;            // words per 128-byte tile row
-    static constexpr int R = W <= 2 ? 256 : 128;  // source rows per tile (planner agrees)
-    static constexpr int NT = W == 1 ? 128 : 256; // threads
-    static constexpr int S = W == 1 ? LC_TILE_STAGES_W1 : W == 2 ? LC_TILE_STAGES_W2 : LC_TILE_STAGES_WIDE;
+    static constexpr int V = 16 / W;    // words per 16-byte chunk
+    static constexpr int TY = 128 / W;  // words per 128-byte tile row
+    static constexpr int R = W == 1 ? LC_TILE_ROWS_W1 : W == 2 ? LC_TILE_ROWS_W2 : W == 4 ? LC_TILE_ROWS_W4
+                           : W == 8 ? LC_TILE_ROWS_W8 : LC_TILE_ROWS_W16;  // source rows per tile
+    static constexpr int NT = W == 1 ? 128 : 256;                          // threads
+    static constexpr int S = W == 1 ? LC_TILE_STAGES_W1 : LC_TILE_STAGES_WIDE;  // ring stages
     static constexpr int TILE_BYTES = 128 * R;
-    static constexpr int MB = 8 * R / V;          // V-row x 16-byte micro-blocks
+    static constexpr int MB = 8 * R / V;  // V-row x 16-byte micro-blocks
     static constexpr int SMEM = 128 + S * TILE_BYTES;
+    static_assert(R <= 256 && R % V == 0, "TMA boxes hold at most 256 rows, whole micro-blocks");
 };
 
 struct TileArgs {
@@ -106,13 +125,27 @@ __device__ __forceinline__ void store_partial(uint8_t *p, const uint32_t (&v)[4]
     }
 }
 
+// Tile index -> (tx, ty, flat batch index).
+__device__ __forceinline__ void tile_coords(const TileArgs &a, int64_t t, int64_t &tx, int64_t &ty, int64_t &b) {
+#if LC_TILE_Y_FASTEST
+    ty = t % a.tiles_y;
+    const int64_t rest = t / a.tiles_y;
+    tx = rest % a.tiles_x;
+    b = rest / a.tiles_x;
+#else
+    tx = t % a.tiles_x;
+    const int64_t rest = t / a.tiles_x;
+    ty = rest % a.tiles_y;
+    b = rest / a.tiles_y;
+#endif
+}
+
 template <int W>
 __device__ __forceinline__ void tile_issue_load(const CUtensorMap *tmap, const TileArgs &a, int64_t t,
                                                 uint32_t dst, uint32_t bar) {
     using C = TileCfg<W>;
-    const int64_t tx = t % a.tiles_x, rest = t / a.tiles_x;
-    const int64_t ty = rest % a.tiles_y;
-    int64_t b = rest / a.tiles_y;
+    int64_t tx, ty, b;
+    tile_coords(a, t, tx, ty, b);
     int32_t b0 = 0, b1 = 0, b2 = 0;  // batch coordinates, outermost first
     if (a.nb == 3) { b2 = static_cast<int32_t>(b % a.be[2]); b /= a.be[2]; }
     if (a.nb >= 2) { b1 = static_cast<int32_t>(b % a.be[1]); b /= a.be[1]; }
@@ -163,9 +196,8 @@ __global__ void __launch_bounds__(TileCfg<W>::NT)
         const int64_t t = blockIdx.x + i * gridDim.x;
         const bool ok = ptx::mbar_wait_bounded(bar0 + 8 * s, parity, a.timeout_ns);
         if (ok) {
-            const int64_t tx = t % a.tiles_x, rest = t / a.tiles_x;
-            const int64_t ty = rest % a.tiles_y;
-            int64_t b = rest / a.tiles_y;
+            int64_t tx, ty, b;
+            tile_coords(a, t, tx, ty, b);
             uint8_t *dbase = a.dst;
             for (int k = a.nb - 1; k >= 0; --k) {
                 dbase += (b % a.be[k]) * a.bd[k];
@@ -236,8 +268,56 @@ EncodeTiledFn encode_tiled() {
 }
 
 template <int W>
-int launch_tile_t(const CUtensorMap &tmap, const TileArgs &a, cudaStream_t stream) {
+int launch_tile_t(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream) {
     using C = TileCfg<W>;
+    const TilePlan &tp = p.tile;
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return LC_ERR_CUDA;
+    const int rank = 2 + tp.batch.n;
+    const int mult = W == 16 ? 2 : 1;  // 16-byte words travel as two 8-byte TMA elements
+    cuuint64_t dims[5], strides[4];
+    cuuint32_t box[5], estr[5];
+    dims[0] = static_cast<cuuint64_t>(tp.Y.e * mult);
+    dims[1] = static_cast<cuuint64_t>(tp.X.e);
+    strides[0] = static_cast<cuuint64_t>(tp.X.s * W);
+    for (int i = 0; i < tp.batch.n; ++i) {  // innermost batch mode first
+        const Mode &b = tp.batch.m[tp.batch.n - 1 - i];
+        dims[2 + i] = static_cast<cuuint64_t>(b.e);
+        strides[1 + i] = static_cast<cuuint64_t>(b.s * W);
+    }
+    box[0] = static_cast<cuuint32_t>(128 / (W / mult));
+    box[1] = static_cast<cuuint32_t>(C::R);
+    for (int i = 2; i < 5; ++i) box[i] = 1;
+    for (int i = 0; i < 5; ++i) estr[i] = 1;
+    CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    if (W == 2) dt = CU_TENSOR_MAP_DATA_TYPE_UINT16;
+    else if (W == 4) dt = CU_TENSOR_MAP_DATA_TYPE_UINT32;
+    else if (W >= 8) dt = CU_TENSOR_MAP_DATA_TYPE_UINT64;
+    CUtensorMap tmap;
+    std::memset(&tmap, 0, sizeof(tmap));
+    void *base = const_cast<uint8_t *>(src + p.src_off * W);
+    if (enc(&tmap, dt, static_cast<cuuint32_t>(rank), base, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return LC_ERR_UNSUPPORTED;  // the driver refused this tensor shape
+
+    TileArgs a{};
+    a.dst = dst + p.dst_off * W;
+    a.eX = tp.X.e;
+    a.eY = tp.Y.e;
+    a.dY = tp.Y.d * W;
+    a.nb = tp.batch.n;
+    int64_t nbatch = 1;
+    for (int i = 0; i < tp.batch.n; ++i) {
+        a.be[i] = tp.batch.m[i].e;
+        a.bd[i] = tp.batch.m[i].d * W;
+        nbatch *= tp.batch.m[i].e;
+    }
+    a.tiles_x = (tp.X.e + C::R - 1) / C::R;
+    a.tiles_y = (tp.Y.e + C::TY - 1) / C::TY;
+    a.n_tiles = a.tiles_x * a.tiles_y * nbatch;
+    a.timeout_ns = wait_limit_ns();
+
     const void *fn = reinterpret_cast<const void *>(&k_tile_transpose<W>);
     int sms, per;
     if (prepare(fn, C::NT, C::SMEM, C::SMEM, &sms, &per) != cudaSuccess) return LC_ERR_CUDA;
@@ -249,60 +329,12 @@ int launch_tile_t(const CUtensorMap &tmap, const TileArgs &a, cudaStream_t strea
 }  // namespace
 
 int launch_tile(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream) {
-    const TilePlan &tp = p.tile;
-    const int w = p.w;
-    EncodeTiledFn enc = encode_tiled();
-    if (!enc) return LC_ERR_CUDA;
-    const int rank = 2 + tp.batch.n;
-    const int mult = w == 16 ? 2 : 1;  // 16-byte words travel as two 8-byte TMA elements
-    cuuint64_t dims[5], strides[4];
-    cuuint32_t box[5], estr[5];
-    dims[0] = static_cast<cuuint64_t>(tp.Y.e * mult);
-    dims[1] = static_cast<cuuint64_t>(tp.X.e);
-    strides[0] = static_cast<cuuint64_t>(tp.X.s * w);
-    for (int i = 0; i < tp.batch.n; ++i) {  // innermost batch mode first
-        const Mode &b = tp.batch.m[tp.batch.n - 1 - i];
-        dims[2 + i] = static_cast<cuuint64_t>(b.e);
-        strides[1 + i] = static_cast<cuuint64_t>(b.s * w);
-    }
-    box[0] = static_cast<cuuint32_t>(128 / (w / mult));
-    box[1] = static_cast<cuuint32_t>(tp.R);
-    for (int i = 2; i < 5; ++i) box[i] = 1;
-    for (int i = 0; i < 5; ++i) estr[i] = 1;
-    CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_UINT8;
-    if (w == 2) dt = CU_TENSOR_MAP_DATA_TYPE_UINT16;
-    else if (w == 4) dt = CU_TENSOR_MAP_DATA_TYPE_UINT32;
-    else if (w >= 8) dt = CU_TENSOR_MAP_DATA_TYPE_UINT64;
-    CUtensorMap tmap;
-    std::memset(&tmap, 0, sizeof(tmap));
-    void *base = const_cast<uint8_t *>(src + p.src_off * w);
-    if (enc(&tmap, dt, static_cast<cuuint32_t>(rank), base, dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return LC_ERR_UNSUPPORTED;  // the driver refused this tensor shape
-
-    TileArgs a{};
-    a.dst = dst + p.dst_off * w;
-    a.eX = tp.X.e;
-    a.eY = tp.Y.e;
-    a.dY = tp.Y.d * w;
-    a.nb = tp.batch.n;
-    int64_t nbatch = 1;
-    for (int i = 0; i < tp.batch.n; ++i) {
-        a.be[i] = tp.batch.m[i].e;
-        a.bd[i] = tp.batch.m[i].d * w;
-        nbatch *= tp.batch.m[i].e;
-    }
-    a.tiles_x = (tp.X.e + tp.R - 1) / tp.R;
-    a.tiles_y = (tp.Y.e + tp.TY - 1) / tp.TY;
-    a.n_tiles = a.tiles_x * a.tiles_y * nbatch;
-    a.timeout_ns = wait_limit_ns();
-    switch (w) {
-        case 1: return launch_tile_t<1>(tmap, a, stream);
-        case 2: return launch_tile_t<2>(tmap, a, stream);
-        case 4: return launch_tile_t<4>(tmap, a, stream);
-        case 8: return launch_tile_t<8>(tmap, a, stream);
-        case 16: return launch_tile_t<16>(tmap, a, stream);
+    switch (p.w) {
+        case 1: return launch_tile_t<1>(p, src, dst, stream);
+        case 2: return launch_tile_t<2>(p, src, dst, stream);
+        case 4: return launch_tile_t<4>(p, src, dst, stream);
+        case 8: return launch_tile_t<8>(p, src, dst, stream);
+        case 16: return launch_tile_t<16>(p, src, dst, stream);
     }
     return LC_ERR_UNSUPPORTED;
 }

@@ -339,8 +339,9 @@ bool plan_tile(Plan *p, const PtrInfo &ptr) {
     if (!a16(p->src_off * w) || !a16(p->dst_off * w)) return false;
     if (ptr.check && (ptr.src % 16 || ptr.dst % 16)) return false;
     tp.TY = 128 / w;
-    tp.R = w <= 2 ? 256 : 128;  // must match TileCfg in kernels.cu
-    tp.S = 4;  // ring depth reported for information (kernels.cu's TileCfg decides)
+    // reported for information; the kernel's per-width table decides
+    tp.R = w <= 4 ? 256 : 128;
+    tp.S = w == 1 ? 2 : 4;
     tp.threads = w == 1 ? 128 : 256;
     return true;
 }
@@ -495,6 +496,35 @@ std::string cache_key(const lc_tile_layout *src, const lc_tile_layout *dst, int3
     return k;
 }
 
+int cached_plan(const lc_tile_layout *src, const lc_tile_layout *dst, int32_t w, int64_t n_tiles,
+                int32_t kernel, const PtrInfo &mod, Plan *out) {
+    const std::string key = cache_key(src, dst, w, n_tiles, kernel, mod);
+    {
+        std::lock_guard<std::mutex> lk(g_cache_mu);
+        auto it = g_cache.find(key);
+        if (it != g_cache.end()) { *out = it->second; return LC_OK; }
+    }
+    const int st = make_plan_core(src, dst, w, n_tiles, kernel, mod, out);
+    if (st) return st;
+    std::lock_guard<std::mutex> lk(g_cache_mu);
+    if (g_cache.size() >= kCacheMax) g_cache.clear();
+    g_cache.emplace(key, *out);
+    return LC_OK;
+}
+
+// An exact in-place permute of dense units: every unit's source bytes are its
+// destination bytes (same base address, equal batch strides).  The warp
+// permute reads a whole group of units into its warp's shared slot before
+// writing any of it back and groups are disjoint, so aliasing is safe
+// ("permute_layout": a barrier between the phases makes aliasing safe).
+bool exact_unit_alias(const Plan &p, const PtrInfo &ptr) {
+    if (p.kernel != LC_KERNEL_WARP_PERMUTE) return false;
+    if (ptr.src + uintptr_t(p.src_off * p.w) != ptr.dst + uintptr_t(p.dst_off * p.w)) return false;
+    for (int i = 0; i < p.warp.batch.n; ++i)
+        if (p.warp.batch.m[i].s != p.warp.batch.m[i].d) return false;
+    return true;
+}
+
 }  // namespace
 
 int make_plan(const lc_tile_layout *src, const lc_tile_layout *dst, int32_t w,
@@ -506,27 +536,22 @@ int make_plan(const lc_tile_layout *src, const lc_tile_layout *dst, int32_t w,
     mod.src = ptr.check ? (ptr.src & 15) : 0;
     mod.dst = ptr.check ? (ptr.dst & 15) : 0;
     mod.check = true;
-    const std::string key = cache_key(src, dst, w, n_tiles, kernel, mod);
-    bool hit = false;
-    {
-        std::lock_guard<std::mutex> lk(g_cache_mu);
-        auto it = g_cache.find(key);
-        if (it != g_cache.end()) { *out = it->second; hit = true; }
-    }
-    if (!hit) {
-        const int st = make_plan_core(src, dst, w, n_tiles, kernel, mod, out);
-        if (st) return st;
-        std::lock_guard<std::mutex> lk(g_cache_mu);
-        if (g_cache.size() >= kCacheMax) g_cache.clear();
-        g_cache.emplace(key, *out);
-    }
+    int st = cached_plan(src, dst, w, n_tiles, kernel, mod, out);
+    if (st) return st;
     if (!ptr.check || out->total == 0) return LC_OK;
     if (!ptr.src || !ptr.dst) return LC_ERR_NULL;
     if (ptr.src % uintptr_t(w) || ptr.dst % uintptr_t(w)) return LC_ERR_ALIGN;
     const uintptr_t s0 = ptr.src + uintptr_t(out->src_lo), s1 = ptr.src + uintptr_t(out->src_hi);
     const uintptr_t d0 = ptr.dst + uintptr_t(out->dst_lo), d1 = ptr.dst + uintptr_t(out->dst_hi);
-    if (s0 < d1 && d0 < s1) return LC_ERR_OVERLAP;
-    return LC_OK;
+    if (!(s0 < d1 && d0 < s1)) return LC_OK;
+    // overlapping ranges: only the exact in-place unit permute is allowed
+    if (kernel != LC_KERNEL_AUTO && kernel != LC_KERNEL_WARP_PERMUTE) return LC_ERR_OVERLAP;
+    if (out->kernel != LC_KERNEL_WARP_PERMUTE) {
+        Plan q;
+        if (cached_plan(src, dst, w, n_tiles, LC_KERNEL_WARP_PERMUTE, mod, &q) != LC_OK) return LC_ERR_OVERLAP;
+        *out = q;
+    }
+    return exact_unit_alias(*out, ptr) ? LC_OK : LC_ERR_OVERLAP;
 }
 
 void fill_info(const Plan &p, lc_plan_info *info) {

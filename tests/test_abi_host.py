@@ -248,3 +248,24 @@ def test_fastdiv_host_mirror():
             n &= 0xFFFFFFFF
             q = (((n * m) >> 32) + n) >> s
             assert q == n // d, (n, d)
+
+
+def test_overlaps_other_than_exact_unit_alias_are_refused(M):
+    """Only an exact in-place permute of dense units may alias; every other
+    overlap is refused before anything is launched."""
+    T = M.TileLayout
+    p = 1 << 20
+    cases = [
+        # a 64 x 64 transpose in place: units would exceed 32 words per lane
+        (p, T((64, 64), (64, 1)), p, T((64, 64), (1, 64)), 4, 1),
+        # unit permute with the destination shifted by one unit: ranges overlap
+        (p, T((4, 32), (32, 1)), p + 512, T((4, 32), (1, 4)), 4, 8),
+        # equal bases but different tile strides
+        (p, T((4, 32), (32, 1), 0, 128), p, T((4, 32), (1, 4), 0, 256), 4, 8),
+        # identical layouts through the vector copy
+        (p, T((4096,), (1,)), p, T((4096,), (1,)), 4, 1),
+    ]
+    for sp, sl, dp, dl, w, n in cases:
+        with pytest.raises(M.LayoutCopyError) as e:
+            M.layout_copy_ptr(sp, sl, dp, dl, w, n, stream=0)
+        assert e.value.status == M.STATUS["LC_ERR_OVERLAP"], (sl, dl)

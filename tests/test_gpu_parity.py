@@ -308,3 +308,31 @@ def test_pointer_errors():
     assert e.value.status == M.STATUS["LC_ERR_NULL"]
     with pytest.raises(ValueError):
         M.layout_copy(buf[:100], l4, buf[1000:], l4, elem_bytes=4)  # tensor too small
+
+
+# ---------------------------------------------------------------------------
+# in place: P4's aliasing case (the destination image is the source image)
+# ---------------------------------------------------------------------------
+
+def run_in_place(lay_src, lay_dst, w, n_tiles, seed=0):
+    n = _footprint(lay_src, n_tiles) * w
+    g = torch.Generator().manual_seed(seed)
+    buf_h = torch.randint(0, 256, (n,), generator=g, dtype=torch.uint8)
+    want = buf_h.numpy().copy()                    # untouched bytes keep their values
+    oracle.copy(buf_h.numpy().copy(), lay_src, want, lay_dst, w, n_tiles)  # reads see the snapshot
+    buf = buf_h.cuda()
+    lc().layout_copy_ptr(buf.data_ptr(), lay_src, buf.data_ptr(), lay_dst, w, n_tiles,
+                         stream=torch.cuda.current_stream().cuda_stream)
+    st, detail = lc().last_device_error()
+    assert st == 0, "device error word %#x" % detail
+    assert np.array_equal(buf.cpu().numpy(), want)
+
+
+def test_in_place_unit_permutes():
+    sh = (2, 1, 4, 32)
+    run_in_place(L(sh, (128, 128, 32, 1)), L(sh, (128, 128, 1, 4)), 4, n_tiles=(1 << 12) + 3, seed=1)
+    # gapped tiles (same tile stride on both sides), every width
+    for w in (1, 2, 4, 8, 16):
+        run_in_place(L((4, 32), (32, 1), 32, 192), L((4, 32), (1, 4), 32, 192), w, n_tiles=57, seed=w)
+    # one 32 x 32 tile transposed in place
+    run_in_place(L((32, 32), (32, 1)), L((32, 32), (1, 32)), 4, n_tiles=1, seed=7)
