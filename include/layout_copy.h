@@ -77,7 +77,8 @@ typedef enum {
     LC_ERR_CUDA = 11,           /* CUDA runtime error at launch */
     LC_ERR_TIMEOUT = 12,        /* a bounded device wait gave up */
     LC_ERR_UNSUPPORTED = 13,    /* a forced kernel class cannot take this copy */
-    LC_ERR_OVERFLOW = 14        /* an offset does not fit in 63 bits */
+    LC_ERR_OVERFLOW = 14,       /* an offset does not fit in 63 bits */
+    LC_ERR_STAGING = 15         /* a staging buffer is too small */
 } lc_status;
 
 /* Kernel classes (the planner picks one; lc_layout_copy_ex can force one). */
@@ -157,6 +158,33 @@ int lc_layout_copy_ex(const void *src, const lc_tile_layout *src_layout,
                       void *dst, const lc_tile_layout *dst_layout,
                       int32_t elem_bytes, int64_t n_tiles, int32_t kernel,
                       lc_stream_t stream);
+
+/* The copy between two HOST buffers.  The tiles are split into chunks that
+ * are moved host -> device, permuted and moved device -> host through
+ * `staging`, a caller-owned device buffer of at least staging_bytes bytes
+ * (lc_host_staging_bytes gives the size for full pipelining, two chunk
+ * slots).  Uploads, permutes and downloads run on two internal copy streams
+ * and on `stream`, overlapped chunk by chunk and ordered by events; the work
+ * is queued behind what `stream` already holds, and `stream` resumes after the
+ * last download, so synchronising `stream` completes the copy.  Host buffers
+ * should be page-locked for the transfers to overlap.  Bytes of dst_host
+ * outside the destination image keep their values (when the image has holes
+ * the chunk's span is uploaded first).  Layout semantics as lc_layout_copy;
+ * host ranges may not overlap (LC_ERR_OVERLAP).  Errors: as lc_layout_copy,
+ * plus LC_ERR_STAGING when staging_bytes cannot hold one chunk, LC_ERR_ALIGN
+ * when staging is not 256-byte aligned.  The library creates its two copy streams and their
+ * events once per device and allocates no memory. */
+int lc_layout_copy_host(const void *src_host, const lc_tile_layout *src_layout,
+                        void *dst_host, const lc_tile_layout *dst_layout,
+                        int32_t elem_bytes, int64_t n_tiles, void *staging,
+                        int64_t staging_bytes, lc_stream_t stream);
+
+/* Staging bytes lc_layout_copy_host needs for this copy (two slots of about
+ * an eighth of the tiles each when the tiles can be chunked, else the whole
+ * source and destination spans); 0 for invalid arguments. */
+int64_t lc_host_staging_bytes(const lc_tile_layout *src_layout,
+                              const lc_tile_layout *dst_layout,
+                              int32_t elem_bytes, int64_t n_tiles);
 
 /* The planner alone: validation and the plan lc_layout_copy_ex would launch
  * for (layouts, elem_bytes, n_tiles, kernel), without touching the GPU.

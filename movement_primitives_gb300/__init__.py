@@ -16,7 +16,8 @@ from typing import Sequence
 from . import _lib
 from ._lib import KERNELS, STATUS, STATUS_NAMES
 
-__all__ = ["TileLayout", "LayoutCopyError", "layout_copy", "layout_copy_ptr", "plan",
+__all__ = ["TileLayout", "LayoutCopyError", "layout_copy", "layout_copy_ptr", "layout_copy_host",
+           "host_staging_bytes", "plan",
            "choose_swizzle", "swizzle_conflicts", "gmem_smem_partition",
            "last_device_error", "debug_wait_timeout", "KERNELS", "STATUS"]
 
@@ -129,6 +130,46 @@ def layout_copy(src, src_layout, dst, dst_layout, n_tiles: int = 1, elem_bytes: 
         if need > have:
             raise ValueError("%s layout reaches %d bytes; the tensor holds %d" % (name, need, have))
     layout_copy_ptr(src.data_ptr(), sl, dst.data_ptr(), dl, w, n_tiles, kernel, _stream_handle(stream))
+
+
+def host_staging_bytes(src_layout, dst_layout, elem_bytes: int, n_tiles: int = 1) -> int:
+    """Device staging bytes layout_copy_host needs for full pipelining."""
+    sl, dl = TileLayout.of(src_layout).to_c(), TileLayout.of(dst_layout).to_c()
+    return int(_lib.lib().lc_host_staging_bytes(ctypes.byref(sl), ctypes.byref(dl), int(elem_bytes),
+                                                int(n_tiles)))
+
+
+def layout_copy_host(src, src_layout, dst, dst_layout, n_tiles: int = 1, elem_bytes: int | None = None,
+                     staging=None, stream=None) -> None:
+    """Copy between two HOST tensors (ideally pinned) through the GPU.
+
+    Transfers and permutes are pipelined over chunks of tiles by the library
+    (lc_layout_copy_host).  ``staging`` is a CUDA uint8 tensor of at least
+    host_staging_bytes(...) bytes; when omitted one is allocated by torch for
+    this call.  Returns once queued on ``stream``; synchronise it to finish.
+    """
+    import torch
+    if src.is_cuda or dst.is_cuda:
+        raise ValueError("layout_copy_host takes host tensors")
+    if not (src.is_contiguous() and dst.is_contiguous()):
+        raise ValueError("pass contiguous tensors; express strides through the layouts")
+    w = int(elem_bytes) if elem_bytes is not None else src.element_size()
+    sl, dl = TileLayout.of(src_layout), TileLayout.of(dst_layout)
+    for name, t, l in (("source", src, sl), ("destination", dst, dl)):
+        need = l.footprint(n_tiles) * w
+        if need > t.numel() * t.element_size():
+            raise ValueError("%s layout reaches %d bytes; the tensor holds %d"
+                             % (name, need, t.numel() * t.element_size()))
+    if staging is None:
+        staging = torch.empty(max(256, host_staging_bytes(sl, dl, w, n_tiles)), dtype=torch.uint8,
+                              device="cuda")
+    cs, cd = sl.to_c(), dl.to_c()
+    st = _lib.lib().lc_layout_copy_host(ctypes.c_void_p(src.data_ptr()), ctypes.byref(cs),
+                                        ctypes.c_void_p(dst.data_ptr()), ctypes.byref(cd), w,
+                                        int(n_tiles), ctypes.c_void_p(staging.data_ptr()),
+                                        staging.numel() * staging.element_size(),
+                                        ctypes.c_void_p(_stream_handle(stream)))
+    _check(st, "layout_copy_host")
 
 
 def plan(src_layout, dst_layout, elem_bytes: int, n_tiles: int = 1, kernel="auto") -> dict:

@@ -142,6 +142,7 @@ extern "C" const char *lc_status_string(int32_t status) {
         case LC_ERR_TIMEOUT: return "a bounded device wait gave up";
         case LC_ERR_UNSUPPORTED: return "the requested kernel class cannot perform this copy";
         case LC_ERR_OVERFLOW: return "an offset does not fit in 63 bits";
+        case LC_ERR_STAGING: return "the staging buffer is too small";
     }
     return "unknown status";
 }

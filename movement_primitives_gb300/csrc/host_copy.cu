@@ -1,0 +1,222 @@
+// Host-buffer entry point: the layout copy between two host buffers, with the
+// transfers pipelined over chunks of tiles through a caller-provided device
+// staging buffer.  Chunk c moves host -> device on a copy stream, is permuted
+// on the caller's stream, and moves device -> host on a second copy stream;
+// two staging slots let chunk c+1's upload and chunk c-1's download run while
+// chunk c is permuted.  Events order the three streams; everything joins back
+// into the caller's stream before the call returns.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <map>
+#include <mutex>
+
+#include "launch.h"
+
+namespace lc {
+namespace {
+
+constexpr int kSlots = 2;
+
+struct DeviceStreams {
+    cudaStream_t up = nullptr, down = nullptr;
+    cudaEvent_t start = nullptr;
+    cudaEvent_t uploaded[kSlots], permuted[kSlots], downloaded[kSlots];
+};
+
+std::mutex g_streams_mu;
+std::map<int, DeviceStreams> g_streams;
+
+// Two non-blocking copy streams and their events, created once per device.
+cudaError_t device_streams(DeviceStreams **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(g_streams_mu);
+    auto it = g_streams.find(dev);
+    if (it == g_streams.end()) {
+        DeviceStreams ds;
+        if ((e = cudaStreamCreateWithFlags(&ds.up, cudaStreamNonBlocking)) != cudaSuccess) return e;
+        if ((e = cudaStreamCreateWithFlags(&ds.down, cudaStreamNonBlocking)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&ds.start, cudaEventDisableTiming)) != cudaSuccess) return e;
+        for (int s = 0; s < kSlots; ++s) {
+            const unsigned f = cudaEventDisableTiming;
+            if ((e = cudaEventCreateWithFlags(&ds.uploaded[s], f)) != cudaSuccess) return e;
+            if ((e = cudaEventCreateWithFlags(&ds.permuted[s], f)) != cudaSuccess) return e;
+            if ((e = cudaEventCreateWithFlags(&ds.downloaded[s], f)) != cudaSuccess) return e;
+        }
+        it = g_streams.emplace(dev, ds).first;
+    }
+    *out = &it->second;
+    return cudaSuccess;
+}
+
+// Byte span [lo, hi) of tiles [t0, t1) of one side (relative to its pointer).
+struct Span {
+    int64_t lo, hi;
+};
+
+Span tile_span(const lc_tile_layout &l, int64_t w, int64_t cos, int64_t ts, int64_t t0, int64_t t1) {
+    return Span{(l.offset + t0 * ts) * w, (l.offset + (t1 - 1) * ts + cos) * w};
+}
+
+int64_t cosize_of(const lc_tile_layout &l) {
+    int64_t c = 1;
+    for (int k = 0; k < l.rank; ++k) {
+        if (l.shape[k] == 0) return 0;
+        c += (l.shape[k] - 1) * l.stride[k];
+    }
+    return c;
+}
+
+int64_t words_of(const lc_tile_layout &l) {
+    int64_t n = 1;
+    for (int k = 0; k < l.rank; ++k) n *= l.shape[k];
+    return n;
+}
+
+int launch_plan(const Plan &p, const uint8_t *s, uint8_t *d, cudaStream_t cs) {
+    switch (p.kernel) {
+        case LC_KERNEL_VEC_COPY: return launch_vec(p, s, d, cs);
+        case LC_KERNEL_WARP_PERMUTE: return launch_warp(p, s, d, cs);
+        case LC_KERNEL_TILE_TRANSPOSE: {
+            const int r = launch_tile(p, s, d, cs);
+            return r == LC_ERR_UNSUPPORTED ? launch_vec(p, s, d, cs) : r;
+        }
+    }
+    return LC_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+}  // namespace lc
+
+extern "C" int lc_layout_copy_host(const void *src_host, const lc_tile_layout *src_layout, void *dst_host,
+                                   const lc_tile_layout *dst_layout, int32_t elem_bytes, int64_t n_tiles,
+                                   void *staging, int64_t staging_bytes, lc_stream_t stream) {
+    using namespace lc;
+    if (!src_layout || !dst_layout) return LC_ERR_NULL;
+    // validate the layouts once (plan of the whole copy, pointers aside)
+    Plan whole;
+    PtrInfo none;
+    int st = make_plan(src_layout, dst_layout, elem_bytes, n_tiles, LC_KERNEL_AUTO, none, &whole);
+    if (st) return st;
+    if (whole.total == 0) return LC_OK;
+    if (!src_host || !dst_host || !staging) return LC_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(staging) % 256) return LC_ERR_ALIGN;
+    {
+        const uintptr_t s0 = reinterpret_cast<uintptr_t>(src_host) + uintptr_t(whole.src_lo);
+        const uintptr_t s1 = reinterpret_cast<uintptr_t>(src_host) + uintptr_t(whole.src_hi);
+        const uintptr_t d0 = reinterpret_cast<uintptr_t>(dst_host) + uintptr_t(whole.dst_lo);
+        const uintptr_t d1 = reinterpret_cast<uintptr_t>(dst_host) + uintptr_t(whole.dst_hi);
+        if (s0 < d1 && d0 < s1) return LC_ERR_OVERLAP;
+    }
+
+    const int64_t w = elem_bytes;
+    const int64_t scos = cosize_of(*src_layout), dcos = cosize_of(*dst_layout);
+    const int64_t sts = src_layout->tile_stride ? src_layout->tile_stride : scos;
+    const int64_t dts = dst_layout->tile_stride ? dst_layout->tile_stride : dcos;
+    // Chunks need disjoint destination spans; otherwise the copy is one chunk.
+    const bool chunkable = n_tiles > 1 && dts >= dcos && sts >= 0;
+    // The destination image covers its span exactly when tiles are packed and
+    // each tile is dense; otherwise the span is staged in first so that bytes
+    // outside the image keep their values.
+    const bool dst_dense = words_of(*dst_layout) == dcos && (n_tiles == 1 || dts == dcos);
+
+    auto round256 = [](int64_t b) { return (b + 255) / 256 * 256; };
+    auto slot_bytes = [&](int64_t tiles) {
+        const Span s = tile_span(*src_layout, w, scos, sts, 0, tiles);
+        const Span d = tile_span(*dst_layout, w, dcos, dts, 0, tiles);
+        return round256(s.hi - s.lo) + round256(d.hi - d.lo);
+    };
+    int64_t chunk = n_tiles;
+    int slots = 1;
+    if (chunkable) {
+        // about eight chunks, two slots of staging
+        chunk = std::max<int64_t>(1, (n_tiles + 7) / 8);
+        while (chunk > 1 && kSlots * slot_bytes(chunk) > staging_bytes) chunk = (chunk + 1) / 2;
+        slots = kSlots;
+        if (kSlots * slot_bytes(chunk) > staging_bytes) {
+            chunk = n_tiles;  // not even two one-tile slots: try a single pass
+            slots = 1;
+        }
+    }
+    if (slots * slot_bytes(chunk) > staging_bytes) return LC_ERR_STAGING;
+    const int64_t slot_size = slot_bytes(chunk);
+    DeviceStreams *ds = nullptr;
+    if (device_streams(&ds) != cudaSuccess) return LC_ERR_CUDA;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *stage = static_cast<uint8_t *>(staging);
+    const uint8_t *sh = static_cast<const uint8_t *>(src_host);
+    uint8_t *dh = static_cast<uint8_t *>(dst_host);
+
+    // the copy streams start after everything already queued on the caller's stream
+    if (cudaEventRecord(ds->start, cs) != cudaSuccess) return LC_ERR_CUDA;
+    if (cudaStreamWaitEvent(ds->up, ds->start, 0) != cudaSuccess) return LC_ERR_CUDA;
+    if (cudaStreamWaitEvent(ds->down, ds->start, 0) != cudaSuccess) return LC_ERR_CUDA;
+
+    int64_t c = 0;
+    for (int64_t t0 = 0; t0 < n_tiles; t0 += chunk, ++c) {
+        const int64_t t1 = std::min(n_tiles, t0 + chunk);
+        const int b = static_cast<int>(c % slots);
+        const Span s = tile_span(*src_layout, w, scos, sts, t0, t1);
+        const Span d = tile_span(*dst_layout, w, dcos, dts, t0, t1);
+        uint8_t *s_dev = stage + b * slot_size;
+        uint8_t *d_dev = s_dev + round256(s.hi - s.lo);
+        // upload once the slot's previous permute has read it
+        if (c >= slots && cudaStreamWaitEvent(ds->up, ds->permuted[b], 0) != cudaSuccess) return LC_ERR_CUDA;
+        if (c >= slots && cudaStreamWaitEvent(ds->up, ds->downloaded[b], 0) != cudaSuccess) return LC_ERR_CUDA;
+        if (cudaMemcpyAsync(s_dev, sh + s.lo, size_t(s.hi - s.lo), cudaMemcpyHostToDevice, ds->up) != cudaSuccess)
+            return LC_ERR_CUDA;
+        if (!dst_dense &&
+            cudaMemcpyAsync(d_dev, dh + d.lo, size_t(d.hi - d.lo), cudaMemcpyHostToDevice, ds->up) != cudaSuccess)
+            return LC_ERR_CUDA;
+        if (cudaEventRecord(ds->uploaded[b], ds->up) != cudaSuccess) return LC_ERR_CUDA;
+        // permute the chunk: the same layouts; each staging copy starts exactly
+        // at the chunk's first tile, so both bases are 0
+        lc_tile_layout sl = *src_layout, dl = *dst_layout;
+        sl.offset = 0;
+        dl.offset = 0;
+        sl.tile_stride = sts;
+        dl.tile_stride = dts;
+        if (cudaStreamWaitEvent(cs, ds->uploaded[b], 0) != cudaSuccess) return LC_ERR_CUDA;
+        Plan p;
+        PtrInfo ptr;
+        ptr.src = reinterpret_cast<uintptr_t>(s_dev);
+        ptr.dst = reinterpret_cast<uintptr_t>(d_dev);
+        ptr.check = true;
+        st = make_plan(&sl, &dl, elem_bytes, t1 - t0, LC_KERNEL_AUTO, ptr, &p);
+        if (st) return st;
+        if ((st = launch_plan(p, s_dev, d_dev, cs))) return st;
+        if (cudaEventRecord(ds->permuted[b], cs) != cudaSuccess) return LC_ERR_CUDA;
+        // download once permuted
+        if (cudaStreamWaitEvent(ds->down, ds->permuted[b], 0) != cudaSuccess) return LC_ERR_CUDA;
+        if (cudaMemcpyAsync(dh + d.lo, d_dev, size_t(d.hi - d.lo), cudaMemcpyDeviceToHost, ds->down) != cudaSuccess)
+            return LC_ERR_CUDA;
+        if (cudaEventRecord(ds->downloaded[b], ds->down) != cudaSuccess) return LC_ERR_CUDA;
+    }
+    // the caller's stream resumes after the last download
+    for (int b = 0; b < slots && b < c; ++b)
+        if (cudaStreamWaitEvent(cs, ds->downloaded[b], 0) != cudaSuccess) return LC_ERR_CUDA;
+    return LC_OK;
+}
+
+extern "C" int64_t lc_host_staging_bytes(const lc_tile_layout *src_layout, const lc_tile_layout *dst_layout,
+                                         int32_t elem_bytes, int64_t n_tiles) {
+    using namespace lc;
+    if (!src_layout || !dst_layout || n_tiles <= 0) return 0;
+    const int64_t w = elem_bytes;
+    const int64_t scos = cosize_of(*src_layout), dcos = cosize_of(*dst_layout);
+    const int64_t sts = src_layout->tile_stride ? src_layout->tile_stride : scos;
+    const int64_t dts = dst_layout->tile_stride ? dst_layout->tile_stride : dcos;
+    auto round256 = [](int64_t b) { return (b + 255) / 256 * 256; };
+    if (n_tiles > 1 && dts >= dcos) {
+        const int64_t chunk = std::max<int64_t>(1, (n_tiles + 7) / 8);
+        const Span s = tile_span(*src_layout, w, scos, sts, 0, chunk);
+        const Span d = tile_span(*dst_layout, w, dcos, dts, 0, chunk);
+        return kSlots * (round256(s.hi - s.lo) + round256(d.hi - d.lo));
+    }
+    const Span s = tile_span(*src_layout, w, scos, sts, 0, n_tiles);
+    const Span d = tile_span(*dst_layout, w, dcos, dts, 0, n_tiles);
+    return round256(s.hi - s.lo) + round256(d.hi - d.lo);
+}

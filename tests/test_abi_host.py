@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(M):
 
 def test_status_and_kernel_names(M):
     lib = M._lib.lib()
-    for code in range(15):
+    for code in range(16):
         assert lib.lc_status_string(code) and lib.lc_status_string(code) != b"unknown status"
     assert lib.lc_kernel_name(2) == b"warp_permute"
 

@@ -336,3 +336,51 @@ def test_in_place_unit_permutes():
         run_in_place(L((4, 32), (32, 1), 32, 192), L((4, 32), (1, 4), 32, 192), w, n_tiles=57, seed=w)
     # one 32 x 32 tile transposed in place
     run_in_place(L((32, 32), (32, 1)), L((32, 32), (1, 32)), 4, n_tiles=1, seed=7)
+
+
+# ---------------------------------------------------------------------------
+# host buffers through the pipelined entry point
+# ---------------------------------------------------------------------------
+
+def run_host_case(src_l, dst_l, w, n_tiles, seed=0, staging_bytes=None):
+    ns = _footprint(src_l, n_tiles) * w
+    nd = _footprint(dst_l, n_tiles) * w
+    g = torch.Generator().manual_seed(seed)
+    src_h = torch.randint(0, 256, (ns,), generator=g, dtype=torch.uint8).pin_memory()
+    dst_h = torch.full((nd,), workloads.SENTINEL, dtype=torch.uint8).pin_memory()
+    want = dst_h.numpy().copy()
+    oracle.copy(src_h.numpy(), src_l, want, dst_l, w, n_tiles)
+    staging = None
+    if staging_bytes is not None:
+        staging = torch.empty(staging_bytes, dtype=torch.uint8, device="cuda")
+    lc().layout_copy_host(src_h, src_l, dst_h, dst_l, n_tiles=n_tiles, elem_bytes=w, staging=staging)
+    torch.cuda.current_stream().synchronize()
+    assert np.array_equal(dst_h.numpy(), want)
+
+
+def test_host_buffers_pipelined():
+    c = workloads.config(2, scale="small")
+    run_host_case(c["src"], c["dst"], 4, c["n_tiles"], seed=1)
+    # a small staging buffer: more, smaller chunks
+    run_host_case(c["src"], c["dst"], 4, c["n_tiles"], seed=2, staging_bytes=1 << 16)
+    # destination with holes between tiles: bytes outside the image survive
+    run_host_case(L((4, 32), (32, 1)), L((4, 32), (1, 4), 8, 200), 2, 301, seed=3)
+    # one tile (no chunking): a transpose and an axis permute
+    c = workloads.config(3, scale="small")
+    run_host_case(c["src"], c["dst"], 2, 1, seed=4)
+    c = workloads.config(5, scale="small")
+    run_host_case(c["src"], c["dst"], 2, 1, seed=5)
+
+
+def test_host_buffers_errors():
+    M = lc()
+    lay = L((16, 16), (16, 1))
+    a = torch.zeros(4096, dtype=torch.uint8).pin_memory()
+    b = torch.zeros(4096, dtype=torch.uint8).pin_memory()
+    small = torch.empty(256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(M.LayoutCopyError) as e:
+        M.layout_copy_host(a, lay, b, L((16, 16), (1, 16)), elem_bytes=4, staging=small)
+    assert e.value.status == M.STATUS["LC_ERR_STAGING"]
+    with pytest.raises(M.LayoutCopyError) as e:
+        M.layout_copy_host(a, lay, a, L((16, 16), (1, 16)), elem_bytes=4)
+    assert e.value.status == M.STATUS["LC_ERR_OVERLAP"]
