@@ -186,6 +186,33 @@ int64_t lc_host_staging_bytes(const lc_tile_layout *src_layout,
                               const lc_tile_layout *dst_layout,
                               int32_t elem_bytes, int64_t n_tiles);
 
+/* Bytes of the staging array built into the library for
+ * lc_layout_copy_host_static (on every GPU that loads the library, for the
+ * life of the process). */
+#define LC_STATIC_STAGING_BYTES (32 * 1024 * 1024)
+
+/* lc_layout_copy_host for callers that cannot allocate device memory.  (The
+ * source pages have no counterpart: this is a deployment convenience.)  Some
+ * callers cannot hand over a staging buffer: a plugin inside an application
+ * whose own allocator owns all device memory, code that must avoid cudaMalloc
+ * because it can synchronise the device, or code that will be captured into a
+ * CUDA graph, where cudaMalloc is not allowed.  This entry point stages through
+ * an LC_STATIC_STAGING_BYTES array that lives in the library and allocates and
+ * frees nothing.  Chunks of tiles are uploaded, permuted and downloaded in
+ * order on `stream` alone (no overlap between transfers); synchronise `stream`
+ * to finish.  The first call on a device, with that device current, looks up
+ * the array's device address (loading the library's code onto the device if
+ * needed): make it before any stream capture.  Every call shares the array
+ * and it keeps the previous call's bytes (nothing in it needs to start at
+ * zero); calls that overlap on the GPU, e.g. on two streams, race on it --
+ * serialise them.  Errors: as lc_layout_copy_host; LC_ERR_STAGING when even
+ * one tile's source and destination spans (each rounded up to 256 bytes)
+ * exceed LC_STATIC_STAGING_BYTES, or when the whole copy must fit at once
+ * (one tile, or destination tiles that interleave) and does not. */
+int lc_layout_copy_host_static(const void *src_host, const lc_tile_layout *src_layout,
+                               void *dst_host, const lc_tile_layout *dst_layout,
+                               int32_t elem_bytes, int64_t n_tiles, lc_stream_t stream);
+
 /* The planner alone: validation and the plan lc_layout_copy_ex would launch
  * for (layouts, elem_bytes, n_tiles, kernel), without touching the GPU.
  * Pointer checks (NULL, alignment, overlap) are skipped.  `out` must not be

@@ -17,7 +17,7 @@ from . import _lib
 from ._lib import KERNELS, STATUS, STATUS_NAMES
 
 __all__ = ["TileLayout", "LayoutCopyError", "layout_copy", "layout_copy_ptr", "layout_copy_host",
-           "host_staging_bytes", "plan",
+           "host_staging_bytes", "layout_copy_host_static", "plan",
            "choose_swizzle", "swizzle_conflicts", "gmem_smem_partition",
            "last_device_error", "debug_wait_timeout", "KERNELS", "STATUS"]
 
@@ -170,6 +170,30 @@ def layout_copy_host(src, src_layout, dst, dst_layout, n_tiles: int = 1, elem_by
                                         staging.numel() * staging.element_size(),
                                         ctypes.c_void_p(_stream_handle(stream)))
     _check(st, "layout_copy_host")
+
+
+def layout_copy_host_static(src, src_layout, dst, dst_layout, n_tiles: int = 1,
+                            elem_bytes: int | None = None, stream=None) -> None:
+    """layout_copy_host for callers that cannot allocate device memory.
+
+    Stages through a fixed 32 MiB array inside the library instead of a
+    caller-provided buffer (see lc_layout_copy_host_static); allocates
+    nothing.  Calls share that array: do not let two calls overlap on the GPU.
+    """
+    if src.is_cuda or dst.is_cuda:
+        raise ValueError("layout_copy_host_static takes host tensors")
+    if not (src.is_contiguous() and dst.is_contiguous()):
+        raise ValueError("pass contiguous tensors; express strides through the layouts")
+    w = int(elem_bytes) if elem_bytes is not None else src.element_size()
+    sl, dl = TileLayout.of(src_layout), TileLayout.of(dst_layout)
+    for name, t, l in (("source", src, sl), ("destination", dst, dl)):
+        if l.footprint(n_tiles) * w > t.numel() * t.element_size():
+            raise ValueError("%s layout reaches past the tensor" % name)
+    cs, cd = sl.to_c(), dl.to_c()
+    st = _lib.lib().lc_layout_copy_host_static(ctypes.c_void_p(src.data_ptr()), ctypes.byref(cs),
+                                               ctypes.c_void_p(dst.data_ptr()), ctypes.byref(cd), w,
+                                               int(n_tiles), ctypes.c_void_p(_stream_handle(stream)))
+    _check(st, "layout_copy_host_static")
 
 
 def plan(src_layout, dst_layout, elem_bytes: int, n_tiles: int = 1, kernel="auto") -> dict:

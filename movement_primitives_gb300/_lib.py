@@ -13,6 +13,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 # compiled with different tuning knobs); by default the in-tree build is used.
 LIB_PATH = os.environ.get("LC_LIBRARY_PATH") or os.path.join(HERE, "liblayoutcopy.so")
 MAX_RANK = 8
+STATIC_STAGING_BYTES = 32 * 1024 * 1024  # LC_STATIC_STAGING_BYTES
 
 OK = 0
 STATUS_NAMES = {
@@ -67,6 +68,8 @@ PROTOTYPES = {
                                            ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p,
                                            ctypes.c_int64, ctypes.c_void_p]),
     "lc_host_staging_bytes": (ctypes.c_int64, [_P_LAYOUT, _P_LAYOUT, ctypes.c_int32, ctypes.c_int64]),
+    "lc_layout_copy_host_static": (ctypes.c_int, [ctypes.c_void_p, _P_LAYOUT, ctypes.c_void_p, _P_LAYOUT,
+                                                  ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p]),
     "lc_plan": (ctypes.c_int, [_P_LAYOUT, _P_LAYOUT, ctypes.c_int32, ctypes.c_int64,
                                ctypes.c_int32, ctypes.POINTER(CPlanInfo)]),
     "lc_choose_swizzle": (ctypes.c_int, [_P_LAYOUT, _P_LAYOUT, ctypes.c_int32, _P_I32, _P_I32,

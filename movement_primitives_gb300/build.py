@@ -21,7 +21,8 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "liblayoutcopy.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 
-SOURCES = ["plan.cpp", "api.cu", "host_copy.cu", "k_vec.cu", "k_warp.cu", "k_tile.cu"]
+SOURCES = ["plan.cpp", "api.cu", "host_copy.cu", "host_copy_static.cu", "k_vec.cu", "k_warp.cu",
+           "k_tile.cu"]
 HEADERS = ["lc_internal.h", "ptx.cuh", "device_common.cuh", "launch.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O3",
