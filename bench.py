@@ -106,7 +106,7 @@ def describe(cfg) -> str:
 
 def kernel_sources_sha(kernel_name: str) -> str:
     files = {"warp_permute": ["k_warp.cu"], "tile_transpose": ["k_tile.cu"],
-             "vec_copy": ["k_vec.cu"]}.get(kernel_name, [])
+             "vec_copy": ["k_vec.cu"], "smem_transpose": ["k_smem.cu"]}.get(kernel_name, [])
     h = hashlib.sha256()
     for f in files + ["ptx.cuh", "device_common.cuh"]:
         with open(os.path.join(ROOT, "movement_primitives_gb300", "csrc", f), "rb") as fh:
@@ -524,8 +524,101 @@ def run_ours(args):
     return 0
 
 
+def run_window_sum(args):
+    """Workload 7: b[i] = a[i] + a[i+1] + a[i+2] over 2^28 float32 outputs."""
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    from oracle import stencil
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    __graft_entry__.build()
+    import movement_primitives_gb300 as lc
+    cfg = workloads.config(7)
+    n, win = cfg["n_out"], cfg["window"]
+    a_h = workloads.make_bytes(n + win - 1, 4, cfg["kind"], cfg["seed"]).view(torch.float32)
+    if args.impl == "reference":
+        cores = host_cores()
+        m = min(n, 1 << 26)
+        t0 = time.perf_counter()
+        passes = 0
+        while time.perf_counter() - t0 < args.cpu_seconds / 2 or passes == 0:
+            stencil.window_sum_f32(a_h.numpy()[:m + win - 1], m, win)
+            passes += 1
+        t = time.perf_counter() - t0
+        value = passes * (2 * m + win - 1) * 4 / t / 1e9
+        print(json.dumps({"metric": METRIC, "value": round(value, 3), "unit": UNIT, "impl": "reference",
+                          "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+                          "data": "synthetic", "config": {"workload": cfg["name"]},
+                          "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+                                           "sample": "%d pass(es) over %d outputs" % (passes, m)},
+                          "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}), flush=True)
+        return 0
+    a = a_h.to(dev)
+    out = torch.empty(n, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    step_bytes = (2 * n + win - 1) * 4
+    for _ in range(max(3, args.warmup)):
+        lc.window_sum(a, out, win, stream=stream)
+    m = 1 << 20
+    if not np.array_equal(out[:m].cpu().numpy(), stencil.window_sum_f32(a_h.numpy()[:m + win - 1], m, win)):
+        raise RuntimeError("spot check against the oracle failed")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(gpu_id_for(0))
+    torch.cuda.synchronize()
+    sampler.start()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(args.steps):
+        ev[k][0].record(stream)
+        lc.window_sum(a, out, win, stream=stream)
+        ev[k][1].record(stream)
+    t1.record(stream)
+    sampler.snapshot()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    elapsed = t0.elapsed_time(t1)
+    launch_ms = statistics.mean(x.elapsed_time(y) for x, y in ev)
+    peak, peak_kind = measured_peak()
+    value = step_bytes * args.steps / (elapsed / 1e3) / 1e9
+    achieved = step_bytes / (launch_ms / 1e3) / 1e9
+    e2e = None
+    if args.e2e_steps > 0:
+        a_pin, o_pin = a_h.pin_memory(), torch.empty(n, dtype=torch.float32).pin_memory()
+        for it in range(args.e2e_steps + 1):
+            if it == 1:
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            a.copy_(a_pin, non_blocking=True)
+            lc.window_sum(a, out, win, stream=stream)
+            o_pin.copy_(out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+        e2e = {"value": round(step_bytes / (e2e_ms / 1e3) / 1e9, 2), "unit": UNIT,
+               "h2d_bytes_per_step": (n + win - 1) * 4, "d2h_bytes_per_step": n * 4,
+               "path": "pinned copies around lc_window_sum_f32 on one stream"}
+    line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(elapsed / args.steps, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "%s: %d outputs, window %d" % (cfg["name"], n, win), "kernel": "window_sum",
+                       "bytes_per_step": step_bytes, "l2": "inputs larger than L2, no flush"},
+            "pct_of_peak": round(100.0 * value / peak, 2),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": None, "peak_kind": peak_kind},
+            "clocks": clocks, "gpu_launches": args.steps, "e2e": e2e, "cpu_baseline": None}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.workload == 7:
+        return run_window_sum(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -104,7 +104,15 @@ typedef enum {
      * shared-memory ring (mbarrier pipelined), 16-byte shared reads, an
      * in-register transpose of the sub-16-byte elements, 16-byte coalesced
      * global stores.  Large 2-D transposes with batch modes. */
-    LC_KERNEL_TILE_TRANSPOSE = 3
+    LC_KERNEL_TILE_TRANSPOSE = 3,
+    /* Shared-memory transpose for any alignment: 32 x 32 tiles, copied
+     * global -> shared in source order and shared -> global in destination
+     * order ("copy -> gmem_smem", its two copies around a swizzled shared
+     * layout), one word per access; the column swizzle
+     * y' = y ^ (((x >> shift) & mask) * granule) is chosen by the bank
+     * simulator so that both copies are conflict-free.  Transposes whose
+     * strides or bases the TMA path cannot take. */
+    LC_KERNEL_SMEM_TRANSPOSE = 4
 } lc_kernel;
 
 /* What the planner decided for one copy (filled by lc_plan). */
@@ -120,10 +128,10 @@ typedef struct {
     /* vector copy */
     int32_t vec;               /* words per vector */
     int64_t run;               /* words in the contiguous inner run (1 if none) */
-    /* warp permute */
+    /* warp permute (P, XOR swizzle); shared-memory transpose (swizzle) */
     int32_t unit_modes;        /* number of modes in one unit (innermost) */
     int32_t P;                 /* words per lane per unit */
-    int32_t k, shift, mask;    /* XOR swizzle */
+    int32_t k, shift, mask;    /* XOR swizzle (mask = 2^k - 1) */
     int32_t conflicts_read, conflicts_write;
     int64_t units_per_chunk;
     /* tile transpose */
@@ -212,6 +220,20 @@ int64_t lc_host_staging_bytes(const lc_tile_layout *src_layout,
 int lc_layout_copy_host_static(const void *src_host, const lc_tile_layout *src_layout,
                                void *dst_host, const lc_tile_layout *dst_layout,
                                int32_t elem_bytes, int64_t n_tiles, lc_stream_t stream);
+
+/* Largest window of lc_window_sum_f32. */
+#define LC_WINDOW_SUM_MAX 64
+
+/* Window sum through a cooperatively fetched shared-memory chunk (MLC course
+ * "Ep7: GPU and Hardware Acceleration", section "Window Sum Example", which
+ * has window 3):  b[i] = a[i] + a[i+1] + ... + a[i+window-1] for i in
+ * [0, n_out), float32 additions left to right.  `a` (device) holds
+ * n_out + window - 1 floats, `b` (device) n_out floats; 4-byte aligned,
+ * non-overlapping.  Asynchronous on `stream`.  Errors: LC_ERR_SHAPE (n_out < 0
+ * or window outside 1..LC_WINDOW_SUM_MAX), LC_ERR_NULL, LC_ERR_ALIGN,
+ * LC_ERR_OVERLAP, LC_ERR_OVERFLOW, LC_ERR_CUDA. */
+int lc_window_sum_f32(const float *a, float *b, int64_t n_out, int32_t window,
+                      lc_stream_t stream);
 
 /* The planner alone: validation and the plan lc_layout_copy_ex would launch
  * for (layouts, elem_bytes, n_tiles, kernel), without touching the GPU.

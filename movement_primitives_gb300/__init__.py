@@ -17,7 +17,7 @@ from . import _lib
 from ._lib import KERNELS, STATUS, STATUS_NAMES
 
 __all__ = ["TileLayout", "LayoutCopyError", "layout_copy", "layout_copy_ptr", "layout_copy_host",
-           "host_staging_bytes", "layout_copy_host_static", "plan",
+           "host_staging_bytes", "layout_copy_host_static", "window_sum", "plan",
            "choose_swizzle", "swizzle_conflicts", "gmem_smem_partition",
            "last_device_error", "debug_wait_timeout", "KERNELS", "STATUS"]
 
@@ -194,6 +194,20 @@ def layout_copy_host_static(src, src_layout, dst, dst_layout, n_tiles: int = 1,
                                                ctypes.c_void_p(dst.data_ptr()), ctypes.byref(cd), w,
                                                int(n_tiles), ctypes.c_void_p(_stream_handle(stream)))
     _check(st, "layout_copy_host_static")
+
+
+def window_sum(a, b, window: int = 3, stream=None) -> None:
+    """b[i] = a[i] + ... + a[i + window - 1] (float32 CUDA tensors, left to right)."""
+    import torch
+    if a.dtype != torch.float32 or b.dtype != torch.float32 or not (a.is_cuda and b.is_cuda):
+        raise ValueError("window_sum takes float32 CUDA tensors")
+    if not (a.is_contiguous() and b.is_contiguous()):
+        raise ValueError("pass contiguous tensors")
+    n = b.numel()
+    if a.numel() < n + window - 1:
+        raise ValueError("a holds %d floats, needs %d" % (a.numel(), n + window - 1))
+    _check(_lib.lib().lc_window_sum_f32(ctypes.c_void_p(a.data_ptr()), ctypes.c_void_p(b.data_ptr()), n,
+                                        int(window), ctypes.c_void_p(_stream_handle(stream))), "window_sum")
 
 
 def plan(src_layout, dst_layout, elem_bytes: int, n_tiles: int = 1, kernel="auto") -> dict:

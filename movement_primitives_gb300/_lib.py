@@ -24,7 +24,7 @@ STATUS_NAMES = {
     13: "LC_ERR_UNSUPPORTED", 14: "LC_ERR_OVERFLOW", 15: "LC_ERR_STAGING",
 }
 STATUS = {v: k for k, v in STATUS_NAMES.items()}
-KERNELS = {"auto": 0, "vec_copy": 1, "warp_permute": 2, "tile_transpose": 3}
+KERNELS = {"auto": 0, "vec_copy": 1, "warp_permute": 2, "tile_transpose": 3, "smem_transpose": 4}
 
 
 class CTileLayout(ctypes.Structure):
@@ -70,6 +70,8 @@ PROTOTYPES = {
     "lc_host_staging_bytes": (ctypes.c_int64, [_P_LAYOUT, _P_LAYOUT, ctypes.c_int32, ctypes.c_int64]),
     "lc_layout_copy_host_static": (ctypes.c_int, [ctypes.c_void_p, _P_LAYOUT, ctypes.c_void_p, _P_LAYOUT,
                                                   ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p]),
+    "lc_window_sum_f32": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32,
+                                         ctypes.c_void_p]),
     "lc_plan": (ctypes.c_int, [_P_LAYOUT, _P_LAYOUT, ctypes.c_int32, ctypes.c_int64,
                                ctypes.c_int32, ctypes.POINTER(CPlanInfo)]),
     "lc_choose_swizzle": (ctypes.c_int, [_P_LAYOUT, _P_LAYOUT, ctypes.c_int32, _P_I32, _P_I32,

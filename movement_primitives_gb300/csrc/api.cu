@@ -71,6 +71,22 @@ cudaError_t prepare(const void *fn, int threads, int smem, int attr_smem, int *s
     return cudaSuccess;
 }
 
+int launch_plan(const Plan &p, const uint8_t *s, uint8_t *d, cudaStream_t cs, bool fallback) {
+    switch (p.kernel) {
+        case LC_KERNEL_VEC_COPY: return launch_vec(p, s, d, cs);
+        case LC_KERNEL_WARP_PERMUTE: return launch_warp(p, s, d, cs);
+        case LC_KERNEL_SMEM_TRANSPOSE: return launch_smem(p, s, d, cs);
+        case LC_KERNEL_TILE_TRANSPOSE: {
+            const int r = launch_tile(p, s, d, cs);
+            if (r != LC_ERR_UNSUPPORTED || !fallback) return r;
+            Plan q = p;  // the driver refused the tensor map: same tiles, shared-memory path
+            q.smem_swz = choose_smem_swizzle(p.w);
+            return launch_smem(q, s, d, cs);
+        }
+    }
+    return LC_ERR_UNSUPPORTED;
+}
+
 }  // namespace lc
 
 extern "C" int lc_layout_copy_ex(const void *src, const lc_tile_layout *src_layout, void *dst,
@@ -84,20 +100,9 @@ extern "C" int lc_layout_copy_ex(const void *src, const lc_tile_layout *src_layo
     const int st = lc::make_plan(src_layout, dst_layout, elem_bytes, n_tiles, kernel, ptr, &p);
     if (st) return st;
     if (p.total == 0) return LC_OK;
-    const uint8_t *s = static_cast<const uint8_t *>(src);
-    uint8_t *d = static_cast<uint8_t *>(dst);
-    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    switch (p.kernel) {
-        case LC_KERNEL_VEC_COPY: return lc::launch_vec(p, s, d, cs);
-        case LC_KERNEL_WARP_PERMUTE: return lc::launch_warp(p, s, d, cs);
-        case LC_KERNEL_TILE_TRANSPOSE: {
-            const int r = lc::launch_tile(p, s, d, cs);
-            // an automatic choice never declines: the vector copy takes any copy
-            if (r == LC_ERR_UNSUPPORTED && kernel == LC_KERNEL_AUTO) return lc::launch_vec(p, s, d, cs);
-            return r;
-        }
-    }
-    return LC_ERR_UNSUPPORTED;
+    // an automatic choice never declines a valid copy
+    return lc::launch_plan(p, static_cast<const uint8_t *>(src), static_cast<uint8_t *>(dst),
+                           reinterpret_cast<cudaStream_t>(stream), kernel == LC_KERNEL_AUTO);
 }
 
 extern "C" int lc_layout_copy(const void *src, const lc_tile_layout *src_layout, void *dst,
@@ -153,6 +158,7 @@ extern "C" const char *lc_kernel_name(int32_t kernel) {
         case LC_KERNEL_VEC_COPY: return "vec_copy";
         case LC_KERNEL_WARP_PERMUTE: return "warp_permute";
         case LC_KERNEL_TILE_TRANSPOSE: return "tile_transpose";
+        case LC_KERNEL_SMEM_TRANSPOSE: return "smem_transpose";
     }
     return "unknown";
 }

@@ -76,18 +76,6 @@ int64_t words_of(const lc_tile_layout &l) {
     return n;
 }
 
-int launch_plan(const Plan &p, const uint8_t *s, uint8_t *d, cudaStream_t cs) {
-    switch (p.kernel) {
-        case LC_KERNEL_VEC_COPY: return launch_vec(p, s, d, cs);
-        case LC_KERNEL_WARP_PERMUTE: return launch_warp(p, s, d, cs);
-        case LC_KERNEL_TILE_TRANSPOSE: {
-            const int r = launch_tile(p, s, d, cs);
-            return r == LC_ERR_UNSUPPORTED ? launch_vec(p, s, d, cs) : r;
-        }
-    }
-    return LC_ERR_UNSUPPORTED;
-}
-
 }  // namespace
 }  // namespace lc
 
@@ -187,7 +175,7 @@ extern "C" int lc_layout_copy_host(const void *src_host, const lc_tile_layout *s
         ptr.check = true;
         st = make_plan(&sl, &dl, elem_bytes, t1 - t0, LC_KERNEL_AUTO, ptr, &p);
         if (st) return st;
-        if ((st = launch_plan(p, s_dev, d_dev, cs))) return st;
+        if ((st = launch_plan(p, s_dev, d_dev, cs, true))) return st;
         if (cudaEventRecord(ds->permuted[b], cs) != cudaSuccess) return LC_ERR_CUDA;
         // download once permuted
         if (cudaStreamWaitEvent(ds->down, ds->permuted[b], 0) != cudaSuccess) return LC_ERR_CUDA;

@@ -59,18 +59,6 @@ int64_t cosize(const lc_tile_layout &l) {
 
 int64_t round256(int64_t b) { return (b + 255) / 256 * 256; }
 
-int launch_chunk(const Plan &p, const uint8_t *s, uint8_t *d, cudaStream_t cs) {
-    switch (p.kernel) {
-        case LC_KERNEL_VEC_COPY: return launch_vec(p, s, d, cs);
-        case LC_KERNEL_WARP_PERMUTE: return launch_warp(p, s, d, cs);
-        case LC_KERNEL_TILE_TRANSPOSE: {
-            const int r = launch_tile(p, s, d, cs);
-            return r == LC_ERR_UNSUPPORTED ? launch_vec(p, s, d, cs) : r;
-        }
-    }
-    return LC_ERR_UNSUPPORTED;
-}
-
 }  // namespace
 }  // namespace lc
 
@@ -143,7 +131,7 @@ extern "C" int lc_layout_copy_host_static(const void *src_host, const lc_tile_la
         ptr.dst = reinterpret_cast<uintptr_t>(d_dev);
         ptr.check = true;
         if ((st = make_plan(&sl, &dl, elem_bytes, t1 - t0, LC_KERNEL_AUTO, ptr, &p))) return st;
-        if ((st = launch_chunk(p, s_dev, d_dev, cs))) return st;
+        if ((st = launch_plan(p, s_dev, d_dev, cs, true))) return st;
         if (cudaMemcpyAsync(dh + d_lo, d_dev, size_t(d_len), cudaMemcpyDeviceToHost, cs) != cudaSuccess)
             return LC_ERR_CUDA;
     }

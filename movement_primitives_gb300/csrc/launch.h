@@ -22,6 +22,11 @@ inline int finish_launch() { return cudaGetLastError() == cudaSuccess ? LC_OK : 
 int launch_vec(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream);
 int launch_warp(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream);
 int launch_tile(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream);
+int launch_smem(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream);
+
+// Launches the plan's kernel class.  With `fallback`, a TMA tile plan whose
+// tensor map the driver refuses runs as the shared-memory transpose instead.
+int launch_plan(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream, bool fallback);
 
 cudaError_t take_error_tile(unsigned long long *v);
 

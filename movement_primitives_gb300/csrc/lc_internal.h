@@ -48,6 +48,12 @@ struct TilePlan {
     int threads = 0;
 };
 
+// Column swizzle of the shared tile of the shared-memory transpose:
+// y' = y ^ (((x >> shift) & mask) * granule).
+struct SmemSwizzle {
+    int shift = 0, mask = 0, granule = 1, cr = 0, cw = 0;
+};
+
 struct Plan {
     int kernel = LC_KERNEL_AUTO;
     int w = 0;                 // word bytes moved (after fusion)
@@ -60,7 +66,8 @@ struct Plan {
     ModeList sorted;           // destination-stride order (fused w)
     VecPlan vec;
     WarpPlan warp;
-    TilePlan tile;
+    TilePlan tile;       // also the X / Y / batch split of the shared-memory transpose
+    SmemSwizzle smem_swz;
 };
 
 // Pointer facts the planner needs (alignment of the two base addresses).
@@ -77,6 +84,13 @@ void fill_info(const Plan &p, lc_plan_info *info);
 void phase_degrees(const ModeList &unit, int w, int k, int shift, int *rd, int *wd);
 // Returns 0 when conflict-free (k, shift) found; 1 otherwise (best returned).
 int choose_xor(const ModeList &unit, int w, int *k, int *shift, int *rd, int *wd);
+
+// Square tile edge (words) of the shared-memory transpose for w-byte words.
+constexpr int smem_tile_words(int w) { return w <= 4 ? 64 : 32; }
+
+// Shared tile swizzle of the shared-memory transpose for w-byte words:
+// smallest (mask, shift) that keeps both copies conflict-free.
+SmemSwizzle choose_smem_swizzle(int w);
 
 // Joint coalescing and shard alignment, exposed for the swizzle queries.
 int align_shards(const lc_tile_layout *src, const lc_tile_layout *dst, ModeList *out);

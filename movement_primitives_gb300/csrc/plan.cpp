@@ -211,6 +211,47 @@ int choose_xor(const ModeList &unit, int w, int *k_out, int *shift_out, int *rd_
     return 1;
 }
 
+// Both copies of the shared-memory transpose, per warp instruction, on a
+// TW x TW tile: copy 1 writes 32 consecutive columns of one row (lanes =
+// columns), copy 2 reads 32 consecutive rows of one column (lanes = rows);
+// element (x, y) sits at column y ^ (((x >> shift) & mask) * granule).
+SmemSwizzle choose_smem_swizzle(int w) {
+    const int tw = smem_tile_words(w);
+    SmemSwizzle best;
+    best.granule = w >= 4 ? 1 : 4 / w;
+    int best_deg = 1 << 30;
+    for (int k = 0; (1 << k) * best.granule <= tw; ++k) {
+        for (int shift = 0; shift <= (k ? 6 - k : 0); ++shift) {
+            const int mask = (1 << k) - 1;
+            int rd = 0, wd = 0;
+            for (int v = 0; v < tw; ++v) {
+                for (int base = 0; base < tw; base += kWarp) {
+                    int64_t wr[kWarp], rdad[kWarp];
+                    for (int lane = 0; lane < kWarp; ++lane) {
+                        // copy 1: row v, column base + lane; copy 2: column v, row base + lane
+                        const int c1 = (base + lane) ^ (((v >> shift) & mask) * best.granule);
+                        const int c2 = v ^ ((((base + lane) >> shift) & mask) * best.granule);
+                        wr[lane] = (int64_t(v) * tw + c1) * w;
+                        rdad[lane] = (int64_t(base + lane) * tw + c2) * w;
+                    }
+                    wd = std::max(wd, access_degree(wr, w));
+                    rd = std::max(rd, access_degree(rdad, w));
+                }
+            }
+            const int deg = std::max(rd, wd);
+            if (deg < best_deg) {
+                best_deg = deg;
+                best.shift = shift;
+                best.mask = mask;
+                best.cr = rd;
+                best.cw = wd;
+            }
+            if (deg <= 1) return best;
+        }
+    }
+    return best;
+}
+
 int align_shards(const lc_tile_layout *src, const lc_tile_layout *dst, ModeList *out) {
     int st;
     if ((st = check_layout(src)) || (st = check_layout(dst))) return st;
@@ -346,6 +387,30 @@ bool plan_tile(Plan *p, const PtrInfo &ptr) {
     return true;
 }
 
+// Shared-memory transpose: a mode contiguous in dst (X) and another in src
+// (Y), any number of batch modes, any alignment beyond the word size.
+bool plan_smem(Plan *p) {
+    const ModeList &sl = p->sorted;
+    int xi = -1, yi = -1;
+    for (int i = 0; i < sl.n; ++i) {
+        if (sl.m[i].d == 1) xi = i;
+        if (sl.m[i].s == 1) yi = i;
+    }
+    if (xi < 0 || yi < 0 || xi == yi) return false;
+    TilePlan &tp = p->tile;
+    tp = TilePlan{};
+    tp.X = sl.m[xi];
+    tp.Y = sl.m[yi];
+    for (int i = 0; i < sl.n; ++i)
+        if (i != xi && i != yi) tp.batch.m[tp.batch.n++] = sl.m[i];
+    tp.R = smem_tile_words(p->w);
+    tp.TY = tp.R;
+    tp.S = 1;
+    tp.threads = 256;
+    p->smem_swz = choose_smem_swizzle(p->w);
+    return true;
+}
+
 // A contiguous run of L words with L * w <= 16 bytes (a power of two) moves
 // as one wider word when every other stride, both offsets and both base
 // addresses allow it: the copy is then a permute of (L * w)-byte words.
@@ -385,7 +450,7 @@ int make_plan_core(const lc_tile_layout *src, const lc_tile_layout *dst, int32_t
     if ((st = check_layout(src)) || (st = check_layout(dst))) return st;
     if (!valid_width(w)) return LC_ERR_ELEM_BYTES;
     if (n_tiles < 0) return LC_ERR_SHAPE;
-    if (kernel < LC_KERNEL_AUTO || kernel > LC_KERNEL_TILE_TRANSPOSE) return LC_ERR_UNSUPPORTED;
+    if (kernel < LC_KERNEL_AUTO || kernel > LC_KERNEL_SMEM_TRANSPOSE) return LC_ERR_UNSUPPORTED;
 
     Plan p;
     p.w = w;
@@ -450,6 +515,12 @@ int make_plan_core(const lc_tile_layout *src, const lc_tile_layout *dst, int32_t
         *out = p;
         return LC_OK;
     }
+    if (kernel == LC_KERNEL_SMEM_TRANSPOSE) {
+        if (!plan_smem(&p)) return LC_ERR_UNSUPPORTED;
+        p.kernel = kernel;
+        *out = p;
+        return LC_OK;
+    }
     if (kernel == LC_KERNEL_VEC_COPY) {
         p.kernel = kernel;
         *out = p;
@@ -467,6 +538,7 @@ int make_plan_core(const lc_tile_layout *src, const lc_tile_layout *dst, int32_t
             if (plan_warp(&q, ptr, true)) { q.kernel = LC_KERNEL_WARP_PERMUTE; *out = q; return LC_OK; }
         }
         if (plan_tile(&p, ptr)) { p.kernel = LC_KERNEL_TILE_TRANSPOSE; *out = p; return LC_OK; }
+        if (plan_smem(&p)) { p.kernel = LC_KERNEL_SMEM_TRANSPOSE; *out = p; return LC_OK; }
     }
     p.kernel = LC_KERNEL_VEC_COPY;
     *out = p;
@@ -579,6 +651,15 @@ void fill_info(const Plan &p, lc_plan_info *info) {
     info->tile_rows = p.tile.R;
     info->tile_cols = p.tile.TY;
     info->stages = p.tile.S;
+    if (p.kernel == LC_KERNEL_SMEM_TRANSPOSE) {
+        int k = 0;
+        while ((1 << k) - 1 < p.smem_swz.mask) ++k;
+        info->k = k;
+        info->shift = p.smem_swz.shift;
+        info->mask = p.smem_swz.mask;
+        info->conflicts_read = p.smem_swz.cr;
+        info->conflicts_write = p.smem_swz.cw;
+    }
 }
 
 }  // namespace lc

@@ -17,9 +17,10 @@ Contents
                "permute_layout")
   banks        the shared-memory bank simulator and the XOR-bit choice
                (Apache TVM "permute_layout", "Algorithm" step 2)
+  stencil      the window sum of MLC "Ep7", "Window Sum Example"
 
 Every function is pinned by at least one test; nothing here is "parity
 unpinned".
 """
-from . import banks, build, definition, index_maps  # noqa: F401
+from . import banks, build, definition, index_maps, stencil  # noqa: F401
 from .definition import Layout, copy, offsets_of, paired_modes, cosize  # noqa: F401

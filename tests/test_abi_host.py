@@ -269,3 +269,35 @@ def test_overlaps_other_than_exact_unit_alias_are_refused(M):
         with pytest.raises(M.LayoutCopyError) as e:
             M.layout_copy_ptr(sp, sl, dp, dl, w, n, stream=0)
         assert e.value.status == M.STATUS["LC_ERR_OVERLAP"], (sl, dl)
+
+
+def test_smem_transpose_swizzle_is_conflict_free_by_the_oracle(M):
+    """The shared-memory transpose's column swizzle, checked with the oracle's
+    own bank model: copy 1 writes a tile row (lanes = columns), copy 2 reads a
+    tile column (lanes = rows); every warp access must be 1-way."""
+    T = M.TileLayout
+    for w in (1, 2, 4, 8, 16):
+        p = M.plan(T((37, 555), (555, 1)), T((37, 555), (1, 37)), w, 1, kernel="smem_transpose")
+        assert p["kernel_name"] == "smem_transpose"
+        shift, mask = p["shift"], p["mask"]
+        tw = p["tile_rows"]
+        assert tw == (64 if w <= 4 else 32)
+        g = 1 if w >= 4 else 4 // w
+        col = lambda x, y: y ^ (((x >> shift) & mask) * g)
+        for v in range(tw):
+            assert sorted(col(v, y) for y in range(tw)) == list(range(tw))  # each row a permutation
+            for base in range(0, tw, 32):
+                writes = [(v * tw + col(v, base + lane)) * w for lane in range(32)]
+                reads = [((base + lane) * tw + col(base + lane, v)) * w for lane in range(32)]
+                assert banks.access_degree(writes, w) == 1, (w, v)
+                assert banks.access_degree(reads, w) == 1, (w, v)
+        assert (p["conflicts_read"], p["conflicts_write"]) == (1, 1)
+
+
+def test_unaligned_transposes_plan_the_smem_transpose(M):
+    T = M.TileLayout
+    for w in (1, 2, 4, 8):
+        p = M.plan(T((37, 555), (555, 1)), T((37, 555), (1, 37)), w, 1)
+        assert p["kernel_name"] == "smem_transpose", w
+    # aligned ones keep the TMA path
+    assert M.plan(T((64, 64), (64, 1)), T((64, 64), (1, 64)), 4, 1)["kernel_name"] == "tile_transpose"

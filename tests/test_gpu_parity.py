@@ -89,7 +89,8 @@ def permuted(shape, perm):
 # the five workloads, reduced (several tiles and a ragged tail), every class
 # ---------------------------------------------------------------------------
 
-SMALL = [(1, None), (2, None), (3, None), (4, 1), (4, 2), (4, 4), (4, 8), (4, 16), (5, None)]
+SMALL = [(1, None), (2, None), (3, None), (4, 1), (4, 2), (4, 4), (4, 8), (4, 16), (5, None),
+         (6, 1), (6, 2), (6, 4), (6, 8)]
 
 
 @pytest.mark.parametrize("cfg,w", SMALL)
@@ -97,7 +98,7 @@ def test_workload_small_auto(cfg, w):
     c = workloads.config(cfg, w, scale="small")
     name = run_case(c["src"], c["dst"], c["elem_bytes"], c["n_tiles"], seed=cfg)
     expect = {1: "warp_permute", 2: "warp_permute", 3: "tile_transpose", 4: "tile_transpose",
-              5: "vec_copy"}[cfg]
+              5: "vec_copy", 6: "smem_transpose"}[cfg]
     assert name == expect
 
 
@@ -122,6 +123,23 @@ def test_tile_transpose_ragged(w):
     # strides TMA cannot take: the automatic choice still gets it right
     for r, c in [(37, 555), (257, 129), (3, 1000)]:
         run_case(L((r, c), (c, 1)), L((r, c), (1, r)), w, seed=r * c)
+
+
+@pytest.mark.parametrize("w", [1, 2, 4, 8, 16])
+def test_smem_transpose_any_alignment(w):
+    for r, c in [(37, 555), (257, 129), (3, 1000), (32, 32), (64, 96), (65, 63), (2, 3)]:
+        run_case(L((r, c), (c, 1)), L((r, c), (1, r)), w, kernel="smem_transpose", seed=r + c)
+    # a single non-unit mode has nothing to transpose: the forced class declines
+    with pytest.raises(lc().LayoutCopyError):
+        run_case(L((1, 2), (2, 1)), L((1, 2), (1, 1)), w, kernel="smem_transpose")
+    # offsets off every alignment grid, tile strides with gaps, batch modes
+    run_case(L((45, 70), (71, 1), 3, 3300), L((45, 70), (1, 47), 5, 3400), w, n_tiles=3,
+             kernel="smem_transpose", seed=w)
+    sh = (3, 5, 33, 31)
+    run_case(L(sh, row_major(sh)), L(sh, permuted(sh, (1, 0, 3, 2))), w, kernel="smem_transpose", seed=9)
+    # misaligned base pointers: the automatic choice takes this path
+    assert run_case(L((64, 96), (96, 1)), L((64, 96), (1, 64)), w, src_shift=w if w < 16 else 0,
+                    dst_shift=0) in ("smem_transpose", "tile_transpose")
 
 
 # ---------------------------------------------------------------------------
@@ -232,7 +250,8 @@ def test_misaligned_bases_still_exact():
 # full-size workloads, in the launch configuration the benchmark times
 # ---------------------------------------------------------------------------
 
-FULL = [(1, None), (2, None), (3, None), (4, 1), (4, 2), (4, 4), (4, 8), (4, 16), (5, None)]
+FULL = [(1, None), (2, None), (3, None), (4, 1), (4, 2), (4, 4), (4, 8), (4, 16), (5, None),
+        (6, 1), (6, 4), (6, 8)]
 
 
 @pytest.mark.parametrize("cfg,w", FULL)
@@ -384,3 +403,33 @@ def test_host_buffers_errors():
     with pytest.raises(M.LayoutCopyError) as e:
         M.layout_copy_host(a, lay, a, L((16, 16), (1, 16)), elem_bytes=4)
     assert e.value.status == M.STATUS["LC_ERR_OVERLAP"]
+
+
+# ---------------------------------------------------------------------------
+# window sum (cooperative fetch + stencil), against the oracle, bit for bit
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("window", [1, 2, 3, 7, 64])
+def test_window_sum_matches_oracle(window):
+    from oracle import stencil
+    rng = np.random.default_rng(window)
+    for n in (1, 5, 1024, 2047, 2048, 2049, 100003, 1 << 20):
+        a_h = rng.standard_normal(n + window - 1).astype(np.float32)
+        want = stencil.window_sum_f32(a_h, n, window)
+        a = torch.from_numpy(a_h).cuda()
+        b = torch.full((n,), float("nan"), dtype=torch.float32, device="cuda")
+        lc().window_sum(a, b, window)
+        got = b.cpu().numpy()
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), (n, window)
+
+
+def test_window_sum_unaligned_and_page_shape():
+    from oracle import stencil
+    a_h = np.random.default_rng(0).standard_normal(1027 + 3).astype(np.float32)
+    a = torch.from_numpy(a_h).cuda()
+    b = torch.empty(1024 + 1, dtype=torch.float32, device="cuda")
+    # the page's shapes (1027 -> 1024), from a base that is not 16-byte aligned
+    lc().window_sum(a[1:1028], b[1:], 3)
+    assert np.array_equal(b[1:].cpu().numpy(), stencil.window_sum_f32(a_h[1:1028], 1024, 3))
+    with pytest.raises(lc().LayoutCopyError):
+        lc().window_sum(a, a[:1000], 3)  # overlapping ranges

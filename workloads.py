@@ -14,6 +14,10 @@ The five workloads are those the library is measured on:
   3  16384x16384 bf16, row-major -> column-major
   4  8192x8192 transpose for element widths 1, 2, 4, 8 and 16 bytes
   5  (256,32,128,128) bf16 axis permute (0,2,1,3)
+  6  8191 x 8193 transpose with row strides off the 16-byte grid (the layouts
+     the TMA path cannot take), 4-byte words by default
+  7  window sum b[i] = a[i] + a[i+1] + a[i+2] over 2^28 float32 outputs (the
+     "Window Sum Example" of MLC Ep7, scaled up)
 Layouts are plain dicts: shape, stride, offset, tile_stride (elements).
 """
 from __future__ import annotations
@@ -64,6 +68,16 @@ def config(cfg: int, elem_bytes: int | None = None, scale: str = "full") -> dict
                     src=_layout((b, h, s, d), (h * s * d, s * d, d, 1)),
                     dst=_layout((b, h, s, d), (h * s * d, d, h * d, 1)),
                     elem_bytes=2, n_tiles=1, kind="normal_bf16", seed=5)
+    if cfg == 6:
+        w = 4 if elem_bytes is None else int(elem_bytes)
+        r, c = (301, 517) if small else (8191, 8193)
+        return dict(name="transpose2d_unaligned_w%d" % w, cfg=6,
+                    src=_layout((r, c), (c, 1)), dst=_layout((r, c), (1, r)),
+                    elem_bytes=w, n_tiles=1, kind="bytes", seed=60 + w)
+    if cfg == 7:
+        n = (1 << 16) + 3 if small else 1 << 28
+        return dict(name="window_sum3_f32", cfg=7, n_out=n, window=3, elem_bytes=4,
+                    kind="uniform_f32", seed=7)
     raise ValueError("unknown workload %r" % cfg)
 
 
