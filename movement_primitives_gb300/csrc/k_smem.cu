@@ -15,6 +15,15 @@
 // picks (shift, mask) so that both copies are conflict-free.  Words move one
 // at a time, so no alignment beyond the word size is needed; tiles on the
 // ragged edge are guarded (the TileLang loop partition's guard).
+//
+// Address arithmetic per word is a constant-stride step.  With STEP = T / TILE
+// rows per round, thread t always has column ly = t % TILE and first row
+// lx = t / TILE < STEP, and round f adds STEP * f to the row.  The row's bits
+// and lx's bits are disjoint, so the swizzle splits into a per-thread part and
+// a per-round constant: sw(lx + STEP f) = sw(lx) ^ sw(STEP f) (shift, mask and
+// the power-of-two granule all distribute over XOR).  Global addresses advance
+// by STEP source (destination) rows per round; the tile's origin is decoded
+// once per tile with invariant-divisor division.
 #include <cuda_runtime.h>
 
 #include "device_common.cuh"
@@ -27,6 +36,7 @@ constexpr int kSmemThreads = 256;
 template <int W> struct SmemCfg {
     static constexpr int TILE = smem_tile_words(W);
     static constexpr int ROUNDS = TILE * TILE / kSmemThreads;
+    static constexpr int STEP = kSmemThreads / TILE;  // rows per round
 };
 
 struct SmemArgs {
@@ -34,45 +44,55 @@ struct SmemArgs {
     uint8_t *dst;
     int64_t eX, eY;      // extents
     int64_t sX, dY;      // source stride of X, destination stride of Y (bytes)
-    int32_t nb;          // batch modes, outermost first (bytes strides)
-    int64_t be[kMaxModes], bs[kMaxModes], bd[kMaxModes];
-    int64_t tiles_x, tiles_y, n_tiles;
+    int32_t nb;          // batch modes, outermost first (byte strides)
+    int64_t bs[kMaxModes], bd[kMaxModes];
+    FastDiv be[kMaxModes];  // batch extents
+    FastDiv tiles_x, tiles_y;
+    uint32_t n_tiles;
     int32_t shift, mask, granule;
 };
 
-// Tile ti -> source / destination bases and the tile's origin and extent.
+// Tile ti -> source / destination addresses of its origin, and its extent.
 struct TileRef {
     const uint8_t *s;
     uint8_t *d;
-    int64_t x0, y0;
     int nx, ny;
 };
 
 template <int TILE>
-__device__ __forceinline__ TileRef tile_ref(const SmemArgs &a, int64_t ti) {
-    const int64_t ty = ti % a.tiles_y, rest = ti / a.tiles_y;  // Y-block fastest
-    const int64_t tx = rest % a.tiles_x;
-    int64_t b = rest / a.tiles_x;
-    TileRef r{a.src, a.dst, tx * TILE, ty * TILE, 0, 0};
+__device__ __forceinline__ TileRef tile_ref(const SmemArgs &a, uint32_t ti, int W) {
+    const uint32_t rest = fast_div(ti, a.tiles_y);  // Y-block fastest
+    const uint32_t ty = ti - rest * a.tiles_y.d;
+    uint32_t b = fast_div(rest, a.tiles_x);
+    const uint32_t tx = rest - b * a.tiles_x.d;
+    const int64_t x0 = int64_t(tx) * TILE, y0 = int64_t(ty) * TILE;
+    TileRef r{a.src + x0 * a.sX + y0 * W, a.dst + y0 * a.dY + x0 * W, 0, 0};
     for (int k = a.nb - 1; k >= 0; --k) {
-        const int64_t c = b % a.be[k];
-        b /= a.be[k];
-        r.s += c * a.bs[k];
-        r.d += c * a.bd[k];
+        const uint32_t q = fast_div(b, a.be[k]);
+        const uint32_t c = b - q * a.be[k].d;
+        b = q;
+        r.s += int64_t(c) * a.bs[k];
+        r.d += int64_t(c) * a.bd[k];
     }
-    r.nx = static_cast<int>(lmin(TILE, a.eX - r.x0));
-    r.ny = static_cast<int>(lmin(TILE, a.eY - r.y0));
+    r.nx = static_cast<int>(lmin(TILE, a.eX - x0));
+    r.ny = static_cast<int>(lmin(TILE, a.eY - y0));
     return r;
 }
 
-// Copy 1's global half: this thread's words of tile r, all loads issued.
-template <int W, int TILE, int ROUNDS, typename T>
-__device__ __forceinline__ void tile_load(const SmemArgs &a, const TileRef &r, T (&v)[ROUNDS]) {
+// Copy 1's global half: this thread's words of tile r (rows lx + STEP f,
+// column ly), all loads issued before any is used.
+template <int W, bool FULL, typename T, int ROUNDS>
+__device__ __forceinline__ void tile_load(const SmemArgs &a, const TileRef &r, int lx, int ly, T (&v)[ROUNDS]) {
+    constexpr int STEP = SmemCfg<W>::STEP;
+    const uint8_t *p = r.s + lx * a.sX + ly * W;
+    const int64_t step = STEP * a.sX;
+    if (FULL) {
 #pragma unroll
-    for (int f = 0; f < ROUNDS; ++f) {
-        const int flat = f * kSmemThreads + threadIdx.x;
-        const int x = flat / TILE, y = flat % TILE;
-        if (x < r.nx && y < r.ny) v[f] = *reinterpret_cast<const T *>(r.s + (r.x0 + x) * a.sX + (r.y0 + y) * W);
+        for (int f = 0; f < ROUNDS; ++f, p += step) v[f] = *reinterpret_cast<const T *>(p);
+    } else if (ly < r.ny) {
+#pragma unroll
+        for (int f = 0; f < ROUNDS; ++f, p += step)
+            if (lx + STEP * f < r.nx) v[f] = *reinterpret_cast<const T *>(p);
     }
 }
 
@@ -82,38 +102,60 @@ __device__ __forceinline__ void tile_load(const SmemArgs &a, const TileRef &r, T
 template <int W>
 __global__ void __launch_bounds__(kSmemThreads) k_smem_transpose(const __grid_constant__ SmemArgs a) {
     using T = typename Word<W>::T;
-    constexpr int kSmemTile = SmemCfg<W>::TILE;
-    constexpr int kRounds = SmemCfg<W>::ROUNDS;
-    __shared__ __align__(16) T tile[kSmemTile][kSmemTile];
+    constexpr int TILE = SmemCfg<W>::TILE;
+    constexpr int ROUNDS = SmemCfg<W>::ROUNDS;
+    constexpr int STEP = SmemCfg<W>::STEP;
+    __shared__ __align__(16) uint8_t tile[TILE * TILE * W];
     const int t = threadIdx.x;
-    int64_t ti = blockIdx.x;
+    const int lx = t / TILE, ly = t % TILE;
+    const int shift = a.shift, mask = a.mask, g = a.granule;
+    // copy 1: row lx + STEP f, column ly ^ sw(lx) ^ sw(STEP f)
+    uint8_t *const wrow = tile + lx * TILE * W;
+    const int c1 = ly ^ (((lx >> shift) & mask) * g);
+    // copy 2: row ly, column (lx + STEP f) ^ sw(ly) = c2 ^ STEP f
+    const uint8_t *const rrow = tile + ly * TILE * W;
+    const int c2 = lx ^ (((ly >> shift) & mask) * g);
+
+    uint32_t ti = blockIdx.x;
     if (ti >= a.n_tiles) return;
-    TileRef r = tile_ref<kSmemTile>(a, ti);
-    T v[kRounds];
-    tile_load<W, kSmemTile, kRounds>(a, r, v);
+    TileRef r = tile_ref<TILE>(a, ti, W);
+    bool full = r.nx == TILE && r.ny == TILE;
+    T v[ROUNDS];
+    if (full)
+        tile_load<W, true>(a, r, lx, ly, v);
+    else
+        tile_load<W, false>(a, r, lx, ly, v);
     for (; ti < a.n_tiles; ti += gridDim.x) {
-        // copy 1's shared half: source order into the swizzled tile
+        // copy 1's shared half (cells outside a ragged tile are written but
+        // never read back)
 #pragma unroll
-        for (int f = 0; f < kRounds; ++f) {
-            const int flat = f * kSmemThreads + t;
-            const int x = flat / kSmemTile, y = flat % kSmemTile;
-            if (x < r.nx && y < r.ny) tile[x][y ^ (((x >> a.shift) & a.mask) * a.granule)] = v[f];
+        for (int f = 0; f < ROUNDS; ++f) {
+            const int col = c1 ^ ((((STEP * f) >> shift) & mask) * g);
+            *reinterpret_cast<T *>(wrow + (STEP * f * TILE + col) * W) = v[f];
         }
         __syncthreads();
         const TileRef cur = r;
+        const bool cur_full = full;
         if (ti + gridDim.x < a.n_tiles) {  // next tile's loads, in flight during copy 2
-            r = tile_ref<kSmemTile>(a, ti + gridDim.x);
-            tile_load<W, kSmemTile, kRounds>(a, r, v);
+            r = tile_ref<TILE>(a, ti + gridDim.x, W);
+            full = r.nx == TILE && r.ny == TILE;
+            if (full)
+                tile_load<W, true>(a, r, lx, ly, v);
+            else
+                tile_load<W, false>(a, r, lx, ly, v);
         }
-        // copy 2: shared -> global, destination order
+        // copy 2: shared -> global, destination order (row lx + STEP f, column ly)
+        uint8_t *q = cur.d + lx * a.dY + ly * W;
+        const int64_t step = STEP * a.dY;
+        if (cur_full) {
 #pragma unroll
-        for (int f = 0; f < kRounds; ++f) {
-            const int flat = f * kSmemThreads + t;
-            const int y = flat / kSmemTile, x = flat % kSmemTile;
-            if (x < cur.nx && y < cur.ny) {
-                const int ys = y ^ (((x >> a.shift) & a.mask) * a.granule);
-                *reinterpret_cast<T *>(cur.d + (cur.y0 + y) * a.dY + (cur.x0 + x) * W) = tile[x][ys];
-            }
+            for (int f = 0; f < ROUNDS; ++f, q += step)
+                *reinterpret_cast<T *>(q) = *reinterpret_cast<const T *>(rrow + (c2 ^ (STEP * f)) * W);
+        } else if (ly < cur.nx) {
+#pragma unroll
+            for (int f = 0; f < ROUNDS; ++f, q += step)
+                if (lx + STEP * f < cur.ny)
+                    *reinterpret_cast<T *>(q) = *reinterpret_cast<const T *>(rrow + (c2 ^ (STEP * f)) * W);
         }
         __syncthreads();
     }
@@ -146,15 +188,18 @@ int launch_smem(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t st
     a.nb = tp.batch.n;
     int64_t nbatch = 1;
     for (int i = 0; i < tp.batch.n; ++i) {
-        a.be[i] = tp.batch.m[i].e;
+        a.be[i] = make_fastdiv(static_cast<uint32_t>(tp.batch.m[i].e));
         a.bs[i] = tp.batch.m[i].s * w;
         a.bd[i] = tp.batch.m[i].d * w;
         nbatch *= tp.batch.m[i].e;
     }
     const int tile = smem_tile_words(w);
-    a.tiles_x = (tp.X.e + tile - 1) / tile;
-    a.tiles_y = (tp.Y.e + tile - 1) / tile;
-    a.n_tiles = a.tiles_x * a.tiles_y * nbatch;
+    const int64_t tx = (tp.X.e + tile - 1) / tile, ty = (tp.Y.e + tile - 1) / tile;
+    const int64_t n_tiles = tx * ty * nbatch;
+    if (n_tiles >= (int64_t(1) << 31)) return LC_ERR_UNSUPPORTED;  // the planner keeps it below
+    a.tiles_x = make_fastdiv(static_cast<uint32_t>(tx));
+    a.tiles_y = make_fastdiv(static_cast<uint32_t>(ty));
+    a.n_tiles = static_cast<uint32_t>(n_tiles);
     a.shift = p.smem_swz.shift;
     a.mask = p.smem_swz.mask;
     a.granule = p.smem_swz.granule;

@@ -404,6 +404,10 @@ bool plan_smem(Plan *p) {
     for (int i = 0; i < sl.n; ++i)
         if (i != xi && i != yi) tp.batch.m[tp.batch.n++] = sl.m[i];
     tp.R = smem_tile_words(p->w);
+    // the kernel decodes tile indices in 32 bits
+    int64_t n_tiles = ((tp.X.e + tp.R - 1) / tp.R) * ((tp.Y.e + tp.R - 1) / tp.R);
+    for (int i = 0; i < tp.batch.n; ++i) n_tiles *= tp.batch.m[i].e;
+    if (n_tiles >= (int64_t(1) << 31)) return false;
     tp.TY = tp.R;
     tp.S = 1;
     tp.threads = 256;
