@@ -1,8 +1,8 @@
 // Shared-memory tile transpose for any alignment: the two global <-> shared
 // copies of Apache TVM docs "copy -> gmem_smem" around a swizzled shared tile.
 //
-// A CTA moves square tiles, 64 x 64 words for words of up to 4 bytes and
-// 32 x 32 for 8- and 16-byte words (X = the destination's contiguous mode,
+// A CTA moves square tiles, 64 x 64 words for words of up to 8 bytes and
+// 32 x 32 for 16-byte words (X = the destination's contiguous mode,
 // Y = the source's).  Copy 1 (global -> shared): thread t, round f takes
 // flat index f * T + t of the tile in source order (y fastest), so a warp
 // reads 32 consecutive source words, and every thread issues all its loads
@@ -33,7 +33,26 @@ namespace lc {
 
 constexpr int kSmemThreads = 256;
 
+// Resident CTAs per SM the register allocation must allow (compile-time knobs
+// so that variants can be measured).  Measured on GB300 on an 8191 x 8193
+// transpose: fewer registers than these make the compiler split each thread's
+// loads into dependent batches, which costs more than the extra CTAs gain.
+#ifndef LC_SMEM_MIN_BLOCKS_W1
+#define LC_SMEM_MIN_BLOCKS_W1 4
+#endif
+#ifndef LC_SMEM_MIN_BLOCKS_W2
+#define LC_SMEM_MIN_BLOCKS_W2 3
+#endif
+#ifndef LC_SMEM_MIN_BLOCKS_W4
+#define LC_SMEM_MIN_BLOCKS_W4 3
+#endif
+#ifndef LC_SMEM_MIN_BLOCKS_WIDE
+#define LC_SMEM_MIN_BLOCKS_WIDE 2
+#endif
+
 template <int W> struct SmemCfg {
+    static constexpr int MIN_BLOCKS = W == 1 ? LC_SMEM_MIN_BLOCKS_W1 : W == 2 ? LC_SMEM_MIN_BLOCKS_W2
+                                    : W == 4 ? LC_SMEM_MIN_BLOCKS_W4 : LC_SMEM_MIN_BLOCKS_WIDE;
     static constexpr int TILE = smem_tile_words(W);
     static constexpr int ROUNDS = TILE * TILE / kSmemThreads;
     static constexpr int STEP = kSmemThreads / TILE;  // rows per round
@@ -100,7 +119,7 @@ __device__ __forceinline__ void tile_load(const SmemArgs &a, const TileRef &r, i
 // issued before tile i's shared -> global copy, so loads stay in flight
 // while the previous tile drains.
 template <int W>
-__global__ void __launch_bounds__(kSmemThreads) k_smem_transpose(const __grid_constant__ SmemArgs a) {
+__global__ void __launch_bounds__(kSmemThreads, SmemCfg<W>::MIN_BLOCKS) k_smem_transpose(const __grid_constant__ SmemArgs a) {
     using T = typename Word<W>::T;
     constexpr int TILE = SmemCfg<W>::TILE;
     constexpr int ROUNDS = SmemCfg<W>::ROUNDS;

@@ -51,10 +51,10 @@ template <int W> struct TileCfg {
     static constexpr int TY = 128 / W;  // words per 128-byte tile row
     static constexpr int R = W == 1 ? LC_TILE_ROWS_W1 : W == 2 ? LC_TILE_ROWS_W2 : W == 4 ? LC_TILE_ROWS_W4
                            : W == 8 ? LC_TILE_ROWS_W8 : LC_TILE_ROWS_W16;  // source rows per tile
-    static constexpr int NT = W == 1 ? 128 : 256;                          // threads
     static constexpr int S = W == 1 ? LC_TILE_STAGES_W1 : LC_TILE_STAGES_WIDE;  // ring stages
     static constexpr int TILE_BYTES = 128 * R;
-    static constexpr int MB = 8 * R / V;  // V-row x 16-byte micro-blocks
+    static constexpr int MB = 8 * R / V;          // V-row x 16-byte micro-blocks
+    static constexpr int NT = MB < 256 ? MB : 256;  // threads: at most one micro-block each per round
     static constexpr int SMEM = 128 + S * TILE_BYTES;
     static_assert(R <= 256 && R % V == 0, "TMA boxes hold at most 256 rows, whole micro-blocks");
 };
@@ -241,6 +241,16 @@ __global__ void __launch_bounds__(TileCfg<W>::NT)
         if (tid == 0 && i + C::S < n_local)
             tile_issue_load<W>(&tmap, a, blockIdx.x + (i + C::S) * gridDim.x, tile0 + s * C::TILE_BYTES,
                                bar0 + 8 * s);
+    }
+}
+
+void tile_geometry(int w, int *rows, int *stages, int *threads) {
+    switch (w) {
+        case 1: *rows = TileCfg<1>::R; *stages = TileCfg<1>::S; *threads = TileCfg<1>::NT; break;
+        case 2: *rows = TileCfg<2>::R; *stages = TileCfg<2>::S; *threads = TileCfg<2>::NT; break;
+        case 4: *rows = TileCfg<4>::R; *stages = TileCfg<4>::S; *threads = TileCfg<4>::NT; break;
+        case 8: *rows = TileCfg<8>::R; *stages = TileCfg<8>::S; *threads = TileCfg<8>::NT; break;
+        default: *rows = TileCfg<16>::R; *stages = TileCfg<16>::S; *threads = TileCfg<16>::NT; break;
     }
 }
 

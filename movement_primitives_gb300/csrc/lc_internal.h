@@ -85,8 +85,27 @@ void phase_degrees(const ModeList &unit, int w, int k, int shift, int *rd, int *
 // Returns 0 when conflict-free (k, shift) found; 1 otherwise (best returned).
 int choose_xor(const ModeList &unit, int w, int *k, int *shift, int *rd, int *wd);
 
-// Square tile edge (words) of the shared-memory transpose for w-byte words.
-constexpr int smem_tile_words(int w) { return w <= 4 ? 64 : 32; }
+// Square tile edge (words) of the shared-memory transpose for w-byte words
+// (compile-time knobs so that variants can be measured).
+#ifndef LC_SMEM_TILE_W1
+#define LC_SMEM_TILE_W1 64
+#endif
+#ifndef LC_SMEM_TILE_W2
+#define LC_SMEM_TILE_W2 64
+#endif
+#ifndef LC_SMEM_TILE_W8
+#define LC_SMEM_TILE_W8 64
+#endif
+#ifndef LC_SMEM_TILE_W16
+#define LC_SMEM_TILE_W16 32
+#endif
+constexpr int smem_tile_words(int w) {
+    return w == 1 ? LC_SMEM_TILE_W1 : w == 2 ? LC_SMEM_TILE_W2 : w == 4 ? 64 : w == 8 ? LC_SMEM_TILE_W8 : LC_SMEM_TILE_W16;
+}
+
+// TMA tile transpose geometry for w-byte words (source rows per tile, ring
+// stages, threads), from the kernel's own compile-time table.
+void tile_geometry(int w, int *rows, int *stages, int *threads);
 
 // Shared tile swizzle of the shared-memory transpose for w-byte words:
 // smallest (mask, shift) that keeps both copies conflict-free.

@@ -380,10 +380,7 @@ bool plan_tile(Plan *p, const PtrInfo &ptr) {
     if (!a16(p->src_off * w) || !a16(p->dst_off * w)) return false;
     if (ptr.check && (ptr.src % 16 || ptr.dst % 16)) return false;
     tp.TY = 128 / w;
-    // reported for information; the kernel's per-width table decides
-    tp.R = w <= 4 ? 256 : 128;
-    tp.S = w == 1 ? 2 : 4;
-    tp.threads = w == 1 ? 128 : 256;
+    tile_geometry(w, &tp.R, &tp.S, &tp.threads);  // the kernel's per-width table
     return true;
 }
 

@@ -281,7 +281,7 @@ def test_smem_transpose_swizzle_is_conflict_free_by_the_oracle(M):
         assert p["kernel_name"] == "smem_transpose"
         shift, mask = p["shift"], p["mask"]
         tw = p["tile_rows"]
-        assert tw == (64 if w <= 4 else 32)
+        assert tw == (64 if w <= 8 else 32)
         g = 1 if w >= 4 else 4 // w
         col = lambda x, y: y ^ (((x >> shift) & mask) * g)
         for v in range(tw):
