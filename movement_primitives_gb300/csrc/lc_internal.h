@@ -48,10 +48,10 @@ struct TilePlan {
     int threads = 0;
 };
 
-// Column swizzle of the shared tile of the shared-memory transpose:
-// y' = y ^ (((x >> shift) & mask) * granule).
+// Chunk swizzle of the shared tile of the shared-memory transpose: chunk k
+// of row x is stored in chunk slot k ^ ((x >> shift) & mask).
 struct SmemSwizzle {
-    int shift = 0, mask = 0, granule = 1, cr = 0, cw = 0;
+    int shift = 0, mask = 0, cr = 0, cw = 0;
 };
 
 struct Plan {
@@ -85,22 +85,19 @@ void phase_degrees(const ModeList &unit, int w, int k, int shift, int *rd, int *
 // Returns 0 when conflict-free (k, shift) found; 1 otherwise (best returned).
 int choose_xor(const ModeList &unit, int w, int *k, int *shift, int *rd, int *wd);
 
-// Square tile edge (words) of the shared-memory transpose for w-byte words
-// (compile-time knobs so that variants can be measured).
-#ifndef LC_SMEM_TILE_W1
-#define LC_SMEM_TILE_W1 64
-#endif
-#ifndef LC_SMEM_TILE_W2
-#define LC_SMEM_TILE_W2 64
-#endif
-#ifndef LC_SMEM_TILE_W8
-#define LC_SMEM_TILE_W8 64
-#endif
-#ifndef LC_SMEM_TILE_W16
-#define LC_SMEM_TILE_W16 32
-#endif
-constexpr int smem_tile_words(int w) {
-    return w == 1 ? LC_SMEM_TILE_W1 : w == 2 ? LC_SMEM_TILE_W2 : w == 4 ? 64 : w == 8 ? LC_SMEM_TILE_W8 : LC_SMEM_TILE_W16;
+// Geometry of the shared-memory transpose for w-byte words: a tile is TX
+// source rows by TYW words; each row is staged as RB bytes of aligned C-byte
+// chunks starting at the chunk boundary at or below the row's first word, so
+// a row holds its lead-in (0 .. C - w bytes) and TYW words.
+struct SmemGeo {
+    int C, RB, TX, TYW;
+};
+constexpr SmemGeo smem_geometry(int w) {
+    return w == 1   ? SmemGeo{4, 256, 64, 252}
+           : w == 2 ? SmemGeo{4, 256, 64, 124}
+           : w == 4 ? SmemGeo{4, 256, 64, 64}
+           : w == 8 ? SmemGeo{8, 512, 64, 64}
+                    : SmemGeo{16, 512, 32, 32};
 }
 
 // TMA tile transpose geometry for w-byte words (source rows per tile, ring

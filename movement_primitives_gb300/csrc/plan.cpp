@@ -211,31 +211,41 @@ int choose_xor(const ModeList &unit, int w, int *k_out, int *shift_out, int *rd_
     return 1;
 }
 
-// Both copies of the shared-memory transpose, per warp instruction, on a
-// TW x TW tile: copy 1 writes 32 consecutive columns of one row (lanes =
-// columns), copy 2 reads 32 consecutive rows of one column (lanes = rows);
-// element (x, y) sits at column y ^ (((x >> shift) & mask) * granule).
+// Both copies of the shared-memory transpose, per warp instruction, on one
+// tile of TX rows x RB bytes (smem_geometry), chunk k of row x stored in
+// slot k ^ ((x >> shift) & mask).  Copy 1: thread t of 256 moves chunk
+// t % NC of row t / NC (+ 256 / NC per round), C bytes.  Copy 2: lanes read
+// word y of 32 consecutive rows; word y of row x starts at byte e + y * w of
+// the row's chunk sequence (e = the row's lead-in, taken as 0: rows with
+// different lead-ins may meet in a bank at most twice).
 SmemSwizzle choose_smem_swizzle(int w) {
-    const int tw = smem_tile_words(w);
+    const SmemGeo g = smem_geometry(w);
+    const int nc = g.RB / g.C;
     SmemSwizzle best;
-    best.granule = w >= 4 ? 1 : 4 / w;
     int best_deg = 1 << 30;
-    for (int k = 0; (1 << k) * best.granule <= tw; ++k) {
+    for (int k = 0; (1 << k) <= nc; ++k) {
         for (int shift = 0; shift <= (k ? 6 - k : 0); ++shift) {
             const int mask = (1 << k) - 1;
+            auto sw = [&](int x) { return (x >> shift) & mask; };
             int rd = 0, wd = 0;
-            for (int v = 0; v < tw; ++v) {
-                for (int base = 0; base < tw; base += kWarp) {
-                    int64_t wr[kWarp], rdad[kWarp];
-                    for (int lane = 0; lane < kWarp; ++lane) {
-                        // copy 1: row v, column base + lane; copy 2: column v, row base + lane
-                        const int c1 = (base + lane) ^ (((v >> shift) & mask) * best.granule);
-                        const int c2 = v ^ ((((base + lane) >> shift) & mask) * best.granule);
-                        wr[lane] = (int64_t(v) * tw + c1) * w;
-                        rdad[lane] = (int64_t(base + lane) * tw + c2) * w;
+            for (int r = 0; r < g.TX * nc / 256; ++r) {
+                for (int t0 = 0; t0 < 256; t0 += kWarp) {
+                    int64_t ad[kWarp];
+                    for (int l = 0; l < kWarp; ++l) {
+                        const int t = t0 + l, x = t / nc + r * (256 / nc), c = t % nc;
+                        ad[l] = int64_t(x) * g.RB + int64_t(c ^ sw(x)) * g.C;
                     }
-                    wd = std::max(wd, access_degree(wr, w));
-                    rd = std::max(rd, access_degree(rdad, w));
+                    wd = std::max(wd, access_degree(ad, g.C));
+                }
+            }
+            for (int y = 0; y < g.TYW; ++y) {
+                for (int base = 0; base < g.TX; base += kWarp) {
+                    int64_t ad[kWarp];
+                    for (int l = 0; l < kWarp; ++l) {
+                        const int x = base + l;
+                        ad[l] = int64_t(x) * g.RB + ((int64_t(y) * w) ^ (int64_t(sw(x)) * g.C));
+                    }
+                    rd = std::max(rd, access_degree(ad, w));
                 }
             }
             const int deg = std::max(rd, wd);
@@ -400,14 +410,15 @@ bool plan_smem(Plan *p) {
     tp.Y = sl.m[yi];
     for (int i = 0; i < sl.n; ++i)
         if (i != xi && i != yi) tp.batch.m[tp.batch.n++] = sl.m[i];
-    tp.R = smem_tile_words(p->w);
-    // the kernel decodes tile indices in 32 bits
-    int64_t n_tiles = ((tp.X.e + tp.R - 1) / tp.R) * ((tp.Y.e + tp.R - 1) / tp.R);
-    for (int i = 0; i < tp.batch.n; ++i) n_tiles *= tp.batch.m[i].e;
-    if (n_tiles >= (int64_t(1) << 31)) return false;
-    tp.TY = tp.R;
+    const SmemGeo g = smem_geometry(p->w);
+    tp.R = g.TX;
+    tp.TY = g.TYW;
     tp.S = 1;
     tp.threads = 256;
+    // the kernel decodes tile indices in 32 bits
+    int64_t n_tiles = ((tp.X.e + tp.R - 1) / tp.R) * ((tp.Y.e + tp.TY - 1) / tp.TY);
+    for (int i = 0; i < tp.batch.n; ++i) n_tiles *= tp.batch.m[i].e;
+    if (n_tiles >= (int64_t(1) << 31)) return false;
     p->smem_swz = choose_smem_swizzle(p->w);
     return true;
 }

@@ -272,25 +272,33 @@ def test_overlaps_other_than_exact_unit_alias_are_refused(M):
 
 
 def test_smem_transpose_swizzle_is_conflict_free_by_the_oracle(M):
-    """The shared-memory transpose's column swizzle, checked with the oracle's
-    own bank model: copy 1 writes a tile row (lanes = columns), copy 2 reads a
-    tile column (lanes = rows); every warp access must be 1-way."""
+    """The shared-memory transpose's chunk swizzle, checked with the oracle's
+    own bank model.  A tile is TX rows of RB bytes; chunk k (C bytes) of row x
+    sits in slot k ^ ((x >> shift) & mask).  Copy 1: thread t of 256 writes
+    chunk t % NC of row t // NC (+ 256 // NC per round).  Copy 2: 32 lanes read
+    word y of 32 consecutive rows (rows without lead-in bytes).  Every warp
+    access must be 1-way."""
     T = M.TileLayout
-    for w in (1, 2, 4, 8, 16):
+    geometry = {1: (4, 256, 64, 252), 2: (4, 256, 64, 124), 4: (4, 256, 64, 64),
+                8: (8, 512, 64, 64), 16: (16, 512, 32, 32)}
+    for w, (C, RB, TX, TYW) in geometry.items():
         p = M.plan(T((37, 555), (555, 1)), T((37, 555), (1, 37)), w, 1, kernel="smem_transpose")
         assert p["kernel_name"] == "smem_transpose"
+        assert (p["tile_rows"], p["tile_cols"]) == (TX, TYW)
         shift, mask = p["shift"], p["mask"]
-        tw = p["tile_rows"]
-        assert tw == (64 if w <= 8 else 32)
-        g = 1 if w >= 4 else 4 // w
-        col = lambda x, y: y ^ (((x >> shift) & mask) * g)
-        for v in range(tw):
-            assert sorted(col(v, y) for y in range(tw)) == list(range(tw))  # each row a permutation
-            for base in range(0, tw, 32):
-                writes = [(v * tw + col(v, base + lane)) * w for lane in range(32)]
-                reads = [((base + lane) * tw + col(base + lane, v)) * w for lane in range(32)]
-                assert banks.access_degree(writes, w) == 1, (w, v)
-                assert banks.access_degree(reads, w) == 1, (w, v)
+        NC = RB // C
+        sw = lambda x: (x >> shift) & mask
+        for x in range(TX):
+            assert sorted(k ^ sw(x) for k in range(NC)) == list(range(NC))  # each row a permutation
+        for r in range(TX * NC // 256):
+            for t0 in range(0, 256, 32):
+                writes = [(t // NC + r * (256 // NC)) * RB + ((t % NC) ^ sw(t // NC + r * (256 // NC))) * C
+                          for t in range(t0, t0 + 32)]
+                assert banks.access_degree(writes, C) == 1, (w, r, t0)
+        for y in range(TYW):
+            for base in range(0, TX, 32):
+                reads = [(base + l) * RB + ((y * w) ^ (sw(base + l) * C)) for l in range(32)]
+                assert banks.access_degree(reads, w) == 1, (w, y)
         assert (p["conflicts_read"], p["conflicts_write"]) == (1, 1)
 
 

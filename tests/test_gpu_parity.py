@@ -129,7 +129,8 @@ def test_tile_transpose_ragged(w):
 def test_smem_transpose_any_alignment(w):
     # whole tiles and ragged edges in both modes; aligned and unaligned rows
     for r, c in [(37, 555), (257, 129), (3, 1000), (32, 32), (64, 96), (65, 63), (2, 3),
-                 (130, 250), (129, 241), (256, 240), (200, 61)]:
+                 (130, 250), (129, 241), (256, 240), (200, 61), (130, 600), (64, 252), (128, 124),
+                 (70, 505)]:
         run_case(L((r, c), (c, 1)), L((r, c), (1, r)), w, kernel="smem_transpose", seed=r + c)
     # a single non-unit mode has nothing to transpose: the forced class declines
     with pytest.raises(lc().LayoutCopyError):
