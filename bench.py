@@ -106,7 +106,8 @@ def describe(cfg) -> str:
 
 def kernel_sources_sha(kernel_name: str) -> str:
     files = {"warp_permute": ["k_warp.cu"], "tile_transpose": ["k_tile.cu"],
-             "vec_copy": ["k_vec.cu"], "smem_transpose": ["k_smem.cu"]}.get(kernel_name, [])
+             "vec_copy": ["k_vec.cu"], "smem_transpose": ["k_smem.cu"],
+             "tma_copy": ["k_tma_copy.cu"]}.get(kernel_name, [])
     h = hashlib.sha256()
     for f in files + ["ptx.cuh", "device_common.cuh"]:
         with open(os.path.join(ROOT, "movement_primitives_gb300", "csrc", f), "rb") as fh:

@@ -105,14 +105,24 @@ typedef enum {
      * in-register transpose of the sub-16-byte elements, 16-byte coalesced
      * global stores.  Large 2-D transposes with batch modes. */
     LC_KERNEL_TILE_TRANSPOSE = 3,
-    /* Shared-memory transpose for any alignment: 32 x 32 tiles, copied
-     * global -> shared in source order and shared -> global in destination
-     * order ("copy -> gmem_smem", its two copies around a swizzled shared
-     * layout), one word per access; the column swizzle
-     * y' = y ^ (((x >> shift) & mask) * granule) is chosen by the bank
+    /* Shared-memory transpose for any alignment: tiles of 64 source rows
+     * (32 for 16-byte words), each row staged as aligned chunks (4 bytes for
+     * words of up to 4 bytes, else the word) from the chunk boundary at or
+     * below its first word; copied global -> shared in source order and
+     * shared -> global in destination order, one word per store ("copy ->
+     * gmem_smem", its two copies around a swizzled shared layout); the chunk
+     * swizzle slot = k ^ ((x >> shift) & mask) is chosen by the bank
      * simulator so that both copies are conflict-free.  Transposes whose
      * strides or bases the TMA path cannot take. */
-    LC_KERNEL_SMEM_TRANSPOSE = 4
+    LC_KERNEL_SMEM_TRANSPOSE = 4,
+    /* TMA tensor copy: the innermost mode is contiguous on both sides (at
+     * least 64 bytes, a multiple of 16) and every other stride is a multiple
+     * of 16 bytes, at most 5 modes.  Boxes of whole inner modes (about
+     * 16 KiB) go global -> shared by TMA tensor loads and shared -> global by
+     * TMA tensor stores through a second tensor map with the destination
+     * strides; one thread per CTA drives a 4-stage ring.  Axis permutes that
+     * keep the last axis, strided slices, row gathers. */
+    LC_KERNEL_TMA_COPY = 5
 } lc_kernel;
 
 /* What the planner decided for one copy (filled by lc_plan). */

@@ -24,7 +24,8 @@ STATUS_NAMES = {
     13: "LC_ERR_UNSUPPORTED", 14: "LC_ERR_OVERFLOW", 15: "LC_ERR_STAGING",
 }
 STATUS = {v: k for k, v in STATUS_NAMES.items()}
-KERNELS = {"auto": 0, "vec_copy": 1, "warp_permute": 2, "tile_transpose": 3, "smem_transpose": 4}
+KERNELS = {"auto": 0, "vec_copy": 1, "warp_permute": 2, "tile_transpose": 3, "smem_transpose": 4,
+           "tma_copy": 5}
 
 
 class CTileLayout(ctypes.Structure):

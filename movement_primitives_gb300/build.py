@@ -22,7 +22,7 @@ LIB_NAME = "liblayoutcopy.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 
 SOURCES = ["plan.cpp", "api.cu", "host_copy.cu", "host_copy_static.cu", "k_vec.cu", "k_warp.cu",
-           "k_tile.cu", "k_smem.cu", "k_stencil.cu"]
+           "k_tile.cu", "k_smem.cu", "k_tma_copy.cu", "k_stencil.cu"]
 HEADERS = ["lc_internal.h", "ptx.cuh", "device_common.cuh", "launch.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O3",

@@ -76,6 +76,11 @@ int launch_plan(const Plan &p, const uint8_t *s, uint8_t *d, cudaStream_t cs, bo
         case LC_KERNEL_VEC_COPY: return launch_vec(p, s, d, cs);
         case LC_KERNEL_WARP_PERMUTE: return launch_warp(p, s, d, cs);
         case LC_KERNEL_SMEM_TRANSPOSE: return launch_smem(p, s, d, cs);
+        case LC_KERNEL_TMA_COPY: {
+            const int r = launch_tma_copy(p, s, d, cs);
+            if (r != LC_ERR_UNSUPPORTED || !fallback) return r;
+            return launch_vec(p, s, d, cs);  // the driver refused a tensor map: same copy, vector path
+        }
         case LC_KERNEL_TILE_TRANSPOSE: {
             const int r = launch_tile(p, s, d, cs);
             if (r != LC_ERR_UNSUPPORTED || !fallback) return r;
@@ -113,8 +118,9 @@ extern "C" int lc_layout_copy(const void *src, const lc_tile_layout *src_layout,
 
 extern "C" int lc_last_device_error(lc_stream_t stream, uint64_t *detail) {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return LC_ERR_CUDA;
-    unsigned long long words[2] = {0, 0};
-    if (lc::take_module_error(&words[0]) != cudaSuccess || lc::take_error_tile(&words[1]) != cudaSuccess)
+    unsigned long long words[3] = {0, 0, 0};
+    if (lc::take_module_error(&words[0]) != cudaSuccess || lc::take_error_tile(&words[1]) != cudaSuccess ||
+        lc::take_error_tma_copy(&words[2]) != cudaSuccess)
         return LC_ERR_CUDA;
     unsigned long long v = 0;
     for (unsigned long long w : words)
@@ -159,6 +165,7 @@ extern "C" const char *lc_kernel_name(int32_t kernel) {
         case LC_KERNEL_WARP_PERMUTE: return "warp_permute";
         case LC_KERNEL_TILE_TRANSPOSE: return "tile_transpose";
         case LC_KERNEL_SMEM_TRANSPOSE: return "smem_transpose";
+        case LC_KERNEL_TMA_COPY: return "tma_copy";
     }
     return "unknown";
 }

@@ -8,10 +8,10 @@
 #include <cuda_runtime.h>
 
 #include <cstring>
-#include <mutex>
 
 #include "device_common.cuh"
 #include "launch.h"
+#include "tensor_map.h"
 
 namespace lc {
 
@@ -255,27 +255,6 @@ void tile_geometry(int w, int *rows, int *stages, int *threads) {
 }
 
 namespace {
-
-// cuTensorMapEncodeTiled, fetched from the driver at run time so that the
-// library links against the CUDA runtime only.
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_tiled() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    });
-    return fn;
-}
 
 template <int W>
 int launch_tile_t(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream) {

@@ -23,11 +23,14 @@ int launch_vec(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t str
 int launch_warp(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream);
 int launch_tile(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream);
 int launch_smem(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream);
+int launch_tma_copy(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream);
 
-// Launches the plan's kernel class.  With `fallback`, a TMA tile plan whose
-// tensor map the driver refuses runs as the shared-memory transpose instead.
+// Launches the plan's kernel class.  With `fallback`, a TMA plan whose tensor
+// map the driver refuses runs on the non-TMA class of the same copy instead
+// (tile transpose -> shared-memory transpose, tensor copy -> vector copy).
 int launch_plan(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream, bool fallback);
 
 cudaError_t take_error_tile(unsigned long long *v);
+cudaError_t take_error_tma_copy(unsigned long long *v);
 
 }  // namespace lc

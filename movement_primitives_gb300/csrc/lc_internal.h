@@ -48,6 +48,15 @@ struct TilePlan {
     int threads = 0;
 };
 
+// TMA tensor copy: the modes of the destination order, innermost first, as
+// tensor dimensions of both tensor maps; box[k] words of dimension k per tile
+// (in TMA elements: 16-byte words travel as two 8-byte elements).
+struct TmaPlan {
+    int rank = 0;
+    int box[5] = {0, 0, 0, 0, 0};
+    int64_t stage_bytes = 0;
+};
+
 // Chunk swizzle of the shared tile of the shared-memory transpose: chunk k
 // of row x is stored in chunk slot k ^ ((x >> shift) & mask).
 struct SmemSwizzle {
@@ -68,6 +77,7 @@ struct Plan {
     WarpPlan warp;
     TilePlan tile;       // also the X / Y / batch split of the shared-memory transpose
     SmemSwizzle smem_swz;
+    TmaPlan tma;
 };
 
 // Pointer facts the planner needs (alignment of the two base addresses).

@@ -423,6 +423,56 @@ bool plan_smem(Plan *p) {
     return true;
 }
 
+// TMA tensor copy: the innermost destination-ordered mode is contiguous on
+// both sides; the modes, innermost first, become the dimensions of a source
+// and a destination tensor map.  The box grows from the innermost dimension
+// outwards (at most 256 per dimension) while the tile stays within
+// kTmaTileBytes.
+constexpr int64_t kTmaMinRunBytes = 64;
+constexpr int64_t kTmaTileBytes = 16384;
+constexpr int kTmaStagesPlan = 4;
+
+bool plan_tma(Plan *p, const PtrInfo &ptr) {
+    const ModeList &sl = p->sorted;
+    const int w = p->w;
+    if (sl.n < 2 || sl.n > 5) return false;
+    const Mode &in = sl.m[sl.n - 1];
+    if (in.s != 1 || in.d != 1) return false;
+    if ((in.e * w) % 16 || in.e * w < kTmaMinRunBytes) return false;
+    const int mult = w == 16 ? 2 : 1;  // 16-byte words travel as two 8-byte elements
+    const int eb = w / mult;
+    if (in.e * mult >= (int64_t(1) << 31)) return false;
+    for (int i = 0; i + 1 < sl.n; ++i) {
+        const Mode &m = sl.m[i];
+        if (m.s <= 0 || m.d <= 0 || (m.s * w) % 16 || (m.d * w) % 16) return false;
+        if (m.s * w >= (int64_t(1) << 40) || m.d * w >= (int64_t(1) << 40) || m.e >= (int64_t(1) << 31)) return false;
+    }
+    if ((p->src_off * w) % 16 || (p->dst_off * w) % 16) return false;
+    if (ptr.check && (ptr.src % 16 || ptr.dst % 16)) return false;
+    TmaPlan &tp = p->tma;
+    tp = TmaPlan{};
+    tp.rank = sl.n;
+    int64_t dims[5];
+    for (int k = 0; k < sl.n; ++k) dims[k] = sl.m[sl.n - 1 - k].e * (k == 0 ? mult : 1);
+    tp.box[0] = static_cast<int>(std::min<int64_t>(dims[0], 256));
+    int64_t bytes = int64_t(tp.box[0]) * eb;
+    for (int k = 1; k < sl.n; ++k) {
+        const int64_t b = std::max<int64_t>(1, std::min<int64_t>({dims[k], 256, kTmaTileBytes / bytes}));
+        tp.box[k] = static_cast<int>(b);
+        bytes *= b;
+    }
+    uint64_t n_tiles = 1;
+    for (int k = 0; k < sl.n; ++k) n_tiles *= uint64_t((dims[k] + tp.box[k] - 1) / tp.box[k]);
+    if (n_tiles >= (uint64_t(1) << 32)) return false;
+    tp.stage_bytes = bytes;
+    p->tile = TilePlan{};
+    p->tile.R = tp.box[1];
+    p->tile.TY = tp.box[0];
+    p->tile.S = kTmaStagesPlan;
+    p->tile.threads = 32;
+    return true;
+}
+
 // A contiguous run of L words with L * w <= 16 bytes (a power of two) moves
 // as one wider word when every other stride, both offsets and both base
 // addresses allow it: the copy is then a permute of (L * w)-byte words.
@@ -462,7 +512,7 @@ int make_plan_core(const lc_tile_layout *src, const lc_tile_layout *dst, int32_t
     if ((st = check_layout(src)) || (st = check_layout(dst))) return st;
     if (!valid_width(w)) return LC_ERR_ELEM_BYTES;
     if (n_tiles < 0) return LC_ERR_SHAPE;
-    if (kernel < LC_KERNEL_AUTO || kernel > LC_KERNEL_SMEM_TRANSPOSE) return LC_ERR_UNSUPPORTED;
+    if (kernel < LC_KERNEL_AUTO || kernel > LC_KERNEL_TMA_COPY) return LC_ERR_UNSUPPORTED;
 
     Plan p;
     p.w = w;
@@ -533,6 +583,12 @@ int make_plan_core(const lc_tile_layout *src, const lc_tile_layout *dst, int32_t
         *out = p;
         return LC_OK;
     }
+    if (kernel == LC_KERNEL_TMA_COPY) {
+        if (!plan_tma(&p, ptr)) return LC_ERR_UNSUPPORTED;
+        p.kernel = kernel;
+        *out = p;
+        return LC_OK;
+    }
     if (kernel == LC_KERNEL_VEC_COPY) {
         p.kernel = kernel;
         *out = p;
@@ -552,6 +608,7 @@ int make_plan_core(const lc_tile_layout *src, const lc_tile_layout *dst, int32_t
         if (plan_tile(&p, ptr)) { p.kernel = LC_KERNEL_TILE_TRANSPOSE; *out = p; return LC_OK; }
         if (plan_smem(&p)) { p.kernel = LC_KERNEL_SMEM_TRANSPOSE; *out = p; return LC_OK; }
     }
+    if (run && plan_tma(&p, ptr)) { p.kernel = LC_KERNEL_TMA_COPY; *out = p; return LC_OK; }
     p.kernel = LC_KERNEL_VEC_COPY;
     *out = p;
     return LC_OK;

@@ -67,7 +67,7 @@ def test_plan_scale_factor_transpose(M):
 
 def test_plan_workloads(M):
     import workloads
-    expect = {1: "warp_permute", 3: "tile_transpose", 5: "vec_copy"}
+    expect = {1: "warp_permute", 3: "tile_transpose", 5: "tma_copy"}
     for cfg, kname in expect.items():
         c = workloads.config(cfg)
         assert M.plan(c["src"], c["dst"], c["elem_bytes"], c["n_tiles"])["kernel_name"] == kname
@@ -76,7 +76,9 @@ def test_plan_workloads(M):
         p = M.plan(c["src"], c["dst"], w, 1)
         assert p["kernel_name"] == "tile_transpose" and p["tile_cols"] * w == 128
     p = M.plan(workloads.config(5)["src"], workloads.config(5)["dst"], 2)
-    assert (p["vec"], p["run"]) == (8, 128)  # 16-byte vectors over 256-byte runs
+    assert (p["vec"], p["run"]) == (8, 128)  # the vector fallback: 16-byte vectors over 256-byte runs
+    # TMA boxes: the 128-word run, its 32 rows, 2 of the next mode (16 KiB)
+    assert (p["tile_cols"], p["tile_rows"], p["stages"]) == (128, 32, 4)
 
 
 def test_gmem_smem_partition_table(M):
@@ -300,6 +302,35 @@ def test_smem_transpose_swizzle_is_conflict_free_by_the_oracle(M):
                 reads = [(base + l) * RB + ((y * w) ^ (sw(base + l) * C)) for l in range(32)]
                 assert banks.access_degree(reads, w) == 1, (w, y)
         assert (p["conflicts_read"], p["conflicts_write"]) == (1, 1)
+
+
+def test_tma_copy_plans(M):
+    """The TMA tensor copy takes layouts whose innermost mode is contiguous on
+    both sides (at least 64 bytes, 16-byte multiples), at most 5 modes, all
+    other strides 16-byte multiples; everything else stays on other classes."""
+    T = M.TileLayout
+    perm = lambda w: M.plan(T((8, 3, 64), (192, 64, 1)), T((8, 3, 64), (64, 512, 1)), w)
+    for w in (1, 2, 4, 8, 16):
+        p = perm(w)
+        assert p["kernel_name"] == "tma_copy", w
+        eb = w if w < 16 else 8  # 16-byte words travel as two 8-byte TMA elements
+        assert p["tile_cols"] * eb == min(64 * w, 256 * eb)  # the whole 64-word run
+        assert p["tile_cols"] * eb * p["tile_rows"] <= 16384
+    # 48-byte runs: too short; 40 one-byte words: not a 16-byte multiple
+    assert M.plan(T((8, 3, 24), (72, 24, 1)), T((8, 3, 24), (24, 192, 1)), 2)["kernel_name"] == "vec_copy"
+    assert M.plan(T((8, 3, 40), (120, 40, 1)), T((8, 3, 40), (40, 320, 1)), 1)["kernel_name"] == "vec_copy"
+    # odd outer strides (not 16-byte multiples)
+    assert M.plan(T((8, 3, 64), (193, 64, 1)), T((8, 3, 64), (64, 512, 1)), 2)["kernel_name"] == "vec_copy"
+    # six modes after coalescing: beyond a tensor map's five dimensions
+    sh = (2, 2, 2, 2, 2, 64)
+    st = (64 * 32, 64 * 16, 64 * 8, 64 * 4, 64 * 2, 1)
+    dt = (64 * 2, 64 * 4, 64 * 8, 64 * 16, 64 * 32, 1)
+    assert M.plan(T(sh, st), T(sh, dt), 4)["kernel_name"] == "vec_copy"
+    # a single contiguous mode (an identity copy) stays on the vector copy
+    assert M.plan(T((4096,), (1,)), T((4096,), (1,)), 4)["kernel_name"] == "vec_copy"
+    # the forced class declines what it cannot take
+    with pytest.raises(M.LayoutCopyError):
+        M.plan(T((8, 3, 24), (72, 24, 1)), T((8, 3, 24), (24, 192, 1)), 2, kernel="tma_copy")
 
 
 def test_unaligned_transposes_plan_the_smem_transpose(M):

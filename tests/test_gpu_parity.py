@@ -98,7 +98,7 @@ def test_workload_small_auto(cfg, w):
     c = workloads.config(cfg, w, scale="small")
     name = run_case(c["src"], c["dst"], c["elem_bytes"], c["n_tiles"], seed=cfg)
     expect = {1: "warp_permute", 2: "warp_permute", 3: "tile_transpose", 4: "tile_transpose",
-              5: "vec_copy", 6: "smem_transpose"}[cfg]
+              5: "tma_copy", 6: "smem_transpose"}[cfg]
     assert name == expect
 
 
@@ -143,6 +143,26 @@ def test_smem_transpose_any_alignment(w):
     # misaligned base pointers: the automatic choice takes this path
     assert run_case(L((64, 96), (96, 1)), L((64, 96), (1, 64)), w, src_shift=w if w < 16 else 0,
                     dst_shift=0) in ("smem_transpose", "tile_transpose")
+
+
+@pytest.mark.parametrize("w", [1, 2, 4, 8, 16])
+def test_tma_copy_layouts(w):
+    # axis permutes that keep the last axis: boxes of whole runs, ragged outer modes
+    for sh, perm in [((8, 3, 64), (1, 0, 2)), ((5, 37, 3, 96), (2, 0, 1, 3)), ((7, 9, 48), (1, 0, 2)),
+                     ((3, 4, 5, 2, 64), (3, 2, 0, 1, 4))]:
+        if (sh[-1] * w) % 16 or sh[-1] * w < 64:
+            continue
+        assert run_case(L(sh, row_major(sh)), L(sh, permuted(sh, perm)), w, kernel="tma_copy",
+                        seed=sum(sh)) == "tma_copy"
+    # runs longer than one box (boxes of 256 elements, several per run)
+    sh = (6, 1024)
+    run_case(L(sh, (1040, 1)), L(sh, (1024 + 16, 1)), w, kernel="tma_copy", seed=w)
+    # strided slices with offsets and tiles spaced apart on both sides
+    run_case(L((10, 64), (96, 1), 32, 1280), L((10, 64), (80, 1), 16, 1024), w, n_tiles=5,
+             kernel="tma_copy", seed=3 * w)
+    # the automatic choice takes it for a head permute (B, S, H, D) -> (B, H, S, D)
+    sh = (2, 33, 6, 64)
+    assert run_case(L(sh, row_major(sh)), L(sh, permuted(sh, (0, 2, 1, 3))), w, seed=7) == "tma_copy"
 
 
 # ---------------------------------------------------------------------------
