@@ -107,7 +107,7 @@ def describe(cfg) -> str:
 def kernel_sources_sha(kernel_name: str) -> str:
     files = {"warp_permute": ["k_warp.cu"], "tile_transpose": ["k_tile.cu"],
              "vec_copy": ["k_vec.cu"], "smem_transpose": ["k_smem.cu"],
-             "tma_copy": ["k_tma_copy.cu"]}.get(kernel_name, [])
+             "tma_copy": ["k_tma_copy.cu"], "window_sum": ["k_stencil.cu"]}.get(kernel_name, [])
     h = hashlib.sha256()
     for f in files + ["ptx.cuh", "device_common.cuh"]:
         with open(os.path.join(ROOT, "movement_primitives_gb300", "csrc", f), "rb") as fh:
@@ -610,7 +610,8 @@ def run_window_sum(args):
                        "bytes_per_step": step_bytes, "l2": "inputs larger than L2, no flush"},
             "pct_of_peak": round(100.0 * value / peak, 2),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "traffic": None, "peak_kind": peak_kind},
+                         "frac": round(achieved / peak, 4), "traffic": profiled_traffic("window_sum", cfg["name"]),
+                         "peak_kind": peak_kind},
             "clocks": clocks, "gpu_launches": args.steps, "e2e": e2e, "cpu_baseline": None}
     print(json.dumps(line), flush=True)
     return 0

@@ -22,7 +22,7 @@
 
 namespace lc {
 
-constexpr int kTmaStages = 4;
+constexpr int kTmaStages = LC_TMA_STAGES;
 constexpr int kTmaThreads = 32;  // one warp; lane 0 issues every copy
 
 struct TmaCopyArgs {

@@ -50,7 +50,14 @@ struct TilePlan {
 
 // TMA tensor copy: the modes of the destination order, innermost first, as
 // tensor dimensions of both tensor maps; box[k] words of dimension k per tile
-// (in TMA elements: 16-byte words travel as two 8-byte elements).
+// (in TMA elements: 16-byte words travel as two 8-byte elements).  Ring
+// depth and tile size are compile-time knobs so that variants can be measured.
+#ifndef LC_TMA_STAGES
+#define LC_TMA_STAGES 6
+#endif
+#ifndef LC_TMA_TILE_BYTES
+#define LC_TMA_TILE_BYTES 16384
+#endif
 struct TmaPlan {
     int rank = 0;
     int box[5] = {0, 0, 0, 0, 0};

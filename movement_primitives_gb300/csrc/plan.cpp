@@ -429,8 +429,7 @@ bool plan_smem(Plan *p) {
 // outwards (at most 256 per dimension) while the tile stays within
 // kTmaTileBytes.
 constexpr int64_t kTmaMinRunBytes = 64;
-constexpr int64_t kTmaTileBytes = 16384;
-constexpr int kTmaStagesPlan = 4;
+constexpr int64_t kTmaTileBytes = LC_TMA_TILE_BYTES;
 
 bool plan_tma(Plan *p, const PtrInfo &ptr) {
     const ModeList &sl = p->sorted;
@@ -468,7 +467,7 @@ bool plan_tma(Plan *p, const PtrInfo &ptr) {
     p->tile = TilePlan{};
     p->tile.R = tp.box[1];
     p->tile.TY = tp.box[0];
-    p->tile.S = kTmaStagesPlan;
+    p->tile.S = LC_TMA_STAGES;
     p->tile.threads = 32;
     return true;
 }

@@ -78,7 +78,7 @@ def test_plan_workloads(M):
     p = M.plan(workloads.config(5)["src"], workloads.config(5)["dst"], 2)
     assert (p["vec"], p["run"]) == (8, 128)  # the vector fallback: 16-byte vectors over 256-byte runs
     # TMA boxes: the 128-word run, its 32 rows, 2 of the next mode (16 KiB)
-    assert (p["tile_cols"], p["tile_rows"], p["stages"]) == (128, 32, 4)
+    assert (p["tile_cols"], p["tile_rows"], p["stages"]) == (128, 32, 6)
 
 
 def test_gmem_smem_partition_table(M):

@@ -432,7 +432,7 @@ def test_host_buffers_errors():
 # window sum (cooperative fetch + stencil), against the oracle, bit for bit
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("window", [1, 2, 3, 7, 64])
+@pytest.mark.parametrize("window", [1, 2, 3, 4, 5, 6, 7, 64])
 def test_window_sum_matches_oracle(window):
     from oracle import stencil
     rng = np.random.default_rng(window)
@@ -454,5 +454,17 @@ def test_window_sum_unaligned_and_page_shape():
     # the page's shapes (1027 -> 1024), from a base that is not 16-byte aligned
     lc().window_sum(a[1:1028], b[1:], 3)
     assert np.array_equal(b[1:].cpu().numpy(), stencil.window_sum_f32(a_h[1:1028], 1024, 3))
+    # aligned input, output off the 16-byte grid (scalar stores), and the reverse
+    for win in (3, 5, 9):
+        n = 5000
+        a2_h = np.random.default_rng(win).standard_normal(n + win).astype(np.float32)
+        a2 = torch.from_numpy(a2_h).cuda()
+        b2 = torch.empty(n + 1, dtype=torch.float32, device="cuda")
+        lc().window_sum(a2[:n + win - 1], b2[1:], win)
+        assert np.array_equal(b2[1:].cpu().numpy().view(np.uint32),
+                              stencil.window_sum_f32(a2_h[:n + win - 1], n, win).view(np.uint32))
+        lc().window_sum(a2[1:n + win], b2[:n], win)
+        assert np.array_equal(b2[:n].cpu().numpy().view(np.uint32),
+                              stencil.window_sum_f32(a2_h[1:n + win], n, win).view(np.uint32))
     with pytest.raises(lc().LayoutCopyError):
         lc().window_sum(a, a[:1000], 3)  # overlapping ranges
