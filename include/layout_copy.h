@@ -180,8 +180,8 @@ int lc_layout_copy_ex(const void *src, const lc_tile_layout *src_layout,
 /* The copy between two HOST buffers.  The tiles are split into chunks that
  * are moved host -> device, permuted and moved device -> host through
  * `staging`, a caller-owned device buffer of at least staging_bytes bytes
- * (lc_host_staging_bytes gives the size for full pipelining, two chunk
- * slots).  Uploads, permutes and downloads run on two internal copy streams
+ * (lc_host_staging_bytes gives the size for full pipelining, three chunk
+ * slots; a smaller buffer gets smaller chunks).  Uploads, permutes and downloads run on two internal copy streams
  * and on `stream`, overlapped chunk by chunk and ordered by events; the work
  * is queued behind what `stream` already holds, and `stream` resumes after the
  * last download, so synchronising `stream` completes the copy.  Host buffers
@@ -197,9 +197,10 @@ int lc_layout_copy_host(const void *src_host, const lc_tile_layout *src_layout,
                         int32_t elem_bytes, int64_t n_tiles, void *staging,
                         int64_t staging_bytes, lc_stream_t stream);
 
-/* Staging bytes lc_layout_copy_host needs for this copy (two slots of about
- * an eighth of the tiles each when the tiles can be chunked, else the whole
- * source and destination spans); 0 for invalid arguments. */
+/* Staging bytes lc_layout_copy_host needs for this copy (three slots of a
+ * chunk of about 48 MiB of source tiles -- at least one tile, at most 1024
+ * chunks -- when the tiles can be chunked, else the whole source and
+ * destination spans); 0 for invalid arguments. */
 int64_t lc_host_staging_bytes(const lc_tile_layout *src_layout,
                               const lc_tile_layout *dst_layout,
                               int32_t elem_bytes, int64_t n_tiles);

@@ -2,9 +2,12 @@
 // transfers pipelined over chunks of tiles through a caller-provided device
 // staging buffer.  Chunk c moves host -> device on a copy stream, is permuted
 // on the caller's stream, and moves device -> host on a second copy stream;
-// two staging slots let chunk c+1's upload and chunk c-1's download run while
-// chunk c is permuted.  Events order the three streams; everything joins back
-// into the caller's stream before the call returns.
+// three staging slots let chunk c+1's upload and chunk c-1's download run
+// while chunk c is permuted, with one chunk of slack.  Chunks hold about LC_HOST_CHUNK_BYTES of source, so
+// the pipeline's fill (the first upload) and drain (the last download), which
+// run without the other direction, stay a small part of the call.  Events
+// order the three streams; everything joins back into the caller's stream
+// before the call returns.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -17,7 +20,30 @@
 namespace lc {
 namespace {
 
-constexpr int kSlots = 2;
+// Staging slots and source bytes per chunk (compile-time knobs so that
+// variants can be measured).  Measured on GB300 on a 1 GiB permute: two
+// slots leave the upload stream idle while chunk c-2's download waits for
+// its permute (310 GB/s at best); below about 32 MiB per chunk the per-chunk
+// cost of the copies and event hops (about 13 us) dominates; three slots of
+// 32-64 MiB reach 318-320 GB/s.
+#ifndef LC_HOST_SLOTS
+#define LC_HOST_SLOTS 3
+#endif
+#ifndef LC_HOST_CHUNK_BYTES
+#define LC_HOST_CHUNK_BYTES (48ll << 20)
+#endif
+constexpr int kSlots = LC_HOST_SLOTS;
+constexpr int64_t kChunkBytes = LC_HOST_CHUNK_BYTES;
+constexpr int64_t kMaxChunks = 1024;
+
+// Tiles per chunk: about kChunkBytes of source span (tile stride sts words of
+// w bytes), at least one tile, at most kMaxChunks chunks.
+int64_t default_chunk(int64_t n_tiles, int64_t sts, int64_t w) {
+    const int64_t tile_bytes = std::max<int64_t>(1, sts * w);
+    int64_t c = std::max<int64_t>(1, kChunkBytes / tile_bytes);
+    c = std::max(c, (n_tiles + kMaxChunks - 1) / kMaxChunks);
+    return std::min(c, n_tiles);
+}
 
 struct DeviceStreams {
     cudaStream_t up = nullptr, down = nullptr;
@@ -120,8 +146,7 @@ extern "C" int lc_layout_copy_host(const void *src_host, const lc_tile_layout *s
     int64_t chunk = n_tiles;
     int slots = 1;
     if (chunkable) {
-        // about eight chunks, two slots of staging
-        chunk = std::max<int64_t>(1, (n_tiles + 7) / 8);
+        chunk = default_chunk(n_tiles, std::max<int64_t>(sts, scos), w);
         while (chunk > 1 && kSlots * slot_bytes(chunk) > staging_bytes) chunk = (chunk + 1) / 2;
         slots = kSlots;
         if (kSlots * slot_bytes(chunk) > staging_bytes) {
@@ -199,7 +224,7 @@ extern "C" int64_t lc_host_staging_bytes(const lc_tile_layout *src_layout, const
     const int64_t dts = dst_layout->tile_stride ? dst_layout->tile_stride : dcos;
     auto round256 = [](int64_t b) { return (b + 255) / 256 * 256; };
     if (n_tiles > 1 && dts >= dcos) {
-        const int64_t chunk = std::max<int64_t>(1, (n_tiles + 7) / 8);
+        const int64_t chunk = default_chunk(n_tiles, std::max<int64_t>(sts, scos), w);
         const Span s = tile_span(*src_layout, w, scos, sts, 0, chunk);
         const Span d = tile_span(*dst_layout, w, dcos, dts, 0, chunk);
         return kSlots * (round256(s.hi - s.lo) + round256(d.hi - d.lo));
