@@ -311,6 +311,54 @@ int lc_last_device_error(lc_stream_t stream, uint64_t *detail);
  * LC_ERR_TIMEOUT. */
 int lc_debug_wait_timeout(int64_t timeout_ns, lc_stream_t stream);
 
+/* ---- P4's warp permute on shared-memory buffers ------------------------
+ * Apache TVM docs "permute_layout" define the permute as a warp-scope op
+ * between two layout-carrying buffers in shared memory, safe when they
+ * alias.  lc_warp_unit is one such op, planned on the host: the aligned
+ * modes of one unit (logical order, last mode fastest; strides in words),
+ * P = words per lane (the unit holds 32 * P words), and the XOR swizzle
+ * j = r ^ ((lane >> shift) & mask) chosen by the bank simulator.  The
+ * device side is in layout_copy_device.cuh (warp_unit_offsets,
+ * warp_unit_permute). */
+#define LC_WARP_UNIT_MAX_P 32
+
+typedef struct {
+    int32_t n_modes;
+    int32_t extent[LC_MAX_RANK];
+    int32_t src_stride[LC_MAX_RANK];
+    int32_t dst_stride[LC_MAX_RANK];
+    int32_t P, k, shift, mask;
+    int32_t conflicts_read, conflicts_write;  /* worst bank degree per phase */
+    int32_t src_cosize, dst_cosize;           /* words each buffer spans */
+} lc_warp_unit;
+
+/* Plans one warp-scope permute of a single tile (n_tiles = 1) between
+ * buffers with these layouts ("permute_layout", sections "What it accepts"
+ * and "Algorithm").  Host only.  Errors: as lc_layout_copy's validation;
+ * LC_ERR_SHAPE when the element count is not 32 * P with 1 <= P <=
+ * LC_WARP_UNIT_MAX_P, or a stride or span does not fit 31 bits;
+ * LC_ERR_NO_SWIZZLE when no (k, shift) is conflict-free -- `out` then holds
+ * the pair with the lowest worst degree and the op still runs correctly. */
+int lc_warp_unit_plan(const lc_tile_layout *src_layout, const lc_tile_layout *dst_layout,
+                      int32_t elem_bytes, lc_warp_unit *out);
+
+/* Runs the op on n_units units, each staged in shared memory.  src holds
+ * n_units source buffers back to back (unit i at i * src_cosize * elem_bytes
+ * bytes), dst likewise with dst_cosize.  One warp per unit copies the source
+ * buffer into shared buffer A and (in_place = 0) the destination buffer into
+ * shared buffer B, permutes A -> B (in_place = 0) or A -> A (in_place = 1,
+ * the aliased form: the destination layout is applied inside A, which needs
+ * src_cosize >= dst_cosize), and copies the destination buffer back to dst.
+ * Bytes of the destination buffer outside its image keep their values
+ * (in_place = 0) or hold A's (in_place = 1).  Each buffer must fit
+ * LC_WARP_UNIT_MAX_BYTES.  Asynchronous on `stream`.  Errors: LC_ERR_NULL,
+ * LC_ERR_SHAPE (buffers too large, bad counts), LC_ERR_ALIGN (pointers not
+ * 16-byte aligned), LC_ERR_OVERLAP (src and dst ranges overlap),
+ * LC_ERR_CUDA. */
+#define LC_WARP_UNIT_MAX_BYTES 8192
+int lc_warp_unit_run(const void *src, void *dst, const lc_warp_unit *unit, int32_t elem_bytes,
+                     int64_t n_units, int32_t in_place, lc_stream_t stream);
+
 /* Human-readable name of a status / kernel class (static strings). */
 const char *lc_status_string(int32_t status);
 const char *lc_kernel_name(int32_t kernel);

@@ -224,6 +224,42 @@ def plan(src_layout, dst_layout, elem_bytes: int, n_tiles: int = 1, kernel="auto
     return out
 
 
+def warp_unit_plan(src_layout, dst_layout, elem_bytes: int):
+    """Plan of P4's warp-scope permute between two shared-memory buffers
+    (lc_warp_unit_plan).  Returns (plan, info): `plan` is the C struct to pass
+    to warp_unit_run or to device code, `info` a dict of its fields plus
+    `conflict_free` (False when no XOR choice removes every bank conflict; the
+    plan still runs correctly)."""
+    sl, dl = TileLayout.of(src_layout).to_c(), TileLayout.of(dst_layout).to_c()
+    u = _lib.CWarpUnit()
+    st = _lib.lib().lc_warp_unit_plan(ctypes.byref(sl), ctypes.byref(dl), int(elem_bytes), ctypes.byref(u))
+    if st not in (0, STATUS["LC_ERR_NO_SWIZZLE"]):
+        _check(st, "warp_unit_plan")
+    n = u.n_modes
+    info = {f: getattr(u, f) for f, _ in _lib.CWarpUnit._fields_
+            if f not in ("extent", "src_stride", "dst_stride")}
+    info["modes"] = [(u.extent[i], u.src_stride[i], u.dst_stride[i]) for i in range(n)]
+    info["conflict_free"] = st == 0
+    return u, info
+
+
+def warp_unit_run(src, dst, plan, elem_bytes: int, n_units: int, in_place: bool = False, stream=None) -> None:
+    """Runs the warp-scope permute on n_units units staged in shared memory
+    (lc_warp_unit_run).  src / dst: CUDA uint8 tensors holding n_units source
+    (destination) buffers back to back, src_cosize (dst_cosize) words each."""
+    import torch
+    for t in (src, dst):
+        if not (isinstance(t, torch.Tensor) and t.is_cuda and t.is_contiguous()):
+            raise ValueError("pass contiguous CUDA tensors")
+    if src.numel() * src.element_size() < n_units * plan.src_cosize * elem_bytes:
+        raise ValueError("src holds fewer than n_units source buffers")
+    if dst.numel() * dst.element_size() < n_units * plan.dst_cosize * elem_bytes:
+        raise ValueError("dst holds fewer than n_units destination buffers")
+    _check(_lib.lib().lc_warp_unit_run(ctypes.c_void_p(src.data_ptr()), ctypes.c_void_p(dst.data_ptr()),
+                                       ctypes.byref(plan), int(elem_bytes), int(n_units), int(bool(in_place)),
+                                       ctypes.c_void_p(_stream_handle(stream))), "warp_unit_run")
+
+
 def choose_swizzle(src_layout, dst_layout, elem_bytes: int) -> dict:
     """The warp permute's XOR swizzle for one warp shard (see lc_choose_swizzle)."""
     sl, dl = TileLayout.of(src_layout).to_c(), TileLayout.of(dst_layout).to_c()

@@ -14,6 +14,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.environ.get("LC_LIBRARY_PATH") or os.path.join(HERE, "liblayoutcopy.so")
 MAX_RANK = 8
 STATIC_STAGING_BYTES = 32 * 1024 * 1024  # LC_STATIC_STAGING_BYTES
+WARP_UNIT_MAX_P = 32  # LC_WARP_UNIT_MAX_P
+WARP_UNIT_MAX_BYTES = 8192  # LC_WARP_UNIT_MAX_BYTES
 
 OK = 0
 STATUS_NAMES = {
@@ -54,6 +56,17 @@ class CPlanInfo(ctypes.Structure):
                 ("grid", ctypes.c_int32), ("block", ctypes.c_int32), ("smem_bytes", ctypes.c_int32)]
 
 
+class CWarpUnit(ctypes.Structure):
+    _R = MAX_RANK
+    _fields_ = [("n_modes", ctypes.c_int32),
+                ("extent", ctypes.c_int32 * _R), ("src_stride", ctypes.c_int32 * _R),
+                ("dst_stride", ctypes.c_int32 * _R),
+                ("P", ctypes.c_int32), ("k", ctypes.c_int32), ("shift", ctypes.c_int32),
+                ("mask", ctypes.c_int32), ("conflicts_read", ctypes.c_int32),
+                ("conflicts_write", ctypes.c_int32), ("src_cosize", ctypes.c_int32),
+                ("dst_cosize", ctypes.c_int32)]
+
+
 _P_LAYOUT = ctypes.POINTER(CTileLayout)
 _P_I32 = ctypes.POINTER(ctypes.c_int32)
 _P_I64 = ctypes.POINTER(ctypes.c_int64)
@@ -83,6 +96,9 @@ PROTOTYPES = {
                                               ctypes.c_int32, _P_I32, _P_I64]),
     "lc_last_device_error": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint64)]),
     "lc_debug_wait_timeout": (ctypes.c_int, [ctypes.c_int64, ctypes.c_void_p]),
+    "lc_warp_unit_plan": (ctypes.c_int, [_P_LAYOUT, _P_LAYOUT, ctypes.c_int32, ctypes.POINTER(CWarpUnit)]),
+    "lc_warp_unit_run": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(CWarpUnit),
+                                        ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p]),
     "lc_status_string": (ctypes.c_char_p, [ctypes.c_int32]),
     "lc_kernel_name": (ctypes.c_char_p, [ctypes.c_int32]),
 }

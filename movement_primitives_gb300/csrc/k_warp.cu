@@ -13,6 +13,7 @@
 
 #include "device_common.cuh"
 #include "launch.h"
+#include "layout_copy_device.cuh"
 
 namespace lc {
 
@@ -32,9 +33,7 @@ constexpr int kWarpSlotMax = 16 * 1024;  // the planner's units are at most 16 K
 struct WarpArgs {
     const uint8_t *src;  // address of source word offset 0
     uint8_t *dst;
-    int32_t un;  // unit modes, logical order (words)
-    int32_t ue[kMaxModes], us[kMaxModes], ud[kMaxModes];
-    int32_t P, shift, mask;
+    lc_warp_unit unit;  // unit modes (logical order, words), P, XOR swizzle
     uint32_t unit_bytes;
     int32_t nb;  // batch modes (BYTES strides), outermost first
     int64_t be[kMaxModes], bs[kMaxModes], bd[kMaxModes];
@@ -68,32 +67,13 @@ __device__ __forceinline__ int64_t unit_offset(const WarpArgs &a, int64_t u, con
 
 constexpr int kChunksInFlight = 8;  // 16-byte chunks each lane keeps in flight
 
-// Per-lane byte offsets, inside one unit, of the P words lane `lane` stages:
-// step r holds iteration j = r ^ ((lane >> shift) & mask), i.e. the logical
-// index unflatten(lane + 32 j) over the unit's extents (last mode fastest).
-template <int W, int PMAX>
-__device__ __forceinline__ void lane_offsets(const WarpArgs &a, int lane, int32_t (&soff)[PMAX],
-                                             int32_t (&doff)[PMAX]) {
-#pragma unroll
-    for (int r = 0; r < PMAX; ++r) {
-        int32_t flat = lane + 32 * (r ^ ((lane >> a.shift) & a.mask)), so = 0, dof = 0;
-        for (int i = a.un - 1; i >= 0; --i) {
-            const int32_t c = flat % a.ue[i];
-            flat /= a.ue[i];
-            so += c * a.us[i];
-            dof += c * a.ud[i];
-        }
-        soff[r] = so * W;
-        doff[r] = dof * W;
-    }
-}
-
 // Each warp owns a private shared-memory slot of G = units_per_stage units and
 // loops over groups of G consecutive units:
 //   in    the group's 16-byte chunks f = lane + 32 k are loaded (all loads
 //         issued before any shared store) and stored to the slot: the
 //         copy -> gmem_smem split [outer, threads = 32, vec = 16 bytes];
-//   P4    the two register-staged phases on every unit of the slot, in place;
+//   P4    the two register-staged phases on every unit of the slot, in place
+//         (lc_device::warp_unit_permute, the shared-buffer op of the ABI);
 //   out   the slot's chunks leave with 16-byte stores to the destination.
 // Only __syncwarp orders the phases; warps never wait for each other.
 // CONTIG: the units are packed back to back on both sides (one batch mode of
@@ -101,11 +81,10 @@ __device__ __forceinline__ void lane_offsets(const WarpArgs &a, int lane, int32_
 // address is base + 16 f; otherwise each chunk finds its unit by division.
 template <int W, int PMAX, bool CONTIG>
 __global__ void __launch_bounds__(kWarpThreads, LC_WARP_MIN_BLOCKS) k_warp_permute(const __grid_constant__ WarpArgs a) {
-    using T = typename Word<W>::T;
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int32_t soff[PMAX], doff[PMAX];
-    lane_offsets<W, PMAX>(a, lane, soff, doff);
+    lc_device::warp_unit_offsets<W, PMAX>(a.unit, lane, soff, doff);
     uint8_t *slot = smem + static_cast<size_t>(warp) * a.stage_bytes;
     const uint32_t cpu = a.unit_bytes / 16;  // chunks per unit
     const int64_t n_groups = (a.n_units + a.units_per_stage - 1) / a.units_per_stage;
@@ -141,15 +120,7 @@ __global__ void __launch_bounds__(kWarpThreads, LC_WARP_MIN_BLOCKS) k_warp_permu
         __syncwarp();
         for (int u = 0; u < cnt; ++u) {
             uint8_t *ub = slot + static_cast<size_t>(u) * a.unit_bytes;
-            T regs[PMAX];
-#pragma unroll
-            for (int r = 0; r < PMAX; ++r)
-                if (r < a.P) regs[r] = *reinterpret_cast<const T *>(ub + soff[r]);
-            __syncwarp();
-#pragma unroll
-            for (int r = 0; r < PMAX; ++r)
-                if (r < a.P) *reinterpret_cast<T *>(ub + doff[r]) = regs[r];
-            __syncwarp();
+            lc_device::warp_unit_permute<W, PMAX>(ub, ub, a.unit.P, soff, doff);
         }
         for (int f = lane; f < nchunks; f += 32) {
             uint8_t *p;
@@ -161,6 +132,52 @@ __global__ void __launch_bounds__(kWarpThreads, LC_WARP_MIN_BLOCKS) k_warp_permu
             }
             *reinterpret_cast<uint4 *>(p) = *reinterpret_cast<const uint4 *>(slot + 16 * f);
         }
+        __syncwarp();
+    }
+}
+
+// lc_warp_unit_run: P4's op between two shared-memory buffers, one warp per
+// unit.  The warp copies the unit's source buffer into shared buffer A (and
+// the destination buffer into B unless in place), permutes A -> B or A -> A
+// with lc_device::warp_unit_permute, and copies the destination buffer out.
+constexpr int kUnitWarps = 4;
+
+struct UnitArgs {
+    const uint8_t *src;
+    uint8_t *dst;
+    lc_warp_unit unit;
+    int64_t n_units;
+    uint32_t sbytes, dbytes;  // bytes of one source / destination buffer
+    uint32_t buf;             // shared bytes per buffer (16-byte multiple)
+    int32_t in_place;
+};
+
+// Byte copy by one warp: 16-byte words when both ends and the size allow.
+__device__ __forceinline__ void warp_copy(uint8_t *d, const uint8_t *s, uint32_t n, int lane) {
+    if (((reinterpret_cast<uintptr_t>(d) | reinterpret_cast<uintptr_t>(s) | n) & 15) == 0) {
+        for (uint32_t f = lane; f < n / 16; f += 32)
+            reinterpret_cast<uint4 *>(d)[f] = reinterpret_cast<const uint4 *>(s)[f];
+    } else {
+        for (uint32_t f = lane; f < n; f += 32) d[f] = s[f];
+    }
+}
+
+template <int W, int PMAX>
+__global__ void __launch_bounds__(kUnitWarps * 32) k_warp_unit_shared(const __grid_constant__ UnitArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint8_t *A = smem + static_cast<size_t>(warp) * 2 * a.buf;
+    uint8_t *B = A + a.buf;
+    int32_t soff[PMAX], doff[PMAX];
+    lc_device::warp_unit_offsets<W, PMAX>(a.unit, lane, soff, doff);
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kUnitWarps + warp; i < a.n_units;
+         i += static_cast<int64_t>(gridDim.x) * kUnitWarps) {
+        warp_copy(A, a.src + i * a.sbytes, a.sbytes, lane);
+        if (!a.in_place) warp_copy(B, a.dst + i * a.dbytes, a.dbytes, lane);
+        __syncwarp();
+        uint8_t *out = a.in_place ? A : B;
+        lc_device::warp_unit_permute<W, PMAX>(out, A, a.unit.P, soff, doff);
+        warp_copy(a.dst + i * a.dbytes, out, a.dbytes, lane);
         __syncwarp();
     }
 }
@@ -184,6 +201,25 @@ int launch_warp_t(const WarpArgs &a, cudaStream_t stream) {
     return finish_launch();
 }
 
+template <int W, int PMAX>
+int launch_unit_t(const UnitArgs &a, cudaStream_t stream) {
+    const void *fn = reinterpret_cast<const void *>(&k_warp_unit_shared<W, PMAX>);
+    const int smem = kUnitWarps * 2 * static_cast<int>(a.buf);
+    int sms, per;
+    if (prepare(fn, kUnitWarps * 32, smem, kUnitWarps * 2 * LC_WARP_UNIT_MAX_BYTES, &sms, &per) != cudaSuccess)
+        return LC_ERR_CUDA;
+    const int64_t grid = lmin((a.n_units + kUnitWarps - 1) / kUnitWarps, int64_t(sms) * std::max(per, 1));
+    k_warp_unit_shared<W, PMAX><<<static_cast<unsigned>(grid), kUnitWarps * 32, smem, stream>>>(a);
+    return finish_launch();
+}
+
+template <int W>
+int launch_unit_w(const UnitArgs &a, cudaStream_t s) {
+    if (a.unit.P <= 4) return launch_unit_t<W, 4>(a, s);
+    if (a.unit.P <= 8) return launch_unit_t<W, 8>(a, s);
+    return launch_unit_t<W, 32>(a, s);
+}
+
 template <int W>
 int launch_warp_w(int P, const WarpArgs &a, cudaStream_t s) {
     if (P <= 4) return launch_warp_t<W, 4>(a, s);
@@ -198,15 +234,17 @@ int launch_warp(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t st
     WarpArgs a{};
     a.src = src + p.src_off * p.w;
     a.dst = dst + p.dst_off * p.w;
-    a.un = wp.unit.n;
+    if (wp.unit.n > LC_MAX_RANK) return LC_ERR_UNSUPPORTED;  // the planner keeps it below
+    a.unit.n_modes = wp.unit.n;
     for (int i = 0; i < wp.unit.n; ++i) {
-        a.ue[i] = static_cast<int32_t>(wp.unit.m[i].e);
-        a.us[i] = static_cast<int32_t>(wp.unit.m[i].s);
-        a.ud[i] = static_cast<int32_t>(wp.unit.m[i].d);
+        a.unit.extent[i] = static_cast<int32_t>(wp.unit.m[i].e);
+        a.unit.src_stride[i] = static_cast<int32_t>(wp.unit.m[i].s);
+        a.unit.dst_stride[i] = static_cast<int32_t>(wp.unit.m[i].d);
     }
-    a.P = wp.P;
-    a.shift = wp.shift;
-    a.mask = wp.mask;
+    a.unit.P = wp.P;
+    a.unit.k = wp.k;
+    a.unit.shift = wp.shift;
+    a.unit.mask = wp.mask;
     a.unit_bytes = static_cast<uint32_t>(wp.U * p.w);
     a.nb = wp.batch.n;
     for (int i = 0; i < wp.batch.n; ++i) {
@@ -235,3 +273,57 @@ int launch_warp(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t st
 }
 
 }  // namespace lc
+
+// A caller-supplied plan is checked in full, so that every offset the kernel
+// forms stays inside its buffer: extents and strides consistent with P and
+// the cosizes, and the XOR keeping j below P.
+static bool unit_is_consistent(const lc_warp_unit &u) {
+    if (u.n_modes < 1 || u.n_modes > LC_MAX_RANK || u.P < 1 || u.P > LC_WARP_UNIT_MAX_P) return false;
+    int64_t total = 1, scos = 1, dcos = 1;
+    for (int i = 0; i < u.n_modes; ++i) {
+        if (u.extent[i] < 1 || u.src_stride[i] < 0 || u.dst_stride[i] < 0) return false;
+        total *= u.extent[i];
+        scos += int64_t(u.extent[i] - 1) * u.src_stride[i];
+        dcos += int64_t(u.extent[i] - 1) * u.dst_stride[i];
+    }
+    if (total != int64_t(32) * u.P || scos != u.src_cosize || dcos != u.dst_cosize) return false;
+    if (u.k < 0 || u.k > 5 || u.mask != (1 << u.k) - 1 || u.shift < 0 || u.shift > 31) return false;
+    if (u.mask >= u.P || (u.mask && (u.P & (u.P - 1)))) return false;  // j = r ^ (.. & mask) < P
+    return true;
+}
+
+extern "C" int lc_warp_unit_run(const void *src, void *dst, const lc_warp_unit *unit, int32_t elem_bytes,
+                                int64_t n_units, int32_t in_place, lc_stream_t stream) {
+    using namespace lc;
+    if (!unit) return LC_ERR_NULL;
+    if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8 && elem_bytes != 16)
+        return LC_ERR_ELEM_BYTES;
+    if (n_units < 0 || !unit_is_consistent(*unit)) return LC_ERR_SHAPE;
+    if (n_units == 0) return LC_OK;
+    if (!src || !dst) return LC_ERR_NULL;
+    const int64_t sb = int64_t(unit->src_cosize) * elem_bytes, db = int64_t(unit->dst_cosize) * elem_bytes;
+    if (sb > LC_WARP_UNIT_MAX_BYTES || db > LC_WARP_UNIT_MAX_BYTES) return LC_ERR_SHAPE;
+    if (in_place && unit->src_cosize < unit->dst_cosize) return LC_ERR_SHAPE;
+    if (reinterpret_cast<uintptr_t>(src) % 16 || reinterpret_cast<uintptr_t>(dst) % 16) return LC_ERR_ALIGN;
+    if (n_units > (int64_t(1) << 62) / std::max(sb, db)) return LC_ERR_OVERFLOW;
+    const uintptr_t s0 = reinterpret_cast<uintptr_t>(src), s1 = s0 + uintptr_t(n_units * sb);
+    const uintptr_t d0 = reinterpret_cast<uintptr_t>(dst), d1 = d0 + uintptr_t(n_units * db);
+    if (s0 < d1 && d0 < s1) return LC_ERR_OVERLAP;
+    UnitArgs a{};
+    a.src = static_cast<const uint8_t *>(src);
+    a.dst = static_cast<uint8_t *>(dst);
+    a.unit = *unit;
+    a.n_units = n_units;
+    a.sbytes = static_cast<uint32_t>(sb);
+    a.dbytes = static_cast<uint32_t>(db);
+    a.buf = static_cast<uint32_t>((std::max(sb, db) + 15) / 16 * 16);
+    a.in_place = in_place ? 1 : 0;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    switch (elem_bytes) {
+        case 1: return launch_unit_w<1>(a, cs);
+        case 2: return launch_unit_w<2>(a, cs);
+        case 4: return launch_unit_w<4>(a, cs);
+        case 8: return launch_unit_w<8>(a, cs);
+        default: return launch_unit_w<16>(a, cs);
+    }
+}

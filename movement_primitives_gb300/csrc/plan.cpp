@@ -338,7 +338,7 @@ bool plan_warp(Plan *p, const PtrInfo &ptr, bool need_conflict_free) {
         if (U > 32 * kWarp) break;
         if (U % kWarp == 0 && dense(lg, i, true) && dense(lg, i, false)) { first = i; break; }
     }
-    if (first < 0) return false;
+    if (first < 0 || lg.n - first > LC_MAX_RANK) return false;
     if ((U * w) % 16) return false;
     for (int i = 0; i < first; ++i)
         if ((lg.m[i].s * w) % 16 || (lg.m[i].d * w) % 16) return false;
@@ -829,4 +829,49 @@ extern "C" int lc_gmem_smem_partition(const lc_tile_layout *global_layout,
         }
     }
     return LC_ERR_SHAPE;
+}
+
+extern "C" int lc_warp_unit_plan(const lc_tile_layout *src_layout, const lc_tile_layout *dst_layout,
+                                 int32_t elem_bytes, lc_warp_unit *out) {
+    if (!src_layout || !dst_layout || !out) return LC_ERR_NULL;
+    if (!lc::valid_width(elem_bytes)) return LC_ERR_ELEM_BYTES;
+    for (int k = 0; k < src_layout->rank && k < LC_MAX_RANK; ++k)
+        if (src_layout->stride[k] < 0) return LC_ERR_BAD_STRIDE;
+    for (int k = 0; k < dst_layout->rank && k < LC_MAX_RANK; ++k)
+        if (dst_layout->shape[k] != 1 && dst_layout->stride[k] <= 0) return LC_ERR_BAD_STRIDE;
+    lc::ModeList unit;
+    int st = lc::align_shards(src_layout, dst_layout, &unit);
+    if (st) return st;
+    if (unit.n > LC_MAX_RANK) return LC_ERR_SHAPE;
+    int64_t total = 1;
+    for (int i = 0; i < unit.n; ++i) total *= unit.m[i].e;
+    if (total == 0 || total % 32 || total / 32 > LC_WARP_UNIT_MAX_P) return LC_ERR_SHAPE;
+    // word offsets and byte spans stay in 31 bits on the device
+    int64_t scos = 1, dcos = 1;
+    for (int i = 0; i < unit.n; ++i) {
+        scos += (unit.m[i].e - 1) * unit.m[i].s;
+        dcos += (unit.m[i].e - 1) * unit.m[i].d;
+    }
+    if (scos * elem_bytes >= (int64_t(1) << 31) || dcos * elem_bytes >= (int64_t(1) << 31)) return LC_ERR_SHAPE;
+    if ((st = lc::dst_injective(unit, total))) return st;
+    lc_warp_unit u;
+    std::memset(&u, 0, sizeof(u));
+    u.n_modes = unit.n;
+    for (int i = 0; i < unit.n; ++i) {
+        u.extent[i] = static_cast<int32_t>(unit.m[i].e);
+        u.src_stride[i] = static_cast<int32_t>(unit.m[i].s);
+        u.dst_stride[i] = static_cast<int32_t>(unit.m[i].d);
+    }
+    u.P = static_cast<int32_t>(total / 32);
+    int kk, ss, rd, wd;
+    const int bad = lc::choose_xor(unit, elem_bytes, &kk, &ss, &rd, &wd);
+    u.k = kk;
+    u.shift = ss;
+    u.mask = (1 << kk) - 1;
+    u.conflicts_read = rd;
+    u.conflicts_write = wd;
+    u.src_cosize = static_cast<int32_t>(scos);
+    u.dst_cosize = static_cast<int32_t>(dcos);
+    *out = u;
+    return bad ? LC_ERR_NO_SWIZZLE : LC_OK;
 }

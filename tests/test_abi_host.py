@@ -340,3 +340,54 @@ def test_unaligned_transposes_plan_the_smem_transpose(M):
         assert p["kernel_name"] == "smem_transpose", w
     # aligned ones keep the TMA path
     assert M.plan(T((64, 64), (64, 1)), T((64, 64), (1, 64)), 4, 1)["kernel_name"] == "tile_transpose"
+
+
+def test_warp_unit_plan_matches_the_page_and_the_oracle(M):
+    """P4's shared-buffer op, planned on the host: the worked example's shard
+    alignment and swizzle, and for random dense and strided units the same
+    alignment as the oracle's permute_align and the bank degrees the
+    oracle's simulator gives at the chosen (k, shift)."""
+    T = M.TileLayout
+    _, info = M.warp_unit_plan(T((4, 32), (32, 1)), T((4, 32), (1, 4)), 4)
+    assert info["modes"] == [(4, 32, 1), (32, 1, 4)]
+    assert (info["P"], info["k"], info["shift"], info["mask"]) == (4, 2, 3, 3)
+    assert info["conflict_free"] and (info["src_cosize"], info["dst_cosize"]) == (128, 128)
+    # the hand-worked rank-3 case with no conflict-free choice still plans
+    _, info = M.warp_unit_plan(T((2, 2, 16), (16, 32, 1)), T((2, 2, 16), (2, 1, 4)), 4)
+    assert not info["conflict_free"] and max(info["conflicts_read"], info["conflicts_write"]) == 2
+    rng = random.Random(11)
+    for _ in range(60):
+        rank = rng.randint(1, 3)
+        while True:
+            ext = [rng.choice([1, 2, 4, 8, 16, 32]) for _ in range(rank)]
+            total = int(np.prod(ext))
+            if total % 32 == 0 and total // 32 <= 32:
+                break
+        order_s, order_d = list(range(rank)), list(range(rank))
+        rng.shuffle(order_s)
+        rng.shuffle(order_d)
+
+        def strides(order, gap):
+            st, acc = [0] * rank, 1
+            for m in reversed(order):
+                st[m] = acc
+                acc *= ext[m] + gap
+            return st
+
+        src = T(ext, strides(order_s, rng.choice([0, 0, 1])))
+        dst = T(ext, strides(order_d, rng.choice([0, 0, 3])))
+        w = rng.choice([1, 2, 4, 8, 16])
+        _, info = M.warp_unit_plan(src, dst, w)
+        extent, sstr, dstr, P = index_maps.permute_align(src, dst)
+        assert info["modes"] == list(zip(extent, sstr, dstr)) and info["P"] == P
+        rd, wd = banks.phase_degrees(extent, sstr, dstr, w, info["k"], info["shift"])
+        assert (rd, wd) == (info["conflicts_read"], info["conflicts_write"])
+        assert info["conflict_free"] == (rd == 1 and wd == 1)
+    # P need not be a power of two (then only k = 0); shapes the op does not take
+    _, info = M.warp_unit_plan(T((3, 32), (32, 1)), T((3, 32), (1, 3)), 4)
+    assert (info["P"], info["k"]) == (3, 0)
+    for bad in [(T((33,), (1,)), T((33,), (1,))),               # not a multiple of 32
+                (T((64, 32), (32, 1)), T((64, 32), (1, 64))),   # P = 64 > LC_WARP_UNIT_MAX_P
+                (T((4, 32), (32, 1)), T((4, 32), (1, 2)))]:     # destination not injective
+        with pytest.raises(M.LayoutCopyError):
+            M.warp_unit_plan(*bad, 4)

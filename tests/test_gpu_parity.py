@@ -468,3 +468,82 @@ def test_window_sum_unaligned_and_page_shape():
                               stencil.window_sum_f32(a2_h[1:n + win], n, win).view(np.uint32))
     with pytest.raises(lc().LayoutCopyError):
         lc().window_sum(a, a[:1000], 3)  # overlapping ranges
+
+
+# ---------------------------------------------------------------------------
+# P4's warp-scope permute between shared-memory buffers (lc_warp_unit_run)
+# ---------------------------------------------------------------------------
+
+def _unit_layouts(rng):
+    rank = rng.randint(1, 3)
+    while True:
+        ext = [rng.choice([1, 2, 4, 8, 16, 32, 3]) for _ in range(rank)]
+        total = int(np.prod(ext))
+        if total % 32 == 0 and 1 <= total // 32 <= 32:
+            break
+    so, do = list(range(rank)), list(range(rank))
+    rng.shuffle(so)
+    rng.shuffle(do)
+
+    def strides(order, gap):
+        st, acc = [0] * rank, 1
+        for m in reversed(order):
+            st[m] = acc
+            acc *= ext[m] + gap
+        return st
+
+    return L(ext, strides(so, rng.choice([0, 0, 1]))), L(ext, strides(do, rng.choice([0, 0, 2])))
+
+
+@pytest.mark.parametrize("in_place", [False, True])
+def test_warp_unit_on_shared_buffers(in_place):
+    M = lc()
+    rng = random.Random(21 + in_place)
+    done = 0
+    while done < 40:
+        src_l, dst_l = _unit_layouts(rng)
+        w = rng.choice([1, 2, 4, 8, 16])
+        plan, info = M.warp_unit_plan(src_l, dst_l, w)
+        scos, dcos = info["src_cosize"], info["dst_cosize"]
+        if max(scos, dcos) * w > 8192 or (in_place and scos < dcos):
+            continue
+        n = rng.choice([1, 3, 37])
+        g = torch.Generator().manual_seed(done)
+        src_h = torch.randint(0, 256, (n * scos * w,), generator=g, dtype=torch.uint8)
+        if in_place:  # the destination buffer starts as the source buffer
+            start = np.concatenate([src_h.numpy()[i * scos * w:(i * scos + dcos) * w] for i in range(n)])
+        else:
+            start = np.full(n * dcos * w, workloads.SENTINEL, np.uint8)
+        want = start.copy()
+        oracle.copy(src_h.numpy(), dict(src_l, tile_stride=scos), want, dict(dst_l, tile_stride=dcos), w, n)
+        src_d = src_h.cuda()
+        dst_d = torch.from_numpy(start.copy()).cuda()
+        M.warp_unit_run(src_d, dst_d, plan, w, n, in_place=in_place,
+                        stream=torch.cuda.current_stream().cuda_stream)
+        torch.cuda.synchronize()
+        got = dst_d.cpu().numpy()
+        assert np.array_equal(got, want), (src_l, dst_l, w, n, info)
+        done += 1
+
+
+def test_warp_unit_run_refusals():
+    M = lc()
+    plan, _ = M.warp_unit_plan(L((4, 32), (32, 1)), L((4, 32), (1, 4)), 4)
+    buf = torch.zeros(4 * 128 * 4 + 16, dtype=torch.uint8, device="cuda")
+    out = torch.zeros(4 * 128 * 4 + 16, dtype=torch.uint8, device="cuda")
+    lib, stream = M._lib.lib(), torch.cuda.current_stream().cuda_stream
+    import ctypes
+    run = lambda s, d, n, ip=0, p=plan: lib.lc_warp_unit_run(ctypes.c_void_p(s), ctypes.c_void_p(d),
+                                                              ctypes.byref(p), 4, n, ip, ctypes.c_void_p(stream))
+    assert run(buf.data_ptr(), out.data_ptr(), 4) == 0
+    assert run(buf.data_ptr() + 4, out.data_ptr(), 4) == M.STATUS["LC_ERR_ALIGN"]
+    assert run(buf.data_ptr(), buf.data_ptr() + 16, 2) == M.STATUS["LC_ERR_OVERLAP"]
+    bad = M._lib.CWarpUnit.from_buffer_copy(plan)
+    bad.P = 5  # extents no longer hold 32 * P words
+    assert run(buf.data_ptr(), out.data_ptr(), 1, p=bad) == M.STATUS["LC_ERR_SHAPE"]
+    bad = M._lib.CWarpUnit.from_buffer_copy(plan)
+    bad.mask, bad.k = 7, 3  # the XOR would leave [0, P)
+    assert run(buf.data_ptr(), out.data_ptr(), 1, p=bad) == M.STATUS["LC_ERR_SHAPE"]
+    torch.cuda.synchronize()
+    st, detail = M.last_device_error()
+    assert st == 0, detail
