@@ -428,7 +428,16 @@ bool plan_smem(Plan *p) {
 // and a destination tensor map.  The box grows from the innermost dimension
 // outwards (at most 256 per dimension) while the tile stays within
 // kTmaTileBytes.
-constexpr int64_t kTmaMinRunBytes = 64;
+#ifndef LC_TMA_MIN_RUN_BYTES
+#define LC_TMA_MIN_RUN_BYTES 64
+#endif
+// Box split between the destination's and the source's next contiguous modes
+// for runs shorter than this many bytes (measured on GB300: head permutes
+// with 64- and 128-byte runs gain 16 % and 9 %; 256-byte runs lose 2-3 %).
+#ifndef LC_TMA_BALANCE_BELOW
+#define LC_TMA_BALANCE_BELOW 256
+#endif
+constexpr int64_t kTmaMinRunBytes = LC_TMA_MIN_RUN_BYTES;
 constexpr int64_t kTmaTileBytes = LC_TMA_TILE_BYTES;
 
 bool plan_tma(Plan *p, const PtrInfo &ptr) {
@@ -455,10 +464,32 @@ bool plan_tma(Plan *p, const PtrInfo &ptr) {
     for (int k = 0; k < sl.n; ++k) dims[k] = sl.m[sl.n - 1 - k].e * (k == 0 ? mult : 1);
     tp.box[0] = static_cast<int>(std::min<int64_t>(dims[0], 256));
     int64_t bytes = int64_t(tp.box[0]) * eb;
-    for (int k = 1; k < sl.n; ++k) {
-        const int64_t b = std::max<int64_t>(1, std::min<int64_t>({dims[k], 256, kTmaTileBytes / bytes}));
-        tp.box[k] = static_cast<int>(b);
-        bytes *= b;
+    for (int k = 1; k < sl.n; ++k) tp.box[k] = 1;
+    // Dimension 1 continues the run on the destination side; the dimension
+    // whose source stride equals the run continues it on the source side.
+    // When they differ and runs are short, the box splits its budget between
+    // the two, so that both sides move segments of several runs instead of
+    // one side moving isolated runs.
+    int ksrc = -1;
+    if (tp.box[0] == dims[0])
+        for (int k = 2; k < sl.n; ++k)
+            if (sl.m[sl.n - 1 - k].s == in.e) { ksrc = k; break; }
+    const int64_t budget = std::max<int64_t>(1, kTmaTileBytes / bytes);
+    if (ksrc > 1 && int64_t(tp.box[0]) * eb < LC_TMA_BALANCE_BELOW) {
+        int64_t bs = 1;
+        while ((bs * 2) * (bs * 2) <= budget) bs *= 2;
+        bs = std::min<int64_t>({bs, dims[ksrc], 256});
+        const int64_t b1 = std::max<int64_t>(1, std::min<int64_t>({dims[1], 256, budget / bs}));
+        bs = std::max<int64_t>(1, std::min<int64_t>({dims[ksrc], 256, budget / b1}));
+        tp.box[1] = static_cast<int>(b1);
+        tp.box[ksrc] = static_cast<int>(bs);
+        bytes *= b1 * bs;
+    } else {
+        for (int k = 1; k < sl.n; ++k) {
+            const int64_t b = std::max<int64_t>(1, std::min<int64_t>({dims[k], 256, kTmaTileBytes / bytes}));
+            tp.box[k] = static_cast<int>(b);
+            bytes *= b;
+        }
     }
     uint64_t n_tiles = 1;
     for (int k = 0; k < sl.n; ++k) n_tiles *= uint64_t((dims[k] + tp.box[k] - 1) / tp.box[k]);

@@ -331,6 +331,14 @@ def test_tma_copy_plans(M):
     # the forced class declines what it cannot take
     with pytest.raises(M.LayoutCopyError):
         M.plan(T((8, 3, 24), (72, 24, 1)), T((8, 3, 24), (24, 192, 1)), 2, kernel="tma_copy")
+    # runs under 256 bytes: the 16 KiB box splits between the destination's
+    # next mode (S) and the source's (H): 32 x 16 x 16 two-byte words for a
+    # (B, S, H, 32) -> (B, H, S, 32) permute; 256-byte runs keep the
+    # destination's next mode whole (32 rows)
+    p = M.plan(T((4, 64, 32, 32), (65536, 1024, 32, 1)), T((4, 64, 32, 32), (65536, 32, 2048, 1)), 2)
+    assert (p["kernel_name"], p["tile_cols"], p["tile_rows"]) == ("tma_copy", 32, 16)
+    p = M.plan(T((4, 64, 32, 128), (262144, 4096, 128, 1)), T((4, 64, 32, 128), (262144, 128, 8192, 1)), 2)
+    assert (p["kernel_name"], p["tile_cols"], p["tile_rows"]) == ("tma_copy", 128, 64)
 
 
 def test_unaligned_transposes_plan_the_smem_transpose(M):
