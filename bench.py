@@ -105,7 +105,7 @@ def describe(cfg) -> str:
 
 
 def kernel_sources_sha(kernel_name: str) -> str:
-    files = {"warp_permute": ["k_warp.cu"], "tile_transpose": ["k_tile.cu"],
+    files = {"warp_permute": ["k_warp.cu", "k_warp.cuh"] + ["k_warp_w%d.cu" % w for w in (1, 2, 4, 8, 16)], "tile_transpose": ["k_tile.cu"],
              "vec_copy": ["k_vec.cu"], "smem_transpose": ["k_smem.cu"],
              "tma_copy": ["k_tma_copy.cu"], "window_sum": ["k_stencil.cu"]}.get(kernel_name, [])
     h = hashlib.sha256()

@@ -1,0 +1,9 @@
+// Warp permute kernels for 16-byte words (see k_warp.cuh).
+#include "k_warp.cuh"
+
+namespace lc {
+
+int launch_warp_width16(int P, const WarpArgs &a, cudaStream_t s) { return launch_warp_w<16>(P, a, s); }
+int launch_unit_width16(const UnitArgs &a, cudaStream_t s) { return launch_unit_w<16>(a, s); }
+
+}  // namespace lc
