@@ -39,7 +39,7 @@ def nvcc() -> str:
 
 def _inputs():
     files = [os.path.join(CSRC, s) for s in SOURCES + HEADERS]
-    files.append(os.path.join(INCLUDE, "layout_copy.h"))
+    files += [os.path.join(INCLUDE, h) for h in ("layout_copy.h", "layout_copy_device.cuh")]
     files.append(os.path.abspath(__file__))
     return files
 

@@ -399,3 +399,22 @@ def test_warp_unit_plan_matches_the_page_and_the_oracle(M):
                 (T((4, 32), (32, 1)), T((4, 32), (1, 2)))]:     # destination not injective
         with pytest.raises(M.LayoutCopyError):
             M.warp_unit_plan(*bad, 4)
+
+
+def test_build_compiles_every_source():
+    """Every translation unit under csrc/ is in the build, every header it
+    includes is tracked for rebuilds, and the library exports no undefined
+    symbol of its own."""
+    import glob
+    import subprocess
+    from movement_primitives_gb300 import build as b
+    csrc = os.path.join(ROOT, "movement_primitives_gb300", "csrc")
+    units = sorted(os.path.basename(p) for p in glob.glob(os.path.join(csrc, "*.cu")) +
+                   glob.glob(os.path.join(csrc, "*.cpp")))
+    assert sorted(b.SOURCES) == units
+    headers = sorted(os.path.basename(p) for p in glob.glob(os.path.join(csrc, "*.h")) +
+                     glob.glob(os.path.join(csrc, "*.cuh")))
+    assert sorted(b.HEADERS) == headers
+    out = subprocess.run(["nm", "-D", "--undefined-only", b.LIB_PATH], capture_output=True, text=True).stdout
+    own = [line for line in out.splitlines() if "lc_" in line.split()[-1] or "_ZN2lc" in line]
+    assert not own, own
