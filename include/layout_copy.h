@@ -158,7 +158,7 @@ typedef struct {
  * In place: src and dst may be the same memory when every dense unit of the
  * warp-permute class is read and written at the same bytes (same base
  * address, equal batch and tile strides) -- the aliasing case of
- * "permute_layout" ("safe even when source and destination alias"); each
+ * "permute_layout" (its introduction: the permute tolerates aliased buffers); each
  * warp stages whole units before writing them back.  Any other overlap of
  * the two byte ranges is refused with LC_ERR_OVERLAP.
  * Errors: LC_ERR_NULL, _RANK, _SHAPE, _EXTENT_MISMATCH, _ELEM_BYTES,

@@ -20,7 +20,7 @@ Readings (the page leaves these open):
 * bank model "strict": as above, but distinct ELEMENTS in one bank count
   separately, so several sub-4-byte elements packed in one word conflict.
   This is the reading under which the page's remark holds that stride-1
-  sub-4-byte reads "pack several lanes into one bank" and can make the choice
+  reads of words under 4 bytes put several lanes in one bank and can make the choice
   fail; for 4-byte and wider elements the two models agree.
 Byte addresses are element offsets times the element size, relative to a
 128-byte-aligned base.

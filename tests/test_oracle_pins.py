@@ -407,7 +407,7 @@ def _dense_permute_cases():
 
 
 def test_four_byte_dense_transposes_admit_k():
-    """'4-byte dtypes always admit a valid k' (permute_layout, "How inputs change"),
+    """The page's claim that 4-byte words always admit a conflict-free k (permute_layout, "How inputs change"),
     read on the op's stated use, a transpose: every dense rank-1/rank-2 case."""
     cases = [c for c in _dense_permute_cases() if len(c[0]) <= 2]
     assert len(cases) > 50
