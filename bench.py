@@ -1,13 +1,19 @@
 """Benchmark of the strided tile layout copy on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload 1..5] [--elem-bytes W4] [--kernel auto|...]
+                    [--workload 1..7] [--elem-bytes W] [--kernel auto|vec_copy|
+                    warp_permute|tile_transpose|smem_transpose|tma_copy]
+                    [--graph] [--copy-ceiling] [--e2e-steps E] [--no-cpu-baseline]
 
 A step is one lc_layout_copy over the whole workload (one kernel launch);
 inputs are synthetic, seeded and resident in HBM; workloads smaller than
-twice the L2 get an L2 flush between steps.  Prints ONE JSON line on rank 0.  The default workload is the
-scale-factor transpose batch: 2^20 tiles of (pipe=2, high=1, 4, 32) fp32,
-strides (128,128,32,1) -> (128,128,1,4).
+twice the L2 get an L2 flush between steps.  Prints ONE JSON line on rank 0.
+The default workload is the scale-factor transpose batch: 2^20 tiles of
+(pipe=2, high=1, 4, 32) fp32, strides (128,128,32,1) -> (128,128,1,4).
+Workloads: 1 one 32x32 fp32 transpose; 2 the default; 3 a 16384^2 bf16
+transpose; 4 an 8192^2 transpose of W-byte words; 5 a (256,32,128,128) bf16
+permute (0,2,1,3); 6 an 8191 x 8193 transpose of W-byte words (strides off
+the 16-byte grid); 7 the window sum of three over 2^28 float32 outputs.
 
 --impl reference times the CPU oracle (the plain C word loop) on the host
 cores over a bounded sample of the same workload; it never touches a GPU.
