@@ -13,7 +13,17 @@
 namespace lc {
 
 constexpr int kVecThreads = 256;
-constexpr int kVecUnroll = 8;  // vectors in flight per thread
+// Vectors in flight per thread and the resident-CTA bound (compile-time knobs
+// so that variants can be measured).  On GB300, 12 in flight beat 8 by
+// 10-17 % on permutes with 32- to 256-byte runs; 32 (206 registers) and
+// fewer with more CTAs per SM were slower.
+#ifndef LC_VEC_UNROLL
+#define LC_VEC_UNROLL 12
+#endif
+#ifndef LC_VEC_MIN_BLOCKS
+#define LC_VEC_MIN_BLOCKS 1
+#endif
+constexpr int kVecUnroll = LC_VEC_UNROLL;  // vectors in flight per thread
 
 struct VecArgs {
     const uint8_t *src;  // address of source word offset 0
@@ -65,7 +75,7 @@ __device__ __forceinline__ void vec_offsets(const VecArgs &a, int64_t g, int64_t
 // access_idx % T, slot = access_idx / T).  All U loads are issued before the
 // U stores so that each thread keeps U vectors in flight.  Tails are guarded.
 template <int VB, bool WIDE>
-__global__ void __launch_bounds__(kVecThreads) k_vec_copy(const __grid_constant__ VecArgs a) {
+__global__ void __launch_bounds__(kVecThreads, LC_VEC_MIN_BLOCKS) k_vec_copy(const __grid_constant__ VecArgs a) {
     using T = typename Word<VB>::T;
     for (int64_t blk = blockIdx.x; blk < a.n_blocks; blk += gridDim.x) {
         const int64_t base = blk * (kVecUnroll * kVecThreads) + threadIdx.x;
