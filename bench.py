@@ -299,9 +299,17 @@ def cpu_baseline(cfg, src_np, seconds: float):
     sample = sampled(cfg, frac)
     t = sum(run_oracle(sample, src_np, dst, cores) for _ in range(passes))
     gbs = passes * workload_bytes(sample) / t / 1e9
+    # the same oracle on one thread, over a sample of a quarter of the time
+    frac1, passes1 = calibrate(cfg, src_np, dst, 1, seconds / 4)
+    sample1 = sampled(cfg, frac1)
+    t1 = sum(run_oracle(sample1, src_np, dst, 1) for _ in range(passes1))
+    gbs1 = passes1 * workload_bytes(sample1) / t1 / 1e9
     return dict(value=round(gbs, 3), unit=UNIT, cores=cores, kind="oracle",
                 sample="%d pass(es) over %.4f of the workload (%d logical words each), %.2f s on %d threads"
-                       % (passes, frac, workloads.logical_elems(sample), t, cores))
+                       % (passes, frac, workloads.logical_elems(sample), t, cores),
+                single_thread={"value": round(gbs1, 3), "unit": UNIT,
+                               "sample": "%d pass(es) over %.4f of the workload, %.2f s on 1 thread"
+                                         % (passes1, frac1, t1)})
 
 
 def run_reference(args):
