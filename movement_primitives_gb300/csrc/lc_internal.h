@@ -109,10 +109,27 @@ int choose_xor(const ModeList &unit, int w, int *k, int *shift, int *rd, int *wd
 struct SmemGeo {
     int C, RB, TX, TYW;
 };
+// Tile rows (TX) and words (TYW) per width: compile-time knobs so that
+// variants can be measured.
+#ifndef LC_SMEM_TX_W1
+#define LC_SMEM_TX_W1 64
+#endif
+#ifndef LC_SMEM_TYW_W1
+#define LC_SMEM_TYW_W1 252
+#endif
+#ifndef LC_SMEM_TX_W2
+#define LC_SMEM_TX_W2 64
+#endif
+#ifndef LC_SMEM_TYW_W2
+#define LC_SMEM_TYW_W2 124
+#endif
+#ifndef LC_SMEM_TX_W4
+#define LC_SMEM_TX_W4 64
+#endif
 constexpr SmemGeo smem_geometry(int w) {
-    return w == 1   ? SmemGeo{4, 256, 64, 252}
-           : w == 2 ? SmemGeo{4, 256, 64, 124}
-           : w == 4 ? SmemGeo{4, 256, 64, 64}
+    return w == 1   ? SmemGeo{4, 256, LC_SMEM_TX_W1, LC_SMEM_TYW_W1}
+           : w == 2 ? SmemGeo{4, 256, LC_SMEM_TX_W2, LC_SMEM_TYW_W2}
+           : w == 4 ? SmemGeo{4, 256, LC_SMEM_TX_W4, 64}
            : w == 8 ? SmemGeo{8, 512, 64, 64}
                     : SmemGeo{16, 512, 32, 32};
 }
