@@ -418,3 +418,17 @@ def test_build_compiles_every_source():
     out = subprocess.run(["nm", "-D", "--undefined-only", b.LIB_PATH], capture_output=True, text=True).stdout
     own = [line for line in out.splitlines() if "lc_" in line.split()[-1] or "_ZN2lc" in line]
     assert not own, own
+
+
+def test_planner_is_thread_safe(M):
+    """Plans from many host threads at once (the plan cache is shared)
+    equal the plans made one at a time."""
+    from concurrent.futures import ThreadPoolExecutor
+    import workloads
+    cfgs = [workloads.config(c, w, scale="small") for c, w in
+            [(1, None), (2, None), (3, None), (4, 1), (4, 8), (5, None), (6, 2)]]
+    args = [(c["src"], c["dst"], c["elem_bytes"], c["n_tiles"]) for c in cfgs] * 20
+    serial = [M.plan(*a) for a in args]
+    with ThreadPoolExecutor(16) as ex:
+        parallel = list(ex.map(lambda a: M.plan(*a), args))
+    assert parallel == serial

@@ -547,3 +547,32 @@ def test_warp_unit_run_refusals():
     torch.cuda.synchronize()
     st, detail = M.last_device_error()
     assert st == 0, detail
+
+
+def test_copies_capture_into_a_cuda_graph():
+    """After one call per kernel class (which sets the kernel attributes and
+    caches the plan), the copy launches nothing but its kernel on the given
+    stream, so it can be captured into a CUDA graph and replayed."""
+    M = lc()
+    cases = [workloads.config(2, scale="small"), workloads.config(3, scale="small"),
+             workloads.config(5, scale="small"), workloads.config(6, 2, scale="small")]
+    for cfg in cases:
+        src_h = workloads.make_src(cfg)
+        want = workloads.make_dst(cfg).numpy().copy()
+        oracle.copy(src_h.numpy(), cfg["src"], want, cfg["dst"], cfg["elem_bytes"], cfg["n_tiles"])
+        src = src_h.cuda()
+        dst = workloads.make_dst(cfg, device="cuda")
+        side = torch.cuda.Stream()
+        run = lambda: M.layout_copy_ptr(src.data_ptr(), cfg["src"], dst.data_ptr(), cfg["dst"],
+                                        cfg["elem_bytes"], cfg["n_tiles"], stream=side.cuda_stream)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            run()  # warm-up outside the capture
+        torch.cuda.synchronize()
+        dst.fill_(workloads.SENTINEL)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            run()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(dst.cpu().numpy(), want), cfg["name"]
