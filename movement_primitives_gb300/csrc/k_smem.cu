@@ -27,7 +27,8 @@
 // Addresses advance by constant strides per round, and the swizzle splits
 // into a per-thread part and a per-round constant: the bits of the thread's
 // first row and of the round's row offset are disjoint, and shift, mask and
-// XOR distribute over them.  The CTA walks tiles blockIdx.x + i * gridDim.x;
+// XOR distribute over them.  The CTA walks tiles blockIdx.x + i * gridDim.x
+// (X-blocks fastest);
 // tile i+1's loads are issued before tile i's copy 2, so they stay in flight
 // while the previous tile drains.
 #include <cuda_runtime.h>
@@ -93,13 +94,31 @@ struct TileRef {
     bool whole;
 };
 
+// Tile visiting order: 1 = X-block (destination row segment) fastest, so
+// that tiles sharing the partly written 32-byte sectors at the ends of each
+// destination row segment run close together; 0 = Y-block fastest.  Odd
+// destination strides leave such sectors at both ends of every segment; with
+// the X-block fastest they are completed in L2 before they leave it.
+// Measured on GB300 (8191 x 8193): 1-, 2-, 4-, 8-byte words 36 -> 48 %,
+// 49 -> 70 %, 77 -> 85 %, 90 -> 95 % of the copy peak against Y-block fastest.
+#ifndef LC_SMEM_X_FASTEST
+#define LC_SMEM_X_FASTEST 1
+#endif
+
 template <int W>
 __device__ __forceinline__ TileRef tile_ref(const SmemArgs &a, uint32_t ti) {
     using G = SmemCfg<W>;
+#if LC_SMEM_X_FASTEST
+    const uint32_t rest = fast_div(ti, a.tiles_x);
+    const uint32_t tx = ti - rest * a.tiles_x.d;
+    uint32_t b = fast_div(rest, a.tiles_y);
+    const uint32_t ty = rest - b * a.tiles_y.d;
+#else
     const uint32_t rest = fast_div(ti, a.tiles_y);  // Y-block fastest
     const uint32_t ty = ti - rest * a.tiles_y.d;
     uint32_t b = fast_div(rest, a.tiles_x);
     const uint32_t tx = rest - b * a.tiles_x.d;
+#endif
     const int64_t x0 = int64_t(tx) * G::TX, y0 = int64_t(ty) * G::TYW;
     const uint8_t *s = a.src + x0 * a.sX + y0 * W;
     uint8_t *d = a.dst + y0 * a.dY + x0 * W;
