@@ -1,6 +1,6 @@
 // TMA tile transpose: tensor tiles in a shared-memory ring (mbarrier
-// pipelined), 16-byte shared reads, in-register transpose of the sub-16-byte
-// words, 16-byte coalesced global stores.
+// pipelined; 128- or 256-byte box rows), 16-byte shared reads, in-register
+// transpose of the sub-16-byte words, 16-byte coalesced global stores.
 //
 // X is the mode contiguous in the destination, Y the one contiguous in the
 // source; up to three batch modes ride along as extra tensor dimensions.
@@ -40,23 +40,49 @@ namespace lc {
 #define LC_TILE_STAGES_WIDE 4
 #endif
 // 1: tiles visited Y-block (source column block) fastest, so CTAs running at
-// the same time read neighbouring 128-byte segments of the same source rows;
+// the same time read neighbouring box-row segments of the same source rows;
 // 0: X-block fastest.
 #ifndef LC_TILE_Y_FASTEST
 #define LC_TILE_Y_FASTEST 1
 #endif
 
+// Bytes per TMA box row (128 or 256) and ring stages per width, measured on
+// GB300: 256-byte rows with 3 stages move the 16384^2 bf16 transpose at
+// 91.8 % (128-byte rows, 4 stages: 90.1 %) and the 8192^2 eight-byte one at
+// 93.2 % (92.4 %); 1-byte words lose with them (61 % against 68 %), 4-byte
+// words slightly (83.7 % against 84.6 %).
+#ifndef LC_TILE_BOXB_W2
+#define LC_TILE_BOXB_W2 256
+#endif
+#ifndef LC_TILE_BOXB_W8
+#define LC_TILE_BOXB_W8 256
+#endif
+#ifndef LC_TILE_BOXB_OTHER
+#define LC_TILE_BOXB_OTHER 128
+#endif
+#ifndef LC_TILE_STAGES_W2
+#define LC_TILE_STAGES_W2 3
+#endif
+#ifndef LC_TILE_STAGES_W8
+#define LC_TILE_STAGES_W8 3
+#endif
+
 template <int W> struct TileCfg {
-    static constexpr int V = 16 / W;    // words per 16-byte chunk
-    static constexpr int TY = 128 / W;  // words per 128-byte tile row
+    static constexpr int BOXB = W == 2 ? LC_TILE_BOXB_W2 : W == 8 ? LC_TILE_BOXB_W8
+                              : LC_TILE_BOXB_OTHER;  // bytes per box row
+    static constexpr int CPR = BOXB / 16;      // 16-byte chunks per box row
+    static constexpr int V = 16 / W;           // words per 16-byte chunk
+    static constexpr int TY = BOXB / W;        // words per box row
     static constexpr int R = W == 1 ? LC_TILE_ROWS_W1 : W == 2 ? LC_TILE_ROWS_W2 : W == 4 ? LC_TILE_ROWS_W4
                            : W == 8 ? LC_TILE_ROWS_W8 : LC_TILE_ROWS_W16;  // source rows per tile
-    static constexpr int S = W == 1 ? LC_TILE_STAGES_W1 : LC_TILE_STAGES_WIDE;  // ring stages
-    static constexpr int TILE_BYTES = 128 * R;
-    static constexpr int MB = 8 * R / V;          // V-row x 16-byte micro-blocks
+    static constexpr int S = W == 1 ? LC_TILE_STAGES_W1 : W == 2 ? LC_TILE_STAGES_W2
+                           : W == 8 ? LC_TILE_STAGES_W8 : LC_TILE_STAGES_WIDE;  // ring stages
+    static constexpr int TILE_BYTES = BOXB * R;
+    static constexpr int MB = CPR * R / V;        // V-row x 16-byte micro-blocks
     static constexpr int NT = MB < 256 ? MB : 256;  // threads: at most one micro-block each per round
     static constexpr int SMEM = 128 + S * TILE_BYTES;
     static_assert(R <= 256 && R % V == 0, "TMA boxes hold at most 256 rows, whole micro-blocks");
+    static_assert((BOXB == 128 || BOXB == 256) && SMEM <= 227 * 1024, "box rows of 128 or 256 bytes, ring fits");
 };
 
 struct TileArgs {
@@ -162,13 +188,13 @@ __device__ __forceinline__ void tile_issue_load(const CUtensorMap *tmap, const T
     }
 }
 
-// Tile t = (batch, ty, tx), tx fastest: TMA brings source rows
-// [tx*R, tx*R + R) x words [ty*TY, ty*TY + TY) (128 bytes per row) into a
-// stage.  Micro-block mb = (row group mr = mb / 8, 16-byte chunk c = mb % 8):
-// V rows x 16 bytes, transposed in registers into V destination chunks,
-// destination rows ty*TY + c*V + q, words tx*R + mr*V .. + V.  The 8 lanes of
-// a 16-byte shared-memory wavefront read the 8 chunks of one 128-byte row,
-// i.e. all 32 banks once: conflict-free with no swizzle.
+// Tile t = (batch, ty, tx): TMA brings source rows [tx*R, tx*R + R) x words
+// [ty*TY, ty*TY + TY) (BOXB bytes per row) into a stage.  Micro-block mb =
+// (row group mr = mb / CPR, 16-byte chunk c = mb % CPR): V rows x 16 bytes,
+// transposed in registers into V destination chunks, destination rows
+// ty*TY + c*V + q, words tx*R + mr*V .. + V.  The 8 lanes of a 16-byte
+// shared-memory wavefront read 8 consecutive chunks of one box row, i.e. all
+// 32 banks once: conflict-free with no swizzle.
 template <int W>
 __global__ void __launch_bounds__(TileCfg<W>::NT)
     k_tile_transpose(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ TileArgs a) {
@@ -205,13 +231,13 @@ __global__ void __launch_bounds__(TileCfg<W>::NT)
             }
             const uint8_t *st = tiles + static_cast<size_t>(s) * C::TILE_BYTES;
             for (int mb = tid; mb < C::MB; mb += C::NT) {
-                const int c = mb & 7, mr = mb >> 3;
+                const int c = mb % C::CPR, mr = mb / C::CPR;
                 const int64_t x0 = tx * C::R + int64_t(mr) * V;
                 if (x0 >= a.eX) continue;  // rows past the tensor (TMA filled them)
                 uint32_t in[V][4], out[V][4];
 #pragma unroll
                 for (int r = 0; r < V; ++r) {
-                    const uint4 q = *reinterpret_cast<const uint4 *>(st + (mr * V + r) * 128 + c * 16);
+                    const uint4 q = *reinterpret_cast<const uint4 *>(st + (mr * V + r) * C::BOXB + c * 16);
                     in[r][0] = q.x; in[r][1] = q.y; in[r][2] = q.z; in[r][3] = q.w;
                 }
                 transpose_chunk<W>(in, out);
@@ -244,13 +270,15 @@ __global__ void __launch_bounds__(TileCfg<W>::NT)
     }
 }
 
-void tile_geometry(int w, int *rows, int *stages, int *threads) {
+void tile_geometry(int w, int *rows, int *cols, int *stages, int *threads) {
     switch (w) {
-        case 1: *rows = TileCfg<1>::R; *stages = TileCfg<1>::S; *threads = TileCfg<1>::NT; break;
-        case 2: *rows = TileCfg<2>::R; *stages = TileCfg<2>::S; *threads = TileCfg<2>::NT; break;
-        case 4: *rows = TileCfg<4>::R; *stages = TileCfg<4>::S; *threads = TileCfg<4>::NT; break;
-        case 8: *rows = TileCfg<8>::R; *stages = TileCfg<8>::S; *threads = TileCfg<8>::NT; break;
-        default: *rows = TileCfg<16>::R; *stages = TileCfg<16>::S; *threads = TileCfg<16>::NT; break;
+        case 1: *rows = TileCfg<1>::R; *cols = TileCfg<1>::TY; *stages = TileCfg<1>::S; *threads = TileCfg<1>::NT; break;
+        case 2: *rows = TileCfg<2>::R; *cols = TileCfg<2>::TY; *stages = TileCfg<2>::S; *threads = TileCfg<2>::NT; break;
+        case 4: *rows = TileCfg<4>::R; *cols = TileCfg<4>::TY; *stages = TileCfg<4>::S; *threads = TileCfg<4>::NT; break;
+        case 8: *rows = TileCfg<8>::R; *cols = TileCfg<8>::TY; *stages = TileCfg<8>::S; *threads = TileCfg<8>::NT; break;
+        default:
+            *rows = TileCfg<16>::R; *cols = TileCfg<16>::TY; *stages = TileCfg<16>::S; *threads = TileCfg<16>::NT;
+            break;
     }
 }
 
@@ -274,7 +302,7 @@ int launch_tile_t(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t 
         dims[2 + i] = static_cast<cuuint64_t>(b.e);
         strides[1 + i] = static_cast<cuuint64_t>(b.s * W);
     }
-    box[0] = static_cast<cuuint32_t>(128 / (W / mult));
+    box[0] = static_cast<cuuint32_t>(C::BOXB / (W / mult));
     box[1] = static_cast<cuuint32_t>(C::R);
     for (int i = 2; i < 5; ++i) box[i] = 1;
     for (int i = 0; i < 5; ++i) estr[i] = 1;

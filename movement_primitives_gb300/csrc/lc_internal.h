@@ -134,9 +134,9 @@ constexpr SmemGeo smem_geometry(int w) {
                     : SmemGeo{16, 512, 32, 32};
 }
 
-// TMA tile transpose geometry for w-byte words (source rows per tile, ring
-// stages, threads), from the kernel's own compile-time table.
-void tile_geometry(int w, int *rows, int *stages, int *threads);
+// TMA tile transpose geometry for w-byte words (source rows and words per
+// tile, ring stages, threads), from the kernel's own compile-time table.
+void tile_geometry(int w, int *rows, int *cols, int *stages, int *threads);
 
 // Shared tile swizzle of the shared-memory transpose for w-byte words:
 // smallest (mask, shift) that keeps both copies conflict-free.

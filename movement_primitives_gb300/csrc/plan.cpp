@@ -389,8 +389,7 @@ bool plan_tile(Plan *p, const PtrInfo &ptr) {
     if (tp.X.e > (int64_t(1) << 31) || tp.Y.e * (w == 16 ? 2 : 1) > (int64_t(1) << 31)) return false;
     if (!a16(p->src_off * w) || !a16(p->dst_off * w)) return false;
     if (ptr.check && (ptr.src % 16 || ptr.dst % 16)) return false;
-    tp.TY = 128 / w;
-    tile_geometry(w, &tp.R, &tp.S, &tp.threads);  // the kernel's per-width table
+    tile_geometry(w, &tp.R, &tp.TY, &tp.S, &tp.threads);  // the kernel's per-width table
     return true;
 }
 
