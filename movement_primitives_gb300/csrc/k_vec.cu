@@ -12,17 +12,23 @@
 
 namespace lc {
 
-constexpr int kVecThreads = 256;
-// Vectors in flight per thread and the resident-CTA bound (compile-time knobs
-// so that variants can be measured).  On GB300, 12 in flight beat 8 by
-// 10-17 % on permutes with 32- to 256-byte runs; 32 (206 registers) and
-// fewer with more CTAs per SM were slower.
+// Threads per CTA, vectors in flight per thread and the resident-CTA bound
+// (compile-time knobs so that variants can be measured).  On GB300, with
+// 512 MiB per side: 1024 threads x 4 vectors reached 88.5 % of the copy peak
+// on a bf16 (0,2,1,3) permute with 64-byte runs against 86.3 % for
+// 256 x 12, and gained 26 % on 16-byte runs and 6-10 % on strided gathers;
+// 1024 x 2, 1024 x 6, 768 x 4, 512 x 4 and 1024 x 4 held to 32 registers
+// (two CTAs per SM) were all slower.
+#ifndef LC_VEC_THREADS
+#define LC_VEC_THREADS 1024
+#endif
 #ifndef LC_VEC_UNROLL
-#define LC_VEC_UNROLL 12
+#define LC_VEC_UNROLL 4
 #endif
 #ifndef LC_VEC_MIN_BLOCKS
 #define LC_VEC_MIN_BLOCKS 1
 #endif
+constexpr int kVecThreads = LC_VEC_THREADS;
 constexpr int kVecUnroll = LC_VEC_UNROLL;  // vectors in flight per thread
 
 struct VecArgs {
