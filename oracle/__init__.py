@@ -11,7 +11,8 @@ Contents
   definition   the copy's definition (every logical index moves one raw word),
                with the word loop in plain C (copy_oracle.c)
   index_maps   flatten / unflatten / default loop partition (TileLang tutorial
-               "loop_mapping.py"); the [outer, threads, vec] partition and its
+               "loop_mapping.py") and its ``loop_layout=`` override, with the
+               override's serial replay; the [outer, threads, vec] partition and its
                serial loop (Apache TVM "copy -> gmem_smem"); the aligned warp
                permute and its two register-staged phases (Apache TVM
                "permute_layout")

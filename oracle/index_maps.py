@@ -10,6 +10,9 @@ TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).
   "copy -> gmem_smem", section "Algorithm" steps 1-3 and section "How inputs
   change the algorithm" (the ``[outer, threads, vec]`` split, the widest-first
   vector width, the serial loop of vector copies).
+* ``loop_layout_plan`` / ``loop_layout_sizes`` / ``default_loop_layout`` /
+  ``loop_layout_replay``: the same tutorial's ``loop_layout=`` override of
+  the default plan (module docstring), under the reading stated at them.
 * ``permute_align`` / ``permute_replay``: Apache TVM docs "permute_layout",
   section "Algorithm" steps 1 and 3 (the aligned ``extent``/``src_str``/
   ``dst_str``, ``P = prod(extent) / 32``, and the two register-staged phases
@@ -19,7 +22,7 @@ Pure-Python loops: these are meant for the small cases the pages show.
 """
 from __future__ import annotations
 
-from .definition import as_layout, paired_modes
+from .definition import as_layout, paired_modes, tile_strides
 
 WARP = 32
 
@@ -61,6 +64,104 @@ def plan(extents, num_thread: int, vector_size: int) -> dict:
         rnd, thread = divmod(group, num_thread)
         out[unflatten(flat, extents)] = (thread, rnd * vector_size + lane_in_vec)
     return out
+
+
+# ---------------------------------------------------------------------------
+# loop_layout= override of the default partition ("loop_mapping.py")
+# ---------------------------------------------------------------------------
+#
+# The page says only that a ``loop_layout=`` annotation on ``T.Parallel``
+# replaces the default plan above.  Reading: an override is again a map from
+# each iteration point to (thread, slot), given as modes
+# (extent, thread_stride, slot_stride), outermost first.  The point's
+# row-major flat index is read as mixed-radix digits over the modes' extents
+# (the last mode fastest); thread = sum(digit * thread_stride) and
+# slot = sum(digit * slot_stride).  An override must be an exact partition:
+# each non-unit mode feeds only the thread or only the slot, every point gets
+# its own (thread, slot), and the pairs fill [0, T) x [0, L).
+
+
+def _product(values) -> int:
+    n = 1
+    for v in values:
+        n *= v
+    return n
+
+
+def loop_layout_plan(extents, loop) -> dict:
+    """{iteration point: (thread, slot)} under the override ``loop``."""
+    total = _product(extents)
+    loop_extents = [m[0] for m in loop]
+    if _product(loop_extents) != total:
+        raise Decline("the loop layout covers %d points, the nest %d"
+                      % (_product(loop_extents), total))
+    out = {}
+    for flat in range(total):
+        digits = unflatten(flat, loop_extents)
+        thread = sum(c * m[1] for c, m in zip(digits, loop))
+        slot = sum(c * m[2] for c, m in zip(digits, loop))
+        out[unflatten(flat, extents)] = (thread, slot)
+    return out
+
+
+def loop_layout_sizes(extents, loop):
+    """(threads T, slots per thread L) of an exact partition; Decline otherwise."""
+    for e, ts, ss in loop:
+        if e < 0 or ts < 0 or ss < 0:
+            raise Decline("negative extent or stride in %r" % (loop,))
+        if e > 1 and (ts > 0) == (ss > 0):
+            raise Decline("mode %r must feed exactly one of thread and slot" % ((e, ts, ss),))
+    pm = loop_layout_plan(extents, loop)
+    if not pm:
+        return 0, 0
+    T = 1 + max(t for t, _ in pm.values())
+    L = 1 + max(s for _, s in pm.values())
+    if len(set(pm.values())) != len(pm) or T * L != len(pm):
+        raise Decline("%r is not an exact partition of %d points" % (loop, len(pm)))
+    return T, L
+
+
+def default_loop_layout(total: int, num_thread: int, vector_size: int):
+    """The default plan restated as an override.
+
+    Its three levels are digits of the flat index: the serial round
+    (total / (T * V), slot stride V), the thread (T, thread stride 1) and the
+    lane in the vector (V, slot stride 1).  Declines when T * V does not
+    divide the total: that is the page's guarded case, which no exact
+    partition expresses.
+    """
+    if total % (num_thread * vector_size):
+        raise Decline("%d points are not whole rounds of %d threads x %d"
+                      % (total, num_thread, vector_size))
+    return [(total // (num_thread * vector_size), 0, vector_size),
+            (num_thread, 1, 0), (vector_size, 0, 1)]
+
+
+def loop_layout_replay(src_words, dst_words, src_layout, dst_layout, loop,
+                       n_tiles: int = 1):
+    """Tile by tile, thread t moves its slots 0..L-1 in order: slot s of
+    thread t is the point the override maps to (t, s), and that point moves
+    one word from its source to its destination offset.
+
+    Python lists of words, for small cases.  Returns the trace
+    {(tile, flat index of the point): t * L + s}.
+    """
+    src_layout, dst_layout = as_layout(src_layout), as_layout(dst_layout)
+    modes = paired_modes(src_layout, dst_layout)
+    extents = [m[0] for m in modes]
+    T, L = loop_layout_sizes(extents, loop)
+    owner = {ts: idx for idx, ts in loop_layout_plan(extents, loop).items()}
+    sts, dts = tile_strides(src_layout, dst_layout)
+    trace = {}
+    for tile in range(n_tiles):
+        for t in range(T):
+            for s in range(L):
+                idx = owner[(t, s)]
+                so = src_layout.offset + tile * sts + project(idx, [m[1] for m in modes])
+                do = dst_layout.offset + tile * dts + project(idx, [m[2] for m in modes])
+                dst_words[do] = src_words[so]
+                trace[(tile, flatten(idx, extents))] = t * L + s
+    return trace
 
 
 # ---------------------------------------------------------------------------

@@ -266,11 +266,11 @@ def _parse_points(text):
             for p in text.split()]
 
 
-def check_loop_mapping_tables():
+def check_loop_mapping_tables(plan_fn=None):
     for line in _read_golden("loop_mapping_t8_v2.txt"):
         ext_s, used, per, t0, t1 = [c.strip() for c in line.split("|")]
         extents = tuple(int(v) for v in ext_s.strip("()").split(",") if v.strip())
-        pm = index_maps.plan(extents, 8, 2)
+        pm = (plan_fn or index_maps.plan)(extents, 8, 2)
         assert len({t for t, _ in pm.values()}) == int(used)
         owned = {}
         for idx in sorted(pm, key=lambda i: index_maps.flatten(i, extents)):
@@ -300,6 +300,110 @@ def test_loop_mapping_levels():
         # fewer points than threads: some threads get nothing (the page's guard case)
         if total < T * V:
             assert len({t for t, _ in pm.values()}) < T
+
+
+# ---------------------------------------------------------------------------
+# loop_layout= override (reading: modes (extent, thread_stride, slot_stride)
+# over the row-major flat index of the nest, an exact partition)
+# ---------------------------------------------------------------------------
+
+def _override_plan(extents, T, V):
+    total = int(np.prod(extents))
+    return index_maps.loop_layout_plan(extents, index_maps.default_loop_layout(total, T, V))
+
+
+def check_default_override_tables():
+    """The default plan written as an override reproduces the page's tables."""
+    check_loop_mapping_tables(_override_plan)
+
+
+def test_default_override_matches_page_tables():
+    check_default_override_tables()
+
+
+def check_override_hand_worked():
+    """Three overrides whose owners were worked out by hand."""
+    # blocked: thread t owns the 8 consecutive points 8t .. 8t + 7, in order
+    pm = index_maps.loop_layout_plan((64,), [(8, 1, 0), (8, 0, 1)])
+    assert [p for p in sorted(pm) if pm[p][0] == 0] == [(i,) for i in range(8)]
+    assert [p for p in sorted(pm, key=lambda q: pm[q][1]) if pm[p][0] == 1] == [(i,) for i in range(8, 16)]
+    # column per thread: point (i, j) goes to thread j, slot i
+    pm = index_maps.loop_layout_plan((8, 8), [(8, 0, 1), (8, 1, 0)])
+    assert pm[(0, 3)] == (3, 0) and pm[(5, 3)] == (3, 5) and pm[(7, 0)] == (0, 7)
+    # (a, b, c) -> thread 4b + c, slot a
+    pm = index_maps.loop_layout_plan((4, 4, 4), [(4, 0, 1), (4, 4, 0), (4, 1, 0)])
+    assert pm[(2, 1, 3)] == (7, 2) and pm[(3, 0, 0)] == (0, 3) and pm[(0, 3, 1)] == (13, 0)
+    # the default plan on 64 points, 8 threads, pairs: flat = 16 r + 2 t + v
+    # gives thread t and slot 2 r + v
+    pm = _override_plan((64,), 8, 2)
+    for flat in range(64):
+        r, rest = divmod(flat, 16)
+        t, v = divmod(rest, 2)
+        assert pm[(flat,)] == (t, 2 * r + v)
+
+
+def test_override_hand_worked():
+    check_override_hand_worked()
+
+
+def check_override_sizes():
+    """Compact thread and slot parts: T and L are the products of their
+    extents; gaps, collisions and mixed modes are refused."""
+    rng = random.Random(7)
+    for _ in range(60):
+        exts = [rng.choice([1, 2, 3, 4]) for _ in range(rng.randint(1, 4))]
+        kinds = [rng.randint(0, 1) for _ in exts]
+        loop, tstride, sstride = [None] * len(exts), 1, 1
+        for i in rng.sample(range(len(exts)), len(exts)):  # compact, in a random order
+            if kinds[i]:
+                loop[i] = (exts[i], tstride, 0)
+                tstride *= exts[i]
+            else:
+                loop[i] = (exts[i], 0, sstride)
+                sstride *= exts[i]
+        total = int(np.prod(exts))
+        assert index_maps.loop_layout_sizes((total,), loop) == (tstride, sstride)
+    for bad in ([(4, 2, 0), (4, 0, 1)],            # threads 0, 2, 4, 6: a gap
+                [(4, 1, 0), (4, 1, 0)],            # two points per thread-slot pair
+                [(4, 1, 1), (4, 0, 4)],            # a mode feeding both
+                [(4, 0, 0), (4, 1, 0)],            # a mode feeding neither
+                [(3, 0, 1), (4, 1, 0)]):           # 12 points for a 16-point nest
+        with pytest.raises(index_maps.Decline):
+            index_maps.loop_layout_sizes((16,), bad)
+    with pytest.raises(index_maps.Decline):
+        index_maps.default_loop_layout(60, 8, 2)   # the guarded case: 60 = 3 x 16 + 12
+
+
+def test_override_sizes():
+    check_override_sizes()
+
+
+def test_override_replay_matches_definition():
+    """Any exact override moves the same words as the definition; the trace
+    records each (thread, slot) pair exactly once per tile."""
+    cases = [
+        (Layout((8, 8), (8, 1)), Layout((8, 8), (1, 8)), [(8, 0, 1), (8, 1, 0)], 1),
+        (Layout((4, 16), (16, 1), 3), Layout((4, 16), (1, 4), 5), [(4, 1, 0), (8, 0, 2), (2, 0, 1)], 2),
+        (Layout((2, 1, 4, 32), (128, 128, 32, 1)), Layout((2, 1, 4, 32), (128, 128, 1, 4)),
+         index_maps.default_loop_layout(256, 64, 4), 3),
+        (Layout((6, 5), (5, 1), 0, 40), Layout((6, 5), (1, 6), 1, 31), [(6, 0, 1), (5, 1, 0)], 2),
+    ]
+    for src_l, dst_l, loop, n_tiles in cases:
+        n_src = src_l.offset + n_tiles * (src_l.tile_stride or definition.cosize(src_l)) + 64
+        n_dst = dst_l.offset + n_tiles * (dst_l.tile_stride or definition.cosize(dst_l)) + 64
+        src = list(range(1000, 1000 + n_src))
+        got = [-1] * n_dst
+        trace = index_maps.loop_layout_replay(src, got, src_l, dst_l, loop, n_tiles)
+        want = np.full(n_dst * 4, 0xFF, np.uint8)
+        definition.copy(np.asarray(src, np.uint32).view(np.uint8), src_l, want, dst_l, 4, n_tiles)
+        assert np.asarray(got, np.int64)[np.asarray(got) >= 0].tolist() == \
+            want.view(np.uint32)[np.asarray(got) >= 0].astype(np.int64).tolist()
+        assert ((want.view(np.uint32) != 0xFFFFFFFF) == (np.asarray(got) >= 0)).all()
+        extents = [m[0] for m in definition.paired_modes(src_l, dst_l)]
+        T, L = index_maps.loop_layout_sizes(extents, loop)
+        N = int(np.prod(extents))
+        assert sorted(trace.values()) == sorted(list(range(T * L)) * n_tiles)
+        assert len(trace) == n_tiles * N
 
 
 def test_flatten_unflatten_roundtrip_and_order():
@@ -489,7 +593,8 @@ def test_chosen_k_is_conflict_free():
 
 ALL_PINS = [check_definition_vs_numpy, check_transpose_vs_numpy, check_axis_permute_vs_numpy,
             check_gmem_smem_table, check_gmem_smem_alignment_rule, check_round_trip_identity,
-            check_loop_mapping_tables, check_sf_transpose_example,
+            check_loop_mapping_tables, check_default_override_tables, check_override_hand_worked,
+            check_override_sizes, check_sf_transpose_example,
             check_bank_degrees_worked_example, check_access_degree_closed_forms]
 
 
@@ -527,6 +632,7 @@ def _mut_paired_swapped(src, dst):
     "unflatten_transposed", "swizzle_dropped", "swizzle_shift_wrong_way",
     "pairing_swapped", "plan_thread_slot_swapped", "vec_ignores_offsets",
     "bank_counts_lanes_not_words", "project_drops_last_term",
+    "override_thread_slot_swapped", "override_digits_column_major",
 ])
 def test_planted_mistakes(monkeypatch, mutation):
     assert not _some_pin_fails()  # the unmutated oracle passes every pin
@@ -571,4 +677,20 @@ def test_planted_mistakes(monkeypatch, mutation):
             return sum(i * s for i, s in zip(idx[:-1], strides[:-1]))
         monkeypatch.setattr(index_maps, "project", bad_project)
         monkeypatch.setattr(banks, "project", bad_project)
+    elif mutation == "override_thread_slot_swapped":
+        orig = index_maps.loop_layout_plan
+
+        def bad_override(extents, loop):
+            return {k: (s, t) for k, (t, s) in orig(extents, loop).items()}
+        monkeypatch.setattr(index_maps, "loop_layout_plan", bad_override)
+    elif mutation == "override_digits_column_major":
+        def bad_override(extents, loop):
+            out = {}
+            for flat in range(int(np.prod(extents))):
+                digits = _mut_unflatten_transposed(flat, [m[0] for m in loop])
+                out[index_maps.unflatten(flat, extents)] = (
+                    sum(c * m[1] for c, m in zip(digits, loop)),
+                    sum(c * m[2] for c, m in zip(digits, loop)))
+            return out
+        monkeypatch.setattr(index_maps, "loop_layout_plan", bad_override)
     assert _some_pin_fails(), mutation
