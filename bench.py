@@ -1,8 +1,9 @@
 """Benchmark of the strided tile layout copy on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload 1..7] [--elem-bytes W] [--kernel auto|vec_copy|
+                    [--workload 1..8] [--elem-bytes W] [--kernel auto|vec_copy|
                     warp_permute|tile_transpose|smem_transpose|tma_copy]
+                    [--loop "[(extent, thread_stride, slot_stride), ...]"]
                     [--graph] [--copy-ceiling] [--e2e-steps E] [--no-cpu-baseline]
 
 A step is one lc_layout_copy over the whole workload (one kernel launch);
@@ -13,7 +14,9 @@ The default workload is the scale-factor transpose batch: 2^20 tiles of
 Workloads: 1 one 32x32 fp32 transpose; 2 the default; 3 a 16384^2 bf16
 transpose; 4 an 8192^2 transpose of W-byte words; 5 a (256,32,128,128) bf16
 permute (0,2,1,3); 6 an 8191 x 8193 transpose of W-byte words (strides off
-the 16-byte grid); 7 the window sum of three over 2^28 float32 outputs.
+the 16-byte grid); 7 the window sum of three over 2^28 float32 outputs;
+8 workload 5's permute as 256 tiles moved under an explicit loop layout
+(lc_layout_copy_loop; --loop replaces the workload's override).
 
 --impl reference times the CPU oracle (the plain C word loop) on the host
 cores over a bounded sample of the same workload; it never touches a GPU.
@@ -59,6 +62,8 @@ def parse_args(argv=None):
                    help="also time a plain device copy of the same byte count (same L2 policy)")
     p.add_argument("--graph", action="store_true",
                    help="replay the K timed launches from one CUDA graph (launch-bound copies)")
+    p.add_argument("--loop", default=None,
+                   help="loop layout for workload 8, a Python literal list of (extent, thread_stride, slot_stride)")
     p.add_argument("--n-tiles", type=int, default=None,
                    help="override the tile count (a smaller case of the same kernel, e.g. for ncu)")
     return p.parse_args(argv)
@@ -113,7 +118,8 @@ def describe(cfg) -> str:
 def kernel_sources_sha(kernel_name: str) -> str:
     files = {"warp_permute": ["k_warp.cu", "k_warp.cuh"] + ["k_warp_w%d.cu" % w for w in (1, 2, 4, 8, 16)], "tile_transpose": ["k_tile.cu"],
              "vec_copy": ["k_vec.cu"], "smem_transpose": ["k_smem.cu"],
-             "tma_copy": ["k_tma_copy.cu"], "window_sum": ["k_stencil.cu"]}.get(kernel_name, [])
+             "tma_copy": ["k_tma_copy.cu"], "window_sum": ["k_stencil.cu"],
+             "loop_copy": ["k_loop.cu"]}.get(kernel_name, [])
     h = hashlib.sha256()
     for f in files + ["ptx.cuh", "device_common.cuh"]:
         with open(os.path.join(ROOT, "movement_primitives_gb300", "csrc", f), "rb") as fh:
@@ -378,11 +384,25 @@ def run_ours(args):
     dst = workloads.make_dst(cfg, device=dev)
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
-    plan = lc.plan(cfg["src"], cfg["dst"], cfg["elem_bytes"], cfg["n_tiles"], args.kernel)
+    loop = cfg.get("loop")
+    if loop is not None and args.loop:
+        import ast
+        loop = [tuple(m) for m in ast.literal_eval(args.loop)]
+    if loop is not None:
+        kernel_name = "loop_copy"
+    else:
+        kernel_name = lc.plan(cfg["src"], cfg["dst"], cfg["elem_bytes"], cfg["n_tiles"], args.kernel)["kernel_name"]
+
+    def launch(stream_handle):
+        if loop is not None:
+            lc.layout_copy_loop_ptr(src.data_ptr(), cfg["src"], dst.data_ptr(), cfg["dst"], cfg["elem_bytes"],
+                                    loop, cfg["n_tiles"], 0, stream_handle)
+        else:
+            lc.layout_copy_ptr(src.data_ptr(), cfg["src"], dst.data_ptr(), cfg["dst"], cfg["elem_bytes"],
+                               cfg["n_tiles"], kernel=args.kernel, stream=stream_handle)
 
     def step():
-        lc.layout_copy_ptr(src.data_ptr(), cfg["src"], dst.data_ptr(), cfg["dst"], cfg["elem_bytes"],
-                           cfg["n_tiles"], kernel=args.kernel, stream=sh)
+        launch(sh)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -414,8 +434,7 @@ def run_ours(args):
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=cap):
             for _ in range(args.steps):
-                lc.layout_copy_ptr(src.data_ptr(), cfg["src"], dst.data_ptr(), cfg["dst"], cfg["elem_bytes"],
-                                   cfg["n_tiles"], kernel=args.kernel, stream=cap.cuda_stream)
+                launch(cap.cuda_stream)
         stream.wait_stream(cap)
         graph.replay()
     barrier()
@@ -456,7 +475,31 @@ def run_ours(args):
     # pinned host destination out; uploads, permutes and downloads pipelined
     # by the library over chunks of tiles, all inside the timed region
     e2e = None
-    if args.e2e_steps > 0:
+    if args.e2e_steps > 0 and loop is not None:
+        # no host-buffer form of the loop copy: pinned upload, the copy, pinned
+        # download, in order on the stream, every step
+        src_pin = src_h.pin_memory()
+        dst_pin = torch.empty(dst.numel(), dtype=torch.uint8).pin_memory()
+        for it in range(args.e2e_steps + 2):
+            if it == 2:
+                barrier()
+                torch.cuda.synchronize()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            src.copy_(src_pin, non_blocking=True)
+            launch(sh)
+            dst_pin.copy_(dst, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, dev)
+        if not torch.equal(dst_pin[:1 << 20], dst[:1 << 20].cpu()):
+            raise RuntimeError("end-to-end result differs from the device result")
+        e2e = {"value": round(world * step_bytes / (e2e_ms / 1e3) / 1e9, 2), "unit": UNIT,
+               "h2d_bytes_per_step": src.numel() * src.element_size(),
+               "d2h_bytes_per_step": dst.numel() * dst.element_size(),
+               "path": "pinned upload, lc_layout_copy_loop, pinned download (one stream, not pipelined)"}
+    elif args.e2e_steps > 0:
         src_pin = src_h.pin_memory()
         dst_pin = torch.empty(dst.numel(), dtype=torch.uint8).pin_memory()
         staging = torch.empty(max(256, lc.host_staging_bytes(cfg["src"], cfg["dst"], cfg["elem_bytes"],
@@ -506,7 +549,7 @@ def run_ours(args):
 
     peak, peak_kind = measured_peak()
     achieved = step_bytes / (launch_ms / 1e3) / 1e9
-    traffic = profiled_traffic(plan["kernel_name"], cfg["name"])
+    traffic = profiled_traffic(kernel_name, cfg["name"])
     if rank == 0:
         cpu = None if args.no_cpu_baseline else cpu_baseline(cfg, src_h.numpy(), args.cpu_seconds)
         value = world * step_bytes * args.steps / (elapsed_ms / 1e3) / 1e9
@@ -517,7 +560,8 @@ def run_ours(args):
             "launch_ms_median": round(launch_median_ms, 5) if launch_median_ms is not None else None,
             "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": dtype_name(cfg), "data": "synthetic",
-            "config": {"workload": describe(cfg), "kernel": plan["kernel_name"],
+            "config": {"workload": describe(cfg), "kernel": kernel_name,
+                       "loop_layout": loop,
                        "bytes_per_step": step_bytes,
                        "l2": ("L2 flushed between steps (%d MiB write outside the timed launches; "
                               "value from per-launch CUDA events)" % (2 * workloads.HBM_L2_BYTES >> 20)
@@ -605,7 +649,31 @@ def run_window_sum(args):
     value = step_bytes * args.steps / (elapsed / 1e3) / 1e9
     achieved = step_bytes / (launch_ms / 1e3) / 1e9
     e2e = None
-    if args.e2e_steps > 0:
+    if args.e2e_steps > 0 and loop is not None:
+        # no host-buffer form of the loop copy: pinned upload, the copy, pinned
+        # download, in order on the stream, every step
+        src_pin = src_h.pin_memory()
+        dst_pin = torch.empty(dst.numel(), dtype=torch.uint8).pin_memory()
+        for it in range(args.e2e_steps + 2):
+            if it == 2:
+                barrier()
+                torch.cuda.synchronize()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            src.copy_(src_pin, non_blocking=True)
+            launch(sh)
+            dst_pin.copy_(dst, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, dev)
+        if not torch.equal(dst_pin[:1 << 20], dst[:1 << 20].cpu()):
+            raise RuntimeError("end-to-end result differs from the device result")
+        e2e = {"value": round(world * step_bytes / (e2e_ms / 1e3) / 1e9, 2), "unit": UNIT,
+               "h2d_bytes_per_step": src.numel() * src.element_size(),
+               "d2h_bytes_per_step": dst.numel() * dst.element_size(),
+               "path": "pinned upload, lc_layout_copy_loop, pinned download (one stream, not pipelined)"}
+    elif args.e2e_steps > 0:
         a_pin, o_pin = a_h.pin_memory(), torch.empty(n, dtype=torch.float32).pin_memory()
         for it in range(args.e2e_steps + 1):
             if it == 1:

@@ -78,7 +78,8 @@ typedef enum {
     LC_ERR_TIMEOUT = 12,        /* a bounded device wait gave up */
     LC_ERR_UNSUPPORTED = 13,    /* a forced kernel class cannot take this copy */
     LC_ERR_OVERFLOW = 14,       /* an offset does not fit in 63 bits */
-    LC_ERR_STAGING = 15         /* a staging buffer is too small */
+    LC_ERR_STAGING = 15,        /* a staging buffer is too small */
+    LC_ERR_LOOP_LAYOUT = 16     /* a loop layout is not an exact partition */
 } lc_status;
 
 /* Kernel classes (the planner picks one; lc_layout_copy_ex can force one). */
@@ -120,7 +121,7 @@ typedef enum {
      * of 16 bytes, at most 5 modes.  Boxes of whole inner modes (about
      * 16 KiB) go global -> shared by TMA tensor loads and shared -> global by
      * TMA tensor stores through a second tensor map with the destination
-     * strides; one thread per CTA drives a 4-stage ring.  Axis permutes that
+     * strides; one thread per CTA drives a 6-stage ring.  Axis permutes that
      * keep the last axis, strided slices, row gathers. */
     LC_KERNEL_TMA_COPY = 5
 } lc_kernel;
@@ -358,6 +359,77 @@ int lc_warp_unit_plan(const lc_tile_layout *src_layout, const lc_tile_layout *ds
 #define LC_WARP_UNIT_MAX_BYTES 8192
 int lc_warp_unit_run(const void *src, void *dst, const lc_warp_unit *unit, int32_t elem_bytes,
                      int64_t n_units, int32_t in_place, lc_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Loop-layout override of the default partition (TileLang tutorial
+ * "loop_mapping.py", module docstring).  The default plan flattens the nest
+ * row-major, groups vector_size consecutive points, rotates the groups over
+ * num_thread threads and turns the rest into a per-thread serial loop; a
+ * ``loop_layout=`` annotation replaces that plan.  The page says no more, so
+ * this library reads an override as follows.
+ *
+ * The nest is one tile's logical box (the non-unit extents both layouts
+ * share, in logical order).  A point's row-major flat index is read as
+ * mixed-radix digits over the loop layout's extents (mode 0 slowest) and
+ *     thread = sum_k digit_k * thread_stride[k],
+ *     slot   = sum_k digit_k * slot_stride[k].
+ * The override must be an exact partition: the extents multiply to the
+ * tile's element count N, each non-unit mode has exactly one of its two
+ * strides non-zero, and the thread modes and the slot modes, each sorted by
+ * stride, form mixed radices (the smallest stride 1, each next stride the
+ * previous stride times its extent).  Then the points fill
+ * [0, T) x [0, L) with T * L = N, T the product of the thread extents and L
+ * of the slot extents, one point per (thread, slot).  The default plan is
+ * the override (N / (T V): slot stride V), (T: thread stride 1),
+ * (V: slot stride 1) -- lc_loop_layout_default.
+ * ------------------------------------------------------------------------- */
+#define LC_LOOP_MAX_THREADS 1024
+
+typedef struct {
+    int32_t rank;                       /* 1..LC_MAX_RANK */
+    int64_t shape[LC_MAX_RANK];         /* >= 0 */
+    int64_t thread_stride[LC_MAX_RANK]; /* >= 0 */
+    int64_t slot_stride[LC_MAX_RANK];   /* >= 0 */
+} lc_loop_layout;
+
+/* The default plan for n_elems points, num_thread threads and vectors of
+ * vector_size points, written as an override into `out` (three modes; unit
+ * modes kept).  Host only.  Errors: LC_ERR_NULL; LC_ERR_SHAPE when a count
+ * is below 1 (n_elems below 0) or num_thread * vector_size does not divide
+ * n_elems (the page's guarded case, which no exact partition expresses). */
+int lc_loop_layout_default(int64_t n_elems, int32_t num_thread, int32_t vector_size,
+                           lc_loop_layout *out);
+
+/* Checks that `loop` is an exact partition of n_elems points and reports
+ * its threads T and slots per thread L.  Host only.  Errors: LC_ERR_NULL,
+ * LC_ERR_RANK, LC_ERR_SHAPE (negative extent or n_elems, or the extents'
+ * product is not n_elems), LC_ERR_BAD_STRIDE (a negative stride, or a
+ * non-unit mode with both or neither stride non-zero), LC_ERR_LOOP_LAYOUT
+ * (the thread or slot modes leave gaps or collide, or T exceeds
+ * LC_LOOP_MAX_THREADS). */
+int lc_loop_layout_info(const lc_loop_layout *loop, int64_t n_elems, int32_t *num_threads,
+                        int64_t *slots_per_thread);
+
+/* lc_layout_copy with the partition given by `loop` instead of the
+ * library's planner: each tile is one CTA of T threads (tiles spread over
+ * the grid), and thread t moves its slots 0 .. L-1 in order, the point of
+ * slot s being the one the override maps to (t, s).  Where the innermost
+ * loop mode is a slot mode of slot stride 1, runs of consecutive slots that
+ * are contiguous on both sides move as one vector of the widest of 16, 8,
+ * 4, 2 bytes that keeps every pointer aligned ("loop_mapping.py": points
+ * that share a lane vectorize; "copy -> gmem_smem" for the width rule).
+ * The copied words equal lc_layout_copy's; only who moves them differs.
+ *   trace  NULL, or n_tiles * N int64 words of device memory that receive
+ *          trace[tile * N + flat] = t * L + s for every point moved (flat =
+ *          the point's row-major index in the tile), to observe the
+ *          partition.
+ * Asynchronous on `stream`.  Errors: as lc_layout_copy (source and
+ * destination may not overlap at all), plus lc_loop_layout_info's errors
+ * for the tile's element count. */
+int lc_layout_copy_loop(const void *src, const lc_tile_layout *src_layout,
+                        void *dst, const lc_tile_layout *dst_layout,
+                        int32_t elem_bytes, int64_t n_tiles, const lc_loop_layout *loop,
+                        int64_t *trace, lc_stream_t stream);
 
 /* Human-readable name of a status / kernel class (static strings). */
 const char *lc_status_string(int32_t status);

@@ -19,7 +19,9 @@ from ._lib import KERNELS, STATUS, STATUS_NAMES
 __all__ = ["TileLayout", "LayoutCopyError", "layout_copy", "layout_copy_ptr", "layout_copy_host",
            "host_staging_bytes", "layout_copy_host_static", "window_sum", "plan",
            "choose_swizzle", "swizzle_conflicts", "gmem_smem_partition",
-           "last_device_error", "debug_wait_timeout", "KERNELS", "STATUS"]
+           "last_device_error", "debug_wait_timeout", "warp_unit_plan", "warp_unit_run",
+           "loop_layout_default", "loop_layout_info", "layout_copy_loop", "layout_copy_loop_ptr",
+           "KERNELS", "STATUS"]
 
 
 @dataclass(frozen=True)
@@ -301,3 +303,82 @@ def last_device_error(stream=None):
 def debug_wait_timeout(timeout_ns: int, stream=None) -> None:
     _check(_lib.lib().lc_debug_wait_timeout(int(timeout_ns), ctypes.c_void_p(_stream_handle(stream))),
            "debug_wait_timeout")
+
+
+# ---------------------------------------------------------------------------
+# loop-layout override: [(extent, thread_stride, slot_stride), ...], outermost
+# first, over the row-major flat index of one tile's logical box
+# ---------------------------------------------------------------------------
+
+def _loop_to_c(loop) -> _lib.CLoopLayout:
+    modes = [tuple(int(x) for x in m) for m in loop]
+    if not 1 <= len(modes) <= _lib.MAX_RANK or any(len(m) != 3 for m in modes):
+        raise ValueError("a loop layout is 1..%d modes (extent, thread_stride, slot_stride)" % _lib.MAX_RANK)
+    c = _lib.CLoopLayout()
+    c.rank = len(modes)
+    for k, (e, ts, ss) in enumerate(modes):
+        c.shape[k], c.thread_stride[k], c.slot_stride[k] = e, ts, ss
+    return c
+
+
+def loop_layout_default(n_elems: int, num_thread: int, vector_size: int):
+    """The default partition of n_elems points as an override (three modes)."""
+    c = _lib.CLoopLayout()
+    _check(_lib.lib().lc_loop_layout_default(int(n_elems), int(num_thread), int(vector_size),
+                                             ctypes.byref(c)), "loop_layout_default")
+    return [(c.shape[k], c.thread_stride[k], c.slot_stride[k]) for k in range(c.rank)]
+
+
+def loop_layout_info(loop, n_elems: int):
+    """(threads, slots per thread) of an exact partition of n_elems points."""
+    c = _loop_to_c(loop)
+    T, L = ctypes.c_int32(), ctypes.c_int64()
+    _check(_lib.lib().lc_loop_layout_info(ctypes.byref(c), int(n_elems), ctypes.byref(T), ctypes.byref(L)),
+           "loop_layout_info")
+    return T.value, L.value
+
+
+def layout_copy_loop_ptr(src_ptr: int, src_layout, dst_ptr: int, dst_layout, elem_bytes: int, loop,
+                         n_tiles: int = 1, trace_ptr: int = 0, stream=0) -> None:
+    """Raw-pointer form of layout_copy_loop (trace_ptr 0: no trace)."""
+    sl, dl = TileLayout.of(src_layout).to_c(), TileLayout.of(dst_layout).to_c()
+    c = _loop_to_c(loop)
+    st = _lib.lib().lc_layout_copy_loop(ctypes.c_void_p(src_ptr), ctypes.byref(sl), ctypes.c_void_p(dst_ptr),
+                                        ctypes.byref(dl), int(elem_bytes), int(n_tiles), ctypes.byref(c),
+                                        ctypes.c_void_p(trace_ptr or None),
+                                        ctypes.c_void_p(_stream_handle(stream)))
+    _check(st, "layout_copy_loop")
+
+
+def layout_copy_loop(src, src_layout, dst, dst_layout, loop, n_tiles: int = 1,
+                     elem_bytes: int | None = None, trace=None, stream=None) -> None:
+    """layout_copy with the partition given by the loop layout ``loop``: one
+    CTA per tile, thread t moving the points the override maps to
+    (t, 0), (t, 1), ... in order.  ``trace``: optional int64 CUDA tensor of at
+    least n_tiles * (points per tile) entries; it receives, for each point,
+    thread * slots_per_thread + slot."""
+    if not (src.is_cuda and dst.is_cuda):
+        raise ValueError("layout_copy_loop needs CUDA tensors (there is no CPU path)")
+    if not (src.is_contiguous() and dst.is_contiguous()):
+        raise ValueError("pass contiguous tensors; express strides through the layouts")
+    w = int(elem_bytes) if elem_bytes is not None else src.element_size()
+    if elem_bytes is None and dst.element_size() != w:
+        raise ValueError("source and destination element sizes differ; pass elem_bytes")
+    sl, dl = TileLayout.of(src_layout), TileLayout.of(dst_layout)
+    for name, t, l in (("source", src, sl), ("destination", dst, dl)):
+        need = l.footprint(n_tiles) * w
+        have = t.numel() * t.element_size()
+        if need > have:
+            raise ValueError("%s layout reaches %d bytes; the tensor holds %d" % (name, need, have))
+    trace_ptr = 0
+    if trace is not None:
+        points = 1
+        for e in sl.shape:
+            points *= int(e)
+        if not trace.is_cuda or not trace.is_contiguous() or trace.element_size() != 8 \
+                or trace.numel() < n_tiles * points:
+            raise ValueError("trace must be a contiguous 8-byte CUDA tensor of >= %d entries"
+                             % (n_tiles * points))
+        trace_ptr = trace.data_ptr()
+    layout_copy_loop_ptr(src.data_ptr(), sl, dst.data_ptr(), dl, w, loop, n_tiles, trace_ptr,
+                         _stream_handle(stream))

@@ -16,6 +16,7 @@ MAX_RANK = 8
 STATIC_STAGING_BYTES = 32 * 1024 * 1024  # LC_STATIC_STAGING_BYTES
 WARP_UNIT_MAX_P = 32  # LC_WARP_UNIT_MAX_P
 WARP_UNIT_MAX_BYTES = 8192  # LC_WARP_UNIT_MAX_BYTES
+LOOP_MAX_THREADS = 1024  # LC_LOOP_MAX_THREADS
 
 OK = 0
 STATUS_NAMES = {
@@ -24,6 +25,7 @@ STATUS_NAMES = {
     7: "LC_ERR_NOT_INJECTIVE", 8: "LC_ERR_OVERLAP", 9: "LC_ERR_ALIGN",
     10: "LC_ERR_NO_SWIZZLE", 11: "LC_ERR_CUDA", 12: "LC_ERR_TIMEOUT",
     13: "LC_ERR_UNSUPPORTED", 14: "LC_ERR_OVERFLOW", 15: "LC_ERR_STAGING",
+    16: "LC_ERR_LOOP_LAYOUT",
 }
 STATUS = {v: k for k, v in STATUS_NAMES.items()}
 KERNELS = {"auto": 0, "vec_copy": 1, "warp_permute": 2, "tile_transpose": 3, "smem_transpose": 4,
@@ -67,7 +69,15 @@ class CWarpUnit(ctypes.Structure):
                 ("dst_cosize", ctypes.c_int32)]
 
 
+class CLoopLayout(ctypes.Structure):
+    _fields_ = [("rank", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * MAX_RANK),
+                ("thread_stride", ctypes.c_int64 * MAX_RANK),
+                ("slot_stride", ctypes.c_int64 * MAX_RANK)]
+
+
 _P_LAYOUT = ctypes.POINTER(CTileLayout)
+_P_LOOP = ctypes.POINTER(CLoopLayout)
 _P_I32 = ctypes.POINTER(ctypes.c_int32)
 _P_I64 = ctypes.POINTER(ctypes.c_int64)
 
@@ -99,6 +109,11 @@ PROTOTYPES = {
     "lc_warp_unit_plan": (ctypes.c_int, [_P_LAYOUT, _P_LAYOUT, ctypes.c_int32, ctypes.POINTER(CWarpUnit)]),
     "lc_warp_unit_run": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(CWarpUnit),
                                         ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p]),
+    "lc_loop_layout_default": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _P_LOOP]),
+    "lc_loop_layout_info": (ctypes.c_int, [_P_LOOP, ctypes.c_int64, _P_I32, _P_I64]),
+    "lc_layout_copy_loop": (ctypes.c_int, [ctypes.c_void_p, _P_LAYOUT, ctypes.c_void_p, _P_LAYOUT,
+                                           ctypes.c_int32, ctypes.c_int64, _P_LOOP, ctypes.c_void_p,
+                                           ctypes.c_void_p]),
     "lc_status_string": (ctypes.c_char_p, [ctypes.c_int32]),
     "lc_kernel_name": (ctypes.c_char_p, [ctypes.c_int32]),
 }

@@ -1,6 +1,6 @@
 """Builds liblayoutcopy.so (the C-ABI library) in-tree for sm_103a.
 
-Two translation units compiled in parallel with nvcc and linked into one
+The translation units are compiled in parallel with nvcc and linked into one
 shared object next to this file; the CUDA runtime is linked statically and
 the driver is reached through the runtime's entry-point query, so the library
 needs nothing but libcuda at run time.
@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(HERE, LIB_NAME)
 
 SOURCES = ["plan.cpp", "api.cu", "host_copy.cu", "host_copy_static.cu", "k_vec.cu", "k_warp.cu",
            "k_warp_w1.cu", "k_warp_w2.cu", "k_warp_w4.cu", "k_warp_w8.cu", "k_warp_w16.cu",
-           "k_tile.cu", "k_smem.cu", "k_tma_copy.cu", "k_stencil.cu"]
+           "k_tile.cu", "k_smem.cu", "k_tma_copy.cu", "k_stencil.cu", "k_loop.cu"]
 HEADERS = ["lc_internal.h", "ptx.cuh", "device_common.cuh", "launch.h", "k_warp.cuh", "tensor_map.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O3",

@@ -144,7 +144,9 @@ extern "C" const char *lc_status_string(int32_t status) {
         case LC_ERR_SHAPE: return "negative extent or tile count, or element count not a multiple of the warp";
         case LC_ERR_EXTENT_MISMATCH: return "non-unit extents of source and destination differ";
         case LC_ERR_ELEM_BYTES: return "element size not in {1,2,4,8,16}";
-        case LC_ERR_BAD_STRIDE: return "negative stride or offset, or zero destination stride";
+        case LC_ERR_BAD_STRIDE:
+            return "negative stride or offset, zero destination stride, or a loop-layout mode feeding both or "
+                   "neither of thread and slot";
         case LC_ERR_NOT_INJECTIVE: return "destination layout maps two logical indices to one offset";
         case LC_ERR_OVERLAP: return "source and destination byte ranges overlap";
         case LC_ERR_ALIGN: return "pointer not aligned to the element size";
@@ -154,6 +156,7 @@ extern "C" const char *lc_status_string(int32_t status) {
         case LC_ERR_UNSUPPORTED: return "the requested kernel class cannot perform this copy";
         case LC_ERR_OVERFLOW: return "an offset does not fit in 63 bits";
         case LC_ERR_STAGING: return "the staging buffer is too small";
+        case LC_ERR_LOOP_LAYOUT: return "the loop layout is not an exact partition of the tile (or has over 1024 threads)";
     }
     return "unknown status";
 }

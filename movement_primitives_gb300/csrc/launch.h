@@ -24,6 +24,7 @@ int launch_warp(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t st
 int launch_tile(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream);
 int launch_smem(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream);
 int launch_tma_copy(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream);
+int launch_loop(const LoopPlan &lp, const uint8_t *src, uint8_t *dst, int64_t *trace, cudaStream_t stream);
 
 // Launches the plan's kernel class.  With `fallback`, a TMA plan whose tensor
 // map the driver refuses runs on the non-TMA class of the same copy instead

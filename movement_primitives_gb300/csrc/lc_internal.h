@@ -97,6 +97,34 @@ int make_plan(const lc_tile_layout *src, const lc_tile_layout *dst, int32_t w,
               int64_t n_tiles, int32_t kernel, const PtrInfo &ptr, Plan *out);
 void fill_info(const Plan &p, lc_plan_info *info);
 
+// A copy under a loop-layout override.  The thread digits and the slot
+// digits are each sorted by their stride (ascending), so digit i of a
+// thread index (or slot index) is (index / stride_i) % e_i; `weight` is the
+// row-major weight of the digit's mode in the tile's flat index.
+struct LoopDigit {
+    int64_t e = 1, weight = 0;
+};
+struct LoopPlan {
+    int w = 0;
+    int64_t n_tiles = 0;
+    int64_t N = 0;                     // words per tile
+    int64_t src_off = 0, dst_off = 0;  // words
+    int64_t sts = 0, dts = 0;          // tile strides, words
+    ModeList logical;                  // one tile's modes, logical order
+    int nt = 0, ns = 0;
+    LoopDigit td[LC_MAX_RANK], sd[LC_MAX_RANK];
+    int64_t T = 0, L = 0;
+    int64_t inner_run = 1;  // innermost non-unit loop mode's extent when it is a slot mode of stride 1
+    int vec = 1;            // words moved per vector
+    // The loop's and the tile's mixed radices nest (their suffix products
+    // form one divisibility chain) and a tile's byte span fits 31 bits: a
+    // point's offsets are then the thread part's plus the slot part's.
+    bool split = false;
+};
+int check_loop(const lc_loop_layout *loop, int64_t n, LoopPlan *out);
+int make_loop_plan(const lc_tile_layout *src, const lc_tile_layout *dst, int32_t w, int64_t n_tiles,
+                   const lc_loop_layout *loop, const PtrInfo &ptr, LoopPlan *out);
+
 // Bank simulator ("permute_layout", section "Algorithm", step 2).
 void phase_degrees(const ModeList &unit, int w, int k, int shift, int *rd, int *wd);
 // Returns 0 when conflict-free (k, shift) found; 1 otherwise (best returned).

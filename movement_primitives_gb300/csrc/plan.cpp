@@ -760,6 +760,137 @@ void fill_info(const Plan &p, lc_plan_info *info) {
     }
 }
 
+// --------------------------------------------------------------------------
+// loop-layout override (TileLang "loop_mapping.py": a loop_layout= annotation
+// replaces the default plan)
+// --------------------------------------------------------------------------
+
+// Validates an override of n points: extents multiplying to n, each non-unit
+// mode feeding exactly one of thread and slot, and each part a mixed radix
+// once sorted by stride (exact partition of [0, T) x [0, L)).
+int check_loop(const lc_loop_layout *loop, int64_t n, LoopPlan *out) {
+    if (!loop || !out) return LC_ERR_NULL;
+    if (loop->rank < 1 || loop->rank > LC_MAX_RANK) return LC_ERR_RANK;
+    if (n < 0) return LC_ERR_SHAPE;
+    int64_t prod = 1;
+    for (int k = 0; k < loop->rank; ++k) {
+        if (loop->shape[k] < 0) return LC_ERR_SHAPE;
+        if (loop->thread_stride[k] < 0 || loop->slot_stride[k] < 0) return LC_ERR_BAD_STRIDE;
+        if (!mul_ok(prod, loop->shape[k], &prod)) return LC_ERR_SHAPE;
+    }
+    if (prod != n) return LC_ERR_SHAPE;
+    out->nt = out->ns = 0;
+    out->T = out->L = 0;
+    out->inner_run = 1;
+    if (n == 0) return LC_OK;
+    struct Part {
+        int64_t e, stride, weight;
+    };
+    Part th[LC_MAX_RANK], sl[LC_MAX_RANK];
+    int nt = 0, ns = 0;
+    int64_t weight = 1;
+    bool innermost = true;
+    for (int k = loop->rank - 1; k >= 0; weight *= loop->shape[k], --k) {
+        const int64_t e = loop->shape[k], ts = loop->thread_stride[k], ss = loop->slot_stride[k];
+        if (e == 1) continue;
+        if ((ts > 0) == (ss > 0)) return LC_ERR_BAD_STRIDE;
+        if (ts > 0) th[nt++] = Part{e, ts, weight};
+        else sl[ns++] = Part{e, ss, weight};
+        if (innermost && ss == 1) out->inner_run = e;
+        innermost = false;
+    }
+    auto by_stride = [](const Part &a, const Part &b) { return a.stride < b.stride; };
+    std::stable_sort(th, th + nt, by_stride);
+    std::stable_sort(sl, sl + ns, by_stride);
+    int64_t T = 1, L = 1;
+    for (int i = 0; i < nt; ++i) {
+        if (th[i].stride != T) return LC_ERR_LOOP_LAYOUT;
+        T *= th[i].e;
+        if (T > LC_LOOP_MAX_THREADS) return LC_ERR_LOOP_LAYOUT;
+        out->td[i] = LoopDigit{th[i].e, th[i].weight};
+    }
+    for (int i = 0; i < ns; ++i) {
+        if (sl[i].stride != L) return LC_ERR_LOOP_LAYOUT;
+        L *= sl[i].e;  // T * L == n, so no overflow
+        out->sd[i] = LoopDigit{sl[i].e, sl[i].weight};
+    }
+    out->nt = nt;
+    out->ns = ns;
+    out->T = T;
+    out->L = L;
+    return LC_OK;
+}
+
+int make_loop_plan(const lc_tile_layout *src, const lc_tile_layout *dst, int32_t w, int64_t n_tiles,
+                   const lc_loop_layout *loop, const PtrInfo &ptr, LoopPlan *out) {
+    if (!out) return LC_ERR_NULL;
+    // every check of lc_layout_copy over all tiles (a forced class, so any
+    // overlap is refused), then one tile's logical modes
+    Plan full, one;
+    int st = make_plan(src, dst, w, n_tiles, LC_KERNEL_VEC_COPY, ptr, &full);
+    if (st) return st;
+    if ((st = make_plan(src, dst, w, 1, LC_KERNEL_VEC_COPY, PtrInfo{}, &one))) return st;
+    LoopPlan lp;
+    if ((st = check_loop(loop, one.total, &lp))) return st;
+    lp.w = w;
+    lp.n_tiles = n_tiles;
+    lp.N = one.total;
+    lp.logical = one.logical;
+    lp.src_off = src->offset;
+    lp.dst_off = dst->offset;
+    int64_t cs, cd;
+    if ((st = cosize(src, &cs)) || (st = cosize(dst, &cd))) return st;
+    lp.sts = src->tile_stride ? src->tile_stride : cs;
+    lp.dts = dst->tile_stride ? dst->tile_stride : cd;
+    // widest vector of consecutive slots that is contiguous and aligned on
+    // both sides in every tile ("copy -> gmem_smem" width rule)
+    lp.vec = 1;
+    const ModeList &lg = lp.logical;
+    for (int bytes = 16; bytes >= 2 * w && lg.n > 0 && lp.N > 0; bytes /= 2) {
+        const int v = bytes / w;
+        const Mode &in = lg.m[lg.n - 1];
+        bool ok = lp.inner_run % v == 0 && in.s == 1 && in.d == 1 && in.e % v == 0 &&
+                  lp.src_off % v == 0 && lp.dst_off % v == 0;
+        for (int i = 0; ok && i + 1 < lg.n; ++i) ok = lg.m[i].s % v == 0 && lg.m[i].d % v == 0;
+        if (ok && n_tiles > 1) ok = lp.sts % v == 0 && lp.dts % v == 0;
+        if (ok && ptr.check)
+            ok = base_addr(ptr.src, lp.src_off, w) % uintptr_t(bytes) == 0 &&
+                 base_addr(ptr.dst, lp.dst_off, w) % uintptr_t(bytes) == 0;
+        if (ok) { lp.vec = v; break; }
+    }
+    // additive split: every suffix product of the loop modes and of the
+    // logical modes (innermost first) lies on one divisibility chain
+    if (lp.N > 0) {
+        std::vector<int64_t> cuts;
+        int64_t c = 1;
+        for (int k = loop->rank - 1; k >= 0; --k) {
+            if (loop->shape[k] == 1) continue;
+            c *= loop->shape[k];
+            cuts.push_back(c);
+        }
+        c = 1;
+        for (int i = lg.n - 1; i >= 0; --i) {
+            c *= lg.m[i].e;
+            cuts.push_back(c);
+        }
+        std::sort(cuts.begin(), cuts.end());
+        bool chain = true;
+        int64_t prev = 1;
+        for (int64_t x : cuts) {
+            if (x % prev) { chain = false; break; }
+            prev = x;
+        }
+        int64_t sspan = 1, dspan = 1;
+        for (int i = 0; i < lg.n; ++i) {
+            sspan += (lg.m[i].e - 1) * lg.m[i].s;
+            dspan += (lg.m[i].e - 1) * lg.m[i].d;
+        }
+        lp.split = chain && sspan * w < (int64_t(1) << 31) && dspan * w < (int64_t(1) << 31);
+    }
+    *out = lp;
+    return LC_OK;
+}
+
 }  // namespace lc
 
 // ----------------------------------------------------------------------------
@@ -904,4 +1035,31 @@ extern "C" int lc_warp_unit_plan(const lc_tile_layout *src_layout, const lc_tile
     u.dst_cosize = static_cast<int32_t>(dcos);
     *out = u;
     return bad ? LC_ERR_NO_SWIZZLE : LC_OK;
+}
+
+extern "C" int lc_loop_layout_default(int64_t n_elems, int32_t num_thread, int32_t vector_size,
+                                      lc_loop_layout *out) {
+    if (!out) return LC_ERR_NULL;
+    if (n_elems < 0 || num_thread < 1 || vector_size < 1) return LC_ERR_SHAPE;
+    const int64_t group = int64_t(num_thread) * vector_size;
+    if (n_elems % group) return LC_ERR_SHAPE;
+    std::memset(out, 0, sizeof(*out));
+    out->rank = 3;
+    out->shape[0] = n_elems / group;  // serial rounds
+    out->slot_stride[0] = vector_size;
+    out->shape[1] = num_thread;       // threads
+    out->thread_stride[1] = 1;
+    out->shape[2] = vector_size;      // points sharing a lane
+    out->slot_stride[2] = 1;
+    return LC_OK;
+}
+
+extern "C" int lc_loop_layout_info(const lc_loop_layout *loop, int64_t n_elems, int32_t *num_threads,
+                                   int64_t *slots_per_thread) {
+    lc::LoopPlan lp;
+    const int st = lc::check_loop(loop, n_elems, &lp);
+    if (st) return st;
+    if (num_threads) *num_threads = static_cast<int32_t>(lp.T);
+    if (slots_per_thread) *slots_per_thread = lp.L;
+    return LC_OK;
 }

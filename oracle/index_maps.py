@@ -10,9 +10,10 @@ TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).
   "copy -> gmem_smem", section "Algorithm" steps 1-3 and section "How inputs
   change the algorithm" (the ``[outer, threads, vec]`` split, the widest-first
   vector width, the serial loop of vector copies).
-* ``loop_layout_plan`` / ``loop_layout_sizes`` / ``default_loop_layout`` /
-  ``loop_layout_replay``: the same tutorial's ``loop_layout=`` override of
-  the default plan (module docstring), under the reading stated at them.
+* ``loop_layout_owner`` / ``loop_layout_plan`` / ``loop_layout_sizes`` /
+  ``default_loop_layout`` / ``loop_layout_replay``: the same tutorial's
+  ``loop_layout=`` override of the default plan (module docstring), under the
+  reading stated at them.
 * ``permute_align`` / ``permute_replay``: Apache TVM docs "permute_layout",
   section "Algorithm" steps 1 and 3 (the aligned ``extent``/``src_str``/
   ``dst_str``, ``P = prod(extent) / 32``, and the two register-staged phases
@@ -88,20 +89,21 @@ def _product(values) -> int:
     return n
 
 
+def loop_layout_owner(flat: int, loop) -> tuple:
+    """(thread, slot) of the point with row-major flat index ``flat``."""
+    digits = unflatten(flat, [m[0] for m in loop])
+    thread = sum(c * m[1] for c, m in zip(digits, loop))
+    slot = sum(c * m[2] for c, m in zip(digits, loop))
+    return thread, slot
+
+
 def loop_layout_plan(extents, loop) -> dict:
     """{iteration point: (thread, slot)} under the override ``loop``."""
     total = _product(extents)
-    loop_extents = [m[0] for m in loop]
-    if _product(loop_extents) != total:
+    if _product(m[0] for m in loop) != total:
         raise Decline("the loop layout covers %d points, the nest %d"
-                      % (_product(loop_extents), total))
-    out = {}
-    for flat in range(total):
-        digits = unflatten(flat, loop_extents)
-        thread = sum(c * m[1] for c, m in zip(digits, loop))
-        slot = sum(c * m[2] for c, m in zip(digits, loop))
-        out[unflatten(flat, extents)] = (thread, slot)
-    return out
+                      % (_product(m[0] for m in loop), total))
+    return {unflatten(flat, extents): loop_layout_owner(flat, loop) for flat in range(total)}
 
 
 def loop_layout_sizes(extents, loop):

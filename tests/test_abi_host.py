@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(M):
 
 def test_status_and_kernel_names(M):
     lib = M._lib.lib()
-    for code in range(16):
+    for code in range(17):
         assert lib.lc_status_string(code) and lib.lc_status_string(code) != b"unknown status"
     assert lib.lc_kernel_name(2) == b"warp_permute"
 
@@ -231,6 +231,87 @@ def test_pointer_checks_before_launch(M):
         with pytest.raises(M.LayoutCopyError) as e:
             M.layout_copy_ptr(*args, stream=0)
         assert e.value.status == M.STATUS[status]
+
+
+# ---------------------------------------------------------------------------
+# loop-layout override
+# ---------------------------------------------------------------------------
+
+def test_loop_layout_default_matches_oracle(M):
+    for total, T, V in [(64, 8, 2), (256, 64, 4), (1 << 19, 1024, 8), (12, 1, 1), (0, 4, 2), (32, 32, 1)]:
+        assert M.loop_layout_default(total, T, V) == index_maps.default_loop_layout(total, T, V)
+    for total, T, V in [(60, 8, 2), (7, 2, 1)]:  # the guarded case
+        with pytest.raises(index_maps.Decline):
+            index_maps.default_loop_layout(total, T, V)
+        with pytest.raises(M.LayoutCopyError) as e:
+            M.loop_layout_default(total, T, V)
+        assert e.value.status == M.STATUS["LC_ERR_SHAPE"]
+
+
+def _random_loops(rng, n):
+    strides = [0, 0, 1, 1, 2, 3, 4, 6, 8, 12, 16]
+    for _ in range(n):
+        r = rng.randint(1, 4)
+        yield [(rng.choice([1, 2, 2, 3, 4]), rng.choice(strides), rng.choice(strides)) for _ in range(r)]
+    for _ in range(n):  # exact partitions, in random mode orders
+        exts = [rng.choice([1, 2, 3, 4]) for _ in range(rng.randint(1, 5))]
+        loop, ts, ss = [None] * len(exts), 1, 1
+        for i in rng.sample(range(len(exts)), len(exts)):
+            if rng.random() < 0.5:
+                loop[i], ts = (exts[i], ts, 0), ts * exts[i]
+            else:
+                loop[i], ss = (exts[i], 0, ss), ss * exts[i]
+        yield loop
+
+
+def test_loop_layout_info_matches_oracle(M):
+    """Accept / refuse and (T, L) agree with the oracle's brute-force check."""
+    rng = random.Random(11)
+    accepted = refused = 0
+    for loop in _random_loops(rng, 400):
+        total = int(np.prod([m[0] for m in loop]))
+        try:
+            want = index_maps.loop_layout_sizes((total,), loop)
+        except index_maps.Decline:
+            want = None
+        try:
+            got = M.loop_layout_info(loop, total)
+        except M.LayoutCopyError:
+            got = None
+        assert got == want, loop
+        accepted += want is not None
+        refused += want is None
+    assert accepted > 300 and refused > 100
+    with pytest.raises(M.LayoutCopyError) as e:
+        M.loop_layout_info([(2048, 1, 0)], 2048)
+    assert e.value.status == M.STATUS["LC_ERR_LOOP_LAYOUT"]  # over 1024 threads
+    with pytest.raises(M.LayoutCopyError) as e:
+        M.loop_layout_info([(4, 1, 0)], 8)
+    assert e.value.status == M.STATUS["LC_ERR_SHAPE"]
+
+
+def test_layout_copy_loop_checks_before_launch(M):
+    """Refusals of lc_layout_copy_loop come before any CUDA call."""
+    T = M.TileLayout
+    src, dst = T((8, 8), (8, 1)), T((8, 8), (1, 8))
+    col = [(8, 0, 1), (8, 1, 0)]
+    cases = [((0, src, 1 << 20, dst, 4, col), "LC_ERR_NULL"),
+             ((4096, src, 4096 + 128, dst, 4, col), "LC_ERR_OVERLAP"),
+             ((4096, src, 1 << 20, dst, 4, [(4, 0, 1), (8, 1, 0)]), "LC_ERR_SHAPE"),
+             ((4096, src, 1 << 20, dst, 4, [(8, 2, 0), (8, 0, 1)]), "LC_ERR_LOOP_LAYOUT"),
+             ((4096, src, 1 << 20, dst, 4, [(8, 1, 1), (8, 0, 8)]), "LC_ERR_BAD_STRIDE"),
+             ((4096, src, 1 << 20, T((8, 7), (7, 1)), 4, col), "LC_ERR_EXTENT_MISMATCH"),
+             ((4098, src, 1 << 20, dst, 4, col), "LC_ERR_ALIGN")]
+    for args, status in cases:
+        with pytest.raises(M.LayoutCopyError) as e:
+            M.layout_copy_loop_ptr(*args, stream=0)
+        assert e.value.status == M.STATUS[status], (args, status)
+    with pytest.raises(M.LayoutCopyError) as e:  # a misaligned trace
+        M.layout_copy_loop_ptr(4096, src, 1 << 20, dst, 4, col, 1, trace_ptr=(1 << 22) + 4)
+    assert e.value.status == M.STATUS["LC_ERR_ALIGN"]
+    # nothing to move: no launch, no error
+    M.layout_copy_loop_ptr(4096, src, 1 << 20, dst, 4, col, n_tiles=0)
+    M.layout_copy_loop_ptr(4096, T((0, 8), (8, 1)), 1 << 20, T((0, 8), (1, 8)), 4, [(0, 1, 0)])
 
 
 def test_fastdiv_host_mirror():

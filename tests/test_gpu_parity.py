@@ -576,3 +576,153 @@ def test_copies_capture_into_a_cuda_graph():
         graph.replay()
         torch.cuda.synchronize()
         assert np.array_equal(dst.cpu().numpy(), want), cfg["name"]
+
+
+# ---------------------------------------------------------------------------
+# loop-layout override: the words against the definition, the partition (the
+# trace of who moved what) against the oracle's (thread, slot) of each point
+# ---------------------------------------------------------------------------
+
+def _loop_trace_want(src_l, dst_l, loop, n_tiles):
+    extents = [m[0] for m in oracle.paired_modes(src_l, dst_l)]
+    T, L_ = oracle.index_maps.loop_layout_sizes(extents, loop)
+    N = int(np.prod(extents))
+    one = np.empty(N, np.int64)
+    for flat in range(N):
+        t, slot = oracle.index_maps.loop_layout_owner(flat, loop)
+        one[flat] = t * L_ + slot
+    return np.tile(one, n_tiles)
+
+
+def run_loop_case(src_l, dst_l, w, loop, n_tiles=1, seed=0, src_shift=0, dst_shift=0):
+    ns = _footprint(src_l, n_tiles) * w + src_shift
+    nd = _footprint(dst_l, n_tiles) * w + dst_shift
+    g = torch.Generator().manual_seed(seed)
+    src_h = torch.randint(0, 256, (max(ns, 1),), generator=g, dtype=torch.uint8)
+    dst_h = torch.full((max(nd, 1),), workloads.SENTINEL, dtype=torch.uint8)
+    want = dst_h.numpy().copy()
+    oracle.copy(src_h.numpy()[src_shift:].copy(), src_l, want[dst_shift:], dst_l, w, n_tiles)
+    trace_want = _loop_trace_want(src_l, dst_l, loop, n_tiles)
+    src_d, dst_d = src_h.cuda(), dst_h.cuda()
+    trace_d = torch.full((max(trace_want.size, 1),), -1, dtype=torch.int64, device="cuda")
+    lc().layout_copy_loop_ptr(src_d.data_ptr() + src_shift, src_l, dst_d.data_ptr() + dst_shift, dst_l, w,
+                              loop, n_tiles, trace_d.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    st, detail = lc().last_device_error()
+    assert st == 0, "device error word %#x" % detail
+    got = dst_d.cpu().numpy()
+    if not np.array_equal(got, want):
+        bad = np.flatnonzero(got != want)
+        raise AssertionError("%d bytes differ, first at %d (got %d want %d)"
+                             % (bad.size, bad[0], got[bad[0]], want[bad[0]]))
+    got_trace = trace_d.cpu().numpy()[:trace_want.size]
+    assert np.array_equal(got_trace, trace_want), "the partition differs from the override"
+
+
+@pytest.mark.parametrize("w", [1, 2, 4, 8, 16])
+def test_loop_layout_copies(w):
+    dl = oracle.index_maps.default_loop_layout
+    # the scale-factor transpose batch under the default plan (64 threads x 4)
+    run_loop_case(L((2, 1, 4, 32), (128, 128, 32, 1)), L((2, 1, 4, 32), (128, 128, 1, 4)), w,
+                  dl(256, 64, 4), n_tiles=37, seed=w)
+    # one column per thread (no vectors)
+    run_loop_case(L((8, 8), (8, 1)), L((8, 8), (1, 8)), w, [(8, 0, 1), (8, 1, 0)], n_tiles=3)
+    # thread-major blocks of an identity copy (vectors of consecutive slots)
+    run_loop_case(L((64, 128), (128, 1)), L((64, 128), (128, 1)), w,
+                  [(16, 1, 0), (4, 0, 128), (128, 0, 1)], n_tiles=2)
+    # ... the same with both bases moved off the vector grid
+    run_loop_case(L((64, 128), (128, 1)), L((64, 128), (128, 1)), w,
+                  [(16, 1, 0), (4, 0, 128), (128, 0, 1)], src_shift=w, dst_shift=3 * w)
+    # ragged: 5 threads x 6 slots, offsets, padded tile strides
+    run_loop_case(L((6, 5), (5, 1), 2, 40), L((6, 5), (1, 6), 1, 31), w, [(6, 0, 1), (5, 1, 0)], n_tiles=3)
+    # 1024 threads of one slot, and one thread of 64 slots
+    run_loop_case(L((32, 32), (32, 1)), L((32, 32), (1, 32)), w, [(32, 1, 0), (32, 32, 0)], n_tiles=2)
+    run_loop_case(L((8, 8), (8, 1)), L((8, 8), (1, 8)), w, [(8, 0, 8), (8, 0, 1)])
+    # radices that do not nest (suffix products 1, 6, 12 against 1, 4, 12):
+    # the general path, every vector's offsets decoded from its flat index
+    run_loop_case(L((3, 4), (4, 1)), L((3, 4), (1, 3)), w, [(2, 1, 0), (6, 0, 1)], n_tiles=2)
+    run_loop_case(L((9, 10), (10, 1), 1), L((9, 10), (1, 9)), w, [(3, 0, 6), (5, 1, 0), (6, 0, 1)], n_tiles=2)
+    # gapped and broadcast source strides
+    run_loop_case(L((16, 16), (40, 2)), L((16, 16), (1, 16)), w, [(16, 0, 1), (16, 1, 0)])
+    run_loop_case(L((12, 10), (0, 1)), L((12, 10), (10, 1)), w, dl(120, 12, 2), n_tiles=2)
+
+
+def test_loop_layout_small_workload_and_random_partitions():
+    c = workloads.config(8, scale="small")
+    assert c["loop"] == oracle.index_maps.default_loop_layout(8 * 16 * 32, 128, 8)
+    run_loop_case(c["src"], c["dst"], c["elem_bytes"], c["loop"], c["n_tiles"], seed=8)
+    rng = random.Random(88)
+    ran = 0
+    for i in range(30):
+        src, dst, w, n_tiles = _random_layout_pair(rng)
+        extents = [m[0] for m in oracle.paired_modes(src, dst)]
+        N = int(np.prod(extents))
+        if N == 0 or N > 1 << 14:
+            continue
+        # an exact partition: factor N into digits, each a thread or a slot digit
+        digits, rest = [], N
+        for p in (2, 3, 5, 7, 11, 13):
+            while rest % p == 0:
+                digits.append(p)
+                rest //= p
+        if rest > 1:
+            digits.append(rest)
+        digits = digits or [1]  # a one-point nest: one unit mode
+        rng.shuffle(digits)
+        while len(digits) > 6:  # merge digits: at most 8 modes
+            last = digits.pop()
+            digits[rng.randrange(len(digits))] *= last
+        loop, ts, ss = [None] * len(digits), 1, 1
+        for k in rng.sample(range(len(digits)), len(digits)):
+            if rng.random() < 0.5 and ts * digits[k] <= 1024:
+                loop[k], ts = (digits[k], ts, 0), ts * digits[k]
+            else:
+                loop[k], ss = (digits[k], 0, ss), ss * digits[k]
+        run_loop_case(src, dst, w, loop, n_tiles, seed=i)
+        ran += 1
+    assert ran >= 15
+
+
+def test_loop_layout_empty_and_refused():
+    run_loop_case(L((0, 4), (4, 1)), L((0, 4), (1, 4)), 4, [(0, 1, 0), (4, 0, 1)])
+    run_loop_case(L((4, 4), (4, 1)), L((4, 4), (1, 4)), 4, [(4, 1, 0), (4, 0, 1)], n_tiles=0)
+    buf = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
+    p = buf.data_ptr()
+    for loop, status in [([(4, 2, 0), (4, 0, 1)], "LC_ERR_LOOP_LAYOUT"),
+                         ([(2048, 1, 0)], "LC_ERR_SHAPE"),
+                         ([(4, 0, 1), (4, 1, 1)], "LC_ERR_BAD_STRIDE")]:
+        with pytest.raises(lc().LayoutCopyError) as e:
+            lc().layout_copy_loop_ptr(p, L((4, 4), (4, 1)), p + 4096, L((4, 4), (1, 4)), 4, loop)
+        assert e.value.status == lc().STATUS[status]
+    with pytest.raises(lc().LayoutCopyError) as e:
+        lc().layout_copy_loop_ptr(p, L((4, 4), (4, 1)), p + 32, L((4, 4), (1, 4)), 4, [(4, 1, 0), (4, 0, 1)])
+    assert e.value.status == lc().STATUS["LC_ERR_OVERLAP"]
+    assert (buf == 0).all()
+
+
+def test_loop_layout_full_workload_sampled():
+    c = workloads.config(8)
+    assert c["loop"] == oracle.index_maps.default_loop_layout(32 * 128 * 128, 1024, 8)
+    src_d = workloads.make_src(c).cuda()
+    dst_d = workloads.make_dst(c, device="cuda")
+    N = 32 * 128 * 128
+    trace = torch.full((c["n_tiles"] * N,), -1, dtype=torch.int64, device="cuda")
+    lc().layout_copy_loop(src_d, c["src"], dst_d, c["dst"], c["loop"], n_tiles=c["n_tiles"],
+                          elem_bytes=2, trace=trace)
+    st, detail = lc().last_device_error()
+    assert st == 0, "device error word %#x" % detail
+    rng = np.random.default_rng(8)
+    pts = rng.integers(0, c["n_tiles"] * N, size=1 << 18, dtype=np.int64)
+    pts[:2] = [0, c["n_tiles"] * N - 1]
+    so, do = oracle.offsets_of(c["src"], c["dst"], c["n_tiles"], pts)
+    sv, dv = src_d.view(torch.int16), dst_d.view(torch.int16)
+    assert torch.equal(sv[torch.from_numpy(so).cuda()], dv[torch.from_numpy(do).cuda()])
+    T, L_ = 1024, N // 1024
+    want = np.empty(pts.size, np.int64)
+    for i, f in enumerate(pts[:4096]):
+        t, slot = oracle.index_maps.loop_layout_owner(int(f % N), c["loop"])
+        want[i] = t * L_ + slot
+    got = trace[torch.from_numpy(pts[:4096]).cuda()].cpu().numpy()
+    assert np.array_equal(got, want[:4096])
+    # every point moved exactly once per tile: the trace is a permutation of 0..N-1
+    assert torch.equal(torch.sort(trace[:N]).values, torch.arange(N, device="cuda"))
+    assert torch.equal(torch.sort(trace[-N:]).values, torch.arange(N, device="cuda"))

@@ -18,6 +18,11 @@ The five workloads are those the library is measured on:
      the TMA path cannot take), 4-byte words by default
   7  window sum b[i] = a[i] + a[i+1] + a[i+2] over 2^28 float32 outputs (the
      "Window Sum Example" of MLC Ep7, scaled up)
+  8  workload 5's permute as 256 tiles of (32,128,128), one per batch entry,
+     moved under an explicit loop layout (the "loop_layout=" override of the
+     TileLang "loop_mapping.py" page): (64: slot stride 8), (1024: thread
+     stride 1), (8: slot stride 1), which restates the default partition with
+     1024 threads and vectors of 8 words
 Layouts are plain dicts: shape, stride, offset, tile_stride (elements).
 """
 from __future__ import annotations
@@ -78,6 +83,13 @@ def config(cfg: int, elem_bytes: int | None = None, scale: str = "full") -> dict
         n = (1 << 16) + 3 if small else 1 << 28
         return dict(name="window_sum3_f32", cfg=7, n_out=n, window=3, elem_bytes=4,
                     kind="uniform_f32", seed=7)
+    if cfg == 8:
+        b, (h, s, d) = (5, (8, 16, 32)) if small else (256, (32, 128, 128))
+        loop = [(4, 0, 8), (128, 1, 0), (8, 0, 1)] if small else [(64, 0, 8), (1024, 1, 0), (8, 0, 1)]
+        return dict(name="permute0213_loop_bf16", cfg=8,
+                    src=_layout((h, s, d), (s * d, d, 1), 0, h * s * d),
+                    dst=_layout((h, s, d), (d, h * d, 1), 0, h * s * d),
+                    elem_bytes=2, n_tiles=b, kind="normal_bf16", seed=8, loop=loop)
     raise ValueError("unknown workload %r" % cfg)
 
 
