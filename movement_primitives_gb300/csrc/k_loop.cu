@@ -26,8 +26,16 @@
 
 namespace lc {
 
-constexpr int kLoopUnroll = 4;    // vectors in flight per thread
-constexpr int kLoopTable = 2048;  // slot vectors per shared offset table (16 KiB)
+// Vectors in flight per thread and slot vectors per shared offset table
+// (compile-time knobs so that variants can be measured).
+#ifndef LC_LOOP_UNROLL
+#define LC_LOOP_UNROLL 4
+#endif
+#ifndef LC_LOOP_TABLE
+#define LC_LOOP_TABLE 2048
+#endif
+constexpr int kLoopUnroll = LC_LOOP_UNROLL;
+constexpr int kLoopTable = LC_LOOP_TABLE;  // 8 bytes per entry
 
 struct LoopArgs {
     const uint8_t *src;  // word 0 of tile 0
