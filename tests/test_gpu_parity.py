@@ -726,3 +726,69 @@ def test_loop_layout_full_workload_sampled():
     # every point moved exactly once per tile: the trace is a permutation of 0..N-1
     assert torch.equal(torch.sort(trace[:N]).values, torch.arange(N, device="cuda"))
     assert torch.equal(torch.sort(trace[-N:]).values, torch.arange(N, device="cuda"))
+
+
+# ---------------------------------------------------------------------------
+# maximum sizes: indices past 32 bits (the 64-bit index paths) and the split
+# path's 2^31-byte cut-off; inputs drawn on the device from a seeded
+# generator, offsets of sampled points from the oracle, and whole-buffer
+# equality of the slices the definition pairs
+# ---------------------------------------------------------------------------
+
+def _device_bytes(n, seed):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    return torch.randint(0, 256, (n,), generator=g, dtype=torch.uint8, device="cuda")
+
+
+def _sampled_points_agree(src_d, dst_d, src_l, dst_l, n_tiles, n_points, seed, edges=()):
+    rng = np.random.default_rng(seed)
+    pts = np.concatenate([np.asarray(edges, np.int64), rng.integers(0, n_points, 1 << 16, dtype=np.int64)])
+    so, do = oracle.offsets_of(src_l, dst_l, n_tiles, pts)
+    assert torch.equal(src_d[torch.from_numpy(so).cuda()], dst_d[torch.from_numpy(do).cuda()])
+
+
+def test_vector_copy_past_32_bit_indices():
+    n = (1 << 32) + 5  # one-byte words gathered at stride 2: 2^32 + 5 vectors
+    src_d = _device_bytes(2 * n, 321)
+    dst_d = torch.full((n,), workloads.SENTINEL, dtype=torch.uint8, device="cuda")
+    src_l, dst_l = L((n,), (2,)), L((n,), (1,))
+    assert lc().plan(src_l, dst_l, 1)["kernel_name"] == "vec_copy"
+    lc().layout_copy(src_d, src_l, dst_d, dst_l, elem_bytes=1)
+    assert lc().last_device_error()[0] == 0
+    _sampled_points_agree(src_d, dst_d, src_l, dst_l, 1, n, 3, edges=[0, (1 << 32) - 1, 1 << 32, n - 1])
+    assert torch.equal(dst_d, src_d[::2])
+    del src_d, dst_d
+    torch.cuda.empty_cache()
+
+
+def test_loop_copy_past_32_bit_indices():
+    m = (1 << 31) + (1 << 13)  # two rows of m one-byte words: 2^32 + 2^14 points in one tile
+    n = 2 * m
+    gap = 64
+    src_d = _device_bytes(n + gap, 322)
+    dst_d = torch.full((n,), workloads.SENTINEL, dtype=torch.uint8, device="cuda")
+    src_l, dst_l = L((2, m), (m + gap, 1)), L((2, m), (m, 1))
+    loop = [((n >> 14), 0, 16), (1024, 1, 0), (16, 0, 1)]
+    assert lc().loop_layout_info(loop, n) == (1024, n // 1024)
+    lc().layout_copy_loop(src_d, src_l, dst_d, dst_l, loop, elem_bytes=1)
+    assert lc().last_device_error()[0] == 0
+    _sampled_points_agree(src_d, dst_d, src_l, dst_l, 1, n, 4, edges=[0, m - 1, m, (1 << 32) - 1, 1 << 32, n - 1])
+    assert torch.equal(dst_d[:m], src_d[:m]) and torch.equal(dst_d[m:], src_d[m + gap:])
+    del src_d, dst_d
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("n", [(1 << 31) - (1 << 14), (1 << 31) + (1 << 20)])
+def test_loop_copy_around_the_split_cut_off(n):
+    """Tiles just under and just over 2^31 bytes: the first takes the split
+    path (31-bit byte offsets), the second the general path."""
+    src_d = _device_bytes(2 * n, 323)
+    dst_d = torch.full((2 * n,), workloads.SENTINEL, dtype=torch.uint8, device="cuda")
+    src_l, dst_l = L((n,), (1,)), L((n,), (1,))
+    loop = [(n >> 14, 0, 16), (1024, 1, 0), (16, 0, 1)]
+    lc().layout_copy_loop(src_d, src_l, dst_d, dst_l, loop, n_tiles=2, elem_bytes=1)
+    assert lc().last_device_error()[0] == 0
+    assert torch.equal(dst_d, src_d)
+    del src_d, dst_d
+    torch.cuda.empty_cache()
