@@ -1,5 +1,5 @@
 // Internal planner structures shared by the host planner (plan.cpp) and the
-// kernel launchers (kernels.cu).  Not part of the ABI.
+// kernel launchers (the k_*.cu translation units).  Not part of the ABI.
 #pragma once
 
 #include <cstdint>
