@@ -124,6 +124,9 @@ def kernel_sources_sha(kernel_name: str) -> str:
     for f in files + ["ptx.cuh", "device_common.cuh"]:
         with open(os.path.join(ROOT, "movement_primitives_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
+    if kernel_name == "warp_permute":  # its device functions live in the public device header
+        with open(os.path.join(ROOT, "include", "layout_copy_device.cuh"), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 

@@ -37,11 +37,13 @@ template <> struct unit_word<16> { using type = uint4; };
 /* Byte offsets, inside the two buffers, of the P words lane `lane` moves:
  * step r takes iteration j = r ^ ((lane >> shift) & mask), the logical index
  * unflatten(lane + 32 j) over the unit's extents (last mode fastest), and its
- * offset on each side. */
+ * offset on each side.  Computed once per lane; unrolled only for small
+ * PMAX, since 32 copies of the division loop make the code large enough that
+ * a lone warp waits on instruction fetch. */
 template <int W, int PMAX>
 __device__ __forceinline__ void warp_unit_offsets(const lc_warp_unit &u, int lane, int32_t (&soff)[PMAX],
                                                   int32_t (&doff)[PMAX]) {
-#pragma unroll
+#pragma unroll(PMAX <= 8 ? PMAX : 1)
     for (int r = 0; r < PMAX; ++r) {
         int32_t flat = lane + 32 * (r ^ ((lane >> u.shift) & u.mask)), so = 0, dof = 0;
         for (int i = u.n_modes - 1; i >= 0; --i) {

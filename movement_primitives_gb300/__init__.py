@@ -73,6 +73,37 @@ class TileLayout:
         return self.offset + (n_tiles - 1) * (self.tile_stride or span) + span
 
 
+_LAYOUT_CACHE = {}  # layout value -> (TileLayout, its C struct); the library only reads the struct
+_LAYOUT_CACHE_MAX = 1024
+
+
+def _layout_pair(obj):
+    """(TileLayout, CTileLayout) of a layout given as a TileLayout, a dict or a
+    sequence, converted once per distinct value (the conversion costs more
+    than the library's own cached planning of a small copy)."""
+    if isinstance(obj, TileLayout):
+        key = (obj.shape, obj.stride, obj.offset, obj.tile_stride)
+    elif isinstance(obj, dict):
+        st = obj.get("stride")
+        key = (tuple(obj["shape"]), None if st is None else tuple(st), obj.get("offset", 0),
+               obj.get("tile_stride", 0))
+    else:
+        key = None
+    pair = _LAYOUT_CACHE.get(key) if key is not None else None
+    if pair is None:
+        lay = TileLayout.of(obj)
+        pair = (lay, lay.to_c())
+        if key is not None:
+            if len(_LAYOUT_CACHE) >= _LAYOUT_CACHE_MAX:
+                _LAYOUT_CACHE.clear()
+            _LAYOUT_CACHE[key] = pair
+    return pair
+
+
+def _c_layout(obj) -> _lib.CTileLayout:
+    return _layout_pair(obj)[1]
+
+
 class LayoutCopyError(RuntimeError):
     def __init__(self, status: int, what: str = ""):
         self.status = status
@@ -102,7 +133,7 @@ def _stream_handle(stream) -> int:
 def layout_copy_ptr(src_ptr: int, src_layout, dst_ptr: int, dst_layout, elem_bytes: int,
                     n_tiles: int = 1, kernel="auto", stream=0) -> None:
     """Raw-pointer form: device addresses, layouts in elements, stream handle."""
-    sl, dl = TileLayout.of(src_layout).to_c(), TileLayout.of(dst_layout).to_c()
+    sl, dl = _c_layout(src_layout), _c_layout(dst_layout)
     st = _lib.lib().lc_layout_copy_ex(ctypes.c_void_p(src_ptr), ctypes.byref(sl),
                                       ctypes.c_void_p(dst_ptr), ctypes.byref(dl),
                                       int(elem_bytes), int(n_tiles), _kernel_id(kernel),
@@ -125,7 +156,7 @@ def layout_copy(src, src_layout, dst, dst_layout, n_tiles: int = 1, elem_bytes: 
     w = int(elem_bytes) if elem_bytes is not None else src.element_size()
     if elem_bytes is None and dst.element_size() != w:
         raise ValueError("source and destination element sizes differ; pass elem_bytes")
-    sl, dl = TileLayout.of(src_layout), TileLayout.of(dst_layout)
+    sl, dl = _layout_pair(src_layout)[0], _layout_pair(dst_layout)[0]
     for name, t, l in (("source", src, sl), ("destination", dst, dl)):
         need = l.footprint(n_tiles) * w
         have = t.numel() * t.element_size()
@@ -136,7 +167,7 @@ def layout_copy(src, src_layout, dst, dst_layout, n_tiles: int = 1, elem_bytes: 
 
 def host_staging_bytes(src_layout, dst_layout, elem_bytes: int, n_tiles: int = 1) -> int:
     """Device staging bytes layout_copy_host needs for full pipelining."""
-    sl, dl = TileLayout.of(src_layout).to_c(), TileLayout.of(dst_layout).to_c()
+    sl, dl = _c_layout(src_layout), _c_layout(dst_layout)
     return int(_lib.lib().lc_host_staging_bytes(ctypes.byref(sl), ctypes.byref(dl), int(elem_bytes),
                                                 int(n_tiles)))
 
@@ -156,7 +187,7 @@ def layout_copy_host(src, src_layout, dst, dst_layout, n_tiles: int = 1, elem_by
     if not (src.is_contiguous() and dst.is_contiguous()):
         raise ValueError("pass contiguous tensors; express strides through the layouts")
     w = int(elem_bytes) if elem_bytes is not None else src.element_size()
-    sl, dl = TileLayout.of(src_layout), TileLayout.of(dst_layout)
+    sl, dl = _layout_pair(src_layout)[0], _layout_pair(dst_layout)[0]
     for name, t, l in (("source", src, sl), ("destination", dst, dl)):
         need = l.footprint(n_tiles) * w
         if need > t.numel() * t.element_size():
@@ -187,7 +218,7 @@ def layout_copy_host_static(src, src_layout, dst, dst_layout, n_tiles: int = 1,
     if not (src.is_contiguous() and dst.is_contiguous()):
         raise ValueError("pass contiguous tensors; express strides through the layouts")
     w = int(elem_bytes) if elem_bytes is not None else src.element_size()
-    sl, dl = TileLayout.of(src_layout), TileLayout.of(dst_layout)
+    sl, dl = _layout_pair(src_layout)[0], _layout_pair(dst_layout)[0]
     for name, t, l in (("source", src, sl), ("destination", dst, dl)):
         if l.footprint(n_tiles) * w > t.numel() * t.element_size():
             raise ValueError("%s layout reaches past the tensor" % name)
@@ -214,7 +245,7 @@ def window_sum(a, b, window: int = 3, stream=None) -> None:
 
 def plan(src_layout, dst_layout, elem_bytes: int, n_tiles: int = 1, kernel="auto") -> dict:
     """What the planner would launch (host only; pointers assumed aligned)."""
-    sl, dl = TileLayout.of(src_layout).to_c(), TileLayout.of(dst_layout).to_c()
+    sl, dl = _c_layout(src_layout), _c_layout(dst_layout)
     info = _lib.CPlanInfo()
     _check(_lib.lib().lc_plan(ctypes.byref(sl), ctypes.byref(dl), int(elem_bytes), int(n_tiles),
                               _kernel_id(kernel), ctypes.byref(info)), "plan")
@@ -232,7 +263,7 @@ def warp_unit_plan(src_layout, dst_layout, elem_bytes: int):
     to warp_unit_run or to device code, `info` a dict of its fields plus
     `conflict_free` (False when no XOR choice removes every bank conflict; the
     plan still runs correctly)."""
-    sl, dl = TileLayout.of(src_layout).to_c(), TileLayout.of(dst_layout).to_c()
+    sl, dl = _c_layout(src_layout), _c_layout(dst_layout)
     u = _lib.CWarpUnit()
     st = _lib.lib().lc_warp_unit_plan(ctypes.byref(sl), ctypes.byref(dl), int(elem_bytes), ctypes.byref(u))
     if st not in (0, STATUS["LC_ERR_NO_SWIZZLE"]):
@@ -264,7 +295,7 @@ def warp_unit_run(src, dst, plan, elem_bytes: int, n_units: int, in_place: bool 
 
 def choose_swizzle(src_layout, dst_layout, elem_bytes: int) -> dict:
     """The warp permute's XOR swizzle for one warp shard (see lc_choose_swizzle)."""
-    sl, dl = TileLayout.of(src_layout).to_c(), TileLayout.of(dst_layout).to_c()
+    sl, dl = _c_layout(src_layout), _c_layout(dst_layout)
     v = [ctypes.c_int32() for _ in range(5)]
     st = _lib.lib().lc_choose_swizzle(ctypes.byref(sl), ctypes.byref(dl), int(elem_bytes),
                                       *[ctypes.byref(x) for x in v])
@@ -275,7 +306,7 @@ def choose_swizzle(src_layout, dst_layout, elem_bytes: int) -> dict:
 
 
 def swizzle_conflicts(src_layout, dst_layout, elem_bytes: int, k: int, shift: int):
-    sl, dl = TileLayout.of(src_layout).to_c(), TileLayout.of(dst_layout).to_c()
+    sl, dl = _c_layout(src_layout), _c_layout(dst_layout)
     cr, cw = ctypes.c_int32(), ctypes.c_int32()
     _check(_lib.lib().lc_swizzle_conflicts(ctypes.byref(sl), ctypes.byref(dl), int(elem_bytes),
                                            int(k), int(shift), ctypes.byref(cr), ctypes.byref(cw)),
@@ -341,7 +372,7 @@ def loop_layout_info(loop, n_elems: int):
 def layout_copy_loop_ptr(src_ptr: int, src_layout, dst_ptr: int, dst_layout, elem_bytes: int, loop,
                          n_tiles: int = 1, trace_ptr: int = 0, stream=0) -> None:
     """Raw-pointer form of layout_copy_loop (trace_ptr 0: no trace)."""
-    sl, dl = TileLayout.of(src_layout).to_c(), TileLayout.of(dst_layout).to_c()
+    sl, dl = _c_layout(src_layout), _c_layout(dst_layout)
     c = _loop_to_c(loop)
     st = _lib.lib().lc_layout_copy_loop(ctypes.c_void_p(src_ptr), ctypes.byref(sl), ctypes.c_void_p(dst_ptr),
                                         ctypes.byref(dl), int(elem_bytes), int(n_tiles), ctypes.byref(c),
@@ -364,7 +395,7 @@ def layout_copy_loop(src, src_layout, dst, dst_layout, loop, n_tiles: int = 1,
     w = int(elem_bytes) if elem_bytes is not None else src.element_size()
     if elem_bytes is None and dst.element_size() != w:
         raise ValueError("source and destination element sizes differ; pass elem_bytes")
-    sl, dl = TileLayout.of(src_layout), TileLayout.of(dst_layout)
+    sl, dl = _layout_pair(src_layout)[0], _layout_pair(dst_layout)[0]
     for name, t, l in (("source", src, sl), ("destination", dst, dl)):
         need = l.footprint(n_tiles) * w
         have = t.numel() * t.element_size()

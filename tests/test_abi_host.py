@@ -314,6 +314,24 @@ def test_layout_copy_loop_checks_before_launch(M):
     M.layout_copy_loop_ptr(4096, T((0, 8), (8, 1)), 1 << 20, T((0, 8), (1, 8)), 4, [(0, 1, 0)])
 
 
+def test_layout_conversion_cache(M):
+    """Layouts are converted to their C struct once per distinct value: a
+    changed dict gives a fresh struct, equal values share one, and the
+    bounded cache stays correct when it is cleared."""
+    d = {"shape": (4, 8), "stride": (8, 1), "offset": 3, "tile_stride": 0}
+    a = M._c_layout(d)
+    assert M._c_layout(dict(d)) is a
+    assert (a.rank, list(a.shape)[:2], list(a.stride)[:2], a.offset) == (2, [4, 8], [8, 1], 3)
+    d["offset"] = 5
+    b = M._c_layout(d)
+    assert b is not a and b.offset == 5 and a.offset == 3
+    assert M._c_layout(M.TileLayout((4, 8), (8, 1), 5)).offset == 5
+    for i in range(M._LAYOUT_CACHE_MAX + 10):  # overflow clears the cache
+        assert M._c_layout({"shape": (i + 1,), "stride": (1,)}).shape[0] == i + 1
+    assert M._c_layout(d).offset == 5
+    assert M.plan(M.TileLayout((32, 32)), M.TileLayout((32, 32), (1, 32)), 4)["kernel_name"] == "warp_permute"
+
+
 def test_fastdiv_host_mirror():
     """The invariant-divisor division used by the vector copy, re-derived here
     from the published method and checked against integer division."""

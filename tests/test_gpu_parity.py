@@ -555,7 +555,8 @@ def test_copies_capture_into_a_cuda_graph():
     stream, so it can be captured into a CUDA graph and replayed."""
     M = lc()
     cases = [workloads.config(2, scale="small"), workloads.config(3, scale="small"),
-             workloads.config(5, scale="small"), workloads.config(6, 2, scale="small")]
+             workloads.config(5, scale="small"), workloads.config(6, 2, scale="small"),
+             workloads.config(8, scale="small")]  # the last through lc_layout_copy_loop
     for cfg in cases:
         src_h = workloads.make_src(cfg)
         want = workloads.make_dst(cfg).numpy().copy()
@@ -563,8 +564,13 @@ def test_copies_capture_into_a_cuda_graph():
         src = src_h.cuda()
         dst = workloads.make_dst(cfg, device="cuda")
         side = torch.cuda.Stream()
-        run = lambda: M.layout_copy_ptr(src.data_ptr(), cfg["src"], dst.data_ptr(), cfg["dst"],
-                                        cfg["elem_bytes"], cfg["n_tiles"], stream=side.cuda_stream)
+        if "loop" in cfg:
+            run = lambda: M.layout_copy_loop_ptr(src.data_ptr(), cfg["src"], dst.data_ptr(), cfg["dst"],
+                                                 cfg["elem_bytes"], cfg["loop"], cfg["n_tiles"],
+                                                 stream=side.cuda_stream)
+        else:
+            run = lambda: M.layout_copy_ptr(src.data_ptr(), cfg["src"], dst.data_ptr(), cfg["dst"],
+                                            cfg["elem_bytes"], cfg["n_tiles"], stream=side.cuda_stream)
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):
             run()  # warm-up outside the capture
