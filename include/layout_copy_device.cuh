@@ -34,24 +34,53 @@ template <> struct unit_word<4> { using type = uint32_t; };
 template <> struct unit_word<8> { using type = uint2; };
 template <> struct unit_word<16> { using type = uint4; };
 
+/* Element offsets of flat index `flat` of a unit (last mode fastest). */
+__device__ __forceinline__ void unit_point(const lc_warp_unit &u, int32_t flat, int32_t &so, int32_t &dof) {
+    so = 0;
+    dof = 0;
+    for (int i = u.n_modes - 1; i >= 0; --i) {
+        const int32_t c = flat % u.extent[i];
+        flat /= u.extent[i];
+        so += c * u.src_stride[i];
+        dof += c * u.dst_stride[i];
+    }
+}
+
 /* Byte offsets, inside the two buffers, of the P words lane `lane` moves:
  * step r takes iteration j = r ^ ((lane >> shift) & mask), the logical index
  * unflatten(lane + 32 j) over the unit's extents (last mode fastest), and its
- * offset on each side.  Computed once per lane; unrolled only for small
- * PMAX, since 32 copies of the division loop make the code large enough that
- * a lone warp waits on instruction fetch. */
+ * offset on each side.  When 32 lies on the divisibility chain of the unit's
+ * suffix products (every suffix product divides 32 or is a multiple of it),
+ * the lane digits and the j digits of lane + 32 j are disjoint, so its
+ * offsets are those of lane plus those of 32 j: each lane unflattens its own
+ * index and 32 * lane, and the j parts travel by warp shuffles.  Otherwise
+ * each step unflattens its index.  Call with all 32 lanes of the warp. */
 template <int W, int PMAX>
 __device__ __forceinline__ void warp_unit_offsets(const lc_warp_unit &u, int lane, int32_t (&soff)[PMAX],
                                                   int32_t (&doff)[PMAX]) {
+    bool nests = true;
+    int32_t suffix = 1;
+    for (int i = u.n_modes - 1; i >= 0; --i) {
+        suffix *= u.extent[i];
+        nests = nests && (suffix % 32 == 0 || 32 % suffix == 0);
+    }
+    const int sw = (lane >> u.shift) & u.mask;
+    if (nests) {
+        int32_t ls, ld, js, jd;
+        unit_point(u, lane, ls, ld);
+        unit_point(u, lane < u.P ? 32 * lane : 0, js, jd);
+#pragma unroll
+        for (int r = 0; r < PMAX; ++r) {
+            const int j = (r ^ sw) & 31;
+            soff[r] = (ls + __shfl_sync(0xffffffffu, js, j)) * W;
+            doff[r] = (ld + __shfl_sync(0xffffffffu, jd, j)) * W;
+        }
+        return;
+    }
 #pragma unroll(PMAX <= 8 ? PMAX : 1)
     for (int r = 0; r < PMAX; ++r) {
-        int32_t flat = lane + 32 * (r ^ ((lane >> u.shift) & u.mask)), so = 0, dof = 0;
-        for (int i = u.n_modes - 1; i >= 0; --i) {
-            const int32_t c = flat % u.extent[i];
-            flat /= u.extent[i];
-            so += c * u.src_stride[i];
-            dof += c * u.dst_stride[i];
-        }
+        int32_t so, dof;
+        unit_point(u, lane + 32 * (r ^ sw), so, dof);
         soff[r] = so * W;
         doff[r] = dof * W;
     }
