@@ -526,6 +526,33 @@ def test_warp_unit_on_shared_buffers(in_place):
         done += 1
 
 
+@pytest.mark.parametrize("shape", [(6, 48), (2, 3, 16), (3, 32), (32, 32), (4, 8, 32)])
+def test_warp_units_whose_radix_does_or_does_not_nest_32(shape):
+    """Lane offsets come from shuffles where 32 lies on the divisibility chain
+    of the unit's suffix products ((3, 32), (32, 32), (4, 8, 32)) and from a
+    per-step unflatten where it does not ((6, 48): 48; (2, 3, 16): 48): both,
+    in the global warp permute and in the shared-buffer op, against the
+    oracle."""
+    M = lc()
+    perm = tuple(reversed(range(len(shape))))
+    src_l, dst_l = L(shape, row_major(shape)), L(shape, permuted(shape, perm))
+    for w in (1, 4, 16):
+        assert run_case(src_l, dst_l, w, n_tiles=5, kernel="warp_permute", seed=w) == "warp_permute"
+        plan, info = M.warp_unit_plan(src_l, dst_l, w)
+        scos, dcos = info["src_cosize"], info["dst_cosize"]
+        if max(scos, dcos) * w > 8192:
+            continue
+        n = 7
+        g = torch.Generator().manual_seed(w)
+        src_h = torch.randint(0, 256, (n * scos * w,), generator=g, dtype=torch.uint8)
+        want = np.full(n * dcos * w, workloads.SENTINEL, np.uint8)
+        oracle.copy(src_h.numpy(), dict(src_l, tile_stride=scos), want, dict(dst_l, tile_stride=dcos), w, n)
+        dst_d = torch.from_numpy(np.full(n * dcos * w, workloads.SENTINEL, np.uint8)).cuda()
+        M.warp_unit_run(src_h.cuda(), dst_d, plan, w, n, stream=torch.cuda.current_stream().cuda_stream)
+        torch.cuda.synchronize()
+        assert np.array_equal(dst_d.cpu().numpy(), want), (shape, w)
+
+
 def test_warp_unit_run_refusals():
     M = lc()
     plan, _ = M.warp_unit_plan(L((4, 32), (32, 1)), L((4, 32), (1, 4)), 4)
