@@ -4,6 +4,7 @@
                     [--workload 1..8] [--elem-bytes W] [--kernel auto|vec_copy|
                     warp_permute|tile_transpose|smem_transpose|tma_copy]
                     [--loop "[(extent, thread_stride, slot_stride), ...]"]
+                    [--in-place | --unit-run]
                     [--graph] [--copy-ceiling] [--e2e-steps E] [--no-cpu-baseline]
 
 A step is one lc_layout_copy over the whole workload (one kernel launch);
@@ -16,7 +17,11 @@ transpose; 4 an 8192^2 transpose of W-byte words; 5 a (256,32,128,128) bf16
 permute (0,2,1,3); 6 an 8191 x 8193 transpose of W-byte words (strides off
 the 16-byte grid); 7 the window sum of three over 2^28 float32 outputs;
 8 workload 5's permute as 256 tiles moved under an explicit loop layout
-(lc_layout_copy_loop; --loop replaces the workload's override).
+(lc_layout_copy_loop; --loop replaces the workload's override).  With
+workload 2, --in-place permutes the buffer in place (destination = source,
+the aliasing the warp permute allows) and --unit-run moves the same units
+through lc_warp_unit_run (the op between shared-memory buffers, staged from
+and back to HBM).
 
 --impl reference times the CPU oracle (the plain C word loop) on the host
 cores over a bounded sample of the same workload; it never touches a GPU.
@@ -64,6 +69,10 @@ def parse_args(argv=None):
                    help="replay the K timed launches from one CUDA graph (launch-bound copies)")
     p.add_argument("--loop", default=None,
                    help="loop layout for workload 8, a Python literal list of (extent, thread_stride, slot_stride)")
+    p.add_argument("--in-place", action="store_true",
+                   help="workload 2 permuted in place (destination = source buffer)")
+    p.add_argument("--unit-run", action="store_true",
+                   help="workload 2's units through lc_warp_unit_run (shared-memory buffers)")
     p.add_argument("--n-tiles", type=int, default=None,
                    help="override the tile count (a smaller case of the same kernel, e.g. for ncu)")
     return p.parse_args(argv)
@@ -116,7 +125,8 @@ def describe(cfg) -> str:
 
 
 def kernel_sources_sha(kernel_name: str) -> str:
-    files = {"warp_permute": ["k_warp.cu", "k_warp.cuh"] + ["k_warp_w%d.cu" % w for w in (1, 2, 4, 8, 16)], "tile_transpose": ["k_tile.cu"],
+    warp = ["k_warp.cu", "k_warp.cuh"] + ["k_warp_w%d.cu" % w for w in (1, 2, 4, 8, 16)]
+    files = {"warp_permute": warp, "warp_unit_shared": warp, "tile_transpose": ["k_tile.cu"],
              "vec_copy": ["k_vec.cu"], "smem_transpose": ["k_smem.cu"],
              "tma_copy": ["k_tma_copy.cu"], "window_sum": ["k_stencil.cu"],
              "loop_copy": ["k_loop.cu"]}.get(kernel_name, [])
@@ -124,7 +134,7 @@ def kernel_sources_sha(kernel_name: str) -> str:
     for f in files + ["ptx.cuh", "device_common.cuh"]:
         with open(os.path.join(ROOT, "movement_primitives_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
-    if kernel_name == "warp_permute":  # its device functions live in the public device header
+    if kernel_name in ("warp_permute", "warp_unit_shared"):  # device functions in the public device header
         with open(os.path.join(ROOT, "include", "layout_copy_device.cuh"), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -381,6 +391,12 @@ def run_ours(args):
     cfg = workloads.config(args.workload, args.elem_bytes)
     if args.n_tiles:
         cfg["n_tiles"] = args.n_tiles
+    mode = "in_place" if args.in_place else "unit_run" if args.unit_run else None
+    if mode and (args.workload != 2 or (args.in_place and args.unit_run)):
+        raise SystemExit("--in-place or --unit-run (one of them) applies to workload 2")
+    if mode:
+        cfg["name"] += "_" + mode
+        args.e2e_steps = 0  # the host-buffer entry point has no such variant
     step_bytes = workload_bytes(cfg)
     src_h = workloads.make_src(cfg)
     src = src_h.to(dev)
@@ -388,21 +404,45 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
     loop = cfg.get("loop")
+    unit = None
+    if mode == "unit_run":
+        # workload 2's tiles are two (4, 32) units back to back on both sides
+        unit, _info = lc.warp_unit_plan(dict(shape=(4, 32), stride=(32, 1)), dict(shape=(4, 32), stride=(1, 4)),
+                                        cfg["elem_bytes"])
+        n_units = cfg["n_tiles"] * 2
     if loop is not None and args.loop:
         import ast
         loop = [tuple(m) for m in ast.literal_eval(args.loop)]
     if loop is not None:
         kernel_name = "loop_copy"
+    elif unit is not None:
+        kernel_name = "warp_unit_shared"
     else:
         kernel_name = lc.plan(cfg["src"], cfg["dst"], cfg["elem_bytes"], cfg["n_tiles"], args.kernel)["kernel_name"]
 
-    def launch(stream_handle):
-        if loop is not None:
+    def launch(stream_handle, out=None):
+        out = dst if out is None else out
+        if unit is not None:
+            lc.warp_unit_run(src, out, unit, cfg["elem_bytes"], n_units, stream=stream_handle)
+        elif mode == "in_place":
+            lc.layout_copy_ptr(out.data_ptr(), cfg["src"], out.data_ptr(), cfg["dst"], cfg["elem_bytes"],
+                               cfg["n_tiles"], kernel=args.kernel, stream=stream_handle)
+        elif loop is not None:
             lc.layout_copy_loop_ptr(src.data_ptr(), cfg["src"], dst.data_ptr(), cfg["dst"], cfg["elem_bytes"],
                                     loop, cfg["n_tiles"], 0, stream_handle)
         else:
-            lc.layout_copy_ptr(src.data_ptr(), cfg["src"], dst.data_ptr(), cfg["dst"], cfg["elem_bytes"],
+            lc.layout_copy_ptr(src.data_ptr(), cfg["src"], out.data_ptr(), cfg["dst"], cfg["elem_bytes"],
                                cfg["n_tiles"], kernel=args.kernel, stream=stream_handle)
+
+    if mode == "in_place":
+        # one in-place step on a copy of the source is checked below; the
+        # timed steps keep permuting the same buffer (same work every step)
+        del dst
+        dst = src.clone()
+        launch(sh, dst)
+        torch.cuda.synchronize()
+        checked = dst.clone()
+        dst = src
 
     def step():
         launch(sh)
@@ -418,8 +458,8 @@ def run_ours(args):
     pts = np.random.default_rng(0).integers(0, n, 4096)
     so, do = oracle.offsets_of(cfg["src"], cfg["dst"], cfg["n_tiles"], pts)
     w = cfg["elem_bytes"]
-    sv = src.view(-1, w)
-    dv = dst.view(-1, w)
+    sv = src_h.to(dev).view(-1, w) if mode == "in_place" else src.view(-1, w)
+    dv = (checked if mode == "in_place" else dst).view(-1, w)
     if not torch.equal(sv[torch.from_numpy(so).to(dev)], dv[torch.from_numpy(do).to(dev)]):
         raise RuntimeError("spot check against the oracle failed")
 
@@ -564,7 +604,7 @@ def run_ours(args):
             "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": dtype_name(cfg), "data": "synthetic",
             "config": {"workload": describe(cfg), "kernel": kernel_name,
-                       "loop_layout": loop,
+                       "loop_layout": loop, "mode": mode,
                        "bytes_per_step": step_bytes,
                        "l2": ("L2 flushed between steps (%d MiB write outside the timed launches; "
                               "value from per-launch CUDA events)" % (2 * workloads.HBM_L2_BYTES >> 20)

@@ -345,13 +345,15 @@ int lc_warp_unit_plan(const lc_tile_layout *src_layout, const lc_tile_layout *ds
 
 /* Runs the op on n_units units, each staged in shared memory.  src holds
  * n_units source buffers back to back (unit i at i * src_cosize * elem_bytes
- * bytes), dst likewise with dst_cosize.  One warp per unit copies the source
- * buffer into shared buffer A and (in_place = 0) the destination buffer into
- * shared buffer B, permutes A -> B (in_place = 0) or A -> A (in_place = 1,
+ * bytes), dst likewise with dst_cosize.  For each unit, a warp copies the
+ * source buffer into shared buffer A and (in_place = 0) the destination
+ * buffer into shared buffer B, permutes A -> B (in_place = 0) or A -> A (in_place = 1,
  * the aliased form: the destination layout is applied inside A, which needs
  * src_cosize >= dst_cosize), and copies the destination buffer back to dst.
  * Bytes of the destination buffer outside its image keep their values
- * (in_place = 0) or hold A's (in_place = 1).  Each buffer must fit
+ * (in_place = 0) or hold A's (in_place = 1).  A warp stages up to 8 units
+ * at a time (2 KiB of each buffer kind), copying them in 16-byte chunks when
+ * both buffer sizes are multiples of 16 bytes.  Each buffer must fit
  * LC_WARP_UNIT_MAX_BYTES.  Asynchronous on `stream`.  Errors: LC_ERR_NULL,
  * LC_ERR_SHAPE (buffers too large, bad counts), LC_ERR_ALIGN (pointers not
  * 16-byte aligned), LC_ERR_OVERLAP (src and dst ranges overlap),

@@ -107,6 +107,12 @@ extern "C" int lc_warp_unit_run(const void *src, void *dst, const lc_warp_unit *
     a.sbytes = static_cast<uint32_t>(sb);
     a.dbytes = static_cast<uint32_t>(db);
     a.buf = static_cast<uint32_t>((std::max(sb, db) + 15) / 16 * 16);
+    a.upw = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(kUnitMaxPerWarp, kUnitStageBytes / a.buf)));
+    a.chunked = sb % 16 == 0 && db % 16 == 0;
+    if (a.chunked) {
+        a.schunks = make_fastdiv(static_cast<uint32_t>(sb / 16));
+        a.dchunks = make_fastdiv(static_cast<uint32_t>(db / 16));
+    }
     a.in_place = in_place ? 1 : 0;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     switch (elem_bytes) {

@@ -154,6 +154,11 @@ __global__ void __launch_bounds__(kWarpThreads, LC_WARP_MIN_BLOCKS) k_warp_permu
 // with lc_device::warp_unit_permute, and copies the destination buffer out.
 constexpr int kUnitWarps = 4;
 
+// Units staged per warp at a time: as many as fit 2 KiB of each buffer kind,
+// at most 8, so that a lane keeps several 16-byte chunks in flight.
+constexpr uint32_t kUnitStageBytes = 2048;
+constexpr int kUnitMaxPerWarp = 8;
+
 struct UnitArgs {
     const uint8_t *src;
     uint8_t *dst;
@@ -162,6 +167,9 @@ struct UnitArgs {
     uint32_t sbytes, dbytes;  // bytes of one source / destination buffer
     uint32_t buf;             // shared bytes per buffer (16-byte multiple)
     int32_t in_place;
+    int32_t upw;              // units staged per warp at a time
+    int32_t chunked;          // sbytes and dbytes are 16-byte multiples
+    FastDiv schunks, dchunks;  // 16-byte chunks per source / destination buffer
 };
 
 // Byte copy by one warp: 16-byte words when both ends and the size allow.
@@ -174,22 +182,70 @@ __device__ __forceinline__ void warp_copy(uint8_t *d, const uint8_t *s, uint32_t
     }
 }
 
+// Buffers of `cnt` units, `bytes` each back to back in global memory, into
+// (to_shared) or out of their shared buffers, unit u's at slot + u * pitch:
+// 16-byte chunks, kChunksInFlight per lane loaded before any is stored.
+template <bool TO_SHARED>
+__device__ __forceinline__ void unit_chunks(uint8_t *slot, uint32_t pitch, uint8_t *g, uint32_t bytes,
+                                            const FastDiv &per, int cnt, int lane) {
+    const int n = cnt * static_cast<int>(bytes / 16);
+    for (int base = 0; base < n; base += 32 * kChunksInFlight) {
+        uint4 v[kChunksInFlight];
+        uint8_t *to[kChunksInFlight];
+#pragma unroll
+        for (int k = 0; k < kChunksInFlight; ++k) {
+            const int f = base + lane + 32 * k;
+            to[k] = nullptr;
+            if (f < n) {
+                const uint32_t u = fast_div(static_cast<uint32_t>(f), per);
+                uint8_t *sh = slot + u * pitch + 16 * (f - u * per.d);
+                uint8_t *gl = g + 16 * static_cast<int64_t>(f);
+                v[k] = *reinterpret_cast<const uint4 *>(TO_SHARED ? gl : sh);
+                to[k] = TO_SHARED ? sh : gl;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kChunksInFlight; ++k)
+            if (to[k]) *reinterpret_cast<uint4 *>(to[k]) = v[k];
+    }
+}
+
 template <int W, int PMAX>
 __global__ void __launch_bounds__(kUnitWarps * 32) k_warp_unit_shared(const __grid_constant__ UnitArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint8_t *A = smem + static_cast<size_t>(warp) * 2 * a.buf;
-    uint8_t *B = A + a.buf;
+    // unit u of this warp's stage: A = slot + u * 2 buf, B = A + buf
+    uint8_t *const slot = smem + static_cast<size_t>(warp) * a.upw * 2 * a.buf;
+    const uint32_t pitch = 2 * a.buf;
     int32_t soff[PMAX], doff[PMAX];
     lc_device::warp_unit_offsets<W, PMAX>(a.unit, lane, soff, doff);
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kUnitWarps + warp; i < a.n_units;
-         i += static_cast<int64_t>(gridDim.x) * kUnitWarps) {
-        warp_copy(A, a.src + i * a.sbytes, a.sbytes, lane);
-        if (!a.in_place) warp_copy(B, a.dst + i * a.dbytes, a.dbytes, lane);
+    const int64_t n_groups = (a.n_units + a.upw - 1) / a.upw;
+    for (int64_t g = static_cast<int64_t>(blockIdx.x) * kUnitWarps + warp; g < n_groups;
+         g += static_cast<int64_t>(gridDim.x) * kUnitWarps) {
+        const int64_t first = g * a.upw;
+        const int cnt = static_cast<int>(lmin(a.upw, a.n_units - first));
+        uint8_t *const sg = const_cast<uint8_t *>(a.src) + first * a.sbytes;
+        uint8_t *const dg = a.dst + first * a.dbytes;
+        if (a.chunked) {
+            unit_chunks<true>(slot, pitch, sg, a.sbytes, a.schunks, cnt, lane);
+            if (!a.in_place) unit_chunks<true>(slot + a.buf, pitch, dg, a.dbytes, a.dchunks, cnt, lane);
+        } else {
+            for (int u = 0; u < cnt; ++u) {
+                warp_copy(slot + u * pitch, sg + static_cast<int64_t>(u) * a.sbytes, a.sbytes, lane);
+                if (!a.in_place) warp_copy(slot + u * pitch + a.buf, dg + static_cast<int64_t>(u) * a.dbytes,
+                                           a.dbytes, lane);
+            }
+        }
         __syncwarp();
-        uint8_t *out = a.in_place ? A : B;
-        lc_device::warp_unit_permute<W, PMAX>(out, A, a.unit.P, soff, doff);
-        warp_copy(a.dst + i * a.dbytes, out, a.dbytes, lane);
+        const uint32_t out = a.in_place ? 0 : a.buf;  // offset of the permuted buffer in a unit's slot
+        for (int u = 0; u < cnt; ++u)
+            lc_device::warp_unit_permute<W, PMAX>(slot + u * pitch + out, slot + u * pitch, a.unit.P, soff, doff);
+        if (a.chunked) {
+            unit_chunks<false>(slot + out, pitch, dg, a.dbytes, a.dchunks, cnt, lane);
+        } else {
+            for (int u = 0; u < cnt; ++u)
+                warp_copy(dg + static_cast<int64_t>(u) * a.dbytes, slot + u * pitch + out, a.dbytes, lane);
+        }
         __syncwarp();
     }
 }
@@ -214,11 +270,12 @@ int launch_warp_t(const WarpArgs &a, cudaStream_t stream) {
 template <int W, int PMAX>
 int launch_unit_t(const UnitArgs &a, cudaStream_t stream) {
     const void *fn = reinterpret_cast<const void *>(&k_warp_unit_shared<W, PMAX>);
-    const int smem = kUnitWarps * 2 * static_cast<int>(a.buf);
+    const int smem = kUnitWarps * a.upw * 2 * static_cast<int>(a.buf);
     int sms, per;
     if (prepare(fn, kUnitWarps * 32, smem, kUnitWarps * 2 * LC_WARP_UNIT_MAX_BYTES, &sms, &per) != cudaSuccess)
         return LC_ERR_CUDA;
-    const int64_t grid = lmin((a.n_units + kUnitWarps - 1) / kUnitWarps, int64_t(sms) * std::max(per, 1));
+    const int64_t groups = (a.n_units + a.upw - 1) / a.upw;
+    const int64_t grid = lmin((groups + kUnitWarps - 1) / kUnitWarps, int64_t(sms) * std::max(per, 1));
     k_warp_unit_shared<W, PMAX><<<static_cast<unsigned>(grid), kUnitWarps * 32, smem, stream>>>(a);
     return finish_launch();
 }
