@@ -392,8 +392,7 @@ def run_ours(args):
     if args.n_tiles:
         cfg["n_tiles"] = args.n_tiles
     mode = "in_place" if args.in_place else "unit_run" if args.unit_run else None
-    if mode and (args.workload != 2 or (args.in_place and args.unit_run)):
-        raise SystemExit("--in-place or --unit-run (one of them) applies to workload 2")
+    check_args(args)
     if mode:
         cfg["name"] += "_" + mode
         args.e2e_steps = 0  # the host-buffer entry point has no such variant
@@ -746,8 +745,17 @@ def run_window_sum(args):
     return 0
 
 
+def check_args(args) -> None:
+    """Refuses flag combinations that name no workload."""
+    if (args.in_place or args.unit_run) and (args.workload != 2 or (args.in_place and args.unit_run)):
+        raise SystemExit("--in-place or --unit-run (one of them) applies to workload 2")
+    if args.loop and args.workload != 8:
+        raise SystemExit("--loop applies to workload 8")
+
+
 def main(argv=None):
     args = parse_args(argv)
+    check_args(args)
     if args.workload == 7:
         return run_window_sum(args)
     if args.impl == "reference":

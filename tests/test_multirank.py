@@ -69,3 +69,14 @@ def test_single_process_helpers():
     one = dict(cfg, n_tiles=1)
     s = bench.sampled(one, 0.5)
     assert s["src"]["shape"] == (2, 4) and s["dst"]["shape"] == (2, 4)
+
+
+def test_bench_flag_combinations():
+    """Mode flags that name no workload are refused before any GPU work."""
+    import bench
+    for argv in (["--in-place", "--workload", "5"], ["--unit-run", "--in-place"], ["--loop", "[(1, 1, 0)]"],
+                 ["--unit-run", "--workload", "8"]):
+        with pytest.raises(SystemExit):
+            bench.check_args(bench.parse_args(argv))
+    for argv in ([], ["--in-place"], ["--unit-run"], ["--workload", "8", "--loop", "[(4, 1, 0)]"]):
+        bench.check_args(bench.parse_args(argv))
