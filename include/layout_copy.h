@@ -412,6 +412,27 @@ int lc_loop_layout_default(int64_t n_elems, int32_t num_thread, int32_t vector_s
 int lc_loop_layout_info(const lc_loop_layout *loop, int64_t n_elems, int32_t *num_threads,
                         int64_t *slots_per_thread);
 
+/* What lc_layout_copy_loop would do for these layouts, with both base
+ * pointers assumed 16-byte aligned (host only, like lc_plan):
+ *   num_threads, slots_per_thread  T and L of the override
+ *   points_per_tile                N = T * L
+ *   vec                            words moved per vector (1 = single words)
+ *   split                          1 when the loop's and the tile's radices
+ *                                  nest and a tile spans under 2^31 bytes:
+ *                                  offsets are a per-thread part plus a
+ *                                  per-slot part from a shared table
+ * Errors: as lc_layout_copy_loop's validation. */
+typedef struct {
+    int32_t num_threads;
+    int64_t slots_per_thread;
+    int64_t points_per_tile;
+    int32_t vec;
+    int32_t split;
+} lc_loop_plan_info;
+
+int lc_loop_plan(const lc_tile_layout *src_layout, const lc_tile_layout *dst_layout, int32_t elem_bytes,
+                 int64_t n_tiles, const lc_loop_layout *loop, lc_loop_plan_info *out);
+
 /* lc_layout_copy with the partition given by `loop` instead of the
  * library's planner: each tile is one CTA of T threads (tiles spread over
  * the grid), and thread t moves its slots 0 .. L-1 in order, the point of

@@ -20,7 +20,7 @@ __all__ = ["TileLayout", "LayoutCopyError", "layout_copy", "layout_copy_ptr", "l
            "host_staging_bytes", "layout_copy_host_static", "window_sum", "plan",
            "choose_swizzle", "swizzle_conflicts", "gmem_smem_partition",
            "last_device_error", "debug_wait_timeout", "warp_unit_plan", "warp_unit_run",
-           "loop_layout_default", "loop_layout_info", "layout_copy_loop", "layout_copy_loop_ptr",
+           "loop_layout_default", "loop_layout_info", "loop_plan", "layout_copy_loop", "layout_copy_loop_ptr",
            "KERNELS", "STATUS"]
 
 
@@ -367,6 +367,16 @@ def loop_layout_info(loop, n_elems: int):
     _check(_lib.lib().lc_loop_layout_info(ctypes.byref(c), int(n_elems), ctypes.byref(T), ctypes.byref(L)),
            "loop_layout_info")
     return T.value, L.value
+
+
+def loop_plan(src_layout, dst_layout, elem_bytes: int, loop, n_tiles: int = 1) -> dict:
+    """What layout_copy_loop would do (bases assumed aligned): threads,
+    slots per thread, points per tile, vector width in words, split path."""
+    info = _lib.CLoopPlanInfo()
+    _check(_lib.lib().lc_loop_plan(ctypes.byref(_c_layout(src_layout)), ctypes.byref(_c_layout(dst_layout)),
+                                   int(elem_bytes), int(n_tiles), ctypes.byref(_loop_to_c(loop)),
+                                   ctypes.byref(info)), "loop_plan")
+    return {f: getattr(info, f) for f, _ in _lib.CLoopPlanInfo._fields_}
 
 
 def layout_copy_loop_ptr(src_ptr: int, src_layout, dst_ptr: int, dst_layout, elem_bytes: int, loop,

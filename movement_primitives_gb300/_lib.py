@@ -76,6 +76,11 @@ class CLoopLayout(ctypes.Structure):
                 ("slot_stride", ctypes.c_int64 * MAX_RANK)]
 
 
+class CLoopPlanInfo(ctypes.Structure):
+    _fields_ = [("num_threads", ctypes.c_int32), ("slots_per_thread", ctypes.c_int64),
+                ("points_per_tile", ctypes.c_int64), ("vec", ctypes.c_int32), ("split", ctypes.c_int32)]
+
+
 _P_LAYOUT = ctypes.POINTER(CTileLayout)
 _P_LOOP = ctypes.POINTER(CLoopLayout)
 _P_I32 = ctypes.POINTER(ctypes.c_int32)
@@ -111,6 +116,8 @@ PROTOTYPES = {
                                         ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p]),
     "lc_loop_layout_default": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _P_LOOP]),
     "lc_loop_layout_info": (ctypes.c_int, [_P_LOOP, ctypes.c_int64, _P_I32, _P_I64]),
+    "lc_loop_plan": (ctypes.c_int, [_P_LAYOUT, _P_LAYOUT, ctypes.c_int32, ctypes.c_int64, _P_LOOP,
+                                    ctypes.POINTER(CLoopPlanInfo)]),
     "lc_layout_copy_loop": (ctypes.c_int, [ctypes.c_void_p, _P_LAYOUT, ctypes.c_void_p, _P_LAYOUT,
                                            ctypes.c_int32, ctypes.c_int64, _P_LOOP, ctypes.c_void_p,
                                            ctypes.c_void_p]),

@@ -1063,3 +1063,19 @@ extern "C" int lc_loop_layout_info(const lc_loop_layout *loop, int64_t n_elems, 
     if (slots_per_thread) *slots_per_thread = lp.L;
     return LC_OK;
 }
+
+extern "C" int lc_loop_plan(const lc_tile_layout *src_layout, const lc_tile_layout *dst_layout,
+                            int32_t elem_bytes, int64_t n_tiles, const lc_loop_layout *loop,
+                            lc_loop_plan_info *out) {
+    if (!out) return LC_ERR_NULL;
+    lc::LoopPlan lp;
+    lc::PtrInfo ptr;  // bases assumed aligned
+    const int st = lc::make_loop_plan(src_layout, dst_layout, elem_bytes, n_tiles, loop, ptr, &lp);
+    if (st) return st;
+    out->num_threads = static_cast<int32_t>(lp.T);
+    out->slots_per_thread = lp.L;
+    out->points_per_tile = lp.N;
+    out->vec = lp.vec;
+    out->split = lp.split ? 1 : 0;
+    return LC_OK;
+}

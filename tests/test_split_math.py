@@ -147,3 +147,67 @@ def test_warp_unit_offsets_split_exactly_when_32_nests():
             not_nested += 1
             broke += not splits
     assert nested > 50 and not_nested > 5 and broke > 0
+
+
+# ---------------------------------------------------------------------------
+# the library's own decisions (lc_loop_plan, host only) against these facts
+# ---------------------------------------------------------------------------
+
+def _lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    import movement_primitives_gb300
+    return movement_primitives_gb300
+
+
+def test_loop_plan_decisions():
+    M = _lib()
+    L = lambda sh, st: dict(shape=sh, stride=st)
+    got = M.loop_plan(L((32, 128, 128), (16384, 128, 1)), L((32, 128, 128), (128, 4096, 1)), 2,
+                      [(64, 0, 8), (1024, 1, 0), (8, 0, 1)], 256)
+    assert got == dict(num_threads=1024, slots_per_thread=512, points_per_tile=1 << 19, vec=8, split=1)
+    got = M.loop_plan(L((3, 4), (4, 1)), L((3, 4), (1, 3)), 4, [(2, 1, 0), (6, 0, 1)], 2)
+    assert (got["vec"], got["split"]) == (1, 0)  # suffix products 6 and 4 do not nest
+    got = M.loop_plan(L((64, 128), (128, 1)), L((64, 128), (128, 1)), 4, [(16, 1, 0), (4, 0, 128), (128, 0, 1)], 2)
+    assert (got["vec"], got["split"]) == (4, 1)
+    got = M.loop_plan(L((8, 8), (8, 1)), L((8, 8), (1, 8)), 4, [(8, 0, 1), (8, 1, 0)])
+    assert (got["vec"], got["split"]) == (1, 1)  # the innermost loop mode is a thread mode
+    for n, split in [((1 << 31) - (1 << 14), 1), ((1 << 31) + (1 << 20), 0)]:  # the 2^31-byte cut-off
+        got = M.loop_plan(L((n,), (1,)), L((n,), (1,)), 1, [(n >> 14, 0, 16), (1024, 1, 0), (16, 0, 1)], 2)
+        assert (got["vec"], got["split"]) == (16, split)
+
+
+def test_loop_plan_split_and_vectors_are_sound():
+    """Random tiles and overrides: a split the library takes holds on the
+    oracle's offsets, a nesting chain always gives one, and each vector of
+    `vec` slots covers consecutive offsets on both sides."""
+    M = _lib()
+    rng = random.Random(9)
+    splits = vectors = 0
+    for _ in range(200):
+        modes = _random_tile(rng)
+        ext = tuple(m[0] for m in modes)
+        src = dict(shape=ext, stride=tuple(m[1] for m in modes))
+        dst = dict(shape=ext, stride=tuple(m[2] for m in modes))
+        total = int(np.prod(ext))
+        loop = _random_loop(rng, total)
+        w = rng.choice([1, 2, 4])
+        plan = M.loop_plan(src, dst, w, loop)
+        if _chain(_suffixes([m[0] for m in loop]) + _suffixes(list(ext))):
+            assert plan["split"] == 1, (modes, loop)
+        if plan["split"]:
+            splits += 1
+            for flat in range(total):
+                t, s = _parts(loop, flat)
+                a, b, c = _offsets(modes, flat), _offsets(modes, t), _offsets(modes, s)
+                assert a == (b[0] + c[0], b[1] + c[1]), (modes, loop, flat)
+        v = plan["vec"]
+        if v > 1:
+            vectors += 1
+            inner = next(m for m in reversed(loop) if m[0] > 1)
+            assert inner[2] == 1 and inner[0] % v == 0, (loop, v)
+            for flat in range(0, total, v):
+                base = _offsets(modes, flat)
+                for j in range(1, v):
+                    assert _offsets(modes, flat + j) == (base[0] + j, base[1] + j), (modes, loop, v)
+    assert splits > 50 and vectors > 10
