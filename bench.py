@@ -124,19 +124,31 @@ def describe(cfg) -> str:
         cfg["name"], cfg["n_tiles"], s["shape"], cfg["elem_bytes"], s["stride"], d["stride"])
 
 
+def _code_only(text: bytes) -> bytes:
+    """Source text without comments, runs of spaces collapsed and blank lines
+    dropped (line breaks kept for the preprocessor): a comment edit leaves a
+    kernel's hash alone.  No string literal in the hashed sources holds a
+    comment marker."""
+    s = re.sub(r"/\*.*?\*/", " ", text.decode(), flags=re.S)
+    s = re.sub(r"//[^\n]*", "", s)
+    lines = (re.sub(r"[ \t]+", " ", ln).strip() for ln in s.split("\n"))
+    return "\n".join(ln for ln in lines if ln).encode()
+
+
 def kernel_sources_sha(kernel_name: str) -> str:
+    """Hash of the code (comments excluded) of a kernel class's sources."""
     warp = ["k_warp.cu", "k_warp.cuh"] + ["k_warp_w%d.cu" % w for w in (1, 2, 4, 8, 16)]
     files = {"warp_permute": warp, "warp_unit_shared": warp, "tile_transpose": ["k_tile.cu"],
              "vec_copy": ["k_vec.cu"], "smem_transpose": ["k_smem.cu"],
              "tma_copy": ["k_tma_copy.cu"], "window_sum": ["k_stencil.cu"],
              "loop_copy": ["k_loop.cu"]}.get(kernel_name, [])
-    h = hashlib.sha256()
-    for f in files + ["ptx.cuh", "device_common.cuh"]:
-        with open(os.path.join(ROOT, "movement_primitives_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+    paths = [os.path.join(ROOT, "movement_primitives_gb300", "csrc", f) for f in files + ["ptx.cuh", "device_common.cuh"]]
     if kernel_name in ("warp_permute", "warp_unit_shared"):  # device functions in the public device header
-        with open(os.path.join(ROOT, "include", "layout_copy_device.cuh"), "rb") as fh:
-            h.update(fh.read())
+        paths.append(os.path.join(ROOT, "include", "layout_copy_device.cuh"))
+    h = hashlib.sha256()
+    for path in paths:
+        with open(path, "rb") as fh:
+            h.update(_code_only(fh.read()))
     return h.hexdigest()[:16]
 
 

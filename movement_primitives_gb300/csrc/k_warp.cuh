@@ -148,10 +148,11 @@ __global__ void __launch_bounds__(kWarpThreads, LC_WARP_MIN_BLOCKS) k_warp_permu
     }
 }
 
-// lc_warp_unit_run: P4's op between two shared-memory buffers, one warp per
-// unit.  The warp copies the unit's source buffer into shared buffer A (and
-// the destination buffer into B unless in place), permutes A -> B or A -> A
-// with lc_device::warp_unit_permute, and copies the destination buffer out.
+// lc_warp_unit_run: P4's op between two shared-memory buffers.  Each unit is
+// handled by one warp, which stages up to kUnitMaxPerWarp units at a time:
+// it copies each unit's source buffer into shared buffer A (and the
+// destination buffer into B unless in place), permutes A -> B or A -> A with
+// lc_device::warp_unit_permute, and copies the destination buffer out.
 constexpr int kUnitWarps = 4;
 
 // Units staged per warp at a time: as many as fit 2 KiB of each buffer kind,

@@ -80,3 +80,15 @@ def test_bench_flag_combinations():
             bench.check_args(bench.parse_args(argv))
     for argv in ([], ["--in-place"], ["--unit-run"], ["--workload", "8", "--loop", "[(4, 1, 0)]"]):
         bench.check_args(bench.parse_args(argv))
+
+
+def test_kernel_hash_ignores_comments_but_not_code():
+    """Profiles record a hash of their kernel's code; comment and spacing
+    edits must leave it alone, code edits must not."""
+    import bench
+    a = bench._code_only(b"int a;  // one\n/* two\n three */ int b;\n\n#define X 1\n")
+    b = bench._code_only(b"int a; /* other */\n   int b; // note\n#define X 1\n")
+    c = bench._code_only(b"int a;\nint c;\n#define X 1\n")
+    d = bench._code_only(b"int a;\nint b;\n#define X 2\n")
+    assert a == b and a != c and a != d
+    assert len(bench.kernel_sources_sha("warp_permute")) == 16
