@@ -274,11 +274,30 @@ def test_misaligned_bases_still_exact():
 # ---------------------------------------------------------------------------
 
 FULL = [(1, None), (2, None), (3, None), (4, 1), (4, 2), (4, 4), (4, 8), (4, 16), (5, None),
-        (6, 1), (6, 4), (6, 8)]
+        (6, 1), (6, 2), (6, 4), (6, 8)]
+
+
+def _oracle_full(c, src_np):
+    """The oracle over the whole workload, split over the host's cores (tiles,
+    or slabs of the outermost mode, each its own oracle copy)."""
+    import bench
+    want = workloads.make_dst(c).numpy()
+    bench.run_oracle(c, src_np, want, bench.host_cores())
+    return want
+
+
+def _assert_same_bytes(got, want, what):
+    if not np.array_equal(got, want):
+        bad = np.flatnonzero(got != want)
+        raise AssertionError("%s: %d bytes differ, first at %d (got %d want %d)"
+                             % (what, bad.size, bad[0], got[bad[0]], want[bad[0]]))
 
 
 @pytest.mark.parametrize("cfg,w", FULL)
-def test_workload_full_size_sampled(cfg, w):
+def test_workload_full_size_exact(cfg, w):
+    """Full size, the benchmark's launch: the WHOLE destination buffer equals
+    the oracle's byte for byte (sentinel bytes included), then 2^20 sampled
+    points are checked once more against the oracle's offsets."""
     c = workloads.config(cfg, w)
     src_h = workloads.make_src(c)
     src_d = src_h.cuda()
@@ -286,40 +305,18 @@ def test_workload_full_size_sampled(cfg, w):
     lc().layout_copy(src_d, c["src"], dst_d, c["dst"], n_tiles=c["n_tiles"], elem_bytes=c["elem_bytes"])
     st, detail = lc().last_device_error()
     assert st == 0, "device error word %#x" % detail
+    want = _oracle_full(c, src_h.numpy())
+    _assert_same_bytes(dst_d.cpu().numpy(), want, c["name"])
+    del want
     wbytes = c["elem_bytes"]
     n = workloads.logical_elems(c)
     rng = np.random.default_rng(cfg * 100 + wbytes)
     pts = rng.integers(0, n, size=min(n, 1 << 20), dtype=np.int64)
     pts[:2] = [0, n - 1]
     so, do = oracle.offsets_of(c["src"], c["dst"], c["n_tiles"], pts)
-    words = {1: torch.uint8, 2: torch.int16, 4: torch.int32, 8: torch.int64}
-    if wbytes == 16:
-        sv, dv = src_d.view(torch.int64).view(-1, 2), dst_d.view(torch.int64).view(-1, 2)
-    else:
-        sv, dv = src_d.view(words[wbytes]), dst_d.view(words[wbytes])
-    so_t, do_t = torch.from_numpy(so).cuda(), torch.from_numpy(do).cuda()
-    assert torch.equal(sv[so_t], dv[do_t])
-    # The destination image is the whole buffer in these workloads, so the
-    # destination must hold a permutation of the source's words: order-free
-    # sums over w-byte words (16-byte words as two 8-byte halves) must agree.
-    assert src_d.numel() == dst_d.numel()
-    as_words = {1: torch.uint8, 2: torch.int16, 4: torch.int32, 8: torch.int64, 16: torch.int64}
-    sw = src_d.view(as_words[wbytes]).view(-1, max(1, wbytes // 8))
-    dw = dst_d.view(as_words[wbytes]).view(-1, max(1, wbytes // 8))
-    chunk = 1 << 25
-    s_sum = d_sum = s_sq = d_sq = 0
-    for lo in range(0, sw.shape[0], chunk):
-        # weight the halves of a 16-byte word differently so that swapping
-        # halves between words would show
-        s = sw[lo:lo + chunk].to(torch.int64)
-        d = dw[lo:lo + chunk].to(torch.int64)
-        if s.shape[1] == 2:
-            s = s[:, 0] * 3 + s[:, 1]
-            d = d[:, 0] * 3 + d[:, 1]
-        s_sum += int(s.sum()); d_sum += int(d.sum())
-        s_sq += int((s * s).sum()); d_sq += int((d * d).sum())
-    assert (s_sum - d_sum) % (1 << 64) == 0 and (s_sq - d_sq) % (1 << 64) == 0
-    del src_d, dst_d, sw, dw
+    sv, dv = src_d.view(-1, wbytes), dst_d.view(-1, wbytes)
+    assert torch.equal(sv[torch.from_numpy(so).cuda()], dv[torch.from_numpy(do).cuda()])
+    del src_d, dst_d, sv, dv
 
 
 # ---------------------------------------------------------------------------
@@ -732,10 +729,11 @@ def test_loop_layout_empty_and_refused():
     assert (buf == 0).all()
 
 
-def test_loop_layout_full_workload_sampled():
+def test_loop_layout_full_workload():
     c = workloads.config(8)
     assert c["loop"] == oracle.index_maps.default_loop_layout(32 * 128 * 128, 1024, 8)
-    src_d = workloads.make_src(c).cuda()
+    src_h = workloads.make_src(c)
+    src_d = src_h.cuda()
     dst_d = workloads.make_dst(c, device="cuda")
     N = 32 * 128 * 128
     trace = torch.full((c["n_tiles"] * N,), -1, dtype=torch.int64, device="cuda")
@@ -743,6 +741,7 @@ def test_loop_layout_full_workload_sampled():
                           elem_bytes=2, trace=trace)
     st, detail = lc().last_device_error()
     assert st == 0, "device error word %#x" % detail
+    _assert_same_bytes(dst_d.cpu().numpy(), _oracle_full(c, src_h.numpy()), c["name"])
     rng = np.random.default_rng(8)
     pts = rng.integers(0, c["n_tiles"] * N, size=1 << 18, dtype=np.int64)
     pts[:2] = [0, c["n_tiles"] * N - 1]

@@ -40,17 +40,40 @@ def test_random_floats_within_float32_rounding():
 
 
 def test_left_to_right_order_is_observable():
-    # (1e8 + 1) + (-1e8) = 0 in float32, while 1 + (1e8 + -1e8) would be 1
+    # (1e8 + 1) + (-1e8) = 0 in float32 (1 is below half of 1e8's spacing)
     a = np.array([1e8, 1.0, -1e8], dtype=np.float32)
     assert stencil.window_sum_f32(a, 1, 3)[0] == np.float32(0.0)
+    # (1 + 1e8) + (-1e8) = 0, whereas right to left, (-1e8 + 1e8) + 1, and
+    # 1 + (1e8 + -1e8) both give 1: only the order as written gives 0
+    b = np.array([1.0, 1e8, -1e8], dtype=np.float32)
+    assert stencil.window_sum_f32(b, 1, 3)[0] == np.float32(0.0)
 
 
-def test_planted_off_by_one_is_caught(monkeypatch):
-    def shifted(a, n_out, window=3):
+def test_planted_mistakes_are_caught(monkeypatch):
+    """Each mistake, planted into the oracle itself, fails a pin above."""
+    real = stencil.window_sum_f32
+
+    def shifted(a, n_out, window=3):  # window starts one element late
         a = np.asarray(a, dtype=np.float32)
-        acc = a[1:n_out + 1].copy()
-        for k in range(1, window):
-            acc = (acc + a[k + 1:k + 1 + n_out]).astype(np.float32)
+        return real(a[1:], n_out, window)
+
+    def right_to_left(a, n_out, window=3):  # terms added in the reverse order
+        a = np.asarray(a, dtype=np.float32)
+        acc = a[window - 1:window - 1 + n_out].copy()
+        for k in range(window - 2, -1, -1):
+            acc = (acc + a[k:k + n_out]).astype(np.float32)
         return acc
-    a = np.arange(1027 + 1, dtype=np.float32)
-    assert not np.array_equal(shifted(a, 1024), 3 * np.arange(1024, dtype=np.float32) + 3)
+
+    def short(a, n_out, window=3):  # one term dropped
+        return real(a, n_out, max(1, window - 1))
+
+    for mutant, pins in ((shifted, [test_page_shapes_and_definition]),
+                         (right_to_left, [test_left_to_right_order_is_observable]),
+                         (short, [test_page_shapes_and_definition,
+                                  lambda: test_integer_inputs_match_exact_convolution(5)])):
+        monkeypatch.setattr(stencil, "window_sum_f32", mutant)
+        for pin in pins:
+            with pytest.raises((AssertionError, ValueError)):
+                pin()
+        monkeypatch.setattr(stencil, "window_sum_f32", real)
+    test_page_shapes_and_definition()  # the real oracle passes again
