@@ -6,10 +6,16 @@
                     [--loop "[(extent, thread_stride, slot_stride), ...]"]
                     [--in-place | --unit-run]
                     [--graph] [--copy-ceiling] [--e2e-steps E] [--no-cpu-baseline]
+                    [--flush read|write] [--no-per-config] [--per-config-only 3,4:1,...]
 
 A step is one lc_layout_copy over the whole workload (one kernel launch);
 inputs are synthetic, seeded and resident in HBM; workloads smaller than
-twice the L2 get an L2 flush between steps.  Prints ONE JSON line on rank 0.
+twice the L2 get an L2 flush between steps (by default a read of twice the
+L2 size, so no dirty line of the flush drains into the timed launch; --flush
+write fills the buffer instead).  Prints ONE JSON line on rank 0.  The default
+run (workload 2 on one GPU) adds `per_config`: workloads 1, 3, 4 (1- to
+16-byte words) and 5 measured the same way, each with its kernel, GB/s,
+roofline fraction, a 4096-point oracle check and its clocks.
 The default workload is the scale-factor transpose batch: 2^20 tiles of
 (pipe=2, high=1, 4, 32) fp32, strides (128,128,32,1) -> (128,128,1,4).
 Workloads: 1 one 32x32 fp32 transpose; 2 the default; 3 a 16384^2 bf16
@@ -73,6 +79,12 @@ def parse_args(argv=None):
                    help="workload 2 permuted in place (destination = source buffer)")
     p.add_argument("--unit-run", action="store_true",
                    help="workload 2's units through lc_warp_unit_run (shared-memory buffers)")
+    p.add_argument("--flush", default="read", choices=["read", "write"],
+                   help="how L2 is evicted between timed launches of workloads under twice its size")
+    p.add_argument("--no-per-config", action="store_true",
+                   help="skip the other workloads' measurements added to the default line")
+    p.add_argument("--per-config-only", default=None,
+                   help="comma list of workloads (4:W for workload 4 with W-byte words) for per_config")
     p.add_argument("--n-tiles", type=int, default=None,
                    help="override the tile count (a smaller case of the same kernel, e.g. for ncu)")
     return p.parse_args(argv)
@@ -240,6 +252,36 @@ def gpu_id_for(device_index: int) -> str:
     except Exception:
         vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
         return vis.split(",")[device_index] if vis else str(device_index)
+
+
+class L2Flush:
+    """Evicts L2 between timed launches, outside their event pairs.
+
+    ``read`` (the default) reduces a buffer of twice the L2 size to one
+    8-byte value: L2 is left holding clean lines of that buffer, so the next
+    timed launch neither hits its own previous lines nor pays for the flush's
+    write-back.  ``write`` fills the buffer instead, which leaves L2 full of
+    dirty lines whose write-back overlaps the next launch.
+    """
+
+    def __init__(self, dev, kind: str = "read"):
+        import torch
+        self.kind = kind
+        self.buf = torch.zeros(2 * workloads.HBM_L2_BYTES // 8, dtype=torch.int64, device=dev)
+
+    def __call__(self, k: int) -> None:
+        if self.kind == "read":
+            self.buf.sum()
+        else:
+            self.buf.fill_(k & 0xFF)
+
+    def describe(self) -> str:
+        mib = 2 * workloads.HBM_L2_BYTES >> 20
+        if self.kind == "read":
+            return "L2 flushed between steps by reading a %d MiB buffer (a reduction to 8 bytes) " \
+                   "outside the timed launches; value from per-launch CUDA events" % mib
+        return "L2 flushed between steps by writing a %d MiB buffer outside the timed launches; " \
+               "value from per-launch CUDA events" % mib
 
 
 # ---------------------------------------------------------------------------
@@ -477,7 +519,7 @@ def run_ours(args):
     sampler = ClockSampler(gpu_id_for(dev.index)) if rank == 0 else None
     per_side = step_bytes // 2
     flush = per_side < 2 * workloads.HBM_L2_BYTES and not args.graph
-    flush_buf = torch.empty(2 * workloads.HBM_L2_BYTES, dtype=torch.uint8, device=dev) if flush else None
+    flusher = L2Flush(dev, args.flush) if flush else None
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -501,7 +543,7 @@ def run_ours(args):
     else:
         for k in range(args.steps):
             if flush:
-                flush_buf.fill_(k & 0xFF)  # evicts the previous step's lines from L2
+                flusher(k)  # evicts the previous step's lines from L2
             ev[k][0].record(stream)
             step()
             ev[k][1].record(stream)
@@ -592,7 +634,7 @@ def run_ours(args):
         torch.cuda.synchronize()
         for k, (e0c, e1c) in enumerate(cev):
             if flush:
-                flush_buf.fill_(k & 0xFF)
+                flusher(k)
             e0c.record(stream)
             b_buf.copy_(a_buf)
             e1c.record(stream)
@@ -604,6 +646,13 @@ def run_ours(args):
     peak, peak_kind = measured_peak()
     achieved = step_bytes / (launch_ms / 1e3) / 1e9
     traffic = profiled_traffic(kernel_name, cfg["name"])
+    per_config = None
+    if (rank == 0 and world == 1 and not args.no_per_config and mode is None and loop is None
+            and args.workload == DEFAULT_WORKLOAD and not args.n_tiles and args.kernel == "auto"):
+        per_config = {}
+        for c_id, c_w in parse_per_config(args.per_config_only):
+            other = workloads.config(c_id, c_w)
+            per_config[other["name"]] = measure_workload(other, dev, lc, stream, args.flush, peak)
     if rank == 0:
         cpu = None if args.no_cpu_baseline else cpu_baseline(cfg, src_h.numpy(), args.cpu_seconds)
         value = world * step_bytes * args.steps / (elapsed_ms / 1e3) / 1e9
@@ -617,10 +666,8 @@ def run_ours(args):
             "config": {"workload": describe(cfg), "kernel": kernel_name,
                        "loop_layout": loop, "mode": mode,
                        "bytes_per_step": step_bytes,
-                       "l2": ("L2 flushed between steps (%d MiB write outside the timed launches; "
-                              "value from per-launch CUDA events)" % (2 * workloads.HBM_L2_BYTES >> 20)
-                              if flush else "inputs larger than L2 (%d MiB per side), no flush"
-                              % (step_bytes // 2 >> 20)),
+                       "l2": (flusher.describe() if flush
+                              else "inputs larger than L2 (%d MiB per side), no flush" % (step_bytes // 2 >> 20)),
                        "timing": "one CUDA graph of K launches" if args.graph else "K launches from the host",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "pct_of_peak": round(100.0 * value / world / peak, 2),
@@ -633,12 +680,115 @@ def run_ours(args):
             "copy_ceiling_gbs": copy_ceiling,
             "e2e": e2e,
             "cpu_baseline": cpu,
+            "per_config": per_config,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+# The other workloads of the metric ("per layout permute"), measured after the
+# default one and reported beside it: (workload, element bytes).
+PER_CONFIG = [(1, None), (3, None), (4, 1), (4, 2), (4, 4), (4, 8), (4, 16), (5, None)]
+
+
+def parse_per_config(text):
+    if not text:
+        return PER_CONFIG
+    out = []
+    for item in text.split(","):
+        cfg, _, w = item.partition(":")
+        out.append((int(cfg), int(w) if w else None))
+    return out
+
+
+def measure_workload(cfg, dev, lc, stream, flush_kind, peak, min_ms=250.0):
+    """One workload at full size: planner's kernel, per-launch CUDA-event
+    times (L2 evicted between launches when a side is under twice its size),
+    a 4096-point check of the result against the oracle's offsets, and the
+    clocks seen while the launches ran."""
+    import numpy as np
+    import torch
+
+    import oracle
+    src_h = workloads.make_src(cfg)
+    src = src_h.to(dev)
+    del src_h
+    dst = workloads.make_dst(cfg, device=dev)
+    sh = stream.cuda_stream
+    w, nt = cfg["elem_bytes"], cfg["n_tiles"]
+    kernel_name = lc.plan(cfg["src"], cfg["dst"], w, nt)["kernel_name"]
+
+    def launch():
+        lc.layout_copy_ptr(src.data_ptr(), cfg["src"], dst.data_ptr(), cfg["dst"], w, nt, stream=sh)
+
+    for _ in range(3):
+        launch()
+    st, detail = lc.last_device_error(sh)
+    if st != 0:
+        raise RuntimeError("device error word %#x during warm-up of %s" % (detail, cfg["name"]))
+    n = workloads.logical_elems(cfg)
+    pts = np.random.default_rng(cfg["cfg"]).integers(0, n, 4096)
+    so, do = oracle.offsets_of(cfg["src"], cfg["dst"], nt, pts)
+    sv, dv = src.view(-1, w), dst.view(-1, w)
+    checked = torch.equal(sv[torch.from_numpy(so).to(dev)], dv[torch.from_numpy(do).to(dev)])
+    if not checked:
+        raise RuntimeError("spot check against the oracle failed on %s" % cfg["name"])
+
+    step_bytes = workload_bytes(cfg)
+    flush = step_bytes // 2 < 2 * workloads.HBM_L2_BYTES
+    flushers = {k: L2Flush(dev, k) for k in (("read", "write") if flush else ())}
+
+    def timed(steps, flusher):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for k in range(steps):
+            if flusher is not None:
+                flusher(k)
+            ev[k][0].record(stream)
+            launch()
+            ev[k][1].record(stream)
+        return ev
+
+    probe = timed(5, flushers.get(flush_kind))
+    torch.cuda.synchronize()
+    est = statistics.median(a.elapsed_time(b) for a, b in probe)
+    steps = int(min(2000, max(50, min_ms / max(est, 1e-3))))
+    sampler = ClockSampler(gpu_id_for(dev.index))
+    sampler.start()
+    ev = timed(steps, flushers.get(flush_kind))
+    sampler.snapshot()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    times = [a.elapsed_time(b) for a, b in ev]
+    other = None
+    if flush:
+        other_kind = "write" if flush_kind == "read" else "read"
+        ev2 = timed(min(steps, 200), flushers[other_kind])
+        torch.cuda.synchronize()
+        other = {"flush": other_kind,
+                 "gbs": round(step_bytes / (statistics.mean(a.elapsed_time(b) for a, b in ev2) / 1e3) / 1e9, 2)}
+    st, detail = lc.last_device_error(sh)
+    if st != 0:
+        raise RuntimeError("device error word %#x while timing %s" % (detail, cfg["name"]))
+    mean_ms = statistics.mean(times)
+    gbs = step_bytes / (mean_ms / 1e3) / 1e9
+    out = {"workload": describe(cfg), "kernel": kernel_name, "bytes_per_launch": step_bytes,
+           "launches": steps, "launch_us_mean": round(1e3 * mean_ms, 3),
+           "launch_us_median": round(1e3 * statistics.median(times), 3),
+           "gbs": round(gbs, 2), "pct_of_peak": round(100.0 * gbs / peak, 2),
+           "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peak, "unit": "GB/s",
+                        "frac": round(gbs / peak, 4), "traffic": profiled_traffic(kernel_name, cfg["name"])},
+           "l2": flushers[flush_kind].describe() if flush
+           else "inputs larger than L2 (%d MiB per side), no flush" % (step_bytes // 2 >> 20),
+           "other_flush": other,
+           "spot_check": "4096 random logical points equal at the oracle's offsets",
+           "clocks": clocks}
+    del src, dst, flushers
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_window_sum(args):
@@ -703,31 +853,7 @@ def run_window_sum(args):
     value = step_bytes * args.steps / (elapsed / 1e3) / 1e9
     achieved = step_bytes / (launch_ms / 1e3) / 1e9
     e2e = None
-    if args.e2e_steps > 0 and loop is not None:
-        # no host-buffer form of the loop copy: pinned upload, the copy, pinned
-        # download, in order on the stream, every step
-        src_pin = src_h.pin_memory()
-        dst_pin = torch.empty(dst.numel(), dtype=torch.uint8).pin_memory()
-        for it in range(args.e2e_steps + 2):
-            if it == 2:
-                barrier()
-                torch.cuda.synchronize()
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-            src.copy_(src_pin, non_blocking=True)
-            launch(sh)
-            dst_pin.copy_(dst, non_blocking=True)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, dev)
-        if not torch.equal(dst_pin[:1 << 20], dst[:1 << 20].cpu()):
-            raise RuntimeError("end-to-end result differs from the device result")
-        e2e = {"value": round(world * step_bytes / (e2e_ms / 1e3) / 1e9, 2), "unit": UNIT,
-               "h2d_bytes_per_step": src.numel() * src.element_size(),
-               "d2h_bytes_per_step": dst.numel() * dst.element_size(),
-               "path": "pinned upload, lc_layout_copy_loop, pinned download (one stream, not pipelined)"}
-    elif args.e2e_steps > 0:
+    if args.e2e_steps > 0:
         a_pin, o_pin = a_h.pin_memory(), torch.empty(n, dtype=torch.float32).pin_memory()
         for it in range(args.e2e_steps + 1):
             if it == 1:
