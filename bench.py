@@ -2,7 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload 1..8] [--elem-bytes W] [--kernel auto|vec_copy|
-                    warp_permute|tile_transpose|smem_transpose|tma_copy]
+                    warp_permute|warp_shuffle|tile_transpose|smem_transpose|tma_copy]
                     [--loop "[(extent, thread_stride, slot_stride), ...]"]
                     [--in-place | --unit-run]
                     [--graph] [--copy-ceiling] [--e2e-steps E] [--no-cpu-baseline]
@@ -153,7 +153,7 @@ def kernel_sources_sha(kernel_name: str) -> str:
     files = {"warp_permute": warp, "warp_unit_shared": warp, "tile_transpose": ["k_tile.cu"],
              "vec_copy": ["k_vec.cu"], "smem_transpose": ["k_smem.cu"],
              "tma_copy": ["k_tma_copy.cu"], "window_sum": ["k_stencil.cu"],
-             "loop_copy": ["k_loop.cu"]}.get(kernel_name, [])
+             "loop_copy": ["k_loop.cu"], "warp_shuffle": ["k_shuffle.cu"]}.get(kernel_name, [])
     paths = [os.path.join(ROOT, "movement_primitives_gb300", "csrc", f) for f in files + ["ptx.cuh", "device_common.cuh"]]
     if kernel_name in ("warp_permute", "warp_unit_shared"):  # device functions in the public device header
         paths.append(os.path.join(ROOT, "include", "layout_copy_device.cuh"))

@@ -79,7 +79,10 @@ typedef enum {
     LC_ERR_UNSUPPORTED = 13,    /* a forced kernel class cannot take this copy */
     LC_ERR_OVERFLOW = 14,       /* an offset does not fit in 63 bits */
     LC_ERR_STAGING = 15,        /* a staging buffer is too small */
-    LC_ERR_LOOP_LAYOUT = 16     /* a loop layout is not an exact partition */
+    LC_ERR_LOOP_LAYOUT = 16,    /* a loop layout is not an exact partition */
+    LC_ERR_UNDECIDED = 17       /* the destination could not be shown one-to-one:
+                                   no stride split settles it and the modes left
+                                   hold over 2^24 words to enumerate */
 } lc_status;
 
 /* Kernel classes (the planner picks one; lc_layout_copy_ex can force one). */
@@ -123,7 +126,17 @@ typedef enum {
      * TMA tensor stores through a second tensor map with the destination
      * strides; one thread per CTA drives a 6-stage ring.  Axis permutes that
      * keep the last axis, strided slices, row gathers. */
-    LC_KERNEL_TMA_COPY = 5
+    LC_KERNEL_TMA_COPY = 5,
+    /* Warp-shuffle permute: of the mode contiguous in the source and the mode
+     * contiguous in the destination, one spans exactly 16 bytes (V = 16 /
+     * elem_bytes words, elem_bytes <= 8) and the other a multiple of V
+     * words: the scale-factor transpose of "permute_layout" ("Demonstration
+     * program", a (4, 32) fp32 block written with strides (1, 4)) and its
+     * mirror.  Groups of V lanes load one V x V block as V 16-byte chunks,
+     * transpose it in registers by warp shuffles and store V 16-byte chunks;
+     * no shared memory.  Other strides and both bases must be 16-byte
+     * aligned. */
+    LC_KERNEL_WARP_SHUFFLE = 6
 } lc_kernel;
 
 /* What the planner decided for one copy (filled by lc_plan). */
@@ -214,21 +227,29 @@ int64_t lc_host_staging_bytes(const lc_tile_layout *src_layout,
 /* lc_layout_copy_host for callers that cannot allocate device memory.  (The
  * source pages have no counterpart: this is a deployment convenience.)  Some
  * callers cannot hand over a staging buffer: a plugin inside an application
- * whose own allocator owns all device memory, code that must avoid cudaMalloc
- * because it can synchronise the device, or code that will be captured into a
- * CUDA graph, where cudaMalloc is not allowed.  This entry point stages through
- * an LC_STATIC_STAGING_BYTES array that lives in the library and allocates and
- * frees nothing.  Chunks of tiles are uploaded, permuted and downloaded in
- * order on `stream` alone (no overlap between transfers); synchronise `stream`
- * to finish.  The first call on a device, with that device current, looks up
+ * whose own allocator owns all device memory and gives none out, or code
+ * that must avoid cudaMalloc because it can synchronise the whole device.
+ * This entry point stages through an LC_STATIC_STAGING_BYTES array that
+ * lives in the library and allocates and frees nothing.  Chunks of tiles are
+ * uploaded, permuted and downloaded in order on `stream` alone (no overlap
+ * between transfers); synchronise `stream` to finish.  The copies are
+ * asynchronous only for page-locked host buffers; with pageable buffers
+ * CUDA makes them synchronous with the host, and the result is the same.
+ * Set-up: the first call on a device, with that device current, looks up
  * the array's device address (loading the library's code onto the device if
- * needed): make it before any stream capture.  Every call shares the array
- * and it keeps the previous call's bytes (nothing in it needs to start at
- * zero); calls that overlap on the GPU, e.g. on two streams, race on it --
- * serialise them.  Errors: as lc_layout_copy_host; LC_ERR_STAGING when even
- * one tile's source and destination spans (each rounded up to 256 bytes)
- * exceed LC_STATIC_STAGING_BYTES, or when the whole copy must fit at once
- * (one tile, or destination tiles that interleave) and does not. */
+ * needed) before it checks anything else, so any call completes it; make
+ * that first call before any stream capture.  The address is kept for the
+ * life of the process: do not call this entry point on a device after
+ * cudaDeviceReset on it.  Every call shares the array and it keeps the
+ * previous call's bytes (nothing in it needs to start at zero); calls that
+ * overlap on the GPU, e.g. on two streams, race on it -- serialise them.
+ * Errors: as lc_layout_copy_host; LC_ERR_STAGING when even one tile's
+ * source and destination spans (each rounded up to 256 bytes) exceed
+ * LC_STATIC_STAGING_BYTES, or when the whole copy must fit at once (one
+ * tile, or destination tiles that interleave) and does not.  Every check
+ * that can refuse the copy runs before anything is queued; an LC_ERR_CUDA
+ * from a later chunk leaves the chunks before it queued on `stream` (a
+ * partial copy). */
 int lc_layout_copy_host_static(const void *src_host, const lc_tile_layout *src_layout,
                                void *dst_host, const lc_tile_layout *dst_layout,
                                int32_t elem_bytes, int64_t n_tiles, lc_stream_t stream);

@@ -25,11 +25,11 @@ STATUS_NAMES = {
     7: "LC_ERR_NOT_INJECTIVE", 8: "LC_ERR_OVERLAP", 9: "LC_ERR_ALIGN",
     10: "LC_ERR_NO_SWIZZLE", 11: "LC_ERR_CUDA", 12: "LC_ERR_TIMEOUT",
     13: "LC_ERR_UNSUPPORTED", 14: "LC_ERR_OVERFLOW", 15: "LC_ERR_STAGING",
-    16: "LC_ERR_LOOP_LAYOUT",
+    16: "LC_ERR_LOOP_LAYOUT", 17: "LC_ERR_UNDECIDED",
 }
 STATUS = {v: k for k, v in STATUS_NAMES.items()}
 KERNELS = {"auto": 0, "vec_copy": 1, "warp_permute": 2, "tile_transpose": 3, "smem_transpose": 4,
-           "tma_copy": 5}
+           "tma_copy": 5, "warp_shuffle": 6}
 
 
 class CTileLayout(ctypes.Structure):

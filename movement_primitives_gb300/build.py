@@ -21,7 +21,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "liblayoutcopy.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 
-SOURCES = ["plan.cpp", "api.cu", "host_copy.cu", "host_copy_static.cu", "k_vec.cu", "k_warp.cu",
+SOURCES = ["plan.cpp", "api.cu", "host_copy.cu", "host_copy_static.cu", "k_vec.cu", "k_warp.cu", "k_shuffle.cu",
            "k_warp_w1.cu", "k_warp_w2.cu", "k_warp_w4.cu", "k_warp_w8.cu", "k_warp_w16.cu",
            "k_tile.cu", "k_smem.cu", "k_tma_copy.cu", "k_stencil.cu", "k_loop.cu"]
 HEADERS = ["lc_internal.h", "ptx.cuh", "device_common.cuh", "launch.h", "k_warp.cuh", "tensor_map.h"]
@@ -52,17 +52,20 @@ def _stale(target: str) -> bool:
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
-          out: str | None = None, defines=()) -> str:
+          out: str | None = None, defines=(), only=None) -> str:
     """Compile and link if any input changed; returns the library path.
 
     ``out`` / ``defines`` build a variant (compile-time knobs such as
-    LC_TILE_STAGES_NARROW) into another file; the in-tree library is the
-    default build.
+    LC_TILE_ROWS_W1) into another file; the in-tree library is the default
+    build.  ``only`` (a variant build) compiles just those sources with the
+    defines and links them with the default build's other objects.
     """
     lib_path = out or LIB_PATH
     build_dir = BUILD_DIR if out is None else out + ".objs"
     if not force and not _stale(lib_path):
         return lib_path
+    if only is not None and out is not None:
+        build()  # the default objects the variant links with
     os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
     extra = ["-D" + d for d in defines]
@@ -79,8 +82,10 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
             sys.stderr.write(res.stderr)
         return obj
 
+    todo = SOURCES if only is None or out is None else [x for x in SOURCES if x in only]
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(compile_one, SOURCES))
+        built = dict(zip(todo, ex.map(compile_one, todo)))
+    objs = [built.get(x) or os.path.join(BUILD_DIR, os.path.splitext(x)[0] + ".o") for x in SOURCES]
     tmp = lib_path + ".%d.tmp" % os.getpid()
     cmd = [cc, "-shared", "-o", tmp] + objs + ARCH + ["-Xcompiler", "-fPIC"]
     res = subprocess.run(cmd, capture_output=True, text=True)

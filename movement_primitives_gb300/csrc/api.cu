@@ -75,6 +75,7 @@ int launch_plan(const Plan &p, const uint8_t *s, uint8_t *d, cudaStream_t cs, bo
     switch (p.kernel) {
         case LC_KERNEL_VEC_COPY: return launch_vec(p, s, d, cs);
         case LC_KERNEL_WARP_PERMUTE: return launch_warp(p, s, d, cs);
+        case LC_KERNEL_WARP_SHUFFLE: return launch_shuffle(p, s, d, cs);
         case LC_KERNEL_SMEM_TRANSPOSE: return launch_smem(p, s, d, cs);
         case LC_KERNEL_TMA_COPY: {
             const int r = launch_tma_copy(p, s, d, cs);
@@ -157,6 +158,9 @@ extern "C" const char *lc_status_string(int32_t status) {
         case LC_ERR_OVERFLOW: return "an offset does not fit in 63 bits";
         case LC_ERR_STAGING: return "the staging buffer is too small";
         case LC_ERR_LOOP_LAYOUT: return "the loop layout is not an exact partition of the tile (or has over 1024 threads)";
+        case LC_ERR_UNDECIDED:
+            return "the destination could not be shown one-to-one (no stride split settles it, too many words to "
+                   "enumerate)";
     }
     return "unknown status";
 }
@@ -169,6 +173,7 @@ extern "C" const char *lc_kernel_name(int32_t kernel) {
         case LC_KERNEL_TILE_TRANSPOSE: return "tile_transpose";
         case LC_KERNEL_SMEM_TRANSPOSE: return "smem_transpose";
         case LC_KERNEL_TMA_COPY: return "tma_copy";
+        case LC_KERNEL_WARP_SHUFFLE: return "warp_shuffle";
     }
     return "unknown";
 }

@@ -78,30 +78,6 @@ cudaError_t device_streams(DeviceStreams **out) {
     return cudaSuccess;
 }
 
-// Byte span [lo, hi) of tiles [t0, t1) of one side (relative to its pointer).
-struct Span {
-    int64_t lo, hi;
-};
-
-Span tile_span(const lc_tile_layout &l, int64_t w, int64_t cos, int64_t ts, int64_t t0, int64_t t1) {
-    return Span{(l.offset + t0 * ts) * w, (l.offset + (t1 - 1) * ts + cos) * w};
-}
-
-int64_t cosize_of(const lc_tile_layout &l) {
-    int64_t c = 1;
-    for (int k = 0; k < l.rank; ++k) {
-        if (l.shape[k] == 0) return 0;
-        c += (l.shape[k] - 1) * l.stride[k];
-    }
-    return c;
-}
-
-int64_t words_of(const lc_tile_layout &l) {
-    int64_t n = 1;
-    for (int k = 0; k < l.rank; ++k) n *= l.shape[k];
-    return n;
-}
-
 }  // namespace
 }  // namespace lc
 
@@ -126,23 +102,14 @@ extern "C" int lc_layout_copy_host(const void *src_host, const lc_tile_layout *s
         if (s0 < d1 && d0 < s1) return LC_ERR_OVERLAP;
     }
 
-    const int64_t w = elem_bytes;
-    const int64_t scos = cosize_of(*src_layout), dcos = cosize_of(*dst_layout);
-    const int64_t sts = src_layout->tile_stride ? src_layout->tile_stride : scos;
-    const int64_t dts = dst_layout->tile_stride ? dst_layout->tile_stride : dcos;
+    const HostSides hs = host_sides(*src_layout, *dst_layout, elem_bytes, n_tiles);
+    const int64_t w = hs.w, scos = hs.scos, dcos = hs.dcos, sts = hs.sts, dts = hs.dts;
     // Chunks need disjoint destination spans; otherwise the copy is one chunk.
     const bool chunkable = n_tiles > 1 && dts >= dcos && sts >= 0;
-    // The destination image covers its span exactly when tiles are packed and
-    // each tile is dense; otherwise the span is staged in first so that bytes
-    // outside the image keep their values.
-    const bool dst_dense = words_of(*dst_layout) == dcos && (n_tiles == 1 || dts == dcos);
-
-    auto round256 = [](int64_t b) { return (b + 255) / 256 * 256; };
-    auto slot_bytes = [&](int64_t tiles) {
-        const Span s = tile_span(*src_layout, w, scos, sts, 0, tiles);
-        const Span d = tile_span(*dst_layout, w, dcos, dts, 0, tiles);
-        return round256(s.hi - s.lo) + round256(d.hi - d.lo);
-    };
+    // Unless the destination image covers its span exactly, the span is
+    // staged in first so that bytes outside the image keep their values.
+    const bool dst_dense = hs.dst_dense;
+    auto slot_bytes = [&](int64_t tiles) { return hs.slot_bytes(tiles); };
     int64_t chunk = n_tiles;
     int slots = 1;
     if (chunkable) {
@@ -172,8 +139,8 @@ extern "C" int lc_layout_copy_host(const void *src_host, const lc_tile_layout *s
     for (int64_t t0 = 0; t0 < n_tiles; t0 += chunk, ++c) {
         const int64_t t1 = std::min(n_tiles, t0 + chunk);
         const int b = static_cast<int>(c % slots);
-        const Span s = tile_span(*src_layout, w, scos, sts, t0, t1);
-        const Span d = tile_span(*dst_layout, w, dcos, dts, t0, t1);
+        const HostSpan s = hs.src(t0, t1);
+        const HostSpan d = hs.dst(t0, t1);
         uint8_t *s_dev = stage + b * slot_size;
         uint8_t *d_dev = s_dev + round256(s.hi - s.lo);
         // upload once the slot's previous permute has read it
@@ -218,18 +185,8 @@ extern "C" int64_t lc_host_staging_bytes(const lc_tile_layout *src_layout, const
                                          int32_t elem_bytes, int64_t n_tiles) {
     using namespace lc;
     if (!src_layout || !dst_layout || n_tiles <= 0) return 0;
-    const int64_t w = elem_bytes;
-    const int64_t scos = cosize_of(*src_layout), dcos = cosize_of(*dst_layout);
-    const int64_t sts = src_layout->tile_stride ? src_layout->tile_stride : scos;
-    const int64_t dts = dst_layout->tile_stride ? dst_layout->tile_stride : dcos;
-    auto round256 = [](int64_t b) { return (b + 255) / 256 * 256; };
-    if (n_tiles > 1 && dts >= dcos) {
-        const int64_t chunk = default_chunk(n_tiles, std::max<int64_t>(sts, scos), w);
-        const Span s = tile_span(*src_layout, w, scos, sts, 0, chunk);
-        const Span d = tile_span(*dst_layout, w, dcos, dts, 0, chunk);
-        return kSlots * (round256(s.hi - s.lo) + round256(d.hi - d.lo));
-    }
-    const Span s = tile_span(*src_layout, w, scos, sts, 0, n_tiles);
-    const Span d = tile_span(*dst_layout, w, dcos, dts, 0, n_tiles);
-    return round256(s.hi - s.lo) + round256(d.hi - d.lo);
+    const HostSides hs = host_sides(*src_layout, *dst_layout, elem_bytes, n_tiles);
+    if (n_tiles > 1 && hs.dts >= hs.dcos)
+        return kSlots * hs.slot_bytes(default_chunk(n_tiles, std::max<int64_t>(hs.sts, hs.scos), hs.w));
+    return hs.slot_bytes(n_tiles);
 }

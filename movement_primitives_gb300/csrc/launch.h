@@ -21,6 +21,7 @@ inline int finish_launch() { return cudaGetLastError() == cudaSuccess ? LC_OK : 
 
 int launch_vec(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream);
 int launch_warp(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream);
+int launch_shuffle(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream);
 int launch_tile(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream);
 int launch_smem(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream);
 int launch_tma_copy(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream);

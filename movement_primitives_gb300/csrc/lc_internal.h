@@ -64,6 +64,19 @@ struct TmaPlan {
     int64_t stage_bytes = 0;
 };
 
+// Warp-shuffle permute: blocks of V x V words (V = 16 / w) whose rows are
+// 16-byte chunks of the source and whose columns are 16-byte chunks of the
+// destination.  Lane a of a block's group moves the chunk at source word
+// offset a * sa + k * sk and destination word offset a * da + k * dk of
+// block k of its batch entry.
+struct ShflPlan {
+    int V = 0;
+    int64_t sa = 0, sk = 0, da = 0, dk = 0;  // words
+    int64_t kb = 0;                          // blocks per batch entry
+    int64_t n_blocks = 0;
+    ModeList batch;                          // outermost first
+};
+
 // Chunk swizzle of the shared tile of the shared-memory transpose: chunk k
 // of row x is stored in chunk slot k ^ ((x >> shift) & mask).
 struct SmemSwizzle {
@@ -85,6 +98,7 @@ struct Plan {
     TilePlan tile;       // also the X / Y / batch split of the shared-memory transpose
     SmemSwizzle smem_swz;
     TmaPlan tma;
+    ShflPlan shfl;
 };
 
 // Pointer facts the planner needs (alignment of the two base addresses).
@@ -172,6 +186,63 @@ SmemSwizzle choose_smem_swizzle(int w);
 
 // Joint coalescing and shard alignment, exposed for the swizzle queries.
 int align_shards(const lc_tile_layout *src, const lc_tile_layout *dst, ModeList *out);
+
+// Host-buffer copies (host_copy.cu, host_copy_static.cu): the byte spans the
+// tiles of each side reach, relative to that side's pointer.
+struct HostSpan {
+    int64_t lo, hi;
+};
+
+inline int64_t cosize_of(const lc_tile_layout &l) {
+    int64_t c = 1;
+    for (int k = 0; k < l.rank; ++k) {
+        if (l.shape[k] == 0) return 0;
+        c += (l.shape[k] - 1) * l.stride[k];
+    }
+    return c;
+}
+
+inline int64_t words_of(const lc_tile_layout &l) {
+    int64_t n = 1;
+    for (int k = 0; k < l.rank; ++k) n *= l.shape[k];
+    return n;
+}
+
+inline int64_t round256(int64_t b) { return (b + 255) / 256 * 256; }
+
+// Word size, cosizes and tile strides (words) of both sides of a copy.
+struct HostSides {
+    const lc_tile_layout *s = nullptr, *d = nullptr;
+    int64_t w = 0, scos = 0, dcos = 0, sts = 0, dts = 0;
+    // the destination image covers its span exactly (tiles packed, each tile
+    // dense), so nothing of the span needs to be staged in first
+    bool dst_dense = false;
+    HostSpan src(int64_t t0, int64_t t1) const {
+        return HostSpan{(s->offset + t0 * sts) * w, (s->offset + (t1 - 1) * sts + scos) * w};
+    }
+    HostSpan dst(int64_t t0, int64_t t1) const {
+        return HostSpan{(d->offset + t0 * dts) * w, (d->offset + (t1 - 1) * dts + dcos) * w};
+    }
+    // device bytes of one staging slot for `tiles` tiles: both spans, each
+    // rounded up to 256 bytes
+    int64_t slot_bytes(int64_t tiles) const {
+        const HostSpan a = src(0, tiles), b = dst(0, tiles);
+        return round256(a.hi - a.lo) + round256(b.hi - b.lo);
+    }
+};
+
+inline HostSides host_sides(const lc_tile_layout &src, const lc_tile_layout &dst, int64_t w, int64_t n_tiles) {
+    HostSides h;
+    h.s = &src;
+    h.d = &dst;
+    h.w = w;
+    h.scos = cosize_of(src);
+    h.dcos = cosize_of(dst);
+    h.sts = src.tile_stride ? src.tile_stride : h.scos;
+    h.dts = dst.tile_stride ? dst.tile_stride : h.dcos;
+    h.dst_dense = words_of(dst) == h.dcos && (n_tiles == 1 || h.dts == h.dcos);
+    return h;
+}
 
 // Fast unsigned 32-bit division by an invariant divisor: q = n / d for every
 // 32-bit n (Granlund & Montgomery, "Division by invariant integers using

@@ -60,36 +60,66 @@ bool dense(const ModeList &ml, int first, bool src_side) {
     return true;
 }
 
-// Is  i -> sum_k i_k d_k  one-to-one over the modes?  Sorted by stride, a
-// stride larger than everything the smaller modes reach proves it; otherwise
-// small cases are settled by enumeration and large ones are refused.
-int dst_injective(const ModeList &ml, int64_t total) {
-    std::vector<std::pair<int64_t, int64_t>> v;
-    for (int i = 0; i < ml.n; ++i) v.push_back({ml.m[i].d, ml.m[i].e});
-    std::sort(v.begin(), v.end());
-    int64_t reach = 0;
-    bool nested = true;
-    for (auto &p : v) {
-        if (p.first <= reach) { nested = false; break; }
-        reach += (p.second - 1) * p.first;
-    }
-    if (nested) return LC_OK;
-    if (total > kBruteInjective) return LC_ERR_NOT_INJECTIVE;
+// Is  i -> sum_k i_k d_k  one-to-one over the modes (every d_k > 0)?
+// Modes sorted by stride ascending; a split after the first p modes is
+// proof-carrying when everything those modes reach is below G, the gcd of the
+// remaining strides: an offset is then a + G b with a in [0, G) from the
+// first p modes and b from the rest divided by G, a unique decomposition, so
+// the whole map is one-to-one exactly when both parts are.  (A stride larger
+// than everything the smaller modes reach is the case of a single remaining
+// mode.)  Parts no split decides are enumerated up to kBruteInjective words;
+// beyond that the question stays open (LC_ERR_UNDECIDED).
+int64_t gcd64(int64_t a, int64_t b) {
+    while (b) { const int64_t t = a % b; a = b; b = t; }
+    return a;
+}
+
+int enumerate_injective(const std::vector<std::pair<int64_t, int64_t>> &v) {
+    int64_t total = 1;
+    for (auto &p : v) total *= p.second;
+    if (total > kBruteInjective) return LC_ERR_UNDECIDED;
     std::vector<int64_t> offs;
     offs.reserve(size_t(total));
-    std::vector<int64_t> idx(ml.n, 0);
+    std::vector<int64_t> idx(v.size(), 0);
     for (int64_t t = 0; t < total; ++t) {
         int64_t o = 0;
-        for (int i = 0; i < ml.n; ++i) o += idx[i] * ml.m[i].d;
+        for (size_t i = 0; i < v.size(); ++i) o += idx[i] * v[i].first;
         offs.push_back(o);
-        for (int i = ml.n - 1; i >= 0; --i) {
-            if (++idx[i] < ml.m[i].e) break;
+        for (size_t i = v.size(); i-- > 0;) {
+            if (++idx[i] < v[i].second) break;
             idx[i] = 0;
         }
     }
     std::sort(offs.begin(), offs.end());
-    return std::adjacent_find(offs.begin(), offs.end()) == offs.end() ? LC_OK
-                                                                      : LC_ERR_NOT_INJECTIVE;
+    return std::adjacent_find(offs.begin(), offs.end()) == offs.end() ? LC_OK : LC_ERR_NOT_INJECTIVE;
+}
+
+// v: (stride, extent) pairs sorted by stride ascending, every extent > 1.
+int injective_sorted(const std::vector<std::pair<int64_t, int64_t>> &v) {
+    if (v.size() <= 1) return LC_OK;
+    // suffix gcds of the strides
+    std::vector<int64_t> g(v.size() + 1, 0);
+    for (size_t i = v.size(); i-- > 0;) g[i] = gcd64(v[i].first, g[i + 1]);
+    int64_t reach = 0;
+    for (size_t p = 1; p < v.size(); ++p) {
+        reach += (v[p - 1].second - 1) * v[p - 1].first;
+        if (reach < g[p]) {
+            std::vector<std::pair<int64_t, int64_t>> lo(v.begin(), v.begin() + p), hi(v.begin() + p, v.end());
+            for (auto &q : hi) q.first /= g[p];
+            int st = injective_sorted(lo);
+            if (st == LC_OK) st = injective_sorted(hi);
+            return st;
+        }
+    }
+    return enumerate_injective(v);
+}
+
+int dst_injective(const ModeList &ml) {
+    std::vector<std::pair<int64_t, int64_t>> v;
+    for (int i = 0; i < ml.n; ++i)
+        if (ml.m[i].e > 1) v.push_back({ml.m[i].d, ml.m[i].e});
+    std::sort(v.begin(), v.end());
+    return injective_sorted(v);
 }
 
 int check_layout(const lc_tile_layout *l) {
@@ -359,6 +389,66 @@ bool plan_warp(Plan *p, const PtrInfo &ptr, bool need_conflict_free) {
     return true;
 }
 
+// Warp-shuffle permute: X = the mode contiguous in dst, Y = the mode
+// contiguous in src.  One of them spans exactly V = 16 / w words and the
+// other a multiple of V, so that every V x V block has its rows as 16-byte
+// source chunks and its columns as 16-byte destination chunks:
+//   X.e == V (the page's (4, 32) -> strides (1, 4) case): block k of a batch
+//     entry holds columns k V .. k V + V - 1 of Y; lane a reads row a
+//     (source a X.s + k V) and writes column k V + a (destination
+//     (k V + a) Y.d);
+//   Y.e == V (its mirror): block k holds rows k V .. k V + V - 1 of X; lane
+//     a reads row k V + a (source (k V + a) X.s) and writes column a
+//     (destination a Y.d + k V).
+// Every chunk must be 16-byte aligned: X.s and Y.d multiples of V, every
+// batch stride and both base offsets multiples of 16 bytes.
+bool plan_shuffle(Plan *p, const PtrInfo &ptr) {
+    const ModeList &sl = p->sorted;
+    const int w = p->w;
+    if (w > 8) return false;
+    const int64_t V = 16 / w;
+    int xi = -1, yi = -1;
+    for (int i = 0; i < sl.n; ++i) {
+        if (sl.m[i].d == 1) xi = i;
+        if (sl.m[i].s == 1) yi = i;
+    }
+    if (xi < 0 || yi < 0 || xi == yi) return false;
+    const Mode X = sl.m[xi], Y = sl.m[yi];
+    if (X.s % V || Y.d % V) return false;
+    ShflPlan &sp = p->shfl;
+    sp = ShflPlan{};
+    sp.V = int(V);
+    if (X.e == V && Y.e % V == 0) {
+        sp.kb = Y.e / V;
+        sp.sa = X.s;
+        sp.sk = V;
+        sp.da = Y.d;
+        sp.dk = V * Y.d;
+    } else if (Y.e == V && X.e % V == 0) {
+        sp.kb = X.e / V;
+        sp.sa = X.s;
+        sp.sk = V * X.s;
+        sp.da = Y.d;
+        sp.dk = V;
+    } else {
+        return false;
+    }
+    int64_t n_batch = 1;
+    for (int i = 0; i < sl.n; ++i) {
+        if (i == xi || i == yi) continue;
+        const Mode &b = sl.m[i];
+        if ((b.s * w) % 16 || (b.d * w) % 16 || b.e >= (int64_t(1) << 31)) return false;
+        sp.batch.m[sp.batch.n++] = b;
+        n_batch *= b.e;
+    }
+    if ((p->src_off * w) % 16 || (p->dst_off * w) % 16) return false;
+    if (ptr.check && (ptr.src % 16 || ptr.dst % 16)) return false;
+    if (sp.kb >= (int64_t(1) << 31) || n_batch >= (int64_t(1) << 31)) return false;
+    sp.n_blocks = n_batch * sp.kb;
+    if (sp.n_blocks >= (int64_t(1) << 31)) return false;
+    return true;
+}
+
 // Tile transpose: a mode contiguous in dst (X) and another contiguous in src
 // (Y); at most three other (batch) modes; TMA needs 16-byte aligned bases
 // and 16-byte multiple strides, stores need the same on the destination.
@@ -541,7 +631,7 @@ int make_plan_core(const lc_tile_layout *src, const lc_tile_layout *dst, int32_t
     if ((st = check_layout(src)) || (st = check_layout(dst))) return st;
     if (!valid_width(w)) return LC_ERR_ELEM_BYTES;
     if (n_tiles < 0) return LC_ERR_SHAPE;
-    if (kernel < LC_KERNEL_AUTO || kernel > LC_KERNEL_TMA_COPY) return LC_ERR_UNSUPPORTED;
+    if (kernel < LC_KERNEL_AUTO || kernel > LC_KERNEL_WARP_SHUFFLE) return LC_ERR_UNSUPPORTED;
 
     Plan p;
     p.w = w;
@@ -576,7 +666,7 @@ int make_plan_core(const lc_tile_layout *src, const lc_tile_layout *dst, int32_t
     if (n_tiles > 1) lg.m[lg.n++] = Mode{n_tiles, sts, dts};
     for (int i = 0; i < paired.n; ++i) lg.m[lg.n++] = paired.m[i];
     coalesce(&lg);
-    if ((st = dst_injective(lg, total))) return st;
+    if ((st = dst_injective(lg))) return st;
 
     p.src_lo = src->offset * w;
     p.src_hi = (smax + 1) * w;
@@ -600,6 +690,12 @@ int make_plan_core(const lc_tile_layout *src, const lc_tile_layout *dst, int32_t
     }
     fuse_inner_run(&p, ptr);
     plan_vec(&p, ptr);  // always available: the fallback of every other class
+    if (kernel == LC_KERNEL_WARP_SHUFFLE) {
+        if (!plan_shuffle(&p, ptr)) return LC_ERR_UNSUPPORTED;
+        p.kernel = kernel;
+        *out = p;
+        return LC_OK;
+    }
     if (kernel == LC_KERNEL_TILE_TRANSPOSE) {
         if (!plan_tile(&p, ptr)) return LC_ERR_UNSUPPORTED;
         p.kernel = kernel;
@@ -630,6 +726,7 @@ int make_plan_core(const lc_tile_layout *src, const lc_tile_layout *dst, int32_t
     bool has_x = false, has_y = false;
     for (int i = 0; i < sl.n; ++i) { has_x |= sl.m[i].d == 1; has_y |= sl.m[i].s == 1; }
     if (!run && has_x && has_y) {
+        if (plan_shuffle(&p, ptr)) { p.kernel = LC_KERNEL_WARP_SHUFFLE; *out = p; return LC_OK; }
         if (p.fused == 1) {
             Plan q = p;
             if (plan_warp(&q, ptr, true)) { q.kernel = LC_KERNEL_WARP_PERMUTE; *out = q; return LC_OK; }
@@ -749,6 +846,11 @@ void fill_info(const Plan &p, lc_plan_info *info) {
     info->tile_rows = p.tile.R;
     info->tile_cols = p.tile.TY;
     info->stages = p.tile.S;
+    if (p.kernel == LC_KERNEL_WARP_SHUFFLE) {  // V words per lane chunk, blocks per batch entry
+        info->vec = p.shfl.V;
+        info->P = p.shfl.V;
+        info->units_per_chunk = p.shfl.kb;
+    }
     if (p.kernel == LC_KERNEL_SMEM_TRANSPOSE) {
         int k = 0;
         while ((1 << k) - 1 < p.smem_swz.mask) ++k;
@@ -1014,7 +1116,7 @@ extern "C" int lc_warp_unit_plan(const lc_tile_layout *src_layout, const lc_tile
         dcos += (unit.m[i].e - 1) * unit.m[i].d;
     }
     if (scos * elem_bytes >= (int64_t(1) << 31) || dcos * elem_bytes >= (int64_t(1) << 31)) return LC_ERR_SHAPE;
-    if ((st = lc::dst_injective(unit, total))) return st;
+    if ((st = lc::dst_injective(unit))) return st;
     lc_warp_unit u;
     std::memset(&u, 0, sizeof(u));
     u.n_modes = unit.n;

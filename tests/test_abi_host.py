@@ -58,11 +58,17 @@ def test_plan_scale_factor_transpose(M):
     """'permute_layout' demonstration: P = 4, shift = 3, mask = 3 (k = 2)."""
     import workloads
     c = workloads.config(2)
-    p = M.plan(c["src"], c["dst"], 4, c["n_tiles"])
+    p = M.plan(c["src"], c["dst"], 4, c["n_tiles"], "warp_permute")
     assert p["kernel_name"] == "warp_permute"
     assert (p["P"], p["k"], p["shift"], p["mask"]) == (4, 2, 3, 3)
     assert (p["conflicts_read"], p["conflicts_write"]) == (1, 1)
     assert p["modes"][-2:] == [(4, 32, 1), (32, 1, 4)]
+    # the automatic choice moves the same (4, 32) blocks through warp shuffles:
+    # V = 4 words per 16-byte chunk, 32 / 4 = 8 blocks of 4 x 4 words per unit
+    a = M.plan(c["src"], c["dst"], 4, c["n_tiles"])
+    assert a["kernel_name"] == "warp_shuffle"
+    assert (a["vec"], a["units_per_chunk"]) == (4, 8)
+    assert (a["conflicts_read"], a["conflicts_write"]) == (0, 0)  # no shared memory
 
 
 def test_plan_workloads(M):
@@ -207,6 +213,15 @@ def test_validation_codes(M):
     assert code(T((2, 3), (3, 2)), T((2, 3), (3, 2))) == 0
     # tiles that overlap on the destination
     assert code(T((4,), (1,)), T((4,), (1,), 0, 2), n=3) == S["LC_ERR_NOT_INJECTIVE"]
+    # over 2^24 words and not nested: offsets k + 2^23 (2i + 3j) are distinct
+    # (the dense inner mode stays below the other strides' gcd 2^23, and
+    # 2i + 3j is one-to-one on 3 x 2); on 4 x 3, 2i + 3j collides (3,0)/(0,2)
+    big = (3, 2, 1 << 23)
+    assert code(T(big, (2 << 23, 1 << 23, 1)), T(big, (1 << 24, 3 << 23, 1)), w=1) == 0
+    big = (4, 3, 1 << 23)
+    assert code(T(big, (3 << 23, 1 << 23, 1)), T(big, (1 << 24, 3 << 23, 1)), w=1) == S["LC_ERR_NOT_INJECTIVE"]
+    # no stride split settles 3i + 5j and 2^25 words are too many to enumerate
+    assert code(T((1 << 13, 1 << 12), (1 << 12, 1)), T((1 << 13, 1 << 12), (3, 5)), w=1) == S["LC_ERR_UNDECIDED"]
     # zero-size copies are fine
     assert code(T((0, 4), (4, 1)), T((0, 4), (1, 4))) == 0
     assert code(T((4, 4), (4, 1)), T((4, 4), (1, 4)), n=0) == 0
@@ -532,3 +547,30 @@ def test_planner_is_thread_safe(M):
     with ThreadPoolExecutor(16) as ex:
         parallel = list(ex.map(lambda a: M.plan(*a), args))
     assert parallel == serial
+
+
+def test_destination_injectivity_matches_brute_force(M):
+    """The planner's one-to-one decision (stride splits, then enumeration)
+    against a plain set of all destination offsets, on random small layouts."""
+    import itertools
+    import random
+    rng = random.Random(17)
+    T = M.TileLayout
+    for _ in range(3000):
+        rank = rng.randint(1, 4)
+        ext = [rng.randint(1, 5) for _ in range(rank)]
+        dst = [rng.choice([1, 2, 3, 4, 5, 6, 8, 9, 12, 16, 20, 24, 36]) for _ in range(rank)]
+        src = []
+        acc = 1
+        for e in reversed(ext):
+            src.insert(0, acc)
+            acc *= e
+        offs = [sum(i * d for i, d in zip(idx, dst)) for idx in itertools.product(*[range(e) for e in ext])]
+        want = len(set(offs)) == len(offs)
+        try:
+            M.plan(T(tuple(ext), tuple(src)), T(tuple(ext), tuple(dst)), 4, 1)
+            got = True
+        except M.LayoutCopyError as e:
+            assert e.status == M.STATUS["LC_ERR_NOT_INJECTIVE"], (ext, dst, e.status)
+            got = False
+        assert got == want, (ext, dst)

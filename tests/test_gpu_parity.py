@@ -97,7 +97,7 @@ SMALL = [(1, None), (2, None), (3, None), (4, 1), (4, 2), (4, 4), (4, 8), (4, 16
 def test_workload_small_auto(cfg, w):
     c = workloads.config(cfg, w, scale="small")
     name = run_case(c["src"], c["dst"], c["elem_bytes"], c["n_tiles"], seed=cfg)
-    expect = {1: "warp_permute", 2: "warp_permute", 3: "tile_transpose", 4: "tile_transpose",
+    expect = {1: "warp_permute", 2: "warp_shuffle", 3: "tile_transpose", 4: "tile_transpose",
               5: "tma_copy", 6: "smem_transpose"}[cfg]
     assert name == expect
 
@@ -112,6 +112,51 @@ def test_workload_small_vec_copy(cfg, w):
 def test_workload_warp_permute_forced(cfg):
     c = workloads.config(cfg, scale="small")
     run_case(c["src"], c["dst"], c["elem_bytes"], c["n_tiles"], kernel="warp_permute", seed=cfg)
+
+
+@pytest.mark.parametrize("cfg", [1, 2])
+def test_workload_warp_shuffle_or_refused(cfg):
+    # workload 2's (4, 32) blocks are the shuffle's shape; workload 1's 32 x 32
+    # tile is not (neither contiguous mode spans exactly 16 bytes)
+    c = workloads.config(cfg, scale="small")
+    if cfg == 2:
+        run_case(c["src"], c["dst"], c["elem_bytes"], c["n_tiles"], kernel="warp_shuffle", seed=cfg)
+    else:
+        with pytest.raises(RuntimeError):
+            run_case(c["src"], c["dst"], c["elem_bytes"], c["n_tiles"], kernel="warp_shuffle", seed=cfg)
+
+
+def _shuffle_cases(w):
+    """Layout pairs of the warp-shuffle class for w-byte words: V = 16 / w."""
+    V = 16 // w
+    out = []
+    for C in sorted({V, 3 * V, 8 * V, 32 * V // min(V, 8)}):
+        out.append((L((V, C), (C, 1)), L((V, C), (1, V)), 1))            # the page's shape, one block row
+        out.append((L((V, C), (C, 1)), L((V, C), (1, V)), 37))           # tiles back to back, ragged count
+        out.append((L((C, V), (V, 1)), L((C, V), (1, C)), 23))           # the mirror
+    # gaps: source rows and destination columns padded, tiles spaced out
+    out.append((L((V, 4 * V), (6 * V, 1), V, 6 * V * V + 2 * V), L((V, 4 * V), (1, 2 * V), 3 * V, 10 * V * V), 5))
+    out.append((L((4 * V, V), (3 * V, 1), 0, 0), L((4 * V, V), (1, 5 * V), 2 * V, 0), 9))
+    # batch modes in both orders, around the block
+    out.append((L((3, V, 2, 2 * V), (4 * V * V, 2 * V, 2 * V * V, 1)),
+                L((3, V, 2, 2 * V), (4 * V * V, 1, 2 * V * V, V)), 2))
+    out.append((L((V, 5, 2 * V), (2 * V, 2 * V * V, 1)), L((V, 5, 2 * V), (1, 2 * V * V, V)), 3))
+    return out
+
+
+@pytest.mark.parametrize("w", [1, 2, 4, 8])
+def test_warp_shuffle_shapes(w):
+    for i, (src_l, dst_l, nt) in enumerate(_shuffle_cases(w)):
+        assert lc().plan(src_l, dst_l, w, nt)["kernel_name"] == "warp_shuffle", (src_l, dst_l)
+        run_case(src_l, dst_l, w, nt, kernel="warp_shuffle", seed=100 * w + i)
+        run_case(src_l, dst_l, w, nt, seed=200 * w + i)  # the automatic choice
+    # a source base off the 16-byte grid: the planner takes another class,
+    # and the copy is still exact
+    V = 16 // w
+    src_l, dst_l = L((V, 4 * V), (4 * V, 1)), L((V, 4 * V), (1, V))
+    run_case(src_l, dst_l, w, 7, src_shift=w, seed=300 + w)
+    with pytest.raises(RuntimeError):
+        run_case(src_l, dst_l, w, 7, src_shift=w, kernel="warp_shuffle", seed=300 + w)
 
 
 @pytest.mark.parametrize("w", [1, 2, 4, 8, 16])
@@ -258,6 +303,14 @@ def test_edge_cases():
     for w in (1, 2, 4, 8, 16):
         for n in (1, 15, 4097):
             run_case(L((n,), (1,)), L((n,), (1,)), w, seed=n)
+
+
+def test_injective_destination_beyond_enumeration():
+    # 2^25 + 2^24 one-byte words whose destination strides do not nest:
+    # offsets k + 2^23 (2i + 3j), one-to-one by the stride split (the planner
+    # enumerates only the 3 x 2 quotient)
+    big = (3, 2, 1 << 23)
+    run_case(L(big, (2 << 23, 1 << 23, 1)), L(big, (1 << 24, 3 << 23, 1)), 1, seed=77)
 
 
 def test_misaligned_bases_still_exact():

@@ -1,12 +1,14 @@
 """The allocation-free host-buffer copy (lc_layout_copy_host_static).
 
 Callers that cannot allocate device memory -- a plugin whose host
-application's allocator owns all device memory, code that must not call
-cudaMalloc because it can synchronise the device, code about to be captured
-into a CUDA graph -- cannot hand lc_layout_copy_host a staging buffer.  This
-entry point stages through a fixed array inside the library instead.  Here it
-is called through the C ABI and must give exactly what lc_layout_copy_host
-gives, on two calls in a row (the array keeps the previous call's bytes).
+application's allocator owns all device memory, or code that must not call
+cudaMalloc because it can synchronise the whole device -- cannot hand
+lc_layout_copy_host a staging buffer.  This entry point stages through a
+fixed array inside the library instead.  Here it is called through the C ABI
+and must give exactly what lc_layout_copy_host gives, on two calls in a row
+(the array keeps the previous call's bytes), and both must equal the oracle,
+so that a fault shared by the two library paths (the planner, the kernels)
+would show too.
 
 This file is named to be collected last.
 """
@@ -15,6 +17,7 @@ import ctypes
 import numpy as np
 import pytest
 
+import oracle
 import workloads
 
 torch = pytest.importorskip("torch")
@@ -59,6 +62,9 @@ def _compare(M, src_l, dst_l, w, n_tiles, seed):
         assert _static_call(M, src_h, src_l, got, dst_l, w, n_tiles) == 0
         torch.cuda.current_stream().synchronize()
         assert np.array_equal(got.numpy(), want.numpy()), "call %d differs" % call
+        expect = fill.numpy().copy()
+        oracle.copy(src_h.numpy(), src_l, expect, dst_l, w, n_tiles)
+        assert np.array_equal(got.numpy(), expect), "call %d differs from the oracle" % call
 
 
 def test_static_staging_matches_pipelined_host_copy(M):
@@ -69,6 +75,13 @@ def test_static_staging_matches_pipelined_host_copy(M):
     _compare(M, L((4, 32), (32, 1)), L((4, 32), (1, 4), 8, 200), 2, 301, seed=3)  # holes
     c = workloads.config(3, scale="small")                   # one tile, a transpose
     _compare(M, c["src"], c["dst"], 2, 1, seed=4)
+
+
+def test_static_staging_warp_shuffle_and_transposes(M):
+    c = workloads.config(4, 1, scale="small")                # one-byte transpose
+    _compare(M, c["src"], c["dst"], 1, 1, seed=5)
+    V = 4                                                      # the shuffle's blocks, mirrored
+    _compare(M, L((64, V), (V, 1)), L((64, V), (1, 64)), 4, 1001, seed=6)
 
 
 def test_static_staging_refuses_oversized_tiles(M):
