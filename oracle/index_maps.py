@@ -235,9 +235,72 @@ def gmem_smem_partition(shape, g_stride, s_stride, elem_bytes: int,
     raise Decline("no vector width")
 
 
+def gmem_smem_partition_guarded(shape, g_stride, s_stride, elem_bytes: int,
+                                num_threads: int, g_offset: int = 0, s_offset: int = 0,
+                                chunk_bytes: int | None = None):
+    """The same partition with a guard instead of the page's "declines".
+
+    Steps 1 and 2 as in ``gmem_smem_partition`` (global side drives the
+    canonical order; widest vector whose per-thread pointers stay aligned),
+    with two changes from other passages:
+      * the element count need not be a multiple of ``threads * vec``: the
+        rounds are ``outer = ceil(total / (threads * vec))`` and a vector whose
+        first element lies past the end is not moved (TileLang tutorial
+        "loop_mapping.py", closing note of ``compare_shapes``: when the count
+        is below the thread count some threads get no work and the generated
+        code adds a guard);
+      * with a swizzled shared layout (``chunk_bytes`` = its swizzle chunk), a
+        vector is at most one chunk ("copy -> gmem_smem", section "How inputs
+        change the algorithm", last paragraph: a swizzled shared layout caps
+        vec to one swizzle chunk).
+    Returns dict(modes, vec, outer, total, guarded).
+    """
+    if chunk_bytes is not None and chunk_bytes < elem_bytes:
+        raise Decline("a swizzle chunk of %d bytes would split a %d-byte element" % (chunk_bytes, elem_bytes))
+    modes = [(e, g, s) for e, g, s in zip(shape, g_stride, s_stride) if e != 1]
+    modes.sort(key=lambda m: -m[1])
+    modes = _coalesce(modes)
+    total = 1
+    for e, _, _ in modes:
+        total *= e
+    bits_per_elem = 8 * elem_bytes
+    for bits in (128, 64, 32, 16, 8):
+        if bits < bits_per_elem or bits % bits_per_elem:
+            continue
+        if chunk_bytes is not None and bits // 8 > chunk_bytes:
+            continue
+        vec = bits // bits_per_elem
+        if vec > 1:
+            if not modes:
+                continue
+            te, tg, ts = modes[-1]
+            if tg != 1 or ts != 1 or te % vec:
+                continue
+            others = [x for e, g, s in modes[:-1] for x in (g, s)]
+            if any(x % vec for x in others) or g_offset % vec or s_offset % vec:
+                continue
+        per_round = num_threads * vec
+        return dict(modes=modes, vec=vec, outer=-(-total // per_round), total=total,
+                    guarded=total % per_round != 0)
+    raise Decline("no vector width")
+
+
+def xor_swizzle(byte_offset: int, bits: int, chunk_log2: int, row_log2: int) -> int:
+    """Where a shared byte offset is stored under the XOR swizzle: the
+    ``bits``-bit field above ``row_log2`` is XORed into the chunk index
+    (bits ``chunk_log2 .. chunk_log2 + bits``).  Reading of "copy ->
+    gmem_smem" (whose swizzle formula is not given): the per-row XOR of the
+    "permute_layout" page applied to 2^chunk_log2-byte chunks of a shared
+    row; bytes inside a chunk keep their order.  ``bits = 0`` is no swizzle."""
+    return byte_offset ^ (((byte_offset >> row_log2) & ((1 << bits) - 1)) << chunk_log2)
+
+
 def gmem_smem_replay(part, num_threads: int, g_offset: int = 0, s_offset: int = 0):
     """The emitted serial loop: round f, thread tid moves elements
-    ``[(f * threads + tid) * vec, +vec)`` of the canonical order.
+    ``[(f * threads + tid) * vec, +vec)`` of the canonical order; with a
+    guarded partition, a vector starting at or past the element count is not
+    moved (no thread's vector straddles the end: the tail is a multiple of
+    vec).
 
     Yields (f, tid, g_lin, s_lin, [(g_off, s_off) per vector element]); g_lin
     and s_lin are the offsets of the vector's first element, the quantities
@@ -247,6 +310,8 @@ def gmem_smem_replay(part, num_threads: int, g_offset: int = 0, s_offset: int = 
     vec = part["vec"]
     for f in range(part["outer"]):
         for tid in range(num_threads):
+            if (f * num_threads + tid) * vec >= part["total"]:
+                continue  # the guard
             elems = []
             for v in range(vec):
                 idx = unflatten((f * num_threads + tid) * vec + v, extents)

@@ -215,6 +215,116 @@ def check_gmem_smem_alignment_rule():
         index_maps.gmem_smem_partition((3, 7), (7, 1), (7, 1), 4, 32)
 
 
+def check_gmem_smem_guarded():
+    """Guarded partitions ("loop_mapping.py": counts below the thread count
+    leave threads idle behind a guard), worked out by hand."""
+    # 64 fp32 words, 128 threads: 16-byte vectors, one round, threads 0..15
+    part = index_maps.gmem_smem_partition_guarded((64,), (1,), (1,), 4, 128)
+    assert (part["vec"], part["outer"], part["total"], part["guarded"]) == (4, 1, 64, True)
+    moved = {tid: [g for g, _ in el] for _f, tid, _g, _s, el in index_maps.gmem_smem_replay(part, 128)}
+    assert sorted(moved) == list(range(16))
+    assert all(moved[t] == [4 * t + v for v in range(4)] for t in range(16))
+    # 64 eight-byte words, 128 threads: vectors of 2 words, threads 0..31
+    part = index_maps.gmem_smem_partition_guarded((64,), (1,), (1,), 8, 128)
+    assert (part["vec"], part["outer"]) == (2, 1)
+    assert sorted({tid for _f, tid, _g, _s, _e in index_maps.gmem_smem_replay(part, 128)}) == list(range(32))
+    # 100 fp32 words, 8 threads: vec 4, 25 vectors, rounds of 8: 4 rounds, the
+    # last one with thread 0 alone (vector 24 = words 96..99)
+    part = index_maps.gmem_smem_partition_guarded((100,), (1,), (1,), 4, 8)
+    assert (part["vec"], part["outer"], part["guarded"]) == (4, 4, True)
+    last = [(tid, g) for f, tid, g, _s, _e in index_maps.gmem_smem_replay(part, 8) if f == 3]
+    assert last == [(0, 96)]
+    # a 4-byte swizzle chunk caps the vector at one fp32 word
+    part = index_maps.gmem_smem_partition_guarded((32, 32), (32, 1), (32, 1), 4, 32, chunk_bytes=4)
+    assert (part["vec"], part["outer"], part["guarded"]) == (1, 32, False)
+    part = index_maps.gmem_smem_partition_guarded((32, 32), (32, 1), (32, 1), 4, 32, chunk_bytes=16)
+    assert part["vec"] == 4
+    with pytest.raises(index_maps.Decline):
+        index_maps.gmem_smem_partition_guarded((8,), (1,), (1,), 16, 32, chunk_bytes=8)
+
+
+def test_gmem_smem_guarded_partition():
+    check_gmem_smem_guarded()
+
+
+def test_gmem_smem_guarded_agrees_with_the_page_where_exact():
+    """Where the page's partition accepts (the count divides), the guarded one
+    is the same partition (the dtype table of "copy -> gmem_smem" included)."""
+    rng = np.random.default_rng(11)
+    for _ in range(300):
+        rank = int(rng.integers(1, 4))
+        ext = [int(rng.choice([1, 2, 4, 8, 16, 3])) for _ in range(rank)]
+        gs = list(np.cumprod([1] + ext[::-1][:-1])[::-1])
+        ss = list(gs)
+        if rng.random() < 0.5:
+            perm = rng.permutation(rank)
+            pe = [ext[i] for i in perm]
+            st = list(np.cumprod([1] + pe[::-1][:-1])[::-1])
+            ss = [0] * rank
+            for k, i in enumerate(perm):
+                ss[i] = st[k]
+        w = int(rng.choice([1, 2, 4, 8, 16]))
+        threads = int(rng.choice([1, 4, 8, 32]))
+        try:
+            exact = index_maps.gmem_smem_partition(ext, gs, ss, w, threads)
+        except index_maps.Decline:
+            continue
+        guarded = index_maps.gmem_smem_partition_guarded(ext, gs, ss, w, threads)
+        if exact["total"] % (threads * guarded["vec"]) == 0:
+            assert (guarded["vec"], guarded["outer"], guarded["guarded"]) == (exact["vec"], exact["outer"], False)
+            assert guarded["modes"] == exact["modes"]
+
+
+def test_gmem_smem_guarded_replay_is_the_definition():
+    """Brute force on small shapes with counts off the thread grid: the
+    guarded replay moves every element exactly once, as the definition does."""
+    rng = np.random.default_rng(12)
+    for _ in range(200):
+        rank = int(rng.integers(1, 4))
+        ext = [int(rng.choice([1, 2, 3, 5, 7, 8])) for _ in range(rank)]
+        gs = [int(x) for x in np.cumprod([1] + ext[::-1][:-1])[::-1]]
+        perm = rng.permutation(rank)
+        pe = [ext[i] for i in perm]
+        st = [int(x) for x in np.cumprod([1] + pe[::-1][:-1])[::-1]]
+        ss = [0] * rank
+        for k, i in enumerate(perm):
+            ss[i] = st[k]
+        w = int(rng.choice([1, 2, 4, 8]))
+        threads = int(rng.choice([8, 32, 128]))
+        part = index_maps.gmem_smem_partition_guarded(ext, gs, ss, w, threads)
+        seen = [s for _f, _t, _g, _s, el in index_maps.gmem_smem_replay(part, threads) for _gg, s in el]
+        assert sorted(seen) == list(range(int(np.prod(ext))))
+        total = int(np.prod(ext))
+        src = rng.integers(0, 2 ** 31, total, dtype=np.int64).tolist()
+        got = [None] * total
+        index_maps.gmem_smem_copy(src, got, part, threads, g_is_src=True)
+        want = np.empty(total * 8, np.uint8)
+        definition.copy(np.asarray(src, np.int64).view(np.uint8), Layout(tuple(ext), tuple(gs)), want,
+                        Layout(tuple(ext), tuple(ss)), 8)
+        assert got == want.view(np.int64).tolist()
+
+
+def check_xor_swizzle():
+    """The shared-memory XOR swizzle: a bijection that keeps every chunk's
+    bytes together and in order; the 128-byte form puts chunk c of row r at
+    chunk c ^ (r % 8)."""
+    for bits, c, r, span in [(3, 4, 7, 4096), (2, 2, 8, 2048), (5, 2, 7, 8192), (0, 4, 7, 1024), (1, 3, 4, 256)]:
+        image = [index_maps.xor_swizzle(o, bits, c, r) for o in range(span)]
+        assert sorted(image) == list(range(span))
+        for o in range(0, span, 1 << c):
+            assert image[o:o + (1 << c)] == list(range(image[o], image[o] + (1 << c)))
+        if bits == 0:
+            assert image == list(range(span))
+    for row in range(16):
+        for chunk in range(8):
+            o = row * 128 + chunk * 16 + 5
+            assert index_maps.xor_swizzle(o, 3, 4, 7) == row * 128 + (chunk ^ (row % 8)) * 16 + 5
+
+
+def test_xor_swizzle():
+    check_xor_swizzle()
+
+
 def test_gmem_smem_alignment_rule():
     check_gmem_smem_alignment_rule()
 
@@ -593,6 +703,7 @@ def test_chosen_k_is_conflict_free():
 
 ALL_PINS = [check_definition_vs_numpy, check_transpose_vs_numpy, check_axis_permute_vs_numpy,
             check_gmem_smem_table, check_gmem_smem_alignment_rule, check_round_trip_identity,
+            check_gmem_smem_guarded, check_xor_swizzle,
             check_loop_mapping_tables, check_default_override_tables, check_override_hand_worked,
             check_override_sizes, check_sf_transpose_example,
             check_bank_degrees_worked_example, check_access_degree_closed_forms]
@@ -633,6 +744,7 @@ def _mut_paired_swapped(src, dst):
     "pairing_swapped", "plan_thread_slot_swapped", "vec_ignores_offsets",
     "bank_counts_lanes_not_words", "project_drops_last_term",
     "override_thread_slot_swapped", "override_digits_column_major",
+    "guard_drops_last_round", "swizzle_xors_chunk_into_row",
 ])
 def test_planted_mistakes(monkeypatch, mutation):
     assert not _some_pin_fails()  # the unmutated oracle passes every pin
@@ -693,4 +805,16 @@ def test_planted_mistakes(monkeypatch, mutation):
                     sum(c * m[2] for c, m in zip(digits, loop)))
             return out
         monkeypatch.setattr(index_maps, "loop_layout_plan", bad_override)
+    elif mutation == "guard_drops_last_round":
+        orig = index_maps.gmem_smem_partition_guarded
+
+        def bad_guarded(*args, **kw):  # rounds rounded down: the partial round is lost
+            part = dict(orig(*args, **kw))
+            part["outer"] -= 1 if part["guarded"] else 0
+            return part
+        monkeypatch.setattr(index_maps, "gmem_smem_partition_guarded", bad_guarded)
+    elif mutation == "swizzle_xors_chunk_into_row":
+        def bad_swizzle(o, bits, c, r):
+            return o ^ (((o >> c) & ((1 << bits) - 1)) << r)
+        monkeypatch.setattr(index_maps, "xor_swizzle", bad_swizzle)
     assert _some_pin_fails(), mutation
