@@ -136,7 +136,14 @@ typedef enum {
      * transpose it in registers by warp shuffles and store V 16-byte chunks;
      * no shared memory.  Other strides and both bases must be 16-byte
      * aligned. */
-    LC_KERNEL_WARP_SHUFFLE = 6
+    LC_KERNEL_WARP_SHUFFLE = 6,
+    /* Staged tile copy ("copy -> gmem_smem", its demonstration program): one
+     * CTA of 256 threads per tile, global -> shared through the source
+     * layout, a barrier, shared -> global through the destination layout,
+     * the shared tile swizzled by the library's choice; tiles of at most
+     * LC_STAGED_MAX_BYTES (lc_layout_copy_staged sets threads, swizzle and
+     * traces). */
+    LC_KERNEL_SMEM_STAGED = 7
 } lc_kernel;
 
 /* What the planner decided for one copy (filled by lc_plan). */
@@ -367,8 +374,10 @@ int lc_warp_unit_plan(const lc_tile_layout *src_layout, const lc_tile_layout *ds
 /* Runs the op on n_units units, each staged in shared memory.  src holds
  * n_units source buffers back to back (unit i at i * src_cosize * elem_bytes
  * bytes), dst likewise with dst_cosize.  For each unit, a warp copies the
- * source buffer into shared buffer A and (in_place = 0) the destination
- * buffer into shared buffer B, permutes A -> B (in_place = 0) or A -> A (in_place = 1,
+ * source buffer into shared buffer A and (in_place = 0, unless the
+ * destination image is the whole buffer: its strides form an exact mixed
+ * radix) the destination buffer into shared buffer B, permutes A -> B
+ * (in_place = 0) or A -> A (in_place = 1,
  * the aliased form: the destination layout is applied inside A, which needs
  * src_cosize >= dst_cosize), and copies the destination buffer back to dst.
  * Bytes of the destination buffer outside its image keep their values
@@ -382,6 +391,93 @@ int lc_warp_unit_plan(const lc_tile_layout *src_layout, const lc_tile_layout *ds
 #define LC_WARP_UNIT_MAX_BYTES 8192
 int lc_warp_unit_run(const void *src, void *dst, const lc_warp_unit *unit, int32_t elem_bytes,
                      int64_t n_units, int32_t in_place, lc_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * The global <-> shared copy of Apache TVM docs "copy -> gmem_smem" as a
+ * device primitive for kernels that stage through shared memory.
+ *
+ * A shared buffer may be swizzled: the byte at shared offset o (as its
+ * layout places it) is stored at
+ *     o ^ (((o >> row_log2) & ((1 << bits) - 1)) << chunk_log2),
+ * i.e. the `bits`-bit field above row_log2 is XORed into the index of the
+ * 2^chunk_log2-byte chunk; bytes inside a chunk keep their order.  The page
+ * names a swizzle without giving its formula; this XOR form is the library's
+ * reading (the per-row XOR of "permute_layout" applied to chunks).  bits = 0
+ * is no swizzle; otherwise row_log2 >= chunk_log2 + bits (so that the map is
+ * one-to-one) and the chunk holds at least one element.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    int32_t bits;
+    int32_t chunk_log2;
+    int32_t row_log2;
+} lc_smem_swizzle;
+
+/* One copy between a global and a shared buffer by `threads` threads, in the
+ * [outer, threads, vec] split ("copy -> gmem_smem", section "Algorithm"
+ * steps 1-3): the modes in the global side's canonical order (stride
+ * descending, neighbours contiguous on both sides merged), vectors of `vec`
+ * elements, round f of thread tid moving elements
+ * [(f * threads + tid) * vec, + vec) of that order.  When threads * vec does
+ * not divide the element count, the last round is partial and the threads
+ * past the end do nothing (`guarded`; TileLang "loop_mapping.py": such
+ * threads get no work behind a guard).  Filled by lc_gmem_smem_plan; read
+ * by lc_device::gmem_smem_copy in layout_copy_device.cuh. */
+typedef struct {
+    int32_t n_modes;
+    int64_t extent[LC_MAX_RANK];
+    int64_t g_stride[LC_MAX_RANK];   /* elements */
+    int64_t s_stride[LC_MAX_RANK];   /* elements */
+    int64_t g_offset, s_offset;      /* elements */
+    int32_t elem_bytes, vec, threads;
+    int64_t outer;                   /* rounds: ceil(total / (threads * vec)) */
+    int64_t total;                   /* elements (< 2^31) */
+    int32_t guarded;
+    lc_smem_swizzle swizzle;
+    /* vector-start indices are split into mode digits by multiplying:
+     * digit i of n is n - q * extent[i], q = (umulhi(n, div_m[i]) + n) >> div_s[i] */
+    uint32_t div_m[LC_MAX_RANK];
+    int32_t div_s[LC_MAX_RANK];
+} lc_gmem_smem;
+
+/* Plans one global <-> shared copy: the two layouts index the same logical
+ * elements (equal non-unit extents, as for lc_layout_copy; tile_stride is
+ * ignored), `threads` in 1..1024, `swizzle` the shared buffer's swizzle
+ * (NULL = none).  The vector is the widest of 16, 8, 4, 2, 1 bytes with the
+ * innermost mode contiguous on both sides and a multiple of it, every other
+ * stride and both offsets multiples of it, and -- with a swizzle -- at most
+ * one chunk ("copy -> gmem_smem", section "How inputs change the algorithm",
+ * last paragraph).  Host only.  Errors: LC_ERR_NULL, LC_ERR_RANK,
+ * LC_ERR_EXTENT_MISMATCH, LC_ERR_ELEM_BYTES, LC_ERR_BAD_STRIDE (a negative
+ * stride or offset, or a swizzle that is not one-to-one or splits an
+ * element), LC_ERR_SHAPE (threads outside 1..1024, 2^31 elements or more). */
+int lc_gmem_smem_plan(const lc_tile_layout *global_layout, const lc_tile_layout *shared_layout,
+                      int32_t elem_bytes, int32_t threads, const lc_smem_swizzle *swizzle,
+                      lc_gmem_smem *out);
+
+/* Largest shared tile of lc_layout_copy_staged, in bytes. */
+#define LC_STAGED_MAX_BYTES (96 * 1024)
+
+/* "copy -> gmem_smem"'s demonstration program as a copy: each tile is
+ * staged through shared memory by one CTA of `threads` threads (a multiple
+ * of 32, at most 1024), copy 1 global -> shared through the source layout
+ * (the source drives the canonical order), a CTA barrier, copy 2 shared ->
+ * global through the destination layout (the destination drives), both by
+ * lc_device::gmem_smem_copy.  The shared tile holds the tile's logical box
+ * row-major, under `swizzle` (NULL: the library picks, with its bank
+ * simulator, the swizzle that makes both copies' shared accesses least
+ * conflicted).  Tiles are spread over a grid of resident CTAs.
+ *   trace_in, trace_out  NULL, or n_tiles * N int64 words of device memory
+ *          (N = the tile's element count) receiving, at tile * N + the
+ *          element's row-major index in the tile, f * threads + tid of the
+ *          round and thread that moved it in copy 1 / copy 2.
+ * Results equal lc_layout_copy's.  Asynchronous on `stream`.  Errors: as
+ * lc_layout_copy (source and destination may not overlap), plus
+ * LC_ERR_SHAPE when a tile's box exceeds LC_STAGED_MAX_BYTES or `threads` is
+ * invalid, and lc_gmem_smem_plan's errors for the swizzle. */
+int lc_layout_copy_staged(const void *src, const lc_tile_layout *src_layout, void *dst,
+                          const lc_tile_layout *dst_layout, int32_t elem_bytes, int64_t n_tiles,
+                          int32_t threads, const lc_smem_swizzle *swizzle, int64_t *trace_in,
+                          int64_t *trace_out, lc_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Loop-layout override of the default partition (TileLang tutorial
@@ -474,6 +570,19 @@ int lc_layout_copy_loop(const void *src, const lc_tile_layout *src_layout,
                         void *dst, const lc_tile_layout *dst_layout,
                         int32_t elem_bytes, int64_t n_tiles, const lc_loop_layout *loop,
                         int64_t *trace, lc_stream_t stream);
+
+/* Row-major strides of `shape` (the layout S[shape] with no strides given,
+ * "copy -> gmem_smem", section "Demonstration program",
+ * `TileLayout(S[shape])`): stride[rank-1] = 1, stride[k] = stride[k+1] *
+ * max(shape[k+1], 1).  Host only.  Errors: LC_ERR_NULL, LC_ERR_RANK,
+ * LC_ERR_SHAPE (negative extent), LC_ERR_OVERFLOW. */
+int lc_row_major_strides(int32_t rank, const int64_t *shape, int64_t *stride);
+
+/* Elements a buffer must hold for n_tiles tiles of `layout`: offset +
+ * (n_tiles - 1) * tile_stride + cosize (tile_stride 0 = the cosize), or the
+ * offset alone when no word is addressed (n_tiles = 0 or a zero extent).
+ * Host only.  Returns -1 for an invalid layout or count, or on overflow. */
+int64_t lc_layout_footprint(const lc_tile_layout *layout, int64_t n_tiles);
 
 /* Human-readable name of a status / kernel class (static strings). */
 const char *lc_status_string(int32_t status);

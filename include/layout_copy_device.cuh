@@ -1,6 +1,7 @@
 /* Device side of the warp-scope permute between layout-carrying buffers
  * (Apache TVM docs "permute_layout", section "Algorithm", step 3: two
- * register-staged phases under the per-lane XOR swizzle).
+ * register-staged phases under the per-lane XOR swizzle), and of the
+ * global <-> shared copy of "copy -> gmem_smem" (gmem_smem_copy, below).
  *
  * Usage inside a kernel, all 32 lanes of a warp together:
  *
@@ -103,6 +104,78 @@ __device__ __forceinline__ void warp_unit_permute(void *dst, const void *src, in
     for (int r = 0; r < PMAX; ++r)
         if (r < P) *reinterpret_cast<T *>(d + doff[r]) = regs[r];
     __syncwarp();
+}
+
+/* ---- "copy -> gmem_smem": the global <-> shared copy -------------------
+ *
+ * Usage inside a kernel, all `plan.threads` threads of the copy together
+ * (tid in [0, plan.threads)):
+ *
+ *     lc_device::gmem_smem_copy<W>(plan, global_base, shared_base, tid, true);   // global -> shared
+ *     __syncthreads();
+ *     lc_device::gmem_smem_copy<W>(plan2, global2, shared_base, tid, false);     // shared -> global
+ *
+ * `plan` comes from lc_gmem_smem_plan on the host (pass it by value or in
+ * constant memory); W = plan.elem_bytes.  Element offsets are relative to
+ * the two base pointers; global_base must be aligned to the vector
+ * (plan.vec * W bytes) after adding plan.g_offset elements, shared_base to
+ * 16 bytes.  Each thread runs its rounds f = 0 .. plan.outer - 1, stopping
+ * at the first vector past the element count (the guard), and moves its
+ * vector with one plan.vec * W-byte access on each side; the shared address
+ * goes through plan.swizzle.  `trace` (NULL, or one int64 per shared element
+ * offset) receives f * threads + tid for every element moved. */
+
+/* Stored position of shared byte offset o under the swizzle. */
+__device__ __forceinline__ uint32_t smem_swizzle(const lc_smem_swizzle &z, uint32_t o) {
+    return o ^ (((o >> z.row_log2) & ((1u << z.bits) - 1u)) << z.chunk_log2);
+}
+
+template <int B> struct vec_word;
+template <> struct vec_word<1> { using type = uint8_t; };
+template <> struct vec_word<2> { using type = uint16_t; };
+template <> struct vec_word<4> { using type = uint32_t; };
+template <> struct vec_word<8> { using type = uint2; };
+template <> struct vec_word<16> { using type = uint4; };
+
+template <int B>
+__device__ __forceinline__ void move_bytes(void *to, const void *from) {
+    using T = typename vec_word<B>::type;
+    *reinterpret_cast<T *>(to) = *reinterpret_cast<const T *>(from);
+}
+
+template <int W>
+__device__ __forceinline__ void gmem_smem_copy(const lc_gmem_smem &p, void *global, void *shared, int tid,
+                                               bool global_to_shared, int64_t *trace = nullptr) {
+    uint8_t *const gb = static_cast<uint8_t *>(global);
+    uint8_t *const sb = static_cast<uint8_t *>(shared);
+    const int vb = p.vec * W;
+    for (int64_t f = 0; f < p.outer; ++f) {
+        const int64_t first = (f * p.threads + tid) * p.vec;
+        if (first >= p.total) break;  // the guard: nothing past the element count
+        uint32_t rest = static_cast<uint32_t>(first);
+        int64_t g = p.g_offset, s = p.s_offset;
+        for (int i = p.n_modes - 1; i >= 0; --i) {
+            const uint32_t q = static_cast<uint32_t>(
+                (static_cast<uint64_t>(__umulhi(rest, p.div_m[i])) + rest) >> p.div_s[i]);
+            const uint32_t c = rest - q * static_cast<uint32_t>(p.extent[i]);
+            g += static_cast<int64_t>(c) * p.g_stride[i];
+            s += static_cast<int64_t>(c) * p.s_stride[i];
+            rest = q;
+        }
+        uint8_t *gp = gb + g * W;
+        uint8_t *sp = sb + smem_swizzle(p.swizzle, static_cast<uint32_t>(s * W));
+        uint8_t *to = global_to_shared ? sp : gp;
+        const uint8_t *from = global_to_shared ? gp : sp;
+        switch (vb) {
+            case 16: move_bytes<16>(to, from); break;
+            case 8: move_bytes<8>(to, from); break;
+            case 4: move_bytes<4>(to, from); break;
+            case 2: move_bytes<2>(to, from); break;
+            default: move_bytes<1>(to, from); break;
+        }
+        if (trace)
+            for (int v = 0; v < p.vec; ++v) trace[s + v] = f * p.threads + tid;
+    }
 }
 
 }  // namespace lc_device

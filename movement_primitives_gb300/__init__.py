@@ -36,12 +36,11 @@ class TileLayout:
     def __post_init__(self):
         shape = tuple(int(e) for e in self.shape)
         object.__setattr__(self, "shape", shape)
-        if self.stride is None:  # S[shape] alone is row-major
-            st, acc = [], 1
-            for e in reversed(shape):
-                st.append(acc)
-                acc *= max(e, 1)
-            object.__setattr__(self, "stride", tuple(reversed(st)))
+        if self.stride is None:  # S[shape] alone: the library's row-major strides
+            n = len(shape)
+            sh, st = (ctypes.c_int64 * max(n, 1))(*shape), (ctypes.c_int64 * max(n, 1))()
+            _check(_lib.lib().lc_row_major_strides(n, sh, st), "row-major strides of %r" % (shape,))
+            object.__setattr__(self, "stride", tuple(st[:n]))
         else:
             object.__setattr__(self, "stride", tuple(int(s) for s in self.stride))
 
@@ -66,11 +65,13 @@ class TileLayout:
         return c
 
     def footprint(self, n_tiles: int) -> int:
-        """Elements a buffer needs to hold n_tiles tiles (bounds check only)."""
-        if n_tiles <= 0 or any(e == 0 for e in self.shape):
-            return 0
-        span = 1 + sum((e - 1) * s for e, s in zip(self.shape, self.stride))
-        return self.offset + (n_tiles - 1) * (self.tile_stride or span) + span
+        """Elements a buffer needs to hold n_tiles tiles (the library's count;
+        bounds check only)."""
+        c = self.to_c()
+        n = int(_lib.lib().lc_layout_footprint(ctypes.byref(c), int(n_tiles)))
+        if n < 0:
+            raise ValueError("invalid layout or tile count: %r, %d tiles" % (self, n_tiles))
+        return n
 
 
 _LAYOUT_CACHE = {}  # layout value -> (TileLayout, its C struct); the library only reads the struct
@@ -423,3 +424,68 @@ def layout_copy_loop(src, src_layout, dst, dst_layout, loop, n_tiles: int = 1,
         trace_ptr = trace.data_ptr()
     layout_copy_loop_ptr(src.data_ptr(), sl, dst.data_ptr(), dl, w, loop, n_tiles, trace_ptr,
                          _stream_handle(stream))
+
+
+# ---------------------------------------------------------------------------
+# "copy -> gmem_smem": the global <-> shared partition and the staged copy
+# ---------------------------------------------------------------------------
+
+def _swizzle_to_c(swizzle):
+    if swizzle is None:
+        return None
+    bits, chunk_log2, row_log2 = (int(x) for x in swizzle)
+    return _lib.CSmemSwizzle(bits, chunk_log2, row_log2)
+
+
+def gmem_smem_plan(global_layout, shared_layout, elem_bytes: int, threads: int, swizzle=None) -> dict:
+    """The library's partition of one global <-> shared copy by ``threads``
+    threads (host only).  ``swizzle``: (bits, chunk_log2, row_log2) or None."""
+    gl, sl = _c_layout(global_layout), _c_layout(shared_layout)
+    z = _swizzle_to_c(swizzle)
+    out = _lib.CGmemSmem()
+    _check(_lib.lib().lc_gmem_smem_plan(ctypes.byref(gl), ctypes.byref(sl), int(elem_bytes), int(threads),
+                                        ctypes.byref(z) if z is not None else None, ctypes.byref(out)),
+           "gmem_smem_plan")
+    n = out.n_modes
+    return dict(modes=[(out.extent[i], out.g_stride[i], out.s_stride[i]) for i in range(n)],
+                vec=out.vec, outer=out.outer, total=out.total, guarded=bool(out.guarded), threads=out.threads,
+                swizzle=(out.swizzle.bits, out.swizzle.chunk_log2, out.swizzle.row_log2))
+
+
+def layout_copy_staged(src, src_layout, dst, dst_layout, n_tiles: int = 1, elem_bytes: int | None = None,
+                       threads: int = 256, swizzle=None, trace_in=None, trace_out=None, stream=None) -> None:
+    """layout_copy with each tile staged through shared memory by one CTA of
+    ``threads`` threads (the two copies of "copy -> gmem_smem").  ``swizzle``:
+    (bits, chunk_log2, row_log2) of the shared tile, or None for the library's
+    choice.  ``trace_in`` / ``trace_out``: optional int64 CUDA tensors of
+    n_tiles * (elements per tile) entries receiving round * threads + thread
+    of the copy that moved each element, indexed by its row-major position."""
+    if not (src.is_cuda and dst.is_cuda):
+        raise ValueError("layout_copy_staged needs CUDA tensors (there is no CPU path)")
+    if not (src.is_contiguous() and dst.is_contiguous()):
+        raise ValueError("pass contiguous tensors; express strides through the layouts")
+    w = int(elem_bytes) if elem_bytes is not None else src.element_size()
+    sl, dl = _layout_pair(src_layout)[0], _layout_pair(dst_layout)[0]
+    for name, t, l in (("source", src, sl), ("destination", dst, dl)):
+        need = l.footprint(n_tiles) * w
+        if need > t.numel() * t.element_size():
+            raise ValueError("%s layout reaches %d bytes; the tensor holds %d"
+                             % (name, need, t.numel() * t.element_size()))
+    points = 1
+    for e in sl.shape:
+        points *= int(e)
+    ptrs = []
+    for tr in (trace_in, trace_out):
+        if tr is None:
+            ptrs.append(None)
+            continue
+        if not tr.is_cuda or not tr.is_contiguous() or tr.element_size() != 8 or tr.numel() < n_tiles * points:
+            raise ValueError("a trace must be a contiguous 8-byte CUDA tensor of >= %d entries" % (n_tiles * points))
+        ptrs.append(ctypes.c_void_p(tr.data_ptr()))
+    z = _swizzle_to_c(swizzle)
+    cs, cd = sl.to_c(), dl.to_c()
+    _check(_lib.lib().lc_layout_copy_staged(ctypes.c_void_p(src.data_ptr()), ctypes.byref(cs),
+                                            ctypes.c_void_p(dst.data_ptr()), ctypes.byref(cd), w, int(n_tiles),
+                                            int(threads), ctypes.byref(z) if z is not None else None,
+                                            ptrs[0], ptrs[1], ctypes.c_void_p(_stream_handle(stream))),
+           "layout_copy_staged")

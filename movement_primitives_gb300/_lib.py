@@ -29,7 +29,7 @@ STATUS_NAMES = {
 }
 STATUS = {v: k for k, v in STATUS_NAMES.items()}
 KERNELS = {"auto": 0, "vec_copy": 1, "warp_permute": 2, "tile_transpose": 3, "smem_transpose": 4,
-           "tma_copy": 5, "warp_shuffle": 6}
+           "tma_copy": 5, "warp_shuffle": 6, "smem_staged": 7}
 
 
 class CTileLayout(ctypes.Structure):
@@ -81,6 +81,21 @@ class CLoopPlanInfo(ctypes.Structure):
                 ("points_per_tile", ctypes.c_int64), ("vec", ctypes.c_int32), ("split", ctypes.c_int32)]
 
 
+class CSmemSwizzle(ctypes.Structure):
+    _fields_ = [("bits", ctypes.c_int32), ("chunk_log2", ctypes.c_int32), ("row_log2", ctypes.c_int32)]
+
+
+class CGmemSmem(ctypes.Structure):
+    _fields_ = [("n_modes", ctypes.c_int32),
+                ("extent", ctypes.c_int64 * MAX_RANK), ("g_stride", ctypes.c_int64 * MAX_RANK),
+                ("s_stride", ctypes.c_int64 * MAX_RANK),
+                ("g_offset", ctypes.c_int64), ("s_offset", ctypes.c_int64),
+                ("elem_bytes", ctypes.c_int32), ("vec", ctypes.c_int32), ("threads", ctypes.c_int32),
+                ("outer", ctypes.c_int64), ("total", ctypes.c_int64), ("guarded", ctypes.c_int32),
+                ("swizzle", CSmemSwizzle),
+                ("div_m", ctypes.c_uint32 * MAX_RANK), ("div_s", ctypes.c_int32 * MAX_RANK)]
+
+
 _P_LAYOUT = ctypes.POINTER(CTileLayout)
 _P_LOOP = ctypes.POINTER(CLoopLayout)
 _P_I32 = ctypes.POINTER(ctypes.c_int32)
@@ -121,6 +136,14 @@ PROTOTYPES = {
     "lc_layout_copy_loop": (ctypes.c_int, [ctypes.c_void_p, _P_LAYOUT, ctypes.c_void_p, _P_LAYOUT,
                                            ctypes.c_int32, ctypes.c_int64, _P_LOOP, ctypes.c_void_p,
                                            ctypes.c_void_p]),
+    "lc_gmem_smem_plan": (ctypes.c_int, [_P_LAYOUT, _P_LAYOUT, ctypes.c_int32, ctypes.c_int32,
+                                         ctypes.POINTER(CSmemSwizzle), ctypes.POINTER(CGmemSmem)]),
+    "lc_layout_copy_staged": (ctypes.c_int, [ctypes.c_void_p, _P_LAYOUT, ctypes.c_void_p, _P_LAYOUT,
+                                             ctypes.c_int32, ctypes.c_int64, ctypes.c_int32,
+                                             ctypes.POINTER(CSmemSwizzle), ctypes.c_void_p, ctypes.c_void_p,
+                                             ctypes.c_void_p]),
+    "lc_row_major_strides": (ctypes.c_int, [ctypes.c_int32, _P_I64, _P_I64]),
+    "lc_layout_footprint": (ctypes.c_int64, [_P_LAYOUT, ctypes.c_int64]),
     "lc_status_string": (ctypes.c_char_p, [ctypes.c_int32]),
     "lc_kernel_name": (ctypes.c_char_p, [ctypes.c_int32]),
 }

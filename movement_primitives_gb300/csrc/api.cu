@@ -76,6 +76,7 @@ int launch_plan(const Plan &p, const uint8_t *s, uint8_t *d, cudaStream_t cs, bo
         case LC_KERNEL_VEC_COPY: return launch_vec(p, s, d, cs);
         case LC_KERNEL_WARP_PERMUTE: return launch_warp(p, s, d, cs);
         case LC_KERNEL_WARP_SHUFFLE: return launch_shuffle(p, s, d, cs);
+        case LC_KERNEL_SMEM_STAGED: return launch_staged(p, s, d, cs);
         case LC_KERNEL_SMEM_TRANSPOSE: return launch_smem(p, s, d, cs);
         case LC_KERNEL_TMA_COPY: {
             const int r = launch_tma_copy(p, s, d, cs);
@@ -174,6 +175,7 @@ extern "C" const char *lc_kernel_name(int32_t kernel) {
         case LC_KERNEL_SMEM_TRANSPOSE: return "smem_transpose";
         case LC_KERNEL_TMA_COPY: return "tma_copy";
         case LC_KERNEL_WARP_SHUFFLE: return "warp_shuffle";
+        case LC_KERNEL_SMEM_STAGED: return "smem_staged";
     }
     return "unknown";
 }

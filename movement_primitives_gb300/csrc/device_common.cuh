@@ -37,6 +37,23 @@ __device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv &f) {
     return static_cast<uint32_t>((static_cast<uint64_t>(__umulhi(n, f.m)) + n) >> f.s);
 }
 
+// Global stores of the copy kernels: with LC_STORE_CS = 1 (or CS = true for
+// one call site) they carry the streaming cache hint (st.global.cs: the line
+// is likely written once, evict it first).  Measured on GB300: the window
+// sum gains 1.4 points of the copy peak with it (97.9 -> 99.3 %); the vector
+// copy loses 1.2, the tile transpose moves -1.5 .. +2.3 by width, the other
+// classes do not move.
+#ifndef LC_STORE_CS
+#define LC_STORE_CS 0
+#endif
+template <typename T, bool CS = (LC_STORE_CS != 0)>
+__device__ __forceinline__ void store_out(void *p, const T &v) {
+    if constexpr (CS)
+        __stcs(reinterpret_cast<T *>(p), v);
+    else
+        *reinterpret_cast<T *>(p) = v;
+}
+
 template <int B> struct Word;
 template <> struct Word<1> { using T = uint8_t; };
 template <> struct Word<2> { using T = uint16_t; };

@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(LC_LOOP_MAX_THREADS) k_loop_copy(const __grid_
 #pragma unroll
                     for (int u = 0; u < kLoopUnroll; ++u) {
                         if (i0 + u >= n) continue;
-                        *reinterpret_cast<T *>(dst + o[u].y) = v[u];
+                        store_out<T>(dst + o[u].y, v[u]);
                         if (a.trace) trace_vector(a, tile, tflat + slot_flat<WIDE>(a, cb + i0 + u), t, cb + i0 + u);
                     }
                 }
@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(LC_LOOP_MAX_THREADS) k_loop_copy(const __grid_
 #pragma unroll
             for (int u = 0; u < kLoopUnroll; ++u) {
                 if (dofs[u] < 0) continue;
-                *reinterpret_cast<T *>(dst + dofs[u]) = v[u];
+                store_out<T>(dst + dofs[u], v[u]);
                 if (a.trace) trace_vector(a, tile, flats[u], t, q0 + u);
             }
         }

@@ -189,7 +189,7 @@ __device__ __forceinline__ void copy_out(const SmemArgs &a, const TileRef &r, co
 #pragma unroll
     for (int f = 0; f < G::ROUNDS2; ++f, q += step)
         if (FULL || ly + G::STEP2 * f < r.ny)
-            *reinterpret_cast<T *>(q) = *reinterpret_cast<const T *>(row + ((p0 + G::STEP2 * W * f) ^ swc));
+            store_out<T>(q, *reinterpret_cast<const T *>(row + ((p0 + G::STEP2 * W * f) ^ swc)));
 }
 
 template <int W>

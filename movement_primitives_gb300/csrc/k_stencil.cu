@@ -84,7 +84,7 @@ __device__ __forceinline__ void sums4(const StencilArgs &p, const float *cur, in
     }
     const int64_t i = i0 + j;
     if (p.vec_out && i + 4 <= p.n) {
-        *reinterpret_cast<float4 *>(p.b + i) = make_float4(o[0], o[1], o[2], o[3]);
+        store_out<float4, true>(p.b + i, make_float4(o[0], o[1], o[2], o[3]));
     } else {
 #pragma unroll
         for (int v = 0; v < 4; ++v)

@@ -45,6 +45,11 @@ namespace lc {
 #ifndef LC_TILE_Y_FASTEST
 #define LC_TILE_Y_FASTEST 1
 #endif
+// 1: one thread waits on a stage's barrier and the CTA synchronises after it;
+// 0: every thread waits on the barrier itself.
+#ifndef LC_TILE_POLL_ONE
+#define LC_TILE_POLL_ONE 0
+#endif
 
 // Bytes per TMA box row (128 or 256) and ring stages per width, measured on
 // GB300: 256-byte rows with 3 stages move the 16384^2 bf16 transpose at
@@ -67,13 +72,26 @@ namespace lc {
 #define LC_TILE_STAGES_W8 3
 #endif
 
-template <int W> struct TileCfg {
+// Shorter boxes for copies of at most LC_TILE_SHORT_MAX_BYTES a side, 1-,
+// 2- and 4-byte words: measured on GB300 (L2 flushed by a read between
+// launches), 128-row boxes move the 8192^2 transposes at 85 % (2-byte words,
+// against 79 % with 256 rows) and 90 % (4-byte, against 85 %), while the
+// 16384^2 2-byte transpose (512 MiB a side) drops from 91-92 % to 85-87 %.
+#ifndef LC_TILE_SHORT_ROWS
+#define LC_TILE_SHORT_ROWS 128
+#endif
+#ifndef LC_TILE_SHORT_MAX_BYTES
+#define LC_TILE_SHORT_MAX_BYTES (256ll << 20)
+#endif
+
+template <int W, bool SHORT = false> struct TileCfg {
     static constexpr int BOXB = W == 2 ? LC_TILE_BOXB_W2 : W == 8 ? LC_TILE_BOXB_W8
                               : LC_TILE_BOXB_OTHER;  // bytes per box row
     static constexpr int CPR = BOXB / 16;      // 16-byte chunks per box row
     static constexpr int V = 16 / W;           // words per 16-byte chunk
     static constexpr int TY = BOXB / W;        // words per box row
-    static constexpr int R = W == 1 ? LC_TILE_ROWS_W1 : W == 2 ? LC_TILE_ROWS_W2 : W == 4 ? LC_TILE_ROWS_W4
+    static constexpr int R = SHORT ? LC_TILE_SHORT_ROWS
+                           : W == 1 ? LC_TILE_ROWS_W1 : W == 2 ? LC_TILE_ROWS_W2 : W == 4 ? LC_TILE_ROWS_W4
                            : W == 8 ? LC_TILE_ROWS_W8 : LC_TILE_ROWS_W16;  // source rows per tile
     static constexpr int S = W == 1 ? LC_TILE_STAGES_W1 : W == 2 ? LC_TILE_STAGES_W2
                            : W == 8 ? LC_TILE_STAGES_W8 : LC_TILE_STAGES_WIDE;  // ring stages
@@ -92,6 +110,10 @@ struct TileArgs {
     int32_t nb;      // batch modes (<= 3), outermost first
     int64_t be[3], bd[3];
     int64_t tiles_x, tiles_y, n_tiles;
+    // n_tiles < 2^32: tile and batch indices are split by 32-bit invariant
+    // divisors instead of 64-bit division
+    int32_t narrow;
+    FastDiv ftx, fty, fbe[3];
     uint64_t timeout_ns;
 };
 
@@ -153,6 +175,20 @@ __device__ __forceinline__ void store_partial(uint8_t *p, const uint32_t (&v)[4]
 
 // Tile index -> (tx, ty, flat batch index).
 __device__ __forceinline__ void tile_coords(const TileArgs &a, int64_t t, int64_t &tx, int64_t &ty, int64_t &b) {
+    if (a.narrow) {
+        const uint32_t t32 = static_cast<uint32_t>(t);
+#if LC_TILE_Y_FASTEST
+        const uint32_t rest = fast_div(t32, a.fty), b32 = fast_div(rest, a.ftx);
+        ty = t32 - rest * a.fty.d;
+        tx = rest - b32 * a.ftx.d;
+#else
+        const uint32_t rest = fast_div(t32, a.ftx), b32 = fast_div(rest, a.fty);
+        tx = t32 - rest * a.ftx.d;
+        ty = rest - b32 * a.fty.d;
+#endif
+        b = b32;
+        return;
+    }
 #if LC_TILE_Y_FASTEST
     ty = t % a.tiles_y;
     const int64_t rest = t / a.tiles_y;
@@ -166,16 +202,23 @@ __device__ __forceinline__ void tile_coords(const TileArgs &a, int64_t t, int64_
 #endif
 }
 
-template <int W>
+template <int W, bool SHORT>
 __device__ __forceinline__ void tile_issue_load(const CUtensorMap *tmap, const TileArgs &a, int64_t t,
                                                 uint32_t dst, uint32_t bar) {
-    using C = TileCfg<W>;
+    using C = TileCfg<W, SHORT>;
     int64_t tx, ty, b;
     tile_coords(a, t, tx, ty, b);
     int32_t b0 = 0, b1 = 0, b2 = 0;  // batch coordinates, outermost first
-    if (a.nb == 3) { b2 = static_cast<int32_t>(b % a.be[2]); b /= a.be[2]; }
-    if (a.nb >= 2) { b1 = static_cast<int32_t>(b % a.be[1]); b /= a.be[1]; }
-    if (a.nb >= 1) { b0 = static_cast<int32_t>(b % a.be[0]); }
+    if (a.narrow) {
+        uint32_t q = static_cast<uint32_t>(b);
+        if (a.nb == 3) { const uint32_t n = fast_div(q, a.fbe[2]); b2 = static_cast<int32_t>(q - n * a.fbe[2].d); q = n; }
+        if (a.nb >= 2) { const uint32_t n = fast_div(q, a.fbe[1]); b1 = static_cast<int32_t>(q - n * a.fbe[1].d); q = n; }
+        if (a.nb >= 1) b0 = static_cast<int32_t>(q);  // the outermost batch index is below its extent
+    } else {
+        if (a.nb == 3) { b2 = static_cast<int32_t>(b % a.be[2]); b /= a.be[2]; }
+        if (a.nb >= 2) { b1 = static_cast<int32_t>(b % a.be[1]); b /= a.be[1]; }
+        if (a.nb >= 1) { b0 = static_cast<int32_t>(b % a.be[0]); }
+    }
     const int32_t c0 = static_cast<int32_t>(ty * C::TY * (W == 16 ? 2 : 1));
     const int32_t c1 = static_cast<int32_t>(tx * C::R);
     ptx::mbar_arrive_expect_tx(bar, C::TILE_BYTES);
@@ -195,10 +238,10 @@ __device__ __forceinline__ void tile_issue_load(const CUtensorMap *tmap, const T
 // ty*TY + c*V + q, words tx*R + mr*V .. + V.  The 8 lanes of a 16-byte
 // shared-memory wavefront read 8 consecutive chunks of one box row, i.e. all
 // 32 banks once: conflict-free with no swizzle.
-template <int W>
-__global__ void __launch_bounds__(TileCfg<W>::NT)
+template <int W, bool SHORT>
+__global__ void __launch_bounds__(TileCfg<W, SHORT>::NT)
     k_tile_transpose(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ TileArgs a) {
-    using C = TileCfg<W>;
+    using C = TileCfg<W, SHORT>;
     constexpr int V = C::V;
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
@@ -214,20 +257,37 @@ __global__ void __launch_bounds__(TileCfg<W>::NT)
     __syncthreads();
     if (tid == 0)
         for (int64_t i = 0; i < lmin(C::S, n_local); ++i)
-            tile_issue_load<W>(&tmap, a, blockIdx.x + i * gridDim.x, tile0 + i * C::TILE_BYTES, bar0 + 8 * i);
+            tile_issue_load<W, SHORT>(&tmap, a, blockIdx.x + i * gridDim.x, tile0 + i * C::TILE_BYTES, bar0 + 8 * i);
 
     for (int64_t i = 0; i < n_local; ++i) {
         const int s = static_cast<int>(i % C::S);
         const uint32_t parity = static_cast<uint32_t>((i / C::S) & 1);
         const int64_t t = blockIdx.x + i * gridDim.x;
+#if LC_TILE_POLL_ONE
+        __shared__ int stage_ok;
+        if (tid == 0) stage_ok = ptx::mbar_wait_bounded(bar0 + 8 * s, parity, a.timeout_ns) ? 1 : 0;
+        __syncthreads();
+        const bool ok = stage_ok != 0;
+#else
         const bool ok = ptx::mbar_wait_bounded(bar0 + 8 * s, parity, a.timeout_ns);
+#endif
         if (ok) {
             int64_t tx, ty, b;
             tile_coords(a, t, tx, ty, b);
             uint8_t *dbase = a.dst;
-            for (int k = a.nb - 1; k >= 0; --k) {
-                dbase += (b % a.be[k]) * a.bd[k];
-                b /= a.be[k];
+            if (a.narrow) {
+                uint32_t q = static_cast<uint32_t>(b);
+                for (int k = a.nb - 1; k > 0; --k) {
+                    const uint32_t n = fast_div(q, a.fbe[k]);
+                    dbase += static_cast<int64_t>(q - n * a.fbe[k].d) * a.bd[k];
+                    q = n;
+                }
+                if (a.nb > 0) dbase += static_cast<int64_t>(q) * a.bd[0];
+            } else {
+                for (int k = a.nb - 1; k >= 0; --k) {
+                    dbase += (b % a.be[k]) * a.bd[k];
+                    b /= a.be[k];
+                }
             }
             const uint8_t *st = tiles + static_cast<size_t>(s) * C::TILE_BYTES;
             for (int mb = tid; mb < C::MB; mb += C::NT) {
@@ -248,7 +308,7 @@ __global__ void __launch_bounds__(TileCfg<W>::NT)
                     if (y0 + q < a.eY) {
                         uint8_t *p = dbase + (y0 + q) * a.dY + x0 * W;
                         if (nx == V)
-                            *reinterpret_cast<uint4 *>(p) = make_uint4(out[q][0], out[q][1], out[q][2], out[q][3]);
+                            store_out<uint4>(p, make_uint4(out[q][0], out[q][1], out[q][2], out[q][3]));
                         else
                             store_partial<W>(p, out[q], nx);
                     }
@@ -265,28 +325,39 @@ __global__ void __launch_bounds__(TileCfg<W>::NT)
             return;
         }
         if (tid == 0 && i + C::S < n_local)
-            tile_issue_load<W>(&tmap, a, blockIdx.x + (i + C::S) * gridDim.x, tile0 + s * C::TILE_BYTES,
+            tile_issue_load<W, SHORT>(&tmap, a, blockIdx.x + (i + C::S) * gridDim.x, tile0 + s * C::TILE_BYTES,
                                bar0 + 8 * s);
     }
 }
 
-void tile_geometry(int w, int *rows, int *cols, int *stages, int *threads) {
+// Whether a copy of `bytes` a side with w-byte words takes the short boxes.
+static bool tile_short(int w, int64_t bytes) { return w <= 4 && bytes <= LC_TILE_SHORT_MAX_BYTES; }
+
+template <int W, bool SHORT>
+static void geometry_of(int *rows, int *cols, int *stages, int *threads) {
+    using C = TileCfg<W, SHORT>;
+    *rows = C::R;
+    *cols = C::TY;
+    *stages = C::S;
+    *threads = C::NT;
+}
+
+void tile_geometry(int w, int64_t bytes, int *rows, int *cols, int *stages, int *threads) {
+    const bool sh = tile_short(w, bytes);
     switch (w) {
-        case 1: *rows = TileCfg<1>::R; *cols = TileCfg<1>::TY; *stages = TileCfg<1>::S; *threads = TileCfg<1>::NT; break;
-        case 2: *rows = TileCfg<2>::R; *cols = TileCfg<2>::TY; *stages = TileCfg<2>::S; *threads = TileCfg<2>::NT; break;
-        case 4: *rows = TileCfg<4>::R; *cols = TileCfg<4>::TY; *stages = TileCfg<4>::S; *threads = TileCfg<4>::NT; break;
-        case 8: *rows = TileCfg<8>::R; *cols = TileCfg<8>::TY; *stages = TileCfg<8>::S; *threads = TileCfg<8>::NT; break;
-        default:
-            *rows = TileCfg<16>::R; *cols = TileCfg<16>::TY; *stages = TileCfg<16>::S; *threads = TileCfg<16>::NT;
-            break;
+        case 1: sh ? geometry_of<1, true>(rows, cols, stages, threads) : geometry_of<1, false>(rows, cols, stages, threads); break;
+        case 2: sh ? geometry_of<2, true>(rows, cols, stages, threads) : geometry_of<2, false>(rows, cols, stages, threads); break;
+        case 4: sh ? geometry_of<4, true>(rows, cols, stages, threads) : geometry_of<4, false>(rows, cols, stages, threads); break;
+        case 8: geometry_of<8, false>(rows, cols, stages, threads); break;
+        default: geometry_of<16, false>(rows, cols, stages, threads); break;
     }
 }
 
 namespace {
 
-template <int W>
+template <int W, bool SHORT>
 int launch_tile_t(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream) {
-    using C = TileCfg<W>;
+    using C = TileCfg<W, SHORT>;
     const TilePlan &tp = p.tile;
     EncodeTiledFn enc = encode_tiled();
     if (!enc) return LC_ERR_CUDA;
@@ -333,25 +404,35 @@ int launch_tile_t(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t 
     a.tiles_x = (tp.X.e + C::R - 1) / C::R;
     a.tiles_y = (tp.Y.e + C::TY - 1) / C::TY;
     a.n_tiles = a.tiles_x * a.tiles_y * nbatch;
+#ifndef LC_TILE_NARROW_DIV
+#define LC_TILE_NARROW_DIV 1
+#endif
+    a.narrow = LC_TILE_NARROW_DIV && a.n_tiles < (int64_t(1) << 32);
+    if (a.narrow) {
+        a.ftx = make_fastdiv(static_cast<uint32_t>(a.tiles_x));
+        a.fty = make_fastdiv(static_cast<uint32_t>(a.tiles_y));
+        for (int i = 0; i < tp.batch.n; ++i) a.fbe[i] = make_fastdiv(static_cast<uint32_t>(tp.batch.m[i].e));
+    }
     a.timeout_ns = wait_limit_ns();
 
-    const void *fn = reinterpret_cast<const void *>(&k_tile_transpose<W>);
+    const void *fn = reinterpret_cast<const void *>(&k_tile_transpose<W, SHORT>);
     int sms, per;
     if (prepare(fn, C::NT, C::SMEM, C::SMEM, &sms, &per) != cudaSuccess) return LC_ERR_CUDA;
     const int64_t grid = lmin(a.n_tiles, int64_t(sms) * per);
-    k_tile_transpose<W><<<static_cast<unsigned>(grid), C::NT, C::SMEM, stream>>>(tmap, a);
+    k_tile_transpose<W, SHORT><<<static_cast<unsigned>(grid), C::NT, C::SMEM, stream>>>(tmap, a);
     return finish_launch();
 }
 
 }  // namespace
 
 int launch_tile(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream) {
+    const bool sh = tile_short(p.w, p.total * p.w);
     switch (p.w) {
-        case 1: return launch_tile_t<1>(p, src, dst, stream);
-        case 2: return launch_tile_t<2>(p, src, dst, stream);
-        case 4: return launch_tile_t<4>(p, src, dst, stream);
-        case 8: return launch_tile_t<8>(p, src, dst, stream);
-        case 16: return launch_tile_t<16>(p, src, dst, stream);
+        case 1: return sh ? launch_tile_t<1, true>(p, src, dst, stream) : launch_tile_t<1, false>(p, src, dst, stream);
+        case 2: return sh ? launch_tile_t<2, true>(p, src, dst, stream) : launch_tile_t<2, false>(p, src, dst, stream);
+        case 4: return sh ? launch_tile_t<4, true>(p, src, dst, stream) : launch_tile_t<4, false>(p, src, dst, stream);
+        case 8: return launch_tile_t<8, false>(p, src, dst, stream);
+        case 16: return launch_tile_t<16, false>(p, src, dst, stream);
     }
     return LC_ERR_UNSUPPORTED;
 }

@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(kVecThreads, LC_VEC_MIN_BLOCKS) k_vec_copy(con
         }
 #pragma unroll
         for (int f = 0; f < kVecUnroll; ++f)
-            if (dofs[f] >= 0) *reinterpret_cast<T *>(a.dst + dofs[f]) = v[f];
+            if (dofs[f] >= 0) store_out<T>(a.dst + dofs[f], v[f]);
     }
 }
 

@@ -82,6 +82,22 @@ static bool unit_is_consistent(const lc_warp_unit &u) {
     return true;
 }
 
+// The destination modes, sorted by stride, read 1, e_a, e_a e_b, ...: the
+// image is exactly [0, 32 P) words, every word of the buffer written once.
+static bool dst_modes_dense(const lc_warp_unit &u) {
+    std::pair<int32_t, int32_t> m[LC_MAX_RANK];
+    int n = 0;
+    for (int i = 0; i < u.n_modes; ++i)
+        if (u.extent[i] > 1) m[n++] = {u.dst_stride[i], u.extent[i]};
+    std::sort(m, m + n);
+    int64_t expect = 1;
+    for (int i = 0; i < n; ++i) {
+        if (m[i].first != expect) return false;
+        expect *= m[i].second;
+    }
+    return expect == u.dst_cosize;
+}
+
 extern "C" int lc_warp_unit_run(const void *src, void *dst, const lc_warp_unit *unit, int32_t elem_bytes,
                                 int64_t n_units, int32_t in_place, lc_stream_t stream) {
     using namespace lc;
@@ -114,6 +130,7 @@ extern "C" int lc_warp_unit_run(const void *src, void *dst, const lc_warp_unit *
         a.dchunks = make_fastdiv(static_cast<uint32_t>(db / 16));
     }
     a.in_place = in_place ? 1 : 0;
+    a.dst_dense = dst_modes_dense(*unit) ? 1 : 0;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     switch (elem_bytes) {
         case 1: return launch_unit_width1(a, cs);

@@ -77,6 +77,22 @@ __device__ __forceinline__ int64_t unit_offset(const WarpArgs &a, int64_t u, con
 #ifndef LC_WARP_CHUNKS
 #define LC_WARP_CHUNKS 4
 #endif
+// 1: slot loads skip L1 allocation (ld.global.nc.L1::no_allocate).
+#ifndef LC_WARP_LOAD_NA
+#define LC_WARP_LOAD_NA 0
+#endif
+
+__device__ __forceinline__ uint4 warp_slot_load(const void *p) {
+#if LC_WARP_LOAD_NA
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+#else
+    return __ldg(reinterpret_cast<const uint4 *>(p));
+#endif
+}
 constexpr int kChunksInFlight = LC_WARP_CHUNKS;  // 16-byte chunks each lane keeps in flight
 
 // Each warp owns a private shared-memory slot of G = units_per_stage units and
@@ -120,7 +136,7 @@ __global__ void __launch_bounds__(kWarpThreads, LC_WARP_MIN_BLOCKS) k_warp_permu
                         const uint32_t u = fast_div(static_cast<uint32_t>(f), a.cpu_fd);
                         p = a.src + unit_offset(a, first + u, a.bs) + 16 * (f - u * cpu);
                     }
-                    v[k] = __ldg(reinterpret_cast<const uint4 *>(p));
+                    v[k] = warp_slot_load(p);
                 }
             }
 #pragma unroll
@@ -142,7 +158,7 @@ __global__ void __launch_bounds__(kWarpThreads, LC_WARP_MIN_BLOCKS) k_warp_permu
                 const uint32_t u = fast_div(static_cast<uint32_t>(f), a.cpu_fd);
                 p = a.dst + unit_offset(a, first + u, a.bd) + 16 * (f - u * cpu);
             }
-            *reinterpret_cast<uint4 *>(p) = *reinterpret_cast<const uint4 *>(slot + 16 * f);
+            store_out<uint4>(p, *reinterpret_cast<const uint4 *>(slot + 16 * f));
         }
         __syncwarp();
     }
@@ -151,7 +167,9 @@ __global__ void __launch_bounds__(kWarpThreads, LC_WARP_MIN_BLOCKS) k_warp_permu
 // lc_warp_unit_run: P4's op between two shared-memory buffers.  Each unit is
 // handled by one warp, which stages up to kUnitMaxPerWarp units at a time:
 // it copies each unit's source buffer into shared buffer A (and the
-// destination buffer into B unless in place), permutes A -> B or A -> A with
+// destination buffer into B unless in place or unless the permute writes
+// every word of B, i.e. the destination image is the whole buffer), permutes
+// A -> B or A -> A with
 // lc_device::warp_unit_permute, and copies the destination buffer out.
 constexpr int kUnitWarps = 4;
 
@@ -168,6 +186,7 @@ struct UnitArgs {
     uint32_t sbytes, dbytes;  // bytes of one source / destination buffer
     uint32_t buf;             // shared bytes per buffer (16-byte multiple)
     int32_t in_place;
+    int32_t dst_dense;        // the permute writes every word of B: B is not read in
     int32_t upw;              // units staged per warp at a time
     int32_t chunked;          // sbytes and dbytes are 16-byte multiples
     FastDiv schunks, dchunks;  // 16-byte chunks per source / destination buffer
@@ -229,12 +248,13 @@ __global__ void __launch_bounds__(kUnitWarps * 32) k_warp_unit_shared(const __gr
         uint8_t *const dg = a.dst + first * a.dbytes;
         if (a.chunked) {
             unit_chunks<true>(slot, pitch, sg, a.sbytes, a.schunks, cnt, lane);
-            if (!a.in_place) unit_chunks<true>(slot + a.buf, pitch, dg, a.dbytes, a.dchunks, cnt, lane);
+            if (!a.in_place && !a.dst_dense)
+                unit_chunks<true>(slot + a.buf, pitch, dg, a.dbytes, a.dchunks, cnt, lane);
         } else {
             for (int u = 0; u < cnt; ++u) {
                 warp_copy(slot + u * pitch, sg + static_cast<int64_t>(u) * a.sbytes, a.sbytes, lane);
-                if (!a.in_place) warp_copy(slot + u * pitch + a.buf, dg + static_cast<int64_t>(u) * a.dbytes,
-                                           a.dbytes, lane);
+                if (!a.in_place && !a.dst_dense)
+                    warp_copy(slot + u * pitch + a.buf, dg + static_cast<int64_t>(u) * a.dbytes, a.dbytes, lane);
             }
         }
         __syncwarp();

@@ -22,6 +22,11 @@ inline int finish_launch() { return cudaGetLastError() == cudaSuccess ? LC_OK : 
 int launch_vec(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream);
 int launch_warp(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream);
 int launch_shuffle(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream);
+int launch_staged(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream);
+int launch_staged_layouts(const void *src, const lc_tile_layout *src_layout, void *dst,
+                          const lc_tile_layout *dst_layout, int32_t elem_bytes, int64_t n_tiles, int32_t threads,
+                          const lc_smem_swizzle *swizzle, int64_t *trace_in, int64_t *trace_out,
+                          cudaStream_t stream);
 int launch_tile(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream);
 int launch_smem(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream);
 int launch_tma_copy(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream);

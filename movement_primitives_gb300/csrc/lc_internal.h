@@ -99,6 +99,9 @@ struct Plan {
     SmemSwizzle smem_swz;
     TmaPlan tma;
     ShflPlan shfl;
+    // the caller's layouts and tile count (the staged class plans from them)
+    lc_tile_layout src_l{}, dst_l{};
+    int64_t n_tiles = 0;
 };
 
 // Pointer facts the planner needs (alignment of the two base addresses).
@@ -106,6 +109,9 @@ struct PtrInfo {
     uintptr_t src = 0, dst = 0;
     bool check = false;  // false for lc_plan: pointers assumed 256-byte aligned
 };
+
+// Threads of one staged-tile CTA when the planner launches the class.
+constexpr int kStagedThreads = 256;
 
 int make_plan(const lc_tile_layout *src, const lc_tile_layout *dst, int32_t w,
               int64_t n_tiles, int32_t kernel, const PtrInfo &ptr, Plan *out);
@@ -176,9 +182,10 @@ constexpr SmemGeo smem_geometry(int w) {
                     : SmemGeo{16, 512, 32, 32};
 }
 
-// TMA tile transpose geometry for w-byte words (source rows and words per
-// tile, ring stages, threads), from the kernel's own compile-time table.
-void tile_geometry(int w, int *rows, int *cols, int *stages, int *threads);
+// TMA tile transpose geometry for w-byte words and `bytes` moved a side
+// (source rows and words per tile, ring stages, threads), from the kernel's
+// own compile-time table.
+void tile_geometry(int w, int64_t bytes, int *rows, int *cols, int *stages, int *threads);
 
 // Shared tile swizzle of the shared-memory transpose for w-byte words:
 // smallest (mask, shift) that keeps both copies conflict-free.
@@ -252,5 +259,14 @@ struct FastDiv {
     int32_t s = 0;
 };
 FastDiv make_fastdiv(uint32_t d);
+
+// Bank simulator on one warp-wide shared access of `width`-byte words at the
+// 32 lanes' byte addresses: the most distinct 4-byte words one bank serves in
+// a 128-byte wavefront.
+int access_degree_vec(const int64_t *byte_addr, int width);
+
+// int64 multiply / add that report overflow (false) instead of wrapping.
+bool mul_ok_ext(int64_t a, int64_t b, int64_t *r);
+bool add_ok_ext(int64_t a, int64_t b, int64_t *r);
 
 }  // namespace lc

@@ -181,6 +181,11 @@ int64_t unit_size(const ModeList &u) {
 
 }  // namespace
 
+int access_degree_vec(const int64_t *byte_addr, int width) { return access_degree(byte_addr, width); }
+
+bool mul_ok_ext(int64_t a, int64_t b, int64_t *r) { return !__builtin_mul_overflow(a, b, r); }
+bool add_ok_ext(int64_t a, int64_t b, int64_t *r) { return !__builtin_add_overflow(a, b, r); }
+
 FastDiv make_fastdiv(uint32_t d) {
     FastDiv f;
     f.d = d ? d : 1;
@@ -479,7 +484,7 @@ bool plan_tile(Plan *p, const PtrInfo &ptr) {
     if (tp.X.e > (int64_t(1) << 31) || tp.Y.e * (w == 16 ? 2 : 1) > (int64_t(1) << 31)) return false;
     if (!a16(p->src_off * w) || !a16(p->dst_off * w)) return false;
     if (ptr.check && (ptr.src % 16 || ptr.dst % 16)) return false;
-    tile_geometry(w, &tp.R, &tp.TY, &tp.S, &tp.threads);  // the kernel's per-width table
+    tile_geometry(w, p->total * w, &tp.R, &tp.TY, &tp.S, &tp.threads);  // the kernel's per-width table
     return true;
 }
 
@@ -631,7 +636,7 @@ int make_plan_core(const lc_tile_layout *src, const lc_tile_layout *dst, int32_t
     if ((st = check_layout(src)) || (st = check_layout(dst))) return st;
     if (!valid_width(w)) return LC_ERR_ELEM_BYTES;
     if (n_tiles < 0) return LC_ERR_SHAPE;
-    if (kernel < LC_KERNEL_AUTO || kernel > LC_KERNEL_WARP_SHUFFLE) return LC_ERR_UNSUPPORTED;
+    if (kernel < LC_KERNEL_AUTO || kernel > LC_KERNEL_SMEM_STAGED) return LC_ERR_UNSUPPORTED;
 
     Plan p;
     p.w = w;
@@ -681,6 +686,18 @@ int make_plan_core(const lc_tile_layout *src, const lc_tile_layout *dst, int32_t
                      [](const Mode &a, const Mode &b) { return a.d > b.d; });
     coalesce(&p.sorted);
 
+    p.src_l = *src;
+    p.dst_l = *dst;
+    p.n_tiles = n_tiles;
+    if (kernel == LC_KERNEL_SMEM_STAGED) {
+        int64_t N = 1;
+        for (int k = 0; k < src->rank; ++k) N *= src->shape[k];
+        if (N * w > LC_STAGED_MAX_BYTES) return LC_ERR_UNSUPPORTED;
+        plan_vec(&p, ptr);
+        p.kernel = kernel;
+        *out = p;
+        return LC_OK;
+    }
     if (kernel == LC_KERNEL_WARP_PERMUTE) {
         plan_vec(&p, ptr);
         if (!plan_warp(&p, ptr, false)) return LC_ERR_UNSUPPORTED;
@@ -1049,6 +1066,87 @@ extern "C" int lc_swizzle_conflicts(const lc_tile_layout *src_layout, const lc_t
     return LC_OK;
 }
 
+namespace lc {
+namespace {
+// "copy -> gmem_smem", Algorithm step 1: the modes of a global / shared pair
+// (s = global stride, d = shared stride) in the global side's canonical order,
+// stride descending, neighbours contiguous on both sides merged.
+int gmem_smem_modes(const lc_tile_layout *global_layout, const lc_tile_layout *shared_layout, ModeList *ml) {
+    const int st = align_shards(global_layout, shared_layout, ml);
+    if (st) return st;
+    std::stable_sort(ml->m, ml->m + ml->n, [](const Mode &a, const Mode &b) { return a.s > b.s; });
+    int n = 0;
+    for (int i = 0; i < ml->n; ++i) {
+        if (n && ml->m[n - 1].s == ml->m[i].s * ml->m[i].e && ml->m[n - 1].d == ml->m[i].d * ml->m[i].e) {
+            ml->m[n - 1].e *= ml->m[i].e;
+            ml->m[n - 1].s = ml->m[i].s;
+            ml->m[n - 1].d = ml->m[i].d;
+        } else {
+            ml->m[n++] = ml->m[i];
+        }
+    }
+    ml->n = n;
+    return LC_OK;
+}
+}  // namespace
+}  // namespace lc
+
+extern "C" int lc_gmem_smem_plan(const lc_tile_layout *global_layout, const lc_tile_layout *shared_layout,
+                                 int32_t elem_bytes, int32_t threads, const lc_smem_swizzle *swizzle,
+                                 lc_gmem_smem *out) {
+    if (!global_layout || !shared_layout || !out) return LC_ERR_NULL;
+    if (!lc::valid_width(elem_bytes)) return LC_ERR_ELEM_BYTES;
+    if (threads < 1 || threads > 1024) return LC_ERR_SHAPE;
+    lc_smem_swizzle z{0, 0, 0};
+    if (swizzle) z = *swizzle;
+    if (z.bits < 0 || z.bits > 16 || z.chunk_log2 < 0 || z.chunk_log2 > 16 || z.row_log2 < 0 || z.row_log2 > 30)
+        return LC_ERR_BAD_STRIDE;
+    if (z.bits > 0 && (z.row_log2 < z.chunk_log2 + z.bits || (1 << z.chunk_log2) < elem_bytes))
+        return LC_ERR_BAD_STRIDE;  // not one-to-one, or an element split across chunks
+    for (const lc_tile_layout *l : {global_layout, shared_layout}) {
+        if (l->rank < 1 || l->rank > LC_MAX_RANK) return LC_ERR_RANK;
+        if (l->offset < 0) return LC_ERR_BAD_STRIDE;
+        for (int k = 0; k < l->rank; ++k)
+            if (l->shape[k] != 1 && l->stride[k] < 0) return LC_ERR_BAD_STRIDE;
+    }
+    lc::ModeList ml;
+    int st = lc::gmem_smem_modes(global_layout, shared_layout, &ml);
+    if (st) return st;
+    int64_t total = 1;
+    for (int i = 0; i < ml.n; ++i)
+        if (!lc::mul_ok_ext(total, ml.m[i].e, &total) || total >= (int64_t(1) << 31)) return LC_ERR_SHAPE;
+    std::memset(out, 0, sizeof(*out));
+    out->n_modes = ml.n;
+    for (int i = 0; i < ml.n; ++i) {
+        out->extent[i] = ml.m[i].e;
+        out->g_stride[i] = ml.m[i].s;
+        out->s_stride[i] = ml.m[i].d;
+        const lc::FastDiv fd = lc::make_fastdiv(static_cast<uint32_t>(ml.m[i].e ? ml.m[i].e : 1));
+        out->div_m[i] = fd.m;
+        out->div_s[i] = fd.s;
+    }
+    out->g_offset = global_layout->offset;
+    out->s_offset = shared_layout->offset;
+    out->elem_bytes = elem_bytes;
+    out->threads = threads;
+    out->total = total;
+    out->swizzle = z;
+    int v = 1;
+    for (int bytes = 16; bytes > elem_bytes; bytes >>= 1) {
+        if (z.bits > 0 && bytes > (1 << z.chunk_log2)) continue;  // one swizzle chunk at most
+        const int c = bytes / elem_bytes;
+        bool ok = ml.n > 0 && ml.m[ml.n - 1].s == 1 && ml.m[ml.n - 1].d == 1 && ml.m[ml.n - 1].e % c == 0 &&
+                  out->g_offset % c == 0 && out->s_offset % c == 0;
+        for (int i = 0; ok && i + 1 < ml.n; ++i) ok = ml.m[i].s % c == 0 && ml.m[i].d % c == 0;
+        if (ok) { v = c; break; }
+    }
+    out->vec = v;
+    const int64_t per_round = int64_t(threads) * v;
+    out->outer = (total + per_round - 1) / per_round;
+    out->guarded = total % per_round != 0;
+    return LC_OK;
+}
+
 extern "C" int lc_gmem_smem_partition(const lc_tile_layout *global_layout,
                                       const lc_tile_layout *shared_layout, int32_t elem_bytes,
                                       int32_t threads, int32_t *vec, int64_t *outer) {
@@ -1057,22 +1155,8 @@ extern "C" int lc_gmem_smem_partition(const lc_tile_layout *global_layout,
         return LC_ERR_ELEM_BYTES;
     if (threads < 1) return LC_ERR_SHAPE;
     lc::ModeList ml;
-    int st = lc::align_shards(global_layout, shared_layout, &ml);
+    int st = lc::gmem_smem_modes(global_layout, shared_layout, &ml);
     if (st) return st;
-    // the global side drives the canonical (stride-descending) order
-    std::stable_sort(ml.m, ml.m + ml.n, [](const lc::Mode &a, const lc::Mode &b) { return a.s > b.s; });
-    // merge neighbours contiguous on both sides
-    int n = 0;
-    for (int i = 0; i < ml.n; ++i) {
-        if (n && ml.m[n - 1].s == ml.m[i].s * ml.m[i].e && ml.m[n - 1].d == ml.m[i].d * ml.m[i].e) {
-            ml.m[n - 1].e *= ml.m[i].e;
-            ml.m[n - 1].s = ml.m[i].s;
-            ml.m[n - 1].d = ml.m[i].d;
-        } else {
-            ml.m[n++] = ml.m[i];
-        }
-    }
-    ml.n = n;
     int64_t total = 1;
     for (int i = 0; i < ml.n; ++i) total *= ml.m[i].e;
     if (total % threads) return LC_ERR_SHAPE;
@@ -1180,4 +1264,34 @@ extern "C" int lc_loop_plan(const lc_tile_layout *src_layout, const lc_tile_layo
     out->vec = lp.vec;
     out->split = lp.split ? 1 : 0;
     return LC_OK;
+}
+
+extern "C" int lc_row_major_strides(int32_t rank, const int64_t *shape, int64_t *stride) {
+    if (!shape || !stride) return LC_ERR_NULL;
+    if (rank < 1 || rank > LC_MAX_RANK) return LC_ERR_RANK;
+    int64_t acc = 1;
+    for (int k = rank - 1; k >= 0; --k) {
+        if (shape[k] < 0) return LC_ERR_SHAPE;
+        stride[k] = acc;
+        if (!lc::mul_ok_ext(acc, shape[k] > 1 ? shape[k] : 1, &acc)) return LC_ERR_OVERFLOW;
+    }
+    return LC_OK;
+}
+
+extern "C" int64_t lc_layout_footprint(const lc_tile_layout *l, int64_t n_tiles) {
+    if (!l || l->rank < 1 || l->rank > LC_MAX_RANK || n_tiles < 0 || l->offset < 0 || l->tile_stride < 0) return -1;
+    bool empty = n_tiles == 0;
+    for (int k = 0; k < l->rank; ++k) {
+        if (l->shape[k] < 0 || l->stride[k] < 0) return -1;
+        empty = empty || l->shape[k] == 0;
+    }
+    if (empty) return l->offset;
+    int64_t cos = 1, t;
+    for (int k = 0; k < l->rank; ++k)
+        if (!lc::mul_ok_ext(l->shape[k] - 1, l->stride[k], &t) || !lc::add_ok_ext(cos, t, &cos)) return -1;
+    const int64_t ts = l->tile_stride ? l->tile_stride : cos;
+    int64_t out;
+    if (!lc::mul_ok_ext(n_tiles - 1, ts, &t) || !lc::add_ok_ext(t, cos, &out) || !lc::add_ok_ext(out, l->offset, &out))
+        return -1;
+    return out;
 }

@@ -250,9 +250,8 @@ def gmem_smem_partition_guarded(shape, g_stride, s_stride, elem_bytes: int,
         is below the thread count some threads get no work and the generated
         code adds a guard);
       * with a swizzled shared layout (``chunk_bytes`` = its swizzle chunk), a
-        vector is at most one chunk ("copy -> gmem_smem", section "How inputs
-        change the algorithm", last paragraph: a swizzled shared layout caps
-        vec to one swizzle chunk).
+        vector spans no more than one chunk ("copy -> gmem_smem", section
+        "How inputs change the algorithm", last paragraph).
     Returns dict(modes, vec, outer, total, guarded).
     """
     if chunk_bytes is not None and chunk_bytes < elem_bytes:

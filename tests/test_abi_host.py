@@ -574,3 +574,63 @@ def test_destination_injectivity_matches_brute_force(M):
             assert e.status == M.STATUS["LC_ERR_NOT_INJECTIVE"], (ext, dst, e.status)
             got = False
         assert got == want, (ext, dst)
+
+
+def test_gmem_smem_plan_matches_the_oracle(M):
+    """lc_gmem_smem_plan (guarded partition, vector capped by the swizzle
+    chunk) against oracle.index_maps.gmem_smem_partition_guarded."""
+    import random
+    from oracle import index_maps
+    rng = random.Random(31)
+    T = M.TileLayout
+    checked = 0
+    for _ in range(2000):
+        rank = rng.randint(1, 4)
+        ext = [rng.choice([1, 2, 3, 4, 8, 16, 5]) for _ in range(rank)]
+        gs, acc = [0] * rank, 1
+        order = list(range(rank))
+        rng.shuffle(order)
+        for i in reversed(order):
+            gs[i] = acc
+            acc *= ext[i] + rng.choice([0, 0, 2])
+        ss, acc = [0] * rank, 1
+        for i in reversed(range(rank)):
+            ss[i] = acc
+            acc *= ext[i]
+        w = rng.choice([1, 2, 4, 8, 16])
+        threads = rng.choice([1, 32, 96, 128, 1024])
+        goff = rng.choice([0, 0, 1, 4, 16])
+        swz = rng.choice([None, (2, 2, 7), (3, 4, 7), (5, 2, 7), (1, 3, 8)])
+        chunk = None if swz is None else 1 << swz[1]
+        try:
+            want = index_maps.gmem_smem_partition_guarded(ext, gs, ss, w, threads, goff, 0, chunk)
+        except index_maps.Decline:
+            with pytest.raises(M.LayoutCopyError) as e:
+                M.gmem_smem_plan(T(ext, gs, goff), T(ext, ss), w, threads, swz)
+            assert e.value.status == M.STATUS["LC_ERR_BAD_STRIDE"]
+            continue
+        got = M.gmem_smem_plan(T(ext, gs, goff), T(ext, ss), w, threads, swz)
+        assert got["modes"] == [tuple(m) for m in want["modes"]], (ext, gs, ss)
+        assert (got["vec"], got["outer"], got["total"], got["guarded"]) == \
+            (want["vec"], want["outer"], want["total"], want["guarded"]), (ext, gs, w, threads, swz)
+        checked += 1
+    assert checked > 1500
+
+
+def test_gmem_smem_plan_refusals(M):
+    T = M.TileLayout
+    S = M.STATUS
+
+    def code(*args, **kw):
+        try:
+            M.gmem_smem_plan(*args, **kw)
+            return 0
+        except M.LayoutCopyError as e:
+            return e.status
+    assert code(T((8,), (1,)), T((8,), (1,)), 4, 0) == S["LC_ERR_SHAPE"]
+    assert code(T((8,), (1,)), T((8,), (1,)), 4, 1025) == S["LC_ERR_SHAPE"]
+    assert code(T((8,), (1,)), T((8,), (1,)), 3, 32) == S["LC_ERR_ELEM_BYTES"]
+    assert code(T((8,), (1,)), T((9,), (1,)), 4, 32) == S["LC_ERR_EXTENT_MISMATCH"]
+    assert code(T((8,), (1,)), T((8,), (1,)), 4, 32, (3, 4, 6)) == S["LC_ERR_BAD_STRIDE"]  # not one-to-one
+    assert code(T((8,), (1,)), T((8,), (1,)), 16, 32, (2, 2, 7)) == S["LC_ERR_BAD_STRIDE"]  # splits an element
+    assert code(T((1 << 16, 1 << 15), (1 << 15, 1)), T((1 << 16, 1 << 15), (1 << 15, 1)), 1, 32) == S["LC_ERR_SHAPE"]

@@ -877,3 +877,96 @@ def test_loop_copy_around_the_split_cut_off(n):
     assert torch.equal(dst_d, src_d)
     del src_d, dst_d
     torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------------------
+# "copy -> gmem_smem" staged through shared memory: the device primitive
+# (lc_device::gmem_smem_copy) driven by the staged-tile kernel, against the
+# oracle's words and the oracle's replay of both partitions (guard included)
+# ---------------------------------------------------------------------------
+
+def _row_major(shape):
+    st, acc = [], 1
+    for e in reversed(shape):
+        st.insert(0, acc)
+        acc *= max(1, e)
+    return tuple(st)
+
+
+def _staged_case(src_l, dst_l, w, n_tiles, threads, swizzle, seed, check_trace=True, src_shift=0):
+    ns = _footprint(src_l, n_tiles) * w + src_shift
+    nd = _footprint(dst_l, n_tiles) * w
+    g = torch.Generator().manual_seed(seed)
+    src_h = torch.randint(0, 256, (max(ns, 1),), generator=g, dtype=torch.uint8)
+    dst_h = torch.full((max(nd, 1),), workloads.SENTINEL, dtype=torch.uint8)
+    want = dst_h.numpy().copy()
+    oracle.copy(src_h.numpy()[src_shift:].copy(), src_l, want, dst_l, w, n_tiles)
+    N = int(np.prod(src_l["shape"]))
+    tin = torch.full((n_tiles * N,), -1, dtype=torch.int64, device="cuda")
+    tout = torch.full((n_tiles * N,), -1, dtype=torch.int64, device="cuda")
+    src_d, dst_d = src_h.cuda(), dst_h.cuda()
+    view = src_d[src_shift:] if src_shift else src_d
+    lc().layout_copy_staged(view, src_l, dst_d, dst_l, n_tiles=n_tiles, elem_bytes=w, threads=threads,
+                            swizzle=swizzle, trace_in=tin, trace_out=tout)
+    st, detail = lc().last_device_error()
+    assert st == 0, "device error word %#x" % detail
+    got = dst_d.cpu().numpy()
+    assert np.array_equal(got, want), (src_l, dst_l, w, n_tiles, threads, swizzle)
+    if not check_trace:
+        return
+    sh = _row_major(src_l["shape"])
+    chunk = None if swizzle is None or swizzle[0] == 0 else 1 << swizzle[1]
+    for tr, lay in ((tin, src_l), (tout, dst_l)):
+        part = oracle.index_maps.gmem_smem_partition_guarded(lay["shape"], lay["stride"], sh, w, threads,
+                                                             lay["offset"], 0, chunk)
+        one = np.full(N, -1, np.int64)
+        for f, tid, _g, _s, elems in oracle.index_maps.gmem_smem_replay(part, threads, lay["offset"], 0):
+            for _gg, s in elems:
+                one[s] = f * threads + tid
+        assert np.array_equal(tr.cpu().numpy(), np.tile(one, n_tiles)), (lay, part["vec"], part["outer"])
+
+
+def test_staged_copy_guarded_partitions():
+    # the guard: 64 words, 128 threads -> 16 (4-byte) or 32 (8-byte) busy threads
+    _staged_case(L((64,), (1,)), L((64,), (1,)), 4, 3, 128, None, 1)
+    _staged_case(L((64,), (1,)), L((64,), (1,)), 8, 3, 128, None, 2)
+    _staged_case(L((100,), (1,)), L((100,), (1,)), 4, 2, 32, None, 3)
+    # a transposed copy with a thread count that divides nothing
+    sh = (4, 8, 16)
+    _staged_case(L(sh, _row_major(sh)), L(sh, permuted(sh, (0, 2, 1))), 2, 5, 96, (3, 4, 7), 4)
+
+
+def test_staged_copy_page_tile_and_swizzles():
+    # the page's 32 x 32 fp32 tile, transposed: a 4-byte-chunk swizzle makes the
+    # column reads of copy 2 conflict-free and caps copy 1 at one word per access
+    src_l, dst_l = L((32, 32), (32, 1)), L((32, 32), (1, 32))
+    for swz in [(0, 0, 0), (5, 2, 7), (3, 4, 7)]:
+        _staged_case(src_l, dst_l, 4, 1, 256, swz, 5)
+    _staged_case(src_l, dst_l, 4, 3, 1024, (5, 2, 7), 6)
+    sf = (2, 1, 4, 32)
+    _staged_case(L(sf, (128, 128, 32, 1)), L(sf, (128, 128, 1, 4)), 4, 7, 64, (2, 4, 6), 7)
+
+
+@pytest.mark.parametrize("w", [1, 2, 4, 8, 16])
+def test_staged_copy_widths_and_library_swizzle(w):
+    for i, (shape, perm) in enumerate([((16, 24), (1, 0)), ((3, 5, 33), (2, 0, 1)), ((8, 4, 2, 16), (0, 2, 1, 3))]):
+        src_l = L(shape, _row_major(shape))
+        dst_l = L(shape, permuted(shape, perm))
+        _staged_case(src_l, dst_l, w, 4, 128, None, 10 * w + i, check_trace=False)
+        run_case(src_l, dst_l, w, 4, kernel="smem_staged", seed=20 * w + i)
+    # a source base off the vector grid: the copy narrows to single words
+    _staged_case(L((16, 24), (24, 1)), L((16, 24), (1, 16)), w, 2, 64, None, 99, check_trace=False, src_shift=w)
+
+
+def test_staged_copy_refusals():
+    src = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    dst = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    with pytest.raises(lc().LayoutCopyError) as e:
+        lc().layout_copy_staged(src, L((64,), (1,)), dst, L((64,), (1,)), elem_bytes=4, threads=48)
+    assert e.value.status == lc().STATUS["LC_ERR_SHAPE"]
+    with pytest.raises(lc().LayoutCopyError) as e:  # a tile over LC_STAGED_MAX_BYTES
+        lc().layout_copy_staged(src, L((256, 128), (128, 1)), dst, L((256, 128), (1, 256)), elem_bytes=4)
+    assert e.value.status == lc().STATUS["LC_ERR_SHAPE"]
+    with pytest.raises(lc().LayoutCopyError) as e:  # source and destination overlap
+        lc().layout_copy_staged(src, L((64,), (1,)), src[64:], L((64,), (1,)), elem_bytes=4)
+    assert e.value.status == lc().STATUS["LC_ERR_OVERLAP"]
