@@ -73,7 +73,7 @@ def test_plan_scale_factor_transpose(M):
 
 def test_plan_workloads(M):
     import workloads
-    expect = {1: "warp_permute", 3: "tile_transpose", 5: "tma_copy"}
+    expect = {1: "smem_staged", 3: "tile_transpose", 5: "tma_copy"}
     for cfg, kname in expect.items():
         c = workloads.config(cfg)
         assert M.plan(c["src"], c["dst"], c["elem_bytes"], c["n_tiles"])["kernel_name"] == kname
@@ -344,7 +344,9 @@ def test_layout_conversion_cache(M):
     for i in range(M._LAYOUT_CACHE_MAX + 10):  # overflow clears the cache
         assert M._c_layout({"shape": (i + 1,), "stride": (1,)}).shape[0] == i + 1
     assert M._c_layout(d).offset == 5
-    assert M.plan(M.TileLayout((32, 32)), M.TileLayout((32, 32), (1, 32)), 4)["kernel_name"] == "warp_permute"
+    assert M.plan(M.TileLayout((32, 32)), M.TileLayout((32, 32), (1, 32)), 4)["kernel_name"] == "smem_staged"
+    # one tile past the staged copy's automatic size takes a warp or tile class
+    assert M.plan(M.TileLayout((96, 96)), M.TileLayout((96, 96), (1, 96)), 4)["kernel_name"] != "smem_staged"
 
 
 def test_fastdiv_host_mirror():
@@ -458,11 +460,13 @@ def test_tma_copy_plans(M):
 
 def test_unaligned_transposes_plan_the_smem_transpose(M):
     T = M.TileLayout
-    for w in (1, 2, 4, 8):
-        p = M.plan(T((37, 555), (555, 1)), T((37, 555), (1, 37)), w, 1)
+    for w in (1, 2, 4, 8):  # single tiles past the staged copy's automatic size
+        p = M.plan(T((137, 555), (555, 1)), T((137, 555), (1, 137)), w, 1)
         assert p["kernel_name"] == "smem_transpose", w
-    # aligned ones keep the TMA path
-    assert M.plan(T((64, 64), (64, 1)), T((64, 64), (1, 64)), 4, 1)["kernel_name"] == "tile_transpose"
+    # aligned ones keep the TMA path; small single tiles take the staged copy
+    assert M.plan(T((128, 128), (128, 1)), T((128, 128), (1, 128)), 4, 1)["kernel_name"] == "tile_transpose"
+    assert M.plan(T((64, 64), (64, 1)), T((64, 64), (1, 64)), 4, 1)["kernel_name"] == "smem_staged"
+    assert M.plan(T((37, 55), (55, 1)), T((37, 55), (1, 37)), 2, 1)["kernel_name"] == "smem_staged"
 
 
 def test_warp_unit_plan_matches_the_page_and_the_oracle(M):

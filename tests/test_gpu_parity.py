@@ -97,7 +97,7 @@ SMALL = [(1, None), (2, None), (3, None), (4, 1), (4, 2), (4, 4), (4, 8), (4, 16
 def test_workload_small_auto(cfg, w):
     c = workloads.config(cfg, w, scale="small")
     name = run_case(c["src"], c["dst"], c["elem_bytes"], c["n_tiles"], seed=cfg)
-    expect = {1: "warp_permute", 2: "warp_shuffle", 3: "tile_transpose", 4: "tile_transpose",
+    expect = {1: "smem_staged", 2: "warp_shuffle", 3: "tile_transpose", 4: "tile_transpose",
               5: "tma_copy", 6: "smem_transpose"}[cfg]
     assert name == expect
 
@@ -147,7 +147,9 @@ def _shuffle_cases(w):
 @pytest.mark.parametrize("w", [1, 2, 4, 8])
 def test_warp_shuffle_shapes(w):
     for i, (src_l, dst_l, nt) in enumerate(_shuffle_cases(w)):
-        assert lc().plan(src_l, dst_l, w, nt)["kernel_name"] == "warp_shuffle", (src_l, dst_l)
+        assert lc().plan(src_l, dst_l, w, nt, "warp_shuffle")["kernel_name"] == "warp_shuffle", (src_l, dst_l)
+        if nt > 1:  # (single small tiles plan the staged copy)
+            assert lc().plan(src_l, dst_l, w, nt)["kernel_name"] == "warp_shuffle", (src_l, dst_l)
         run_case(src_l, dst_l, w, nt, kernel="warp_shuffle", seed=100 * w + i)
         run_case(src_l, dst_l, w, nt, seed=200 * w + i)  # the automatic choice
     # a source base off the 16-byte grid: the planner takes another class,
@@ -185,9 +187,10 @@ def test_smem_transpose_any_alignment(w):
              kernel="smem_transpose", seed=w)
     sh = (3, 5, 33, 31)
     run_case(L(sh, row_major(sh)), L(sh, permuted(sh, (1, 0, 3, 2))), w, kernel="smem_transpose", seed=9)
-    # misaligned base pointers: the automatic choice takes this path
+    # misaligned base pointers: the automatic choice takes one of the
+    # transpose classes (the staged copy while the single tile is small)
     assert run_case(L((64, 96), (96, 1)), L((64, 96), (1, 64)), w, src_shift=w if w < 16 else 0,
-                    dst_shift=0) in ("smem_transpose", "tile_transpose")
+                    dst_shift=0) in ("smem_transpose", "tile_transpose", "smem_staged")
 
 
 @pytest.mark.parametrize("w", [1, 2, 4, 8, 16])
