@@ -153,9 +153,10 @@ def kernel_sources_sha(kernel_name: str) -> str:
     files = {"warp_permute": warp, "warp_unit_shared": warp, "tile_transpose": ["k_tile.cu"],
              "vec_copy": ["k_vec.cu"], "smem_transpose": ["k_smem.cu"],
              "tma_copy": ["k_tma_copy.cu"], "window_sum": ["k_stencil.cu"],
-             "loop_copy": ["k_loop.cu"], "warp_shuffle": ["k_shuffle.cu"]}.get(kernel_name, [])
+             "loop_copy": ["k_loop.cu"], "warp_shuffle": ["k_shuffle.cu"],
+             "smem_staged": ["k_staged.cu"]}.get(kernel_name, [])
     paths = [os.path.join(ROOT, "movement_primitives_gb300", "csrc", f) for f in files + ["ptx.cuh", "device_common.cuh"]]
-    if kernel_name in ("warp_permute", "warp_unit_shared"):  # device functions in the public device header
+    if kernel_name in ("warp_permute", "warp_unit_shared", "smem_staged"):  # device functions in the public header
         paths.append(os.path.join(ROOT, "include", "layout_copy_device.cuh"))
     h = hashlib.sha256()
     for path in paths:

@@ -308,6 +308,25 @@ def test_edge_cases():
             run_case(L((n,), (1,)), L((n,), (1,)), w, seed=n)
 
 
+@pytest.mark.parametrize("w,rows,cols", [(1, 16384, 16640), (2, 8192, 16640), (4, 8192, 8320)])
+def test_tile_transpose_tall_boxes(w, rows, cols):
+    """Transposes just past 256 MiB a side take the 256-row boxes (and, for
+    1-, 2- and 4-byte words, the 64-bit index path): whole buffer against
+    the oracle."""
+    src_l, dst_l = L((rows, cols), (cols, 1)), L((rows, cols), (1, rows))
+    assert rows * cols * w > 256 << 20
+    p = lc().plan(src_l, dst_l, w, 1)
+    assert p["kernel_name"] == "tile_transpose" and p["tile_rows"] == (256 if w < 8 else 128)
+    c = dict(src=src_l, dst=dst_l, elem_bytes=w, n_tiles=1, kind="bytes", seed=700 + w, cfg=4, name="tall")
+    src_h = workloads.make_src(c)
+    src_d = src_h.cuda()
+    dst_d = workloads.make_dst(c, device="cuda")
+    lc().layout_copy(src_d, src_l, dst_d, dst_l, elem_bytes=w)
+    st, detail = lc().last_device_error()
+    assert st == 0, "device error word %#x" % detail
+    _assert_same_bytes(dst_d.cpu().numpy(), _oracle_full(c, src_h.numpy()), "tall w=%d" % w)
+
+
 def test_injective_destination_beyond_enumeration():
     # 2^25 + 2^24 one-byte words whose destination strides do not nest:
     # offsets k + 2^23 (2i + 3j), one-to-one by the stride split (the planner
