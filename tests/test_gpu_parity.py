@@ -869,6 +869,26 @@ def test_vector_copy_past_32_bit_indices():
     torch.cuda.empty_cache()
 
 
+def test_warp_shuffle_offsets_past_32_bits():
+    # (4, 32) fp32 blocks of tiles spaced 1 GiB apart on the source: the
+    # source span passes 4 GiB, so the kernel forms 64-bit offsets; the
+    # compact destination is checked whole, point by point
+    n_tiles = 5
+    src_l = L((4, 32), (32, 1), 0, 1 << 28)
+    dst_l = L((4, 32), (1, 4))
+    assert lc().plan(src_l, dst_l, 4, n_tiles, "warp_shuffle")["kernel_name"] == "warp_shuffle"
+    src_d = _device_bytes(_footprint(src_l, n_tiles) * 4, 911)
+    dst_d = torch.full((_footprint(dst_l, n_tiles) * 4,), workloads.SENTINEL, dtype=torch.uint8, device="cuda")
+    lc().layout_copy(src_d, src_l, dst_d, dst_l, n_tiles=n_tiles, elem_bytes=4, kernel="warp_shuffle")
+    st, detail = lc().last_device_error()
+    assert st == 0, "device error word %#x" % detail
+    n = n_tiles * 128
+    so, do = oracle.offsets_of(src_l, dst_l, n_tiles, np.arange(n, dtype=np.int64))
+    sv, dv = src_d.view(-1, 4), dst_d.view(-1, 4)
+    assert torch.equal(sv[torch.from_numpy(so).cuda()], dv[torch.from_numpy(do).cuda()])
+    assert sorted(do.tolist()) == list(range(dst_d.numel() // 4))  # every destination word written
+
+
 def test_loop_copy_past_32_bit_indices():
     m = (1 << 31) + (1 << 13)  # two rows of m one-byte words: 2^32 + 2^14 points in one tile
     n = 2 * m
