@@ -84,9 +84,12 @@ std::map<std::string, lc_smem_swizzle> g_swz;  // layouts, width, threads -> cho
 
 }  // namespace
 
-// Swizzle for a staged tile: the candidate whose worse copy has the lowest
-// bank degree, ties broken by the larger sum of the two vectors (fewer
-// rounds), then by the simpler swizzle.
+// Swizzle for a staged tile: among the candidates with the widest vectors
+// (the sum of the two copies' vector widths: global access width decides
+// more than shared bank degree -- on 65536 32 x 32 fp32 transposes a swizzle
+// of 4-byte chunks took the shared load wavefronts from 68.9 M to 2.2 M but
+// capped copy 1 at one word per access and ran at 543 against 362 us), the
+// one whose worse copy has the lowest bank degree, then the simplest.
 int choose_staged_swizzle(const lc_tile_layout &s, const lc_tile_layout &d, const lc_tile_layout &sh, int w,
                           int threads, lc_smem_swizzle *out) {
     std::string key;
@@ -117,7 +120,7 @@ int choose_staged_swizzle(const lc_tile_layout &s, const lc_tile_layout &d, cons
                 if (lc_gmem_smem_plan(&d, &sh, w, threads, &z, &po) != LC_OK) continue;
                 const int deg = std::max(copy_degree(pi), copy_degree(po));
                 const int vec = pi.vec + po.vec;
-                if (deg < best_deg || (deg == best_deg && vec > best_vec)) {
+                if (vec > best_vec || (vec == best_vec && deg < best_deg)) {
                     best_deg = deg;
                     best_vec = vec;
                     best = z;
@@ -159,8 +162,13 @@ int launch_staged_layouts(const void *src, const lc_tile_layout *src_layout, voi
         acc *= std::max<int64_t>(1, src_layout->shape[k]);
     }
     lc_smem_swizzle z{0, 0, 0};
+#ifndef LC_STAGED_SWIZZLE
+#define LC_STAGED_SWIZZLE 1  // 0: the library's choice is no swizzle (for measuring what it buys)
+#endif
     if (swizzle) z = *swizzle;
-    else if ((st = choose_staged_swizzle(*src_layout, *dst_layout, sh, elem_bytes, threads, &z))) return st;
+    else if (LC_STAGED_SWIZZLE &&
+             (st = choose_staged_swizzle(*src_layout, *dst_layout, sh, elem_bytes, threads, &z)))
+        return st;
     StagedArgs a{};
     if ((st = lc_gmem_smem_plan(src_layout, &sh, elem_bytes, threads, &z, &a.in))) return st;
     if ((st = lc_gmem_smem_plan(dst_layout, &sh, elem_bytes, threads, &z, &a.out))) return st;
