@@ -88,9 +88,18 @@ namespace lc {
 #define LC_TILE_BOXB_W1 LC_TILE_BOXB_OTHER
 #endif
 
+// Box rows for 4-byte words on the short boxes: 256 bytes measured 90.5 %
+// against 86.1 % with 128 (8192^2, 128-row boxes, 4 stages).
+#ifndef LC_TILE_BOXB_W4_SHORT
+#define LC_TILE_BOXB_W4_SHORT 256
+#endif
+
 template <int W, bool SHORT = false> struct TileCfg {
-    static constexpr int BOXB = W == 1 ? LC_TILE_BOXB_W1 : W == 2 ? LC_TILE_BOXB_W2 : W == 8 ? LC_TILE_BOXB_W8
-                              : LC_TILE_BOXB_OTHER;  // bytes per box row
+    static constexpr int BOXB = W == 1   ? LC_TILE_BOXB_W1
+                              : W == 2   ? LC_TILE_BOXB_W2
+                              : W == 4   ? (SHORT ? LC_TILE_BOXB_W4_SHORT : LC_TILE_BOXB_OTHER)
+                              : W == 8   ? LC_TILE_BOXB_W8
+                                         : LC_TILE_BOXB_OTHER;  // bytes per box row
     static constexpr int CPR = BOXB / 16;      // 16-byte chunks per box row
     static constexpr int V = 16 / W;           // words per 16-byte chunk
     static constexpr int TY = BOXB / W;        // words per box row
