@@ -472,8 +472,9 @@ int lc_gmem_smem_plan(const lc_tile_layout *global_layout, const lc_tile_layout 
  *          round and thread that moved it in copy 1 / copy 2.
  * Results equal lc_layout_copy's.  Asynchronous on `stream`.  Errors: as
  * lc_layout_copy (source and destination may not overlap), plus
- * LC_ERR_SHAPE when a tile's box exceeds LC_STAGED_MAX_BYTES or `threads` is
- * invalid, and lc_gmem_smem_plan's errors for the swizzle. */
+ * LC_ERR_SHAPE when a tile's box exceeds LC_STAGED_MAX_BYTES (after
+ * rounding up to the swizzle's span, 2^(chunk_log2 + bits) bytes) or
+ * `threads` is invalid, and lc_gmem_smem_plan's errors for the swizzle. */
 int lc_layout_copy_staged(const void *src, const lc_tile_layout *src_layout, void *dst,
                           const lc_tile_layout *dst_layout, int32_t elem_bytes, int64_t n_tiles,
                           int32_t threads, const lc_smem_swizzle *swizzle, int64_t *trace_in,

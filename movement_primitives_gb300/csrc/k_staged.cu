@@ -20,6 +20,12 @@
 #include "launch.h"
 #include "layout_copy_device.cuh"
 
+// 0: the library's choice of shared swizzle is none (a variant for measuring
+// what the swizzle buys).
+#ifndef LC_STAGED_SWIZZLE
+#define LC_STAGED_SWIZZLE 1
+#endif
+
 namespace lc {
 namespace {
 
@@ -162,9 +168,6 @@ int launch_staged_layouts(const void *src, const lc_tile_layout *src_layout, voi
         acc *= std::max<int64_t>(1, src_layout->shape[k]);
     }
     lc_smem_swizzle z{0, 0, 0};
-#ifndef LC_STAGED_SWIZZLE
-#define LC_STAGED_SWIZZLE 1  // 0: the library's choice is no swizzle (for measuring what it buys)
-#endif
     if (swizzle) z = *swizzle;
     else if (LC_STAGED_SWIZZLE &&
              (st = choose_staged_swizzle(*src_layout, *dst_layout, sh, elem_bytes, threads, &z)))
@@ -199,9 +202,10 @@ int launch_staged_layouts(const void *src, const lc_tile_layout *src_layout, voi
     a.trace_out = trace_out;
     // the swizzle only rewrites bits below chunk_log2 + bits: round the buffer
     // up to that span so that every stored offset stays inside it
-    const int64_t span = z.bits ? (int64_t(1) << (z.chunk_log2 + z.bits)) : 16;
-    const int smem = static_cast<int>((N * w + std::max<int64_t>(span, 128) - 1) / std::max<int64_t>(span, 128) *
-                                      std::max<int64_t>(span, 128));
+    const int64_t span = std::max<int64_t>(z.bits ? (int64_t(1) << (z.chunk_log2 + z.bits)) : 16, 128);
+    const int64_t smem_bytes = (N * w + span - 1) / span * span;
+    if (smem_bytes > LC_STAGED_MAX_BYTES + 4096) return LC_ERR_SHAPE;  // a swizzle spanning past the tile budget
+    const int smem = static_cast<int>(smem_bytes);
     const void *fn = nullptr;
     switch (elem_bytes) {
         case 1: fn = reinterpret_cast<const void *>(&k_staged<1>); break;

@@ -1012,3 +1012,6 @@ def test_staged_copy_refusals():
     with pytest.raises(lc().LayoutCopyError) as e:  # source and destination overlap
         lc().layout_copy_staged(src, L((64,), (1,)), src[64:], L((64,), (1,)), elem_bytes=4)
     assert e.value.status == lc().STATUS["LC_ERR_OVERLAP"]
+    with pytest.raises(lc().LayoutCopyError) as e:  # a swizzle whose span is past the tile budget
+        lc().layout_copy_staged(src, L((64,), (1,)), dst, L((64,), (1,)), elem_bytes=4, swizzle=(8, 10, 18))
+    assert e.value.status == lc().STATUS["LC_ERR_SHAPE"]
