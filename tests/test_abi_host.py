@@ -80,8 +80,9 @@ def test_plan_workloads(M):
     for w in (1, 2, 4, 8, 16):
         c = workloads.config(4, w)
         p = M.plan(c["src"], c["dst"], w, 1)
-        # box rows of 256 bytes for 2- and 8-byte words, 128 otherwise
-        assert p["kernel_name"] == "tile_transpose" and p["tile_cols"] * w == (256 if w in (2, 8) else 128)
+        # box rows of 256 bytes for 2- and 8-byte words and for 4-byte words on
+        # the short boxes (workload 4 is 256 MiB a side), 128 otherwise
+        assert p["kernel_name"] == "tile_transpose" and p["tile_cols"] * w == (256 if w in (2, 4, 8) else 128)
     p = M.plan(workloads.config(5)["src"], workloads.config(5)["dst"], 2)
     assert (p["vec"], p["run"]) == (8, 128)  # the vector fallback: 16-byte vectors over 256-byte runs
     # TMA boxes: the 128-word run, its 32 rows, 2 of the next mode (16 KiB)
