@@ -104,10 +104,13 @@ typedef enum {
      * ("permute_layout", section "Algorithm"), and the slot leaves with
      * 16-byte stores.  Small transposed units. */
     LC_KERNEL_WARP_PERMUTE = 2,
-    /* Tile transpose: TMA tensor loads of 128-byte x R-row tiles into a
-     * shared-memory ring (mbarrier pipelined), 16-byte shared reads, an
-     * in-register transpose of the sub-16-byte elements, 16-byte coalesced
-     * global stores.  Large 2-D transposes with batch modes. */
+    /* Tile transpose: TMA tensor loads of 128- or 256-byte x R-row tiles
+     * into a shared-memory ring (mbarrier pipelined), 16-byte shared reads,
+     * an in-register transpose of the sub-16-byte elements, 16-byte
+     * coalesced global stores.  Large 2-D transposes with batch modes.  Its
+     * direct form (1- and 2-byte words, both extents whole 16-byte blocks,
+     * at most 256 MiB a side) loads each block's rows with 16-byte global
+     * loads straight into registers instead: no TMA and no shared memory. */
     LC_KERNEL_TILE_TRANSPOSE = 3,
     /* Shared-memory transpose for any alignment: tiles of 64 source rows
      * (32 for 16-byte words), each row staged as aligned chunks (4 bytes for
@@ -165,10 +168,13 @@ typedef struct {
     int32_t k, shift, mask;    /* XOR swizzle (mask = 2^k - 1) */
     int32_t conflicts_read, conflicts_write;
     int64_t units_per_chunk;
-    /* tile transpose */
-    int32_t tile_rows;         /* R: source rows per tile */
-    int32_t tile_cols;         /* words per 128-byte tile row */
-    int32_t stages;
+    /* tile transpose (also the shared-memory transpose's tile and the TMA
+     * tensor copy's box) */
+    int32_t tile_rows;         /* R: source rows per tile (per warp tile in the direct form) */
+    int32_t tile_cols;         /* words per tile row */
+    int32_t stages;            /* TMA ring stages; 0: the tile transpose's direct form
+                                  (1- and 2-byte words in whole 16-byte blocks, loaded
+                                  straight into registers: no TMA, no shared memory) */
     /* launch */
     int32_t grid, block, smem_bytes;
 } lc_plan_info;

@@ -130,6 +130,23 @@ struct TileArgs {
     uint64_t timeout_ns;
 };
 
+// One-byte words, word t of the 16 input rows -> output rows 4t .. 4t + 3:
+// 4 x 4 byte blocks, rows 4p .. 4p + 3 giving word p of each output row.
+__device__ __forceinline__ void transpose_bytes_word(const uint32_t (&in)[16][4], int t, uint32_t (&o0)[4],
+                                                     uint32_t (&o1)[4], uint32_t (&o2)[4], uint32_t (&o3)[4]) {
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const uint32_t A = in[4 * p][t], B = in[4 * p + 1][t];
+        const uint32_t C = in[4 * p + 2][t], D = in[4 * p + 3][t];
+        const uint32_t ab_lo = __byte_perm(A, B, 0x5140), ab_hi = __byte_perm(A, B, 0x7362);
+        const uint32_t cd_lo = __byte_perm(C, D, 0x5140), cd_hi = __byte_perm(C, D, 0x7362);
+        o0[p] = __byte_perm(ab_lo, cd_lo, 0x5410);
+        o1[p] = __byte_perm(ab_lo, cd_lo, 0x7632);
+        o2[p] = __byte_perm(ab_hi, cd_hi, 0x5410);
+        o3[p] = __byte_perm(ab_hi, cd_hi, 0x7632);
+    }
+}
+
 // V rows of one 16-byte column chunk -> V destination chunks: out[q] holds
 // word q of every input row (a V x V transpose of W-byte words in registers;
 // the 2-byte and 1-byte cases use byte permutes).
@@ -153,20 +170,8 @@ __device__ __forceinline__ void transpose_chunk(const uint32_t (&in)[16 / W][4],
             for (int p = 0; p < 4; ++p)
                 out[q][p] = __byte_perm(in[2 * p][q >> 1], in[2 * p + 1][q >> 1], (q & 1) ? 0x7632 : 0x5410);
     } else {
-        // 4 x 4 byte blocks: rows 4p..4p+3, word t -> outputs 4t..4t+3, word p
 #pragma unroll
-        for (int t = 0; t < 4; ++t)
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                const uint32_t A = in[4 * p][t], B = in[4 * p + 1][t];
-                const uint32_t C = in[4 * p + 2][t], D = in[4 * p + 3][t];
-                const uint32_t ab_lo = __byte_perm(A, B, 0x5140), ab_hi = __byte_perm(A, B, 0x7362);
-                const uint32_t cd_lo = __byte_perm(C, D, 0x5140), cd_hi = __byte_perm(C, D, 0x7362);
-                out[4 * t + 0][p] = __byte_perm(ab_lo, cd_lo, 0x5410);
-                out[4 * t + 1][p] = __byte_perm(ab_lo, cd_lo, 0x7632);
-                out[4 * t + 2][p] = __byte_perm(ab_hi, cd_hi, 0x5410);
-                out[4 * t + 3][p] = __byte_perm(ab_hi, cd_hi, 0x7632);
-            }
+        for (int t = 0; t < 4; ++t) transpose_bytes_word(in, t, out[4 * t], out[4 * t + 1], out[4 * t + 2], out[4 * t + 3]);
     }
 }
 
@@ -187,7 +192,8 @@ __device__ __forceinline__ void store_partial(uint8_t *p, const uint32_t (&v)[4]
 }
 
 // Tile index -> (tx, ty, flat batch index).
-__device__ __forceinline__ void tile_coords(const TileArgs &a, int64_t t, int64_t &tx, int64_t &ty, int64_t &b) {
+template <typename A>
+__device__ __forceinline__ void tile_coords(const A &a, int64_t t, int64_t &tx, int64_t &ty, int64_t &b) {
     if (a.narrow) {
         const uint32_t t32 = static_cast<uint32_t>(t);
 #if LC_TILE_Y_FASTEST
@@ -343,6 +349,156 @@ __global__ void __launch_bounds__(TileCfg<W, SHORT>::NT)
     }
 }
 
+// ---- Direct tile transpose (no TMA, no shared memory) --------------------
+//
+// A warp takes a tile of RB row blocks x CL chunks: lane (rb, c) loads the V
+// source rows of its block, 16 bytes each at chunk c, straight from global
+// memory, transposes the V x V block in registers (transpose_chunk) and
+// stores its V destination chunks.  One load instruction of the warp reads
+// RB segments of CL * 16 contiguous bytes (one per source row), one store
+// writes CL destination rows, RB * 16 bytes each.  Taken only when both
+// extents are whole blocks (multiples of V), so that every block is either
+// in the tensor or out of it.
+// Word widths (bit w) that take the direct kernel, on copies of at most
+// LC_TILE_SHORT_MAX_BYTES a side.  Measured on GB300 (8192^2 transposes, L2
+// flushed by a read between launches): 1-byte words 93.6-95.1 % of the copy
+// peak against 74.7-76.2 % through TMA, 2-byte words 93.1-93.5 % against
+// 87.9-88.2 %; 4- and 8-byte words lose (86.6-87.9 % against 90.8-90.9 %,
+// 83.9-87.8 against 93.5 %), and so does the 16384^2 2-byte transpose (512
+// MiB a side: 75.5-76.0 % against 91.2-91.3 %).
+#ifndef LC_TILE_DIRECT_MASK
+#define LC_TILE_DIRECT_MASK 0x6
+#endif
+// Threads per CTA: 256 for 1-byte words (83.8 % with 512), 512 for 2-byte
+// words (91.1-91.6 % with 256).
+#ifndef LC_DIRECT_THREADS_W1
+#define LC_DIRECT_THREADS_W1 256
+#endif
+#ifndef LC_DIRECT_THREADS_W2
+#define LC_DIRECT_THREADS_W2 512
+#endif
+#ifndef LC_DIRECT_THREADS_WIDE
+#define LC_DIRECT_THREADS_WIDE 256
+#endif
+// 16-byte chunks per source row segment: 8 (128-byte loads, 64-byte store
+// segments), 4 (64-byte loads, 128-byte stores) or 2.  With 8, the 8192^2
+// 1-byte transpose ran at 64.6-73.3 %, the 2-byte one at 83.2-83.6 %; with
+// 2, at 87.1-87.5 % and 77.8 %.
+#ifndef LC_DIRECT_CL
+#define LC_DIRECT_CL 4
+#endif
+#ifndef LC_DIRECT_CL_W1
+#define LC_DIRECT_CL_W1 LC_DIRECT_CL
+#endif
+#ifndef LC_DIRECT_CL_W2
+#define LC_DIRECT_CL_W2 LC_DIRECT_CL
+#endif
+#ifndef LC_DIRECT_CL_W4
+#define LC_DIRECT_CL_W4 LC_DIRECT_CL
+#endif
+#ifndef LC_DIRECT_CL_W8
+#define LC_DIRECT_CL_W8 LC_DIRECT_CL
+#endif
+
+template <int W> struct DirectCfg {
+    static constexpr int V = 16 / W;
+    static constexpr int CL = W == 1 ? LC_DIRECT_CL_W1 : W == 2 ? LC_DIRECT_CL_W2 : W == 4 ? LC_DIRECT_CL_W4
+                                                                                        : LC_DIRECT_CL_W8;
+    static constexpr int RB = 32 / CL;
+    static constexpr int ROWS = RB * V;  // source rows (X) per warp tile
+    static constexpr int COLS = CL * V;  // words (Y) per warp tile
+    static constexpr int NT = W == 1 ? LC_DIRECT_THREADS_W1 : W == 2 ? LC_DIRECT_THREADS_W2 : LC_DIRECT_THREADS_WIDE;
+    static constexpr int MINB = NT >= 512 ? 1 : 512 / NT;  // at most 128 registers a thread
+    static_assert(CL == 2 || CL == 4 || CL == 8, "lanes split as 32 / CL row blocks x CL chunks");
+};
+// Warp tiles per round, all loads issued first (2: 76-77 % and 87.6 % for
+// the 8192^2 1- and 2-byte transposes).
+#ifndef LC_DIRECT_U
+#define LC_DIRECT_U 1
+#endif
+
+struct DirectArgs {
+    const uint8_t *src;  // address of source word offset 0
+    uint8_t *dst;        // address of destination word offset 0
+    int64_t eX, eY;      // words; both multiples of V
+    int64_t sX, dY;      // bytes: source stride of X, destination stride of Y
+    int32_t nb;          // batch modes (<= 3), outermost first
+    int64_t be[3], bs[3], bd[3];  // extents; source and destination strides (bytes)
+    int64_t tiles_x, tiles_y, n_tiles;  // warp tiles, fewer than 2^32 (copies of at most 256 MiB)
+    int32_t narrow;      // always 1: tile and batch indices split by 32-bit invariant divisors
+    FastDiv ftx, fty, fbe[3];
+};
+
+__device__ __forceinline__ uint4 direct_load(const uint8_t *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+template <int W>
+__global__ void __launch_bounds__(DirectCfg<W>::NT, DirectCfg<W>::MINB)
+    k_tile_direct(const __grid_constant__ DirectArgs a) {
+    using C = DirectCfg<W>;
+    constexpr int V = C::V, CL = C::CL, RB = C::RB, U = LC_DIRECT_U;
+    const int lane = threadIdx.x & 31, c = lane % CL, rb = lane / CL;
+    const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
+    int64_t t = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    for (; t < a.n_tiles; t += U * warps) {
+        uint32_t in[U][V][4];
+        uint8_t *dp[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            dp[u] = nullptr;
+            const int64_t tu = t + u * warps;
+            if (tu >= a.n_tiles) continue;
+            int64_t tx, ty, b;
+            tile_coords(a, tu, tx, ty, b);
+            const int64_t x0 = tx * (RB * V) + rb * V, y0 = ty * (CL * V) + c * V;
+            if (x0 >= a.eX || y0 >= a.eY) continue;  // a block past the tensor
+            const uint8_t *sp = a.src + x0 * a.sX + y0 * W;
+            uint8_t *d = a.dst + y0 * a.dY + x0 * W;
+            uint32_t q = static_cast<uint32_t>(b);
+            for (int k = a.nb - 1; k > 0; --k) {
+                const uint32_t n = fast_div(q, a.fbe[k]);
+                const int64_t bk = q - n * a.fbe[k].d;
+                sp += bk * a.bs[k];
+                d += bk * a.bd[k];
+                q = n;
+            }
+            if (a.nb > 0) { sp += int64_t(q) * a.bs[0]; d += int64_t(q) * a.bd[0]; }  // below its extent
+            dp[u] = d;
+#pragma unroll
+            for (int r = 0; r < V; ++r) {
+                const uint4 v = direct_load(sp + r * a.sX);
+                in[u][r][0] = v.x; in[u][r][1] = v.y; in[u][r][2] = v.z; in[u][r][3] = v.w;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (!dp[u]) continue;
+            if constexpr (W == 1) {
+                // four output rows at a time, so that each input word dies as it is used
+#pragma unroll
+                for (int tw = 0; tw < 4; ++tw) {
+                    uint32_t o[4][4];
+                    transpose_bytes_word(in[u], tw, o[0], o[1], o[2], o[3]);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        store_out<uint4>(dp[u] + (4 * tw + k) * a.dY, make_uint4(o[k][0], o[k][1], o[k][2], o[k][3]));
+                }
+            } else {
+                uint32_t out[V][4];
+                transpose_chunk<W>(in[u], out);
+#pragma unroll
+                for (int q = 0; q < V; ++q)
+                    store_out<uint4>(dp[u] + q * a.dY, make_uint4(out[q][0], out[q][1], out[q][2], out[q][3]));
+            }
+        }
+    }
+}
+
 // Whether a copy of `bytes` a side with w-byte words takes the short boxes.
 static bool tile_short(int w, int64_t bytes) { return w <= 4 && bytes <= LC_TILE_SHORT_MAX_BYTES; }
 
@@ -353,6 +509,25 @@ static void geometry_of(int *rows, int *cols, int *stages, int *threads) {
     *cols = C::TY;
     *stages = C::S;
     *threads = C::NT;
+}
+
+template <int W>
+static void direct_geometry_of(int *rows, int *cols, int *threads) {
+    *rows = DirectCfg<W>::ROWS;
+    *cols = DirectCfg<W>::COLS;
+    *threads = DirectCfg<W>::NT;
+}
+
+bool tile_direct_geometry(int w, int64_t bytes, int64_t eX, int64_t eY, int *rows, int *cols, int *threads) {
+    if (w > 8 || !((LC_TILE_DIRECT_MASK >> w) & 1) || bytes > LC_TILE_SHORT_MAX_BYTES) return false;
+    if (eX % (16 / w) || eY % (16 / w)) return false;
+    switch (w) {
+        case 1: direct_geometry_of<1>(rows, cols, threads); break;
+        case 2: direct_geometry_of<2>(rows, cols, threads); break;
+        case 4: direct_geometry_of<4>(rows, cols, threads); break;
+        default: direct_geometry_of<8>(rows, cols, threads); break;
+    }
+    return true;
 }
 
 void tile_geometry(int w, int64_t bytes, int *rows, int *cols, int *stages, int *threads) {
@@ -437,9 +612,56 @@ int launch_tile_t(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t 
     return finish_launch();
 }
 
+template <int W>
+int launch_direct_t(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream) {
+    using C = DirectCfg<W>;
+    constexpr int V = C::V, CL = C::CL, RB = C::RB;
+    const TilePlan &tp = p.tile;
+    if (reinterpret_cast<uintptr_t>(src + p.src_off * W) % 16 || reinterpret_cast<uintptr_t>(dst + p.dst_off * W) % 16)
+        return LC_ERR_UNSUPPORTED;  // the planner checked the pointers it was given
+    DirectArgs a{};
+    a.src = src + p.src_off * W;
+    a.dst = dst + p.dst_off * W;
+    a.eX = tp.X.e;
+    a.eY = tp.Y.e;
+    a.sX = tp.X.s * W;
+    a.dY = tp.Y.d * W;
+    a.nb = tp.batch.n;
+    int64_t nbatch = 1;
+    for (int i = 0; i < tp.batch.n; ++i) {
+        a.be[i] = tp.batch.m[i].e;
+        a.bs[i] = tp.batch.m[i].s * W;
+        a.bd[i] = tp.batch.m[i].d * W;
+        nbatch *= tp.batch.m[i].e;
+    }
+    a.tiles_x = (tp.X.e + RB * V - 1) / (RB * V);
+    a.tiles_y = (tp.Y.e + CL * V - 1) / (CL * V);
+    a.n_tiles = a.tiles_x * a.tiles_y * nbatch;
+    if (a.n_tiles >= (int64_t(1) << 32)) return LC_ERR_UNSUPPORTED;  // not on copies the planner sends here
+    a.narrow = 1;
+    a.ftx = make_fastdiv(static_cast<uint32_t>(a.tiles_x));
+    a.fty = make_fastdiv(static_cast<uint32_t>(a.tiles_y));
+    for (int i = 0; i < tp.batch.n; ++i) a.fbe[i] = make_fastdiv(static_cast<uint32_t>(tp.batch.m[i].e));
+    const void *fn = reinterpret_cast<const void *>(&k_tile_direct<W>);
+    int sms, per;
+    if (prepare(fn, C::NT, 0, 0, &sms, &per) != cudaSuccess) return LC_ERR_CUDA;
+    const int64_t wpb = C::NT / 32;
+    const int64_t grid = lmin((a.n_tiles + wpb - 1) / wpb, int64_t(sms) * per);
+    k_tile_direct<W><<<static_cast<unsigned>(grid), C::NT, 0, stream>>>(a);
+    return finish_launch();
+}
+
 }  // namespace
 
 int launch_tile(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream) {
+    if (p.tile.direct) {
+        switch (p.w) {
+            case 1: return launch_direct_t<1>(p, src, dst, stream);
+            case 2: return launch_direct_t<2>(p, src, dst, stream);
+            case 4: return launch_direct_t<4>(p, src, dst, stream);
+            case 8: return launch_direct_t<8>(p, src, dst, stream);
+        }
+    }
     const bool sh = tile_short(p.w, p.total * p.w);
     switch (p.w) {
         case 1: return sh ? launch_tile_t<1, true>(p, src, dst, stream) : launch_tile_t<1, false>(p, src, dst, stream);

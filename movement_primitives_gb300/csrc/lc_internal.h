@@ -44,8 +44,9 @@ struct TilePlan {
     ModeList batch;   // at most 3 (TMA tensors have at most 5 dims)
     int R = 0;        // source rows (X) per tile
     int TY = 0;       // words (Y) per 128-byte tile row
-    int S = 0;        // pipeline stages
+    int S = 0;        // pipeline stages (0: the direct form, no TMA ring)
     int threads = 0;
+    int direct = 0;   // 1: whole V x V blocks, loaded straight into registers
 };
 
 // TMA tensor copy: the modes of the destination order, innermost first, as
@@ -186,6 +187,11 @@ constexpr SmemGeo smem_geometry(int w) {
 // (source rows and words per tile, ring stages, threads), from the kernel's
 // own compile-time table.
 void tile_geometry(int w, int64_t bytes, int *rows, int *cols, int *stages, int *threads);
+// The direct form of the tile transpose (no TMA, no shared memory): taken
+// for the enabled word widths on copies of at most the short-box size a
+// side when both extents are whole V x V blocks; false leaves the outputs
+// alone.
+bool tile_direct_geometry(int w, int64_t bytes, int64_t eX, int64_t eY, int *rows, int *cols, int *threads);
 
 // Shared tile swizzle of the shared-memory transpose for w-byte words:
 // smallest (mask, shift) that keeps both copies conflict-free.

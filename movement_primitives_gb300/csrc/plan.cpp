@@ -485,7 +485,12 @@ bool plan_tile(Plan *p, const PtrInfo &ptr) {
     if (tp.X.e > (int64_t(1) << 31) || tp.Y.e * (w == 16 ? 2 : 1) > (int64_t(1) << 31)) return false;
     if (!a16(p->src_off * w) || !a16(p->dst_off * w)) return false;
     if (ptr.check && (ptr.src % 16 || ptr.dst % 16)) return false;
-    tile_geometry(w, p->total * w, &tp.R, &tp.TY, &tp.S, &tp.threads);  // the kernel's per-width table
+    if (tile_direct_geometry(w, p->total * w, tp.X.e, tp.Y.e, &tp.R, &tp.TY, &tp.threads)) {
+        tp.S = 0;
+        tp.direct = 1;
+    } else {
+        tile_geometry(w, p->total * w, &tp.R, &tp.TY, &tp.S, &tp.threads);  // the kernel's per-width table
+    }
     return true;
 }
 

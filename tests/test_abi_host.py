@@ -80,13 +80,40 @@ def test_plan_workloads(M):
     for w in (1, 2, 4, 8, 16):
         c = workloads.config(4, w)
         p = M.plan(c["src"], c["dst"], w, 1)
-        # box rows of 256 bytes for 2- and 8-byte words and for 4-byte words on
-        # the short boxes (workload 4 is 256 MiB a side), 128 otherwise
-        assert p["kernel_name"] == "tile_transpose" and p["tile_cols"] * w == (256 if w in (2, 4, 8) else 128)
+        assert p["kernel_name"] == "tile_transpose"
+        if w <= 2:
+            # the direct form: warp tiles of 4 chunks (64 bytes) x 8 blocks of V rows, no ring
+            assert (p["stages"], p["tile_cols"] * w, p["tile_rows"]) == (0, 64, 8 * (16 // w))
+        else:
+            # TMA box rows of 256 bytes for 4- and 8-byte words, 128 for 16-byte words
+            assert p["stages"] > 0 and p["tile_cols"] * w == (256 if w in (4, 8) else 128)
     p = M.plan(workloads.config(5)["src"], workloads.config(5)["dst"], 2)
     assert (p["vec"], p["run"]) == (8, 128)  # the vector fallback: 16-byte vectors over 256-byte runs
     # TMA boxes: the 128-word run, its 32 rows, 2 of the next mode (16 KiB)
     assert (p["tile_cols"], p["tile_rows"], p["stages"]) == (128, 32, 6)
+
+
+def test_plan_tile_direct_form(M):
+    """The tile transpose takes its direct form (stages 0) for 1- and 2-byte
+    words when both extents are whole V x V blocks and the copy is at most
+    256 MiB a side; ragged extents, wider words and larger copies keep the
+    TMA ring."""
+    def plan(shape_src, stride_src, stride_dst, w, n_tiles=1):
+        p = M.plan(dict(shape=shape_src, stride=stride_src), dict(shape=shape_src, stride=stride_dst), w,
+                   n_tiles, "tile_transpose")
+        assert p["kernel_name"] == "tile_transpose"
+        return p["stages"]
+    for w in (1, 2):
+        V = 16 // w
+        assert plan((V, V), (V, 1), (1, V), w) == 0
+        assert plan((9 * V, 5 * V), (5 * V + V, 1), (1, 9 * V + V), w) == 0        # padded rows
+        assert plan((3, 4 * V, 2 * V), (8 * V * V, 2 * V, 1), (8 * V * V, 1, 4 * V), w, 2) == 0  # batch, tiles
+        assert plan((9 * V, 5 * V - 1), (5 * V, 1), (1, 9 * V), w) > 0             # ragged Y
+        assert plan((9 * V - 1, 5 * V), (5 * V, 1), (1, 9 * V), w) > 0             # ragged X
+        big = (16384, 16384 + V) if w == 1 else (8192, 16384 + V)                  # past 256 MiB a side
+        assert plan(big, (big[1], 1), (1, big[0]), w) > 0
+    for w in (4, 8, 16):
+        assert plan((64, 64), (64, 1), (1, 64), w) > 0
 
 
 def test_gmem_smem_partition_table(M):

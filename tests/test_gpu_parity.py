@@ -172,6 +172,35 @@ def test_tile_transpose_ragged(w):
         run_case(L((r, c), (c, 1)), L((r, c), (1, r)), w, seed=r * c)
 
 
+@pytest.mark.parametrize("w", [1, 2])
+def test_tile_transpose_direct_form(w):
+    """Whole V x V blocks of 1- and 2-byte words: the direct form of the tile
+    transpose (plan stages 0; 16-byte loads straight into registers, no TMA,
+    no shared memory).  Extents off the warp tile, padded rows, offsets, tile
+    strides with gaps and up to three batch modes, each against the oracle;
+    ragged extents beside them keep the TMA ring."""
+    V = 16 // w
+
+    def check(src_l, dst_l, n_tiles=1, direct=True, seed=0):
+        p = lc().plan(src_l, dst_l, w, n_tiles, "tile_transpose")
+        assert (p["stages"] == 0) == direct, (src_l, dst_l, p["stages"])
+        assert run_case(src_l, dst_l, w, n_tiles, kernel="tile_transpose", seed=seed) == "tile_transpose"
+
+    for r, c in [(V, V), (V, 3 * V), (9 * V, 5 * V), (144, 80), (1024, 1040), (2000, 336), (128 + V, 64 + V)]:
+        check(L((r, c), (c, 1)), L((r, c), (1, r)), seed=r + c)
+        check(L((r, c), (c + V, 1), 3 * V), L((r, c), (1, r + 2 * V), 5 * V), seed=r * c)  # padded rows, offsets
+    # tiles with gaps between them; a batch mode; three batch modes that do not merge
+    check(L((48, 32), (32, 1), V, 48 * 32 + 4 * V), L((48, 32), (1, 48), 0, 48 * 32 + 2 * V), n_tiles=3, seed=5)
+    sh = (3, 4 * V, 6 * V)
+    check(L(sh, row_major(sh)), L(sh, permuted(sh, (0, 2, 1))), seed=6)
+    sh = (2, 3, 5, 2 * V, 3 * V)
+    check(L(sh, row_major(sh)), L(sh, permuted(sh, (2, 1, 0, 4, 3))), seed=7)
+    # ragged extents with 16-byte rows: the TMA ring
+    for r, c in [(9 * V, 5 * V - 1), (9 * V - 1, 5 * V), (100 + V // 2, 77)]:
+        check(L((r, c), (((c + V - 1) // V) * V, 1)), L((r, c), (1, ((r + V - 1) // V) * V)), direct=False,
+              seed=r + 3 * c)
+
+
 @pytest.mark.parametrize("w", [1, 2, 4, 8, 16])
 def test_smem_transpose_any_alignment(w):
     # whole tiles and ragged edges in both modes; aligned and unaligned rows
