@@ -175,7 +175,9 @@ typedef struct {
     int32_t stages;            /* TMA ring stages; 0: the tile transpose's direct form
                                   (1- and 2-byte words in whole 16-byte blocks, loaded
                                   straight into registers: no TMA, no shared memory) */
-    /* launch */
+    /* reserved, always 0: each launch sizes its grid from the device's SM
+     * count and the kernel's occupancy, which the host-only planner does not
+     * query */
     int32_t grid, block, smem_bytes;
 } lc_plan_info;
 

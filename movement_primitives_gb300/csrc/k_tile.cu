@@ -88,14 +88,37 @@ namespace lc {
 #define LC_TILE_BOXB_W1 LC_TILE_BOXB_OTHER
 #endif
 
-// Box rows for 4-byte words on the short boxes: 256 bytes measured 90.5 %
-// against 86.1 % with 128 (8192^2, 128-row boxes, 4 stages).
+// Box rows for 4-byte words on the short boxes when line stores are off:
+// 256 bytes measured 90.5 % against 86.1 % with 128 (8192^2, 128-row boxes,
+// 4 stages).
 #ifndef LC_TILE_BOXB_W4_SHORT
 #define LC_TILE_BOXB_W4_SHORT 256
 #endif
 
+// 1: on the short boxes of 1-, 2- and 4-byte words, micro-blocks are handed
+// out so that one warp store writes whole 128-byte lines (8 row groups x 4
+// chunks per warp: 4 destination rows x 128 bytes), over boxes of 128-byte
+// rows; 0 (and everywhere else): 8 chunks x 4 row groups (8 destination rows
+// x 64 bytes).  Measured on GB300 (8192^2 transposes, TMA ring, L2 flushed by
+// a read): 1-byte words 86.7 % of the copy peak against 74.8-75.4 %, 2-byte
+// 95.2-95.3 % against 87.5-87.9 %, 4-byte 90.8-91.1 % against 90.7-90.9 %;
+// on 8- and 16-byte words (86.2 against 93.6 %, 85.2 against 92.4 %) and on
+// the 16384^2 2-byte transpose (82.3 against 91.1-91.4 %) line stores lose.
+#ifndef LC_TILE_LINE_STORES
+#define LC_TILE_LINE_STORES 1
+#endif
+// 1: with line stores, the boxes land in shared memory under the TMA 128-byte
+// swizzle (16-byte chunk k of row y at chunk k ^ (y & 7)), which makes the
+// shared reads conflict-free (without it, two row groups of a quarter warp
+// read the same banks: 93.6-94.0 % instead of 95.3 % for 2-byte words).
+#ifndef LC_TILE_SWIZZLE
+#define LC_TILE_SWIZZLE 1
+#endif
+
 template <int W, bool SHORT = false> struct TileCfg {
-    static constexpr int BOXB = W == 1   ? LC_TILE_BOXB_W1
+    static constexpr bool LINES = LC_TILE_LINE_STORES != 0 && SHORT && W <= 4;
+    static constexpr int BOXB = LINES    ? 128
+                              : W == 1   ? LC_TILE_BOXB_W1
                               : W == 2   ? LC_TILE_BOXB_W2
                               : W == 4   ? (SHORT ? LC_TILE_BOXB_W4_SHORT : LC_TILE_BOXB_OTHER)
                               : W == 8   ? LC_TILE_BOXB_W8
@@ -111,8 +134,11 @@ template <int W, bool SHORT = false> struct TileCfg {
     static constexpr int TILE_BYTES = BOXB * R;
     static constexpr int MB = CPR * R / V;        // V-row x 16-byte micro-blocks
     static constexpr int NT = MB < 256 ? MB : 256;  // threads: at most one micro-block each per round
-    static constexpr int SMEM = 128 + S * TILE_BYTES;
+    static constexpr bool SWZ = LINES && LC_TILE_SWIZZLE != 0;
+    // barriers in the first 128 bytes; a swizzled ring starts on a 1024-byte boundary
+    static constexpr int SMEM = 128 + S * TILE_BYTES + (SWZ ? 1024 : 0);
     static_assert(R <= 256 && R % V == 0, "TMA boxes hold at most 256 rows, whole micro-blocks");
+    static_assert(!LINES || ((R / V) % 8 == 0 && CPR % 4 == 0), "line stores: octets of row groups, chunk quads");
     static_assert((BOXB == 128 || BOXB == 256) && SMEM <= 227 * 1024, "box rows of 128 or 256 bytes, ring fits");
 };
 
@@ -250,13 +276,36 @@ __device__ __forceinline__ void tile_issue_load(const CUtensorMap *tmap, const T
     }
 }
 
+// Micro-block mb of a tile -> (16-byte chunk c, row group mr).  With line
+// stores, lane l of a warp's 32 micro-blocks takes chunk 4 g + (l & 3) and
+// one of 8 consecutive row groups; the row-group bit that varies inside a
+// quarter warp (8 lanes, one shared-memory wavefront of 16-byte reads) is
+// the one that changes the swizzle phase (row & 7) of the rows read: bit 0
+// for 4-byte words (V = 4), 1 for 8-byte, 2 for 16-byte words.
+template <typename C>
+__device__ __forceinline__ void micro_block(int mb, int &c, int &mr) {
+    if constexpr (C::LINES) {
+        constexpr int CQ = C::CPR / 4;
+        const int l = mb & 31, g = mb >> 5, m3 = l >> 2;
+        int lo = m3;
+        if constexpr (C::V == 2) lo = ((m3 & 1) << 1) | ((m3 >> 1) & 1) | (m3 & 4);
+        else if constexpr (C::V == 1) lo = ((m3 & 1) << 2) | (m3 >> 1);
+        c = (g % CQ) * 4 + (l & 3);
+        mr = (g / CQ) * 8 + lo;
+    } else {
+        c = mb % C::CPR;
+        mr = mb / C::CPR;
+    }
+}
+
 // Tile t = (batch, ty, tx): TMA brings source rows [tx*R, tx*R + R) x words
 // [ty*TY, ty*TY + TY) (BOXB bytes per row) into a stage.  Micro-block mb =
-// (row group mr = mb / CPR, 16-byte chunk c = mb % CPR): V rows x 16 bytes,
+// (row group mr, 16-byte chunk c; micro_block): V rows x 16 bytes,
 // transposed in registers into V destination chunks, destination rows
-// ty*TY + c*V + q, words tx*R + mr*V .. + V.  The 8 lanes of a 16-byte
-// shared-memory wavefront read 8 consecutive chunks of one box row, i.e. all
-// 32 banks once: conflict-free with no swizzle.
+// ty*TY + c*V + q, words tx*R + mr*V .. + V.  Without line stores the 8
+// lanes of a 16-byte shared-memory wavefront read 8 consecutive chunks of one
+// box row, i.e. all 32 banks once: conflict-free with no swizzle; with line
+// stores they read 4 chunks of two rows whose swizzle phases differ.
 template <int W, bool SHORT>
 __global__ void __launch_bounds__(TileCfg<W, SHORT>::NT)
     k_tile_transpose(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ TileArgs a) {
@@ -264,10 +313,12 @@ __global__ void __launch_bounds__(TileCfg<W, SHORT>::NT)
     constexpr int V = C::V;
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
-    const uint8_t *tiles = smem + 128;
     const int tid = threadIdx.x;
     const int64_t n_local = a.n_tiles > blockIdx.x ? (a.n_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-    const uint32_t bar0 = ptx::smem_addr(bars), tile0 = ptx::smem_addr(tiles);
+    const uint32_t bar0 = ptx::smem_addr(bars);
+    uint32_t tile0 = bar0 + 128;
+    if constexpr (C::SWZ) tile0 = (tile0 + 1023u) & ~1023u;  // the swizzle's phase follows address bits 7-9
+    const uint8_t *tiles = smem + (tile0 - bar0);
     if (tid == 0) {
         ptx::prefetch_tensormap(&tmap);
         for (int s = 0; s < C::S; ++s) ptx::mbar_init(bar0 + 8 * s, 1);
@@ -310,14 +361,37 @@ __global__ void __launch_bounds__(TileCfg<W, SHORT>::NT)
             }
             const uint8_t *st = tiles + static_cast<size_t>(s) * C::TILE_BYTES;
             for (int mb = tid; mb < C::MB; mb += C::NT) {
-                const int c = mb % C::CPR, mr = mb / C::CPR;
+                int c, mr;
+                micro_block<C>(mb, c, mr);
                 const int64_t x0 = tx * C::R + int64_t(mr) * V;
                 if (x0 >= a.eX) continue;  // rows past the tensor (TMA filled them)
                 uint32_t in[V][4], out[V][4];
+                // With 8 or more rows a micro-block, every row group starts on the
+                // same swizzle phase; lanes of odd row groups read their rows in the
+                // order r ^ 4 so that the two row groups of a quarter warp sit on
+                // different phases, and put the rows back in order in registers.
+                constexpr bool FLIP = C::SWZ && C::LINES && V >= 8;
+                const int fl = FLIP ? (mr & 1) * 4 : 0;
 #pragma unroll
                 for (int r = 0; r < V; ++r) {
-                    const uint4 q = *reinterpret_cast<const uint4 *>(st + (mr * V + r) * C::BOXB + c * 16);
+                    const int row = mr * V + (r ^ fl);
+                    const int pc = C::SWZ ? (c ^ (row & 7)) : c;
+                    const uint4 q = *reinterpret_cast<const uint4 *>(st + row * C::BOXB + pc * 16);
                     in[r][0] = q.x; in[r][1] = q.y; in[r][2] = q.z; in[r][3] = q.w;
+                }
+                if constexpr (FLIP) {
+                    if (fl) {
+#pragma unroll
+                        for (int r = 0; r < V; ++r) {
+                            if (r & 4) continue;
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const uint32_t t = in[r][k];
+                                in[r][k] = in[r ^ 4][k];
+                                in[r ^ 4][k] = t;
+                            }
+                        }
+                    }
                 }
                 transpose_chunk<W>(in, out);
                 const int64_t y0 = ty * C::TY + int64_t(c) * V;
@@ -573,7 +647,8 @@ int launch_tile_t(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t 
     std::memset(&tmap, 0, sizeof(tmap));
     void *base = const_cast<uint8_t *>(src + p.src_off * W);
     if (enc(&tmap, dt, static_cast<cuuint32_t>(rank), base, dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, C::SWZ ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return LC_ERR_UNSUPPORTED;  // the driver refused this tensor shape
 

@@ -85,8 +85,9 @@ def test_plan_workloads(M):
             # the direct form: warp tiles of 4 chunks (64 bytes) x 8 blocks of V rows, no ring
             assert (p["stages"], p["tile_cols"] * w, p["tile_rows"]) == (0, 64, 8 * (16 // w))
         else:
-            # TMA box rows of 256 bytes for 4- and 8-byte words, 128 for 16-byte words
-            assert p["stages"] > 0 and p["tile_cols"] * w == (256 if w in (4, 8) else 128)
+            # TMA box rows of 128 bytes for 4-byte words (the short boxes' line
+            # stores, swizzled), 256 for 8-byte words, 128 for 16-byte words
+            assert p["stages"] > 0 and p["tile_cols"] * w == (256 if w == 8 else 128)
     p = M.plan(workloads.config(5)["src"], workloads.config(5)["dst"], 2)
     assert (p["vec"], p["run"]) == (8, 128)  # the vector fallback: 16-byte vectors over 256-byte runs
     # TMA boxes: the 128-word run, its 32 rows, 2 of the next mode (16 KiB)
