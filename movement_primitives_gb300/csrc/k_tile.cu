@@ -115,6 +115,21 @@ namespace lc {
 #define LC_TILE_SWIZZLE 1
 #endif
 
+// Threads per CTA at most (each takes one micro-block per round).  Measured
+// on GB300 against 256: 512 for the 256-row boxes of 2-byte words (16384^2:
+// 91.9 % against 91.1-91.4 %; 8-byte words lose 5 points with 512, 16-byte
+// words 7), 128 for 16-byte words (8192^2: 93.2-93.3 % against 92.4-92.5 %;
+// 4-, 8- and 2-byte words lose 0.7-1.4 points with 128).
+#ifndef LC_TILE_MAX_THREADS
+#define LC_TILE_MAX_THREADS 256
+#endif
+#ifndef LC_TILE_MAX_THREADS_W2_TALL
+#define LC_TILE_MAX_THREADS_W2_TALL 512
+#endif
+#ifndef LC_TILE_MAX_THREADS_W16
+#define LC_TILE_MAX_THREADS_W16 128
+#endif
+
 template <int W, bool SHORT = false> struct TileCfg {
     static constexpr bool LINES = LC_TILE_LINE_STORES != 0 && SHORT && W <= 4;
     static constexpr int BOXB = LINES    ? 128
@@ -133,7 +148,10 @@ template <int W, bool SHORT = false> struct TileCfg {
                            : W == 8 ? LC_TILE_STAGES_W8 : LC_TILE_STAGES_WIDE;  // ring stages
     static constexpr int TILE_BYTES = BOXB * R;
     static constexpr int MB = CPR * R / V;        // V-row x 16-byte micro-blocks
-    static constexpr int NT = MB < 256 ? MB : 256;  // threads: at most one micro-block each per round
+    static constexpr int MAXT = W == 2 && !SHORT ? LC_TILE_MAX_THREADS_W2_TALL
+                              : W == 16           ? LC_TILE_MAX_THREADS_W16
+                                                  : LC_TILE_MAX_THREADS;
+    static constexpr int NT = MB < MAXT ? MB : MAXT;  // at most one micro-block each per round
     static constexpr bool SWZ = LINES && LC_TILE_SWIZZLE != 0;
     // barriers in the first 128 bytes; a swizzled ring starts on a 1024-byte boundary
     static constexpr int SMEM = 128 + S * TILE_BYTES + (SWZ ? 1024 : 0);
