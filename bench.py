@@ -150,9 +150,9 @@ def _code_only(text: bytes) -> bytes:
 def kernel_sources_sha(kernel_name: str) -> str:
     """Hash of the code (comments excluded) of a kernel class's sources."""
     warp = ["k_warp.cu", "k_warp.cuh"] + ["k_warp_w%d.cu" % w for w in (1, 2, 4, 8, 16)]
-    files = {"warp_permute": warp, "warp_unit_shared": warp, "tile_transpose": ["k_tile.cu"],
+    files = {"warp_permute": warp, "warp_unit_shared": warp, "tile_transpose": ["k_tile.cu", "bulk_store.cuh"],
              "vec_copy": ["k_vec.cu"], "smem_transpose": ["k_smem.cu"],
-             "tma_copy": ["k_tma_copy.cu"], "window_sum": ["k_stencil.cu"],
+             "tma_copy": ["k_tma_copy.cu", "bulk_store.cuh"], "window_sum": ["k_stencil.cu"],
              "loop_copy": ["k_loop.cu"], "warp_shuffle": ["k_shuffle.cu"],
              "smem_staged": ["k_staged.cu"]}.get(kernel_name, [])
     paths = [os.path.join(ROOT, "movement_primitives_gb300", "csrc", f) for f in files + ["ptx.cuh", "device_common.cuh"]]

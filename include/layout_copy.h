@@ -110,7 +110,10 @@ typedef enum {
      * coalesced global stores.  Large 2-D transposes with batch modes.  Its
      * direct form (1- and 2-byte words, both extents whole 16-byte blocks,
      * at most 256 MiB a side) loads each block's rows with 16-byte global
-     * loads straight into registers instead: no TMA and no shared memory. */
+     * loads straight into registers instead: no TMA and no shared memory.
+     * Short 4-byte transposes whose destination rows are whole 16-byte
+     * chunks stage each transposed tile in shared memory and store it with
+     * a TMA tensor store (lc_plan_info.tile_form). */
     LC_KERNEL_TILE_TRANSPOSE = 3,
     /* Shared-memory transpose for any alignment: tiles of 64 source rows
      * (32 for 16-byte words), each row staged as aligned chunks (4 bytes for
@@ -179,6 +182,11 @@ typedef struct {
      * count and the kernel's occupancy, which the host-only planner does not
      * query */
     int32_t grid, block, smem_bytes;
+    /* tile transpose: 0 the TMA ring with thread stores, 1 the direct form
+     * (stages 0), 2 the TMA ring whose output tiles leave by TMA tensor
+     * stores (4-byte words, destination rows of whole 16-byte chunks, at most
+     * 256 MiB a side); 0 for the other classes */
+    int32_t tile_form;
 } lc_plan_info;
 
 /* The copy.  Validates, plans (host only, microseconds), launches one

@@ -55,7 +55,8 @@ class CPlanInfo(ctypes.Structure):
                 ("units_per_chunk", ctypes.c_int64),
                 ("tile_rows", ctypes.c_int32), ("tile_cols", ctypes.c_int32),
                 ("stages", ctypes.c_int32),
-                ("grid", ctypes.c_int32), ("block", ctypes.c_int32), ("smem_bytes", ctypes.c_int32)]
+                ("grid", ctypes.c_int32), ("block", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
+                ("tile_form", ctypes.c_int32)]
 
 
 class CWarpUnit(ctypes.Structure):

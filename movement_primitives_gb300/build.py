@@ -24,7 +24,7 @@ LIB_PATH = os.path.join(HERE, LIB_NAME)
 SOURCES = ["plan.cpp", "api.cu", "host_copy.cu", "host_copy_static.cu", "k_vec.cu", "k_warp.cu", "k_shuffle.cu", "k_staged.cu",
            "k_warp_w1.cu", "k_warp_w2.cu", "k_warp_w4.cu", "k_warp_w8.cu", "k_warp_w16.cu",
            "k_tile.cu", "k_smem.cu", "k_tma_copy.cu", "k_stencil.cu", "k_loop.cu"]
-HEADERS = ["lc_internal.h", "ptx.cuh", "device_common.cuh", "launch.h", "k_warp.cuh", "tensor_map.h"]
+HEADERS = ["lc_internal.h", "ptx.cuh", "device_common.cuh", "launch.h", "k_warp.cuh", "tensor_map.h", "bulk_store.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O3",
           "-I", INCLUDE, "-I", CSRC]

@@ -12,6 +12,7 @@
 #include "device_common.cuh"
 #include "launch.h"
 #include "tensor_map.h"
+#include "bulk_store.cuh"
 
 namespace lc {
 
@@ -265,13 +266,9 @@ __device__ __forceinline__ void tile_coords(const A &a, int64_t t, int64_t &tx, 
 #endif
 }
 
-template <int W, bool SHORT>
-__device__ __forceinline__ void tile_issue_load(const CUtensorMap *tmap, const TileArgs &a, int64_t t,
-                                                uint32_t dst, uint32_t bar) {
-    using C = TileCfg<W, SHORT>;
-    int64_t tx, ty, b;
-    tile_coords(a, t, tx, ty, b);
-    int32_t b0 = 0, b1 = 0, b2 = 0;  // batch coordinates, outermost first
+// Flat batch index -> batch coordinates b0 (outermost) .. b2.
+__device__ __forceinline__ void batch_coords(const TileArgs &a, int64_t b, int32_t &b0, int32_t &b1, int32_t &b2) {
+    b0 = b1 = b2 = 0;
     if (a.narrow) {
         uint32_t q = static_cast<uint32_t>(b);
         if (a.nb == 3) { const uint32_t n = fast_div(q, a.fbe[2]); b2 = static_cast<int32_t>(q - n * a.fbe[2].d); q = n; }
@@ -282,6 +279,16 @@ __device__ __forceinline__ void tile_issue_load(const CUtensorMap *tmap, const T
         if (a.nb >= 2) { b1 = static_cast<int32_t>(b % a.be[1]); b /= a.be[1]; }
         if (a.nb >= 1) { b0 = static_cast<int32_t>(b % a.be[0]); }
     }
+}
+
+template <int W, bool SHORT>
+__device__ __forceinline__ void tile_issue_load(const CUtensorMap *tmap, const TileArgs &a, int64_t t,
+                                                uint32_t dst, uint32_t bar) {
+    using C = TileCfg<W, SHORT>;
+    int64_t tx, ty, b;
+    tile_coords(a, t, tx, ty, b);
+    int32_t b0, b1, b2;  // batch coordinates, outermost first
+    batch_coords(a, b, b0, b1, b2);
     const int32_t c0 = static_cast<int32_t>(ty * C::TY * (W == 16 ? 2 : 1));
     const int32_t c1 = static_cast<int32_t>(tx * C::R);
     ptx::mbar_arrive_expect_tx(bar, C::TILE_BYTES);
@@ -439,6 +446,186 @@ __global__ void __launch_bounds__(TileCfg<W, SHORT>::NT)
             tile_issue_load<W, SHORT>(&tmap, a, blockIdx.x + (i + C::S) * gridDim.x, tile0 + s * C::TILE_BYTES,
                                bar0 + 8 * s);
     }
+}
+
+// ---- Tile transpose through TMA stores --------------------------------------
+//
+// Boxes of 128-byte source rows land in a ring under the TMA 128-byte swizzle.
+// A warp takes 8 consecutive row groups x 4 chunks: lane (i, cq) reads the V
+// rows of row group mr = 8 g + i at chunk c in the order r ^ f(i), so that the
+// 8 lanes of a quarter warp read 8 different swizzle phases (conflict-free),
+// puts them back in order with conditional register swaps, transposes V x V
+// words in registers and writes its V destination chunks into an output tile
+// laid out as the destination box (TY rows of R words), the quarter warp
+// writing 128 contiguous bytes.  One thread then stores the output tile with
+// a TMA tensor store through a destination tensor map, which clips it at the
+// tensor's edges (its contiguous mode in 16-byte steps: the form takes only
+// destination rows of whole 16-byte chunks), and refills the stage; O output
+// tiles rotate, each reused once its store has read it.
+// Word widths (bit w) that take TMA stores on copies of at most
+// LC_TILE_SHORT_MAX_BYTES a side (unless the direct form applies).  Measured
+// on GB300 against the ring with thread stores (L2 flushed by a read, same
+// box): 8192^2 4-byte words 91.0-91.5 % of the copy peak against 89.7-90.1 %;
+// 8-byte words 87.4-91.5 % against 92.8-93.1 %, 16-byte words 90.0-90.6 %
+// against 93.2 %, the 16384^2 2-byte transpose 89.5-90.2 % against 91.6-91.8 %.
+#ifndef LC_TILE_TSTORE_MASK
+#define LC_TILE_TSTORE_MASK 0x10
+#endif
+#ifndef LC_TS_ROWS_NARROW
+#define LC_TS_ROWS_NARROW 256
+#endif
+#ifndef LC_TS_ROWS_W8
+#define LC_TS_ROWS_W8 128
+#endif
+#ifndef LC_TS_ROWS_W16
+#define LC_TS_ROWS_W16 128
+#endif
+// Ring stages (4: 89.6-90.0 % on the 8192^2 4-byte transpose) and output
+// tiles; CTAs of 512 threads measured 91.1-91.5 %.
+#ifndef LC_TS_STAGES
+#define LC_TS_STAGES 3
+#endif
+#ifndef LC_TS_OUT
+#define LC_TS_OUT 2
+#endif
+#ifndef LC_TS_THREADS
+#define LC_TS_THREADS 256
+#endif
+
+template <int W> struct TsCfg {
+    static constexpr int V = 16 / W;
+    static constexpr int MULT = W == 16 ? 2 : 1;  // 16-byte words travel as two 8-byte TMA elements
+    static constexpr int TY = 128 / W;            // words of Y per tile: one 128-byte box row
+    static constexpr int R = W == 16 ? LC_TS_ROWS_W16 : W == 8 ? LC_TS_ROWS_W8 : LC_TS_ROWS_NARROW;
+    static constexpr int S = LC_TS_STAGES, O = LC_TS_OUT;
+    static constexpr int TILE_BYTES = 128 * R;    // an input stage, and an output tile (TY rows x R words)
+    static constexpr int MB = 8 * R / V;          // micro-blocks: 8 chunks x R / V row groups
+    static constexpr int NT = MB < LC_TS_THREADS ? MB : LC_TS_THREADS;
+    static constexpr int SMEM = 2048 + (S + O) * TILE_BYTES;  // barriers, alignment slack, ring, outputs
+    static_assert(R * MULT <= 256 && (R / V) % 8 == 0 && NT % 32 == 0 && MB % NT == 0, "whole warps of octets");
+    static_assert(SMEM <= 227 * 1024, "ring and output tiles fit");
+};
+
+template <int W>
+__device__ __forceinline__ void ts_issue_load(const CUtensorMap *tmap, const TileArgs &a, int64_t t, uint32_t dst,
+                                              uint32_t bar) {
+    using C = TsCfg<W>;
+    int64_t tx, ty, b;
+    tile_coords(a, t, tx, ty, b);
+    int32_t b0, b1, b2;
+    batch_coords(a, b, b0, b1, b2);
+    const int32_t c0 = static_cast<int32_t>(ty * C::TY * C::MULT), c1 = static_cast<int32_t>(tx * C::R);
+    ptx::mbar_arrive_expect_tx(bar, C::TILE_BYTES);
+    switch (a.nb) {  // tensor dims: (Y, X, batch innermost .. outermost)
+        case 0: ptx::tma_load_2d(dst, tmap, c0, c1, bar); break;
+        case 1: ptx::tma_load_3d(dst, tmap, c0, c1, b0, bar); break;
+        case 2: ptx::tma_load_4d(dst, tmap, c0, c1, b1, b0, bar); break;
+        default: ptx::tma_load_5d(dst, tmap, c0, c1, b2, b1, b0, bar); break;
+    }
+}
+
+template <int W>
+__device__ __forceinline__ void ts_issue_store(const CUtensorMap *smap, const TileArgs &a, int64_t t, uint32_t src) {
+    using C = TsCfg<W>;
+    int64_t tx, ty, b;
+    tile_coords(a, t, tx, ty, b);
+    int32_t b0, b1, b2;
+    batch_coords(a, b, b0, b1, b2);
+    // tensor dims: (X, Y, batch innermost .. outermost)
+    int32_t c[5] = {static_cast<int32_t>(tx * C::R * C::MULT), static_cast<int32_t>(ty * C::TY), 0, 0, 0};
+    if (a.nb == 1) c[2] = b0;
+    else if (a.nb == 2) { c[2] = b1; c[3] = b0; }
+    else if (a.nb == 3) { c[2] = b2; c[3] = b1; c[4] = b0; }
+    bulk::tma_store(smap, 2 + a.nb, c, src);
+    bulk::commit();
+}
+
+template <int W>
+__global__ void __launch_bounds__(TsCfg<W>::NT)
+    k_tile_tstore(const __grid_constant__ CUtensorMap lmap, const __grid_constant__ CUtensorMap smap,
+                  const __grid_constant__ TileArgs a) {
+    using C = TsCfg<W>;
+    constexpr int V = C::V;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x;
+    const int64_t n_local = a.n_tiles > blockIdx.x ? (a.n_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const uint32_t bar0 = ptx::smem_addr(smem);
+    const uint32_t ring0 = (bar0 + 128u + 1023u) & ~1023u;  // the swizzle's phase follows address bits 7-9
+    const uint32_t out0 = ring0 + C::S * C::TILE_BYTES;
+    const uint8_t *ring = smem + (ring0 - bar0);
+    uint8_t *outp = smem + (out0 - bar0);
+    if (tid == 0) {
+        ptx::prefetch_tensormap(&lmap);
+        ptx::prefetch_tensormap(&smap);
+        for (int s = 0; s < C::S; ++s) ptx::mbar_init(bar0 + 8 * s, 1);
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0)
+        for (int64_t i = 0; i < lmin(C::S, n_local); ++i)
+            ts_issue_load<W>(&lmap, a, blockIdx.x + i * gridDim.x, ring0 + i * C::TILE_BYTES, bar0 + 8 * i);
+
+    for (int64_t i = 0; i < n_local; ++i) {
+        const int s = static_cast<int>(i % C::S), o = static_cast<int>(i % C::O);
+        const int64_t t = blockIdx.x + i * gridDim.x;
+        if (tid == 0 && i >= C::O) bulk::wait_read<C::O - 1>();  // output tile o: its last store has read it
+        const bool ok = ptx::mbar_wait_bounded(bar0 + 8 * s, static_cast<uint32_t>((i / C::S) & 1), a.timeout_ns);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                report_error(LC_ERR_TIMEOUT, LC_KERNEL_TILE_TRANSPOSE);
+                bulk::wait_all();
+                for (int64_t q = i; q < lmin(i + C::S, n_local); ++q)
+                    ptx::mbar_wait_bounded(bar0 + 8 * (q % C::S), static_cast<uint32_t>((q / C::S) & 1),
+                                           a.timeout_ns);
+            }
+            return;
+        }
+        const uint8_t *st = ring + s * C::TILE_BYTES;
+        uint8_t *ot = outp + o * C::TILE_BYTES;
+        for (int mb = tid; mb < C::MB; mb += C::NT) {
+            const int l = mb & 31, g = mb >> 5, i8 = l & 7;
+            const int c = (g & 1) * 4 + (l >> 3);  // 16-byte chunk of the box row
+            const int mr = (g >> 1) * 8 + i8;     // row group
+            const int f = V >= 8 ? i8 : (i8 * V) >> 3;
+            uint32_t in[V][4], out[V][4];
+#pragma unroll
+            for (int k = 0; k < V; ++k) {
+                const int row = mr * V + (k ^ f);
+                const uint4 q = *reinterpret_cast<const uint4 *>(st + row * 128 + ((c ^ (row & 7)) << 4));
+                in[k][0] = q.x; in[k][1] = q.y; in[k][2] = q.z; in[k][3] = q.w;
+            }
+            // in[k] holds row k ^ f: swap by each set bit of f to put row k there
+#pragma unroll
+            for (int bit = 1; bit < 8 && bit < V; bit <<= 1) {
+                if (f & bit) {
+#pragma unroll
+                    for (int k = 0; k < V; ++k) {
+                        if (k & bit) continue;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const uint32_t tmp = in[k][e];
+                            in[k][e] = in[k ^ bit][e];
+                            in[k ^ bit][e] = tmp;
+                        }
+                    }
+                }
+            }
+            transpose_chunk<W>(in, out);
+#pragma unroll
+            for (int q = 0; q < V; ++q)
+                *reinterpret_cast<uint4 *>(ot + (c * V + q) * (C::R * W) + mr * 16) =
+                    make_uint4(out[q][0], out[q][1], out[q][2], out[q][3]);
+        }
+        bulk::fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            ts_issue_store<W>(&smap, a, t, out0 + o * C::TILE_BYTES);
+            if (i + C::S < n_local)
+                ts_issue_load<W>(&lmap, a, blockIdx.x + (i + C::S) * gridDim.x, ring0 + s * C::TILE_BYTES,
+                                 bar0 + 8 * s);
+        }
+    }
+    if (tid == 0) bulk::wait_all();
 }
 
 // ---- Direct tile transpose (no TMA, no shared memory) --------------------
@@ -610,6 +797,29 @@ static void direct_geometry_of(int *rows, int *cols, int *threads) {
     *threads = DirectCfg<W>::NT;
 }
 
+template <int W>
+static void tstore_geometry_of(int *rows, int *cols, int *stages, int *threads) {
+    *rows = TsCfg<W>::R;
+    *cols = TsCfg<W>::TY;
+    *stages = TsCfg<W>::S;
+    *threads = TsCfg<W>::NT;
+}
+
+bool tile_tstore_geometry(int w, int64_t bytes, int64_t eX, int *rows, int *cols, int *stages, int *threads) {
+    // a tensor store clips the destination's contiguous mode in 16-byte steps
+    // (measured: a 71-word row of 2-byte words got its 72nd word written), so
+    // the form takes only destination rows of whole 16-byte chunks
+    if (!((LC_TILE_TSTORE_MASK >> w) & 1) || bytes > LC_TILE_SHORT_MAX_BYTES || (eX * w) % 16) return false;
+    switch (w) {
+        case 1: tstore_geometry_of<1>(rows, cols, stages, threads); break;
+        case 2: tstore_geometry_of<2>(rows, cols, stages, threads); break;
+        case 4: tstore_geometry_of<4>(rows, cols, stages, threads); break;
+        case 8: tstore_geometry_of<8>(rows, cols, stages, threads); break;
+        default: tstore_geometry_of<16>(rows, cols, stages, threads); break;
+    }
+    return true;
+}
+
 bool tile_direct_geometry(int w, int64_t bytes, int64_t eX, int64_t eY, int *rows, int *cols, int *threads) {
     if (w > 8 || !((LC_TILE_DIRECT_MASK >> w) & 1) || bytes > LC_TILE_SHORT_MAX_BYTES) return false;
     if (eX % (16 / w) || eY % (16 / w)) return false;
@@ -705,6 +915,93 @@ int launch_tile_t(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t 
     return finish_launch();
 }
 
+// The tile arguments shared by the ring forms: extents, destination stride
+// of Y, batch modes, tile counts for R x TY tiles, 32-bit divisors when the
+// tile count allows them.
+static TileArgs ring_args(const Plan &p, uint8_t *dst, int w, int R, int TY, bool narrow_ok) {
+    const TilePlan &tp = p.tile;
+    TileArgs a{};
+    a.dst = dst + p.dst_off * w;
+    a.eX = tp.X.e;
+    a.eY = tp.Y.e;
+    a.dY = tp.Y.d * w;
+    a.nb = tp.batch.n;
+    int64_t nbatch = 1;
+    for (int i = 0; i < tp.batch.n; ++i) {
+        a.be[i] = tp.batch.m[i].e;
+        a.bd[i] = tp.batch.m[i].d * w;
+        nbatch *= tp.batch.m[i].e;
+    }
+    a.tiles_x = (tp.X.e + R - 1) / R;
+    a.tiles_y = (tp.Y.e + TY - 1) / TY;
+    a.n_tiles = a.tiles_x * a.tiles_y * nbatch;
+    a.narrow = narrow_ok && a.n_tiles < (int64_t(1) << 32);
+    if (a.narrow) {
+        a.ftx = make_fastdiv(static_cast<uint32_t>(a.tiles_x));
+        a.fty = make_fastdiv(static_cast<uint32_t>(a.tiles_y));
+        for (int i = 0; i < tp.batch.n; ++i) a.fbe[i] = make_fastdiv(static_cast<uint32_t>(tp.batch.m[i].e));
+    }
+    a.timeout_ns = wait_limit_ns();
+    return a;
+}
+
+static CUtensorMapDataType tma_type(int w) {
+    return w == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : w == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16
+         : w == 4 ? CU_TENSOR_MAP_DATA_TYPE_UINT32 : CU_TENSOR_MAP_DATA_TYPE_UINT64;
+}
+
+template <int W>
+int launch_tstore_t(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream) {
+    using C = TsCfg<W>;
+    const TilePlan &tp = p.tile;
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return LC_ERR_CUDA;
+    const int rank = 2 + tp.batch.n;
+    // load map: (Y, X, batch innermost first) over the source, boxes of one
+    // 128-byte row x R rows, swizzled; store map: (X, Y, batch) over the
+    // destination, boxes of R words x TY rows
+    cuuint64_t ld_dims[5], ld_str[4], st_dims[5], st_str[4];
+    cuuint32_t ld_box[5], st_box[5], estr[5];
+    ld_dims[0] = static_cast<cuuint64_t>(tp.Y.e * C::MULT);
+    ld_dims[1] = static_cast<cuuint64_t>(tp.X.e);
+    ld_str[0] = static_cast<cuuint64_t>(tp.X.s * W);
+    st_dims[0] = static_cast<cuuint64_t>(tp.X.e * C::MULT);
+    st_dims[1] = static_cast<cuuint64_t>(tp.Y.e);
+    st_str[0] = static_cast<cuuint64_t>(tp.Y.d * W);
+    for (int i = 0; i < tp.batch.n; ++i) {
+        const Mode &b = tp.batch.m[tp.batch.n - 1 - i];
+        ld_dims[2 + i] = st_dims[2 + i] = static_cast<cuuint64_t>(b.e);
+        ld_str[1 + i] = static_cast<cuuint64_t>(b.s * W);
+        st_str[1 + i] = static_cast<cuuint64_t>(b.d * W);
+    }
+    ld_box[0] = static_cast<cuuint32_t>(128 / (W / C::MULT));
+    ld_box[1] = static_cast<cuuint32_t>(C::R);
+    st_box[0] = static_cast<cuuint32_t>(C::R * C::MULT);
+    st_box[1] = static_cast<cuuint32_t>(C::TY);
+    for (int i = 2; i < 5; ++i) ld_box[i] = st_box[i] = 1;
+    for (int i = 0; i < 5; ++i) estr[i] = 1;
+    const CUtensorMapDataType dt = tma_type(W / C::MULT);
+    CUtensorMap lmap, smap;
+    std::memset(&lmap, 0, sizeof(lmap));
+    std::memset(&smap, 0, sizeof(smap));
+    void *sbase = const_cast<uint8_t *>(src + p.src_off * W);
+    void *dbase = dst + p.dst_off * W;
+    if (enc(&lmap, dt, static_cast<cuuint32_t>(rank), sbase, ld_dims, ld_str, ld_box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+        enc(&smap, dt, static_cast<cuuint32_t>(rank), dbase, st_dims, st_str, st_box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return LC_ERR_UNSUPPORTED;  // the driver refused this tensor shape
+    const TileArgs a = ring_args(p, dst, W, C::R, C::TY, true);
+    const void *fn = reinterpret_cast<const void *>(&k_tile_tstore<W>);
+    int sms, per;
+    if (prepare(fn, C::NT, C::SMEM, C::SMEM, &sms, &per) != cudaSuccess) return LC_ERR_CUDA;
+    const int64_t grid = lmin(a.n_tiles, int64_t(sms) * per);
+    k_tile_tstore<W><<<static_cast<unsigned>(grid), C::NT, C::SMEM, stream>>>(lmap, smap, a);
+    return finish_launch();
+}
+
 template <int W>
 int launch_direct_t(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream) {
     using C = DirectCfg<W>;
@@ -747,6 +1044,15 @@ int launch_direct_t(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_
 }  // namespace
 
 int launch_tile(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream) {
+    if (p.tile.tstore) {
+        switch (p.w) {
+            case 1: return launch_tstore_t<1>(p, src, dst, stream);
+            case 2: return launch_tstore_t<2>(p, src, dst, stream);
+            case 4: return launch_tstore_t<4>(p, src, dst, stream);
+            case 8: return launch_tstore_t<8>(p, src, dst, stream);
+            case 16: return launch_tstore_t<16>(p, src, dst, stream);
+        }
+    }
     if (p.tile.direct) {
         switch (p.w) {
             case 1: return launch_direct_t<1>(p, src, dst, stream);

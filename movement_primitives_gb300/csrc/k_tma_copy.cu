@@ -19,6 +19,7 @@
 #include "device_common.cuh"
 #include "launch.h"
 #include "tensor_map.h"
+#include "bulk_store.cuh"
 
 namespace lc {
 
@@ -36,52 +37,6 @@ struct TmaCopyArgs {
 };
 
 namespace {
-
-// TMA tensor stores from shared memory, completing in bulk groups.
-__device__ __forceinline__ void tma_store(const void *tmap, int rank, const int32_t (&c)[5], uint32_t src) {
-    switch (rank) {
-        case 2:
-            asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(tmap),
-                         "r"(src), "r"(c[0]), "r"(c[1])
-                         : "memory");
-            break;
-        case 3:
-            asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-                             tmap),
-                         "r"(src), "r"(c[0]), "r"(c[1]), "r"(c[2])
-                         : "memory");
-            break;
-        case 4:
-            asm volatile(
-                "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(tmap),
-                "r"(src), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3])
-                : "memory");
-            break;
-        default:
-            asm volatile(
-                "cp.async.bulk.tensor.5d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5, %6}], [%1];" ::"l"(
-                    tmap),
-                "r"(src), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(c[4])
-                : "memory");
-            break;
-    }
-}
-
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-
-// All but the newest N bulk groups have finished reading shared memory.
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
-// All bulk groups have completed.
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-// Shared memory written by the async proxy is read by the async proxy next.
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
 __device__ __forceinline__ void tile_coords(const TmaCopyArgs &a, uint32_t t, int32_t (&c)[5]) {
 #pragma unroll
@@ -135,23 +90,23 @@ __global__ void __launch_bounds__(kTmaThreads)
         const uint32_t s = i % kTmaStages;
         if (!ptx::mbar_wait_bounded(bar0 + 8 * s, (i / kTmaStages) & 1, a.timeout_ns)) {
             report_error(LC_ERR_TIMEOUT, LC_KERNEL_TMA_COPY);
-            bulk_wait_all();  // stores already issued
+            bulk::wait_all();  // stores already issued
             for (uint32_t q = i; q < issued; ++q)  // loads that may still land in this CTA's ring
                 ptx::mbar_wait_bounded(bar0 + 8 * (q % kTmaStages), (q / kTmaStages) & 1, a.timeout_ns);
             return;
         }
-        fence_proxy_async_smem();
+        bulk::fence_proxy_async_smem();
         int32_t c[5];
         tile_coords(a, blockIdx.x + i * gridDim.x, c);
-        tma_store(&dst_map, a.rank, c, buf0 + s * a.stage_stride);
-        bulk_commit();
+        bulk::tma_store(&dst_map, a.rank, c, buf0 + s * a.stage_stride);
+        bulk::commit();
         // refill the stage of tile i - 1 once its store has read it
         if (i >= 1 && issued < n_local) {
-            bulk_wait_read<1>();
+            bulk::wait_read<1>();
             issue_load(issued++);
         }
     }
-    bulk_wait_all();
+    bulk::wait_all();
 }
 
 int launch_tma_copy(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream) {

@@ -47,6 +47,7 @@ struct TilePlan {
     int S = 0;        // pipeline stages (0: the direct form, no TMA ring)
     int threads = 0;
     int direct = 0;   // 1: whole V x V blocks, loaded straight into registers
+    int tstore = 0;   // 1: the ring form whose output tiles leave by TMA tensor stores
 };
 
 // TMA tensor copy: the modes of the destination order, innermost first, as
@@ -192,6 +193,10 @@ void tile_geometry(int w, int64_t bytes, int *rows, int *cols, int *stages, int 
 // side when both extents are whole V x V blocks; false leaves the outputs
 // alone.
 bool tile_direct_geometry(int w, int64_t bytes, int64_t eX, int64_t eY, int *rows, int *cols, int *threads);
+// The ring form with TMA tensor stores, for the word widths it is enabled
+// for, copies of at most the short-box size a side and destination rows of
+// whole 16-byte chunks (eX words); false leaves the outputs alone.
+bool tile_tstore_geometry(int w, int64_t bytes, int64_t eX, int *rows, int *cols, int *stages, int *threads);
 
 // Shared tile swizzle of the shared-memory transpose for w-byte words:
 // smallest (mask, shift) that keeps both copies conflict-free.

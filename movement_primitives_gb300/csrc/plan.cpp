@@ -488,6 +488,8 @@ bool plan_tile(Plan *p, const PtrInfo &ptr) {
     if (tile_direct_geometry(w, p->total * w, tp.X.e, tp.Y.e, &tp.R, &tp.TY, &tp.threads)) {
         tp.S = 0;
         tp.direct = 1;
+    } else if (tile_tstore_geometry(w, p->total * w, tp.X.e, &tp.R, &tp.TY, &tp.S, &tp.threads)) {
+        tp.tstore = 1;
     } else {
         tile_geometry(w, p->total * w, &tp.R, &tp.TY, &tp.S, &tp.threads);  // the kernel's per-width table
     }
@@ -879,6 +881,7 @@ void fill_info(const Plan &p, lc_plan_info *info) {
     info->tile_rows = p.tile.R;
     info->tile_cols = p.tile.TY;
     info->stages = p.tile.S;
+    if (p.kernel == LC_KERNEL_TILE_TRANSPOSE) info->tile_form = p.tile.direct ? 1 : p.tile.tstore ? 2 : 0;
     if (p.kernel == LC_KERNEL_WARP_SHUFFLE) {  // V words per lane chunk, blocks per batch entry
         info->vec = p.shfl.V;
         info->P = p.shfl.V;

@@ -83,11 +83,13 @@ def test_plan_workloads(M):
         assert p["kernel_name"] == "tile_transpose"
         if w <= 2:
             # the direct form: warp tiles of 4 chunks (64 bytes) x 8 blocks of V rows, no ring
-            assert (p["stages"], p["tile_cols"] * w, p["tile_rows"]) == (0, 64, 8 * (16 // w))
+            assert (p["tile_form"], p["stages"], p["tile_cols"] * w, p["tile_rows"]) == (1, 0, 64, 8 * (16 // w))
+        elif w == 4:
+            # TMA stores: swizzled boxes of 128-byte rows x 256 rows in, 32 x 256-word tiles out
+            assert (p["tile_form"], p["tile_cols"], p["tile_rows"], p["stages"]) == (2, 32, 256, 3)
         else:
-            # TMA box rows of 128 bytes for 4-byte words (the short boxes' line
-            # stores, swizzled), 256 for 8-byte words, 128 for 16-byte words
-            assert p["stages"] > 0 and p["tile_cols"] * w == (256 if w == 8 else 128)
+            # the ring with thread stores: box rows of 256 bytes for 8-byte words, 128 for 16-byte words
+            assert p["tile_form"] == 0 and p["stages"] > 0 and p["tile_cols"] * w == (256 if w == 8 else 128)
     p = M.plan(workloads.config(5)["src"], workloads.config(5)["dst"], 2)
     assert (p["vec"], p["run"]) == (8, 128)  # the vector fallback: 16-byte vectors over 256-byte runs
     # TMA boxes: the 128-word run, its 32 rows, 2 of the next mode (16 KiB)
@@ -115,6 +117,26 @@ def test_plan_tile_direct_form(M):
         assert plan(big, (big[1], 1), (1, big[0]), w) > 0
     for w in (4, 8, 16):
         assert plan((64, 64), (64, 1), (1, 64), w) > 0
+
+
+def test_plan_tile_store_forms(M):
+    """4-byte transposes of at most 256 MiB a side whose destination rows are
+    whole 16-byte chunks leave by TMA tensor stores (tile_form 2); ragged
+    destination rows, larger copies and other widths keep thread stores
+    (form 0), whole blocks of 1- and 2-byte words the direct form (1)."""
+    def form(shape, s_stride, d_stride, w, kernel="tile_transpose"):
+        p = M.plan(dict(shape=shape, stride=s_stride), dict(shape=shape, stride=d_stride), w, 1, kernel)
+        assert p["kernel_name"] == "tile_transpose"
+        return p["tile_form"]
+    assert form((64, 36), (36, 1), (1, 64), 4) == 2
+    assert form((61, 36), (36, 1), (1, 64), 4) == 0            # destination rows of 61 words
+    assert form((64, 35), (36, 1), (1, 64), 4) == 2            # ragged source rows: clipped per row
+    assert form((8192, 8200), (8200, 1), (1, 8192), 4) == 0    # past 256 MiB a side
+    assert form((64, 64), (64, 1), (1, 64), 8) == 0
+    assert form((64, 64), (64, 1), (1, 64), 2) == 1
+    assert form((64, 60), (64, 1), (1, 64), 2) == 0
+    p = M.plan(dict(shape=(64, 64), stride=(64, 1)), dict(shape=(64, 64), stride=(64, 1)), 4, 1)
+    assert p["tile_form"] == 0                                 # not a tile transpose
 
 
 def test_gmem_smem_partition_table(M):

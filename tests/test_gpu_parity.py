@@ -184,7 +184,9 @@ def test_tile_transpose_direct_form(w):
     def check(src_l, dst_l, n_tiles=1, direct=True, seed=0):
         p = lc().plan(src_l, dst_l, w, n_tiles, "tile_transpose")
         assert (p["stages"] == 0) == direct, (src_l, dst_l, p["stages"])
-        assert run_case(src_l, dst_l, w, n_tiles, kernel="tile_transpose", seed=seed) == "tile_transpose"
+        # sentinel bytes after the destination catch writes past its last row
+        assert run_case(src_l, dst_l, w, n_tiles, kernel="tile_transpose", seed=seed,
+                        dst_pad=1024) == "tile_transpose"
 
     for r, c in [(V, V), (V, 3 * V), (9 * V, 5 * V), (144, 80), (1024, 1040), (2000, 336), (128 + V, 64 + V)]:
         check(L((r, c), (c, 1)), L((r, c), (1, r)), seed=r + c)
@@ -199,6 +201,35 @@ def test_tile_transpose_direct_form(w):
     for r, c in [(9 * V, 5 * V - 1), (9 * V - 1, 5 * V), (100 + V // 2, 77)]:
         check(L((r, c), (((c + V - 1) // V) * V, 1)), L((r, c), (1, ((r + V - 1) // V) * V)), direct=False,
               seed=r + 3 * c)
+
+
+def test_tile_transpose_tma_store_form():
+    """4-byte transposes whose destination rows are whole 16-byte chunks: the
+    ring whose output tiles leave by TMA tensor stores (tile_form 2), with
+    ragged source rows, extents off the 256 x 32 tile, padded rows, offsets,
+    tile strides with gaps and up to three batch modes; sentinel bytes after
+    the destination catch any write past its last row.  Destination rows
+    that end inside a 16-byte chunk keep thread stores (form 0)."""
+    w = 4
+
+    def check(src_l, dst_l, n_tiles=1, form=2, seed=0):
+        p = lc().plan(src_l, dst_l, w, n_tiles, "tile_transpose")
+        assert p["tile_form"] == form, (src_l, dst_l, p["tile_form"])
+        assert run_case(src_l, dst_l, w, n_tiles, kernel="tile_transpose", seed=seed,
+                        dst_pad=4096) == "tile_transpose"
+
+    for r, c in [(4, 4), (64, 36), (256, 32), (300, 33), (1024, 70), (520, 1000)]:
+        check(L((r, c), (((c + 3) // 4) * 4, 1)), L((r, c), (1, r)), seed=r + c)
+        check(L((r, c), (((c + 3) // 4) * 4 + 8, 1), 12), L((r, c), (1, r + 4), 8), seed=r * c)
+    check(L((48, 30), (32, 1), 4, 48 * 32 + 16), L((48, 30), (1, 48), 0, 48 * 30 + 8), n_tiles=3, seed=5)
+    sh = (3, 260, 40)
+    check(L(sh, row_major(sh)), L(sh, permuted(sh, (0, 2, 1))), seed=6)
+    sh = (2, 3, 5, 36, 20)
+    check(L(sh, row_major(sh)), L(sh, permuted(sh, (2, 1, 0, 4, 3))), seed=7)
+    for r, c in [(61, 36), (257, 33), (3, 40)]:
+        check(L((r, c), (((c + 3) // 4) * 4, 1)), L((r, c), (1, ((r + 3) // 4) * 4)), form=0, seed=r + 3 * c)
+    # the automatic choice on a whole-chunk case
+    assert run_case(L((1024, 520), (520, 1)), L((1024, 520), (1, 1024)), w, dst_pad=4096, seed=9) == "tile_transpose"
 
 
 @pytest.mark.parametrize("w", [1, 2, 4, 8, 16])
@@ -316,6 +347,54 @@ def test_random_layouts(seed):
         src, dst, w, n_tiles = _random_layout_pair(rng)
         run_case(src, dst, w, n_tiles, seed=i)
         run_case(src, dst, w, n_tiles, kernel="vec_copy", seed=i)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_tile_transpose_fuzz(seed):
+    """Seeded transposes through the three forms of the tile class: the
+    direct form (1- and 2-byte words, whole V x V blocks), the swizzled ring
+    with line stores (short boxes of 1-, 2- and 4-byte words) and the plain
+    ring (8- and 16-byte words), with ragged extents, padded rows, offsets,
+    tile strides and up to two batch modes, forced and automatic, each
+    against the oracle."""
+    rng = random.Random(4242 + seed)
+
+    def up(n, m):
+        return (n + m - 1) // m * m
+
+    for i in range(24):
+        w = rng.choice([1, 2, 4, 8, 16])
+        V = 16 // w
+        whole = rng.random() < 0.5
+        if whole:
+            r, c = V * rng.randint(2 if V == 1 else 1, 40), V * rng.randint(2 if V == 1 else 1, 40)
+        else:
+            r, c = rng.randint(2, 40 * V), rng.randint(2, 40 * V)
+        sc = up(c, V) + V * rng.randint(0, 2)        # source row stride (16-byte multiple)
+        dr = up(r, V) + V * rng.randint(0, 2)        # destination row stride
+        batch = [rng.randint(2, 3) for _ in range(rng.randint(0, 2))]
+        sh = tuple(batch) + (r, c)
+        sst, acc = [sc, 1], r * sc + V * rng.randint(0, 1)
+        for e in reversed(batch):
+            sst.insert(0, acc)
+            acc *= e
+        order = list(range(len(batch)))
+        rng.shuffle(order)                           # batch modes in another order on the destination
+        dst_batch = [0] * len(batch)
+        dacc = c * dr
+        for k in reversed(order):
+            dst_batch[k] = dacc
+            dacc *= batch[k]
+        dst_st = tuple(dst_batch) + (1, dr)
+        n_tiles = rng.choice([1, 1, 2])
+        src_l = L(sh, tuple(sst), V * rng.randint(0, 3), acc + V if n_tiles > 1 else 0)
+        dst_l = L(sh, dst_st, V * rng.randint(0, 3), dacc + 2 * V if n_tiles > 1 else 0)
+        p = lc().plan(src_l, dst_l, w, n_tiles, "tile_transpose")
+        direct = w <= 2 and r % V == 0 and c % V == 0
+        assert (p["stages"] == 0) == direct, (sh, w, p["stages"])
+        assert p["tile_form"] == (1 if direct else 2 if w == 4 and r % 4 == 0 else 0), (sh, w, p["tile_form"])
+        assert run_case(src_l, dst_l, w, n_tiles, kernel="tile_transpose", seed=i, dst_pad=1024) == "tile_transpose"
+        run_case(src_l, dst_l, w, n_tiles, seed=100 + i, dst_pad=1024)  # the automatic choice
 
 
 def test_edge_cases():
