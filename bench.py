@@ -742,14 +742,14 @@ def measure_workload(cfg, dev, lc, stream, flush_kind, peak, min_ms=250.0):
     flush = step_bytes // 2 < 2 * workloads.HBM_L2_BYTES
     flushers = {k: L2Flush(dev, k) for k in (("read", "write") if flush else ())}
 
-    def timed(steps, flusher):
+    def timed(steps, flusher, op=launch):
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(steps)]
         for k in range(steps):
             if flusher is not None:
                 flusher(k)
             ev[k][0].record(stream)
-            launch()
+            op()
             ev[k][1].record(stream)
         return ev
 
@@ -787,6 +787,17 @@ def measure_workload(cfg, dev, lc, stream, flush_kind, peak, min_ms=250.0):
            "other_flush": other,
            "spot_check": "4096 random logical points equal at the oracle's offsets",
            "clocks": clocks}
+    if step_bytes < (1 << 20):
+        # latency-bound: the floor any launch pays under the same protocol
+        # (flush, events), from the smallest device operation there is
+        tiny = torch.zeros(1, dtype=torch.int32, device=dev)
+        with torch.cuda.stream(stream):
+            fl = timed(min(steps, 500), flushers.get(flush_kind), op=lambda: tiny.fill_(1))
+        torch.cuda.synchronize()
+        floor_us = 1e3 * statistics.median(a.elapsed_time(b) for a, b in fl)
+        out["latency"] = {"launch_floor_us": round(floor_us, 3),
+                          "floor_op": "a one-element device fill, launched and timed the same way",
+                          "kernel_over_floor_us": round(out["launch_us_median"] - floor_us, 3)}
     del src, dst, flushers
     torch.cuda.empty_cache()
     return out
