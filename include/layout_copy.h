@@ -109,11 +109,14 @@ typedef enum {
      * an in-register transpose of the sub-16-byte elements, 16-byte
      * coalesced global stores.  Large 2-D transposes with batch modes.  Its
      * direct form (1- and 2-byte words, both extents whole 16-byte blocks,
-     * at most 256 MiB a side) loads each block's rows with 16-byte global
-     * loads straight into registers instead: no TMA and no shared memory.
-     * Short 4-byte transposes whose destination rows are whole 16-byte
-     * chunks stage each transposed tile in shared memory and store it with
-     * a TMA tensor store (lc_plan_info.tile_form). */
+     * at most 96 / 64 MiB a side) loads each block's rows with 16-byte
+     * global loads straight into registers instead: no TMA and no shared
+     * memory.  Its TMA-store form stages each transposed tile in shared
+     * memory and stores it with a TMA tensor store: destination rows of
+     * whole 16-byte chunks, 4-byte words at every size, 1- and 2-byte words
+     * above 256 MiB a side (2-byte words not with destination rows a
+     * multiple of 32 KiB apart), 8- and 16-byte words up to 256 MiB
+     * (lc_plan_info.tile_form). */
     LC_KERNEL_TILE_TRANSPOSE = 3,
     /* Shared-memory transpose for any alignment: tiles of 64 source rows
      * (32 for 16-byte words), each row staged as aligned chunks (4 bytes for
@@ -184,8 +187,7 @@ typedef struct {
     int32_t grid, block, smem_bytes;
     /* tile transpose: 0 the TMA ring with thread stores, 1 the direct form
      * (stages 0), 2 the TMA ring whose output tiles leave by TMA tensor
-     * stores (4-byte words, destination rows of whole 16-byte chunks, at most
-     * 256 MiB a side); 0 for the other classes */
+     * stores; 0 for the other classes */
     int32_t tile_form;
 } lc_plan_info;
 

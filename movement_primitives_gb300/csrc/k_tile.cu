@@ -462,14 +462,32 @@ __global__ void __launch_bounds__(TileCfg<W, SHORT>::NT)
 // tensor's edges (its contiguous mode in 16-byte steps: the form takes only
 // destination rows of whole 16-byte chunks), and refills the stage; O output
 // tiles rotate, each reused once its store has read it.
-// Word widths (bit w) that take TMA stores on copies of at most
-// LC_TILE_SHORT_MAX_BYTES a side (unless the direct form applies).  Measured
-// on GB300 against the ring with thread stores (L2 flushed by a read, same
-// box): 8192^2 4-byte words 91.0-91.5 % of the copy peak against 89.7-90.1 %;
-// 8-byte words 87.4-91.5 % against 92.8-93.1 %, 16-byte words 90.0-90.6 %
-// against 93.2 %, the 16384^2 2-byte transpose 89.5-90.2 % against 91.6-91.8 %.
-#ifndef LC_TILE_TSTORE_MASK
-#define LC_TILE_TSTORE_MASK 0x10
+// Sizes (bytes a side) that take TMA stores, per word width (unless the
+// direct form applies): 1- and 2-byte words above LC_TS_MIN_BYTES_NARROW,
+// 4-byte words at every size, 8- and 16-byte words up to
+// LC_TS_MAX_BYTES_WIDE.  Measured on GB300 over square and 4:1 transposes of
+// 64 MiB - 1.5 GiB a side (L2 flushed by a read between launches below 258
+// MiB a side, launches back to back above), against the ring with thread
+// stores: 1-byte words 91.1-96.8 % of the copy peak against 80.2-87.4 % above
+// 256 MiB (84.8-86.9 % against 91.7-94.8 % at 128 MiB); 2-byte words
+// 92.2-97.6 % against 81.9-91.0 % above 256 MiB, except 87.3 % against
+// 89.2 % on the 16384^2 transpose; 4-byte words 88.9-96.5 % against
+// 84.2-96.2 % (never more than a point behind); 8-byte words 92.3-96.4 %
+// against 83.5-84.4 % up to 256 MiB, 86.2-91.3 % against 88.3-93.9 % above;
+// 16-byte words 94.8-97.5 % against 78.9-88.4 % up to 256 MiB, 85.5-91.8 %
+// against 88.1-95.2 % above.  2-byte words whose destination rows are a
+// multiple of LC_TS_W2_PITCH_RING bytes apart keep thread stores: 87.5-87.6 %
+// against 88.9-89.4 % (32 KiB rows), 91.0-91.6 % against 92.5-92.8 % (64 KiB),
+// where rows 16 KiB apart measured 93.8-94.0 % against 92.6 % and rows 24-48
+// KiB apart (not powers of two) 94.2-95.3 % against 70.3-86.6 %.
+#ifndef LC_TS_W2_PITCH_RING
+#define LC_TS_W2_PITCH_RING (32 << 10)
+#endif
+#ifndef LC_TS_MIN_BYTES_NARROW
+#define LC_TS_MIN_BYTES_NARROW (256ll << 20)
+#endif
+#ifndef LC_TS_MAX_BYTES_WIDE
+#define LC_TS_MAX_BYTES_WIDE (256ll << 20)
 #endif
 #ifndef LC_TS_ROWS_NARROW
 #define LC_TS_ROWS_NARROW 256
@@ -638,15 +656,18 @@ __global__ void __launch_bounds__(TsCfg<W>::NT)
 // writes CL destination rows, RB * 16 bytes each.  Taken only when both
 // extents are whole blocks (multiples of V), so that every block is either
 // in the tensor or out of it.
-// Word widths (bit w) that take the direct kernel, on copies of at most
-// LC_TILE_SHORT_MAX_BYTES a side.  Measured on GB300 (8192^2 transposes, L2
-// flushed by a read between launches): 1-byte words 93.6-95.1 % of the copy
-// peak against 74.7-76.2 % through TMA, 2-byte words 93.1-93.5 % against
-// 87.9-88.2 %; 4- and 8-byte words lose (86.6-87.9 % against 90.8-90.9 %,
-// 83.9-87.8 against 93.5 %), and so does the 16384^2 2-byte transpose (512
-// MiB a side: 75.5-76.0 % against 91.2-91.3 %).
-#ifndef LC_TILE_DIRECT_MASK
-#define LC_TILE_DIRECT_MASK 0x6
+// Largest copy (bytes a side) that takes the direct form, per word width (0:
+// never).  Measured on GB300 (same sweep as the TMA-store sizes): 1-byte
+// words 92.3-93.9 % of the copy peak up to 96 MiB against 80.7-88.8 % for the
+// swizzled ring, 90.2-91.6 % against 91.7-94.8 % at 123-128 MiB, 69-83 %
+// from 256 MiB; 2-byte words 91.4 % against 88.9 % at 64 MiB, 91.8-96.3 %
+// against 93.9-97.0 % at 94-128 MiB.  4- and 8-byte words never gained
+// (86.6-87.9 % against 90.8-90.9 %, 83.9-87.8 against 93.5 % at 8192^2).
+#ifndef LC_DIRECT_MAX_BYTES_W1
+#define LC_DIRECT_MAX_BYTES_W1 (96ll << 20)
+#endif
+#ifndef LC_DIRECT_MAX_BYTES_W2
+#define LC_DIRECT_MAX_BYTES_W2 (64ll << 20)
 #endif
 // Threads per CTA: 256 for 1-byte words (83.8 % with 512), 512 for 2-byte
 // words (91.1-91.6 % with 256).
@@ -805,11 +826,14 @@ static void tstore_geometry_of(int *rows, int *cols, int *stages, int *threads) 
     *threads = TsCfg<W>::NT;
 }
 
-bool tile_tstore_geometry(int w, int64_t bytes, int64_t eX, int *rows, int *cols, int *stages, int *threads) {
+bool tile_tstore_geometry(int w, int64_t bytes, int64_t eX, int64_t dY_bytes, int *rows, int *cols, int *stages,
+                          int *threads) {
     // a tensor store clips the destination's contiguous mode in 16-byte steps
     // (measured: a 71-word row of 2-byte words got its 72nd word written), so
     // the form takes only destination rows of whole 16-byte chunks
-    if (!((LC_TILE_TSTORE_MASK >> w) & 1) || bytes > LC_TILE_SHORT_MAX_BYTES || (eX * w) % 16) return false;
+    const bool sized = w <= 2 ? bytes > LC_TS_MIN_BYTES_NARROW : w == 4 ? true : bytes <= LC_TS_MAX_BYTES_WIDE;
+    if (!sized || (eX * w) % 16) return false;
+    if (w == 2 && dY_bytes % LC_TS_W2_PITCH_RING == 0) return false;
     switch (w) {
         case 1: tstore_geometry_of<1>(rows, cols, stages, threads); break;
         case 2: tstore_geometry_of<2>(rows, cols, stages, threads); break;
@@ -821,7 +845,8 @@ bool tile_tstore_geometry(int w, int64_t bytes, int64_t eX, int *rows, int *cols
 }
 
 bool tile_direct_geometry(int w, int64_t bytes, int64_t eX, int64_t eY, int *rows, int *cols, int *threads) {
-    if (w > 8 || !((LC_TILE_DIRECT_MASK >> w) & 1) || bytes > LC_TILE_SHORT_MAX_BYTES) return false;
+    const int64_t max_bytes = w == 1 ? LC_DIRECT_MAX_BYTES_W1 : w == 2 ? LC_DIRECT_MAX_BYTES_W2 : 0;
+    if (bytes > max_bytes) return false;
     if (eX % (16 / w) || eY % (16 / w)) return false;
     switch (w) {
         case 1: direct_geometry_of<1>(rows, cols, threads); break;

@@ -193,10 +193,11 @@ void tile_geometry(int w, int64_t bytes, int *rows, int *cols, int *stages, int 
 // side when both extents are whole V x V blocks; false leaves the outputs
 // alone.
 bool tile_direct_geometry(int w, int64_t bytes, int64_t eX, int64_t eY, int *rows, int *cols, int *threads);
-// The ring form with TMA tensor stores, for the word widths it is enabled
-// for, copies of at most the short-box size a side and destination rows of
-// whole 16-byte chunks (eX words); false leaves the outputs alone.
-bool tile_tstore_geometry(int w, int64_t bytes, int64_t eX, int *rows, int *cols, int *stages, int *threads);
+// The ring form with TMA tensor stores, by word width and bytes a side, for
+// destination rows of whole 16-byte chunks (eX words) dY_bytes apart; false
+// leaves the outputs alone.
+bool tile_tstore_geometry(int w, int64_t bytes, int64_t eX, int64_t dY_bytes, int *rows, int *cols, int *stages,
+                          int *threads);
 
 // Shared tile swizzle of the shared-memory transpose for w-byte words:
 // smallest (mask, shift) that keeps both copies conflict-free.

@@ -488,7 +488,7 @@ bool plan_tile(Plan *p, const PtrInfo &ptr) {
     if (tile_direct_geometry(w, p->total * w, tp.X.e, tp.Y.e, &tp.R, &tp.TY, &tp.threads)) {
         tp.S = 0;
         tp.direct = 1;
-    } else if (tile_tstore_geometry(w, p->total * w, tp.X.e, &tp.R, &tp.TY, &tp.S, &tp.threads)) {
+    } else if (tile_tstore_geometry(w, p->total * w, tp.X.e, tp.Y.d * w, &tp.R, &tp.TY, &tp.S, &tp.threads)) {
         tp.tstore = 1;
     } else {
         tile_geometry(w, p->total * w, &tp.R, &tp.TY, &tp.S, &tp.threads);  // the kernel's per-width table

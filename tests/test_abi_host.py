@@ -81,14 +81,17 @@ def test_plan_workloads(M):
         c = workloads.config(4, w)
         p = M.plan(c["src"], c["dst"], w, 1)
         assert p["kernel_name"] == "tile_transpose"
-        if w <= 2:
-            # the direct form: warp tiles of 4 chunks (64 bytes) x 8 blocks of V rows, no ring
-            assert (p["tile_form"], p["stages"], p["tile_cols"] * w, p["tile_rows"]) == (1, 0, 64, 8 * (16 // w))
+        if w == 1:
+            # 64 MiB a side: the direct form, warp tiles of 4 chunks (64 bytes) x 8 blocks of 16 rows
+            assert (p["tile_form"], p["stages"], p["tile_cols"], p["tile_rows"]) == (1, 0, 64, 128)
+        elif w == 2:
+            # 128 MiB: the ring's short boxes, 128-byte rows (swizzled, line stores), 3 stages
+            assert (p["tile_form"], p["stages"], p["tile_cols"] * w, p["tile_rows"]) == (0, 3, 128, 128)
         elif w == 4:
             # TMA stores: swizzled boxes of 128-byte rows x 256 rows in, 32 x 256-word tiles out
             assert (p["tile_form"], p["tile_cols"], p["tile_rows"], p["stages"]) == (2, 32, 256, 3)
         else:
-            # the ring with thread stores: box rows of 256 bytes for 8-byte words, 128 for 16-byte words
+            # 512 MiB and 1 GiB: the ring with thread stores, box rows of 256 / 128 bytes
             assert p["tile_form"] == 0 and p["stages"] > 0 and p["tile_cols"] * w == (256 if w == 8 else 128)
     p = M.plan(workloads.config(5)["src"], workloads.config(5)["dst"], 2)
     assert (p["vec"], p["run"]) == (8, 128)  # the vector fallback: 16-byte vectors over 256-byte runs
@@ -120,10 +123,12 @@ def test_plan_tile_direct_form(M):
 
 
 def test_plan_tile_store_forms(M):
-    """4-byte transposes of at most 256 MiB a side whose destination rows are
-    whole 16-byte chunks leave by TMA tensor stores (tile_form 2); ragged
-    destination rows, larger copies and other widths keep thread stores
-    (form 0), whole blocks of 1- and 2-byte words the direct form (1)."""
+    """The tile transpose's form by word width and size a side, where the
+    destination rows are whole 16-byte chunks: TMA tensor stores (tile_form
+    2) for 4-byte words at every size, 8- and 16-byte words up to 256 MiB,
+    1- and 2-byte words above it; the direct form (1) for whole blocks of 1-
+    and 2-byte words up to 96 / 64 MiB; thread stores (0) otherwise, and for
+    every destination row that ends inside a 16-byte chunk."""
     def form(shape, s_stride, d_stride, w, kernel="tile_transpose"):
         p = M.plan(dict(shape=shape, stride=s_stride), dict(shape=shape, stride=d_stride), w, 1, kernel)
         assert p["kernel_name"] == "tile_transpose"
@@ -131,10 +136,21 @@ def test_plan_tile_store_forms(M):
     assert form((64, 36), (36, 1), (1, 64), 4) == 2
     assert form((61, 36), (36, 1), (1, 64), 4) == 0            # destination rows of 61 words
     assert form((64, 35), (36, 1), (1, 64), 4) == 2            # ragged source rows: clipped per row
-    assert form((8192, 8200), (8200, 1), (1, 8192), 4) == 0    # past 256 MiB a side
-    assert form((64, 64), (64, 1), (1, 64), 8) == 0
+    assert form((8192, 8200), (8200, 1), (1, 8192), 4) == 2    # past 256 MiB a side
+    assert form((64, 64), (64, 1), (1, 64), 8) == 2
+    assert form((63, 64), (64, 1), (1, 64), 8) == 0
+    assert form((8192, 8192), (8192, 1), (1, 8192), 8) == 0    # 512 MiB
+    assert form((64, 64), (64, 1), (1, 64), 16) == 2
+    assert form((8192, 4160), (4160, 1), (1, 8192), 16) == 0   # past 256 MiB
     assert form((64, 64), (64, 1), (1, 64), 2) == 1
     assert form((64, 60), (64, 1), (1, 64), 2) == 0
+    assert form((8192, 8192), (8192, 1), (1, 8192), 2) == 0    # 128 MiB: the ring's short boxes
+    assert form((12288, 12288), (12288, 1), (1, 12288), 2) == 2  # 288 MiB
+    assert form((16384, 16384), (16384, 1), (1, 16384), 2) == 0  # 512 MiB, destination rows 32 KiB apart
+    assert form((16000, 16000), (16000, 1), (1, 16000), 2) == 2
+    assert form((8192, 8192), (8192, 1), (1, 8192), 1) == 1    # 64 MiB
+    assert form((11520, 11520), (11520, 1), (1, 11520), 1) == 0  # 126 MiB
+    assert form((16384, 16640), (16640, 1), (1, 16384), 1) == 2  # 260 MiB
     p = M.plan(dict(shape=(64, 64), stride=(64, 1)), dict(shape=(64, 64), stride=(64, 1)), 4, 1)
     assert p["tile_form"] == 0                                 # not a tile transpose
 

@@ -392,7 +392,8 @@ def test_tile_transpose_fuzz(seed):
         p = lc().plan(src_l, dst_l, w, n_tiles, "tile_transpose")
         direct = w <= 2 and r % V == 0 and c % V == 0
         assert (p["stages"] == 0) == direct, (sh, w, p["stages"])
-        assert p["tile_form"] == (1 if direct else 2 if w == 4 and r % 4 == 0 else 0), (sh, w, p["tile_form"])
+        tstore = (r * w) % 16 == 0 and w >= 4                # small copies: 4-, 8- and 16-byte words
+        assert p["tile_form"] == (1 if direct else 2 if tstore else 0), (sh, w, p["tile_form"])
         assert run_case(src_l, dst_l, w, n_tiles, kernel="tile_transpose", seed=i, dst_pad=1024) == "tile_transpose"
         run_case(src_l, dst_l, w, n_tiles, seed=100 + i, dst_pad=1024)  # the automatic choice
 
@@ -416,15 +417,18 @@ def test_edge_cases():
             run_case(L((n,), (1,)), L((n,), (1,)), w, seed=n)
 
 
-@pytest.mark.parametrize("w,rows,cols", [(1, 16384, 16640), (2, 8192, 16640), (4, 8192, 8320)])
-def test_tile_transpose_tall_boxes(w, rows, cols):
-    """Transposes just past 256 MiB a side take the 256-row boxes (and, for
-    1-, 2- and 4-byte words, the 64-bit index path): whole buffer against
+@pytest.mark.parametrize("w,rows,cols,form", [(1, 16384, 16640, 2), (1, 16383, 16640, 0), (2, 8192, 16640, 2),
+                                               (2, 8191, 16640, 0), (4, 8192, 8320, 2), (4, 8191, 8320, 0)])
+def test_tile_transpose_tall_boxes(w, rows, cols, form):
+    """Transposes just past 256 MiB a side: with destination rows of whole
+    16-byte chunks the TMA-store form, with rows that end inside one the
+    ring's 256-row boxes (and the 64-bit index path); whole buffer against
     the oracle."""
-    src_l, dst_l = L((rows, cols), (cols, 1)), L((rows, cols), (1, rows))
+    pitch = (rows + 15) // 16 * 16
+    src_l, dst_l = L((rows, cols), (cols, 1)), L((rows, cols), (1, pitch))
     assert rows * cols * w > 256 << 20
     p = lc().plan(src_l, dst_l, w, 1)
-    assert p["kernel_name"] == "tile_transpose" and p["tile_rows"] == (256 if w < 8 else 128)
+    assert p["kernel_name"] == "tile_transpose" and p["tile_form"] == form and p["tile_rows"] == 256
     c = dict(src=src_l, dst=dst_l, elem_bytes=w, n_tiles=1, kind="bytes", seed=700 + w, cfg=4, name="tall")
     src_h = workloads.make_src(c)
     src_d = src_h.cuda()
@@ -592,6 +596,12 @@ def test_host_buffers_pipelined():
     run_host_case(c["src"], c["dst"], 2, 1, seed=4)
     c = workloads.config(5, scale="small")
     run_host_case(c["src"], c["dst"], 2, 1, seed=5)
+    # batches of transposes chunked over a small staging buffer, through the
+    # tile transpose's TMA-store form (4-byte words) and direct form (1-byte)
+    for w, form, (r, cc) in [(4, 2, (64, 48)), (1, 1, (64, 96))]:
+        src_l, dst_l = L((r, cc), (cc, 1)), L((r, cc), (1, r))
+        assert lc().plan(src_l, dst_l, w, 37, "tile_transpose")["tile_form"] == form
+        run_host_case(src_l, dst_l, w, 37, seed=6 + w, staging_bytes=1 << 20)
 
 
 def test_host_buffers_errors():
