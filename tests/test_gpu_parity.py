@@ -439,6 +439,25 @@ def test_tile_transpose_tall_boxes(w, rows, cols, form):
     _assert_same_bytes(dst_d.cpu().numpy(), _oracle_full(c, src_h.numpy()), "tall w=%d" % w)
 
 
+@pytest.mark.parametrize("w,side,form", [(1, 11520, 0), (2, 12288, 2), (8, 4096, 2), (16, 4096, 2)])
+def test_tile_transpose_forms_at_size(w, side, form):
+    """The tile transpose's form chosen by width and size, at sizes no other
+    test reaches: 1-byte words at 126 MiB a side (the swizzled ring), 2-byte
+    words at 288 MiB (TMA stores), 8- and 16-byte words at 128 and 256 MiB
+    (TMA stores); whole buffer against the oracle."""
+    src_l, dst_l = L((side, side), (side, 1)), L((side, side), (1, side))
+    p = lc().plan(src_l, dst_l, w, 1)
+    assert p["kernel_name"] == "tile_transpose" and p["tile_form"] == form
+    c = dict(src=src_l, dst=dst_l, elem_bytes=w, n_tiles=1, kind="bytes", seed=800 + w, cfg=4, name="forms")
+    src_h = workloads.make_src(c)
+    src_d = src_h.cuda()
+    dst_d = workloads.make_dst(c, device="cuda")
+    lc().layout_copy(src_d, src_l, dst_d, dst_l, elem_bytes=w)
+    st, detail = lc().last_device_error()
+    assert st == 0, "device error word %#x" % detail
+    _assert_same_bytes(dst_d.cpu().numpy(), _oracle_full(c, src_h.numpy()), "forms w=%d" % w)
+
+
 def test_injective_destination_beyond_enumeration():
     # 2^25 + 2^24 one-byte words whose destination strides do not nest:
     # offsets k + 2^23 (2i + 3j), one-to-one by the stride split (the planner
