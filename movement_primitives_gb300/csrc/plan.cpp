@@ -488,6 +488,8 @@ bool plan_tile(Plan *p, const PtrInfo &ptr) {
     if (tile_direct_geometry(w, p->total * w, tp.X.e, tp.Y.e, &tp.R, &tp.TY, &tp.threads)) {
         tp.S = 0;
         tp.direct = 1;
+    } else if (ptr.no_tma) {
+        return false;  // the other forms load through TMA tensor maps
     } else if (tile_tstore_geometry(w, p->total * w, tp.X.e, tp.Y.d * w, &tp.R, &tp.TY, &tp.S, &tp.threads)) {
         tp.tstore = 1;
     } else {
@@ -543,6 +545,7 @@ constexpr int64_t kTmaMinRunBytes = LC_TMA_MIN_RUN_BYTES;
 constexpr int64_t kTmaTileBytes = LC_TMA_TILE_BYTES;
 
 bool plan_tma(Plan *p, const PtrInfo &ptr) {
+    if (ptr.no_tma) return false;
     const ModeList &sl = p->sorted;
     const int w = p->w;
     if (sl.n < 2 || sl.n > 5) return false;
@@ -793,7 +796,8 @@ std::string cache_key(const lc_tile_layout *src, const lc_tile_layout *dst, int3
         append(k, &l->offset, sizeof(l->offset));
         append(k, &l->tile_stride, sizeof(l->tile_stride));
     }
-    const int64_t tail[4] = {w, n_tiles, kernel, int64_t((ptr.src & 15) | ((ptr.dst & 15) << 4))};
+    const int64_t tail[4] = {w, n_tiles, kernel,
+                             int64_t((ptr.src & 15) | ((ptr.dst & 15) << 4) | (ptr.no_tma ? 256 : 0))};
     append(k, tail, sizeof(tail));
     return k;
 }
@@ -838,6 +842,7 @@ int make_plan(const lc_tile_layout *src, const lc_tile_layout *dst, int32_t w,
     mod.src = ptr.check ? (ptr.src & 15) : 0;
     mod.dst = ptr.check ? (ptr.dst & 15) : 0;
     mod.check = true;
+    mod.no_tma = ptr.no_tma;
     int st = cached_plan(src, dst, w, n_tiles, kernel, mod, out);
     if (st) return st;
     if (!ptr.check || out->total == 0) return LC_OK;

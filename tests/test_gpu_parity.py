@@ -623,6 +623,80 @@ def test_host_buffers_pipelined():
         run_host_case(src_l, dst_l, w, 37, seed=6 + w, staging_bytes=1 << 20)
 
 
+def run_mapped_case(src_l, dst_l, w, n_tiles=1, seed=0, dst_pad=256):
+    ns = _footprint(src_l, n_tiles) * w
+    nd = _footprint(dst_l, n_tiles) * w + dst_pad
+    g = torch.Generator().manual_seed(seed)
+    src_h = torch.randint(0, 256, (ns,), generator=g, dtype=torch.uint8).pin_memory()
+    dst_h = torch.full((nd,), workloads.SENTINEL, dtype=torch.uint8).pin_memory()
+    want = dst_h.numpy().copy()
+    oracle.copy(src_h.numpy(), src_l, want, dst_l, w, n_tiles)
+    lc().layout_copy_mapped(src_h, src_l, dst_h, dst_l, n_tiles=n_tiles, elem_bytes=w)
+    torch.cuda.current_stream().synchronize()
+    st, detail = lc().last_device_error()
+    assert st == 0, "device error word %#x" % detail
+    _assert_same_bytes(dst_h.numpy(), want, "mapped")
+
+
+@pytest.mark.parametrize("cfg,w", SMALL)
+def test_mapped_host_buffers_workloads(cfg, w):
+    """lc_layout_copy_mapped: the kernels read and write pinned host memory
+    directly; every reduced workload (TMA classes replaced by plain-load
+    ones) against the oracle, sentinel bytes after the destination."""
+    c = workloads.config(cfg, w, scale="small")
+    run_mapped_case(c["src"], c["dst"], c["elem_bytes"], c["n_tiles"], seed=cfg + (w or 0))
+
+
+def test_mapped_host_buffers_edges():
+    M = lc()
+    # ragged transposes and batch modes through the shared-memory transpose,
+    # whole 1-byte blocks through the tile transpose's direct form
+    run_mapped_case(L((300, 33), (36, 1)), L((300, 33), (1, 304)), 4, seed=1)
+    run_mapped_case(L((3, 64, 96), (96 * 64, 96, 1)), L((3, 64, 96), (96 * 64, 1, 64)), 1, seed=2)
+    run_mapped_case(L((45, 70), (71, 1), 3, 3300), L((45, 70), (1, 47), 5, 3400), 2, n_tiles=3, seed=3)
+    # a device source and a pinned host destination: both addressable
+    src_l, dst_l = L((64, 48), (48, 1)), L((64, 48), (1, 64))
+    src_d = torch.randint(0, 256, (64 * 48 * 4,), dtype=torch.uint8, device="cuda")
+    dst_h = torch.full((64 * 48 * 4,), workloads.SENTINEL, dtype=torch.uint8).pin_memory()
+    st = _lib_call_mapped(src_d.data_ptr(), src_l, dst_h.data_ptr(), dst_l, 4)
+    assert st == 0
+    torch.cuda.synchronize()
+    want = dst_h.numpy().copy()
+    oracle.copy(src_d.cpu().numpy(), src_l, want, dst_l, 4, 1)
+    _assert_same_bytes(dst_h.numpy(), want, "device to mapped")
+    # pageable host memory is refused before anything is launched
+    a = torch.zeros(64 * 48 * 4, dtype=torch.uint8)
+    b = torch.zeros(64 * 48 * 4, dtype=torch.uint8).pin_memory()
+    with pytest.raises(M.LayoutCopyError, match="LC_ERR_NOT_MAPPED"):
+        M.layout_copy_mapped(a, src_l, b, dst_l, elem_bytes=4)
+    with pytest.raises(M.LayoutCopyError, match="LC_ERR_NOT_MAPPED"):
+        M.layout_copy_mapped(b, src_l, a, dst_l, elem_bytes=4)
+    assert _lib_call_mapped(a.data_ptr(), src_l, b.data_ptr(), dst_l, 4) == 18
+
+
+def _lib_call_mapped(src_ptr, src_l, dst_ptr, dst_l, w, n_tiles=1):
+    import ctypes
+    M = lc()
+    sl, dl = M.TileLayout(**src_l).to_c(), M.TileLayout(**dst_l).to_c()
+    return M._lib.lib().lc_layout_copy_mapped(ctypes.c_void_p(src_ptr), ctypes.byref(sl), ctypes.c_void_p(dst_ptr),
+                                             ctypes.byref(dl), w, n_tiles,
+                                             ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+
+
+def test_mapped_host_buffers_full_size():
+    """The benchmark's workload (2^20 scale-factor tiles, 1 GiB a side) host to
+    host through lc_layout_copy_mapped: the whole destination against the
+    oracle."""
+    c = workloads.config(2)
+    src_h = workloads.make_src(c).pin_memory()
+    dst_h = workloads.make_dst(c).pin_memory()
+    lc().layout_copy_mapped(src_h, c["src"], dst_h, c["dst"], n_tiles=c["n_tiles"], elem_bytes=c["elem_bytes"])
+    torch.cuda.current_stream().synchronize()
+    st, detail = lc().last_device_error()
+    assert st == 0, "device error word %#x" % detail
+    _assert_same_bytes(dst_h.numpy(), _oracle_full(c, src_h.numpy()), "mapped full size")
+
+
 def test_host_buffers_errors():
     M = lc()
     lay = L((16, 16), (16, 1))
