@@ -255,14 +255,16 @@ int lc_layout_copy_host(const void *src_host, const lc_tile_layout *src_layout,
  * shared-memory transpose, the staged and vector copies): no TMA tensor map
  * is built over host memory.  Asynchronous on `stream`; the caller keeps
  * both buffers alive and unmodified (src) until the stream has run the copy.
- * Errors: as lc_layout_copy, plus LC_ERR_NOT_MAPPED.  Measured on GB300 (a
- * Grace host): the 2^20-tile scale-factor permute moves 336 GB/s of link
- * traffic, host to host, where the copy engines move 340 GB/s in both
- * directions at once and lc_layout_copy_host 320. */
+ * It allocates nothing and needs no staging memory, so callers that cannot
+ * allocate device memory and hold page-locked buffers can use it in place
+ * of lc_layout_copy_host_static.  Errors: as lc_layout_copy, plus
+ * LC_ERR_NOT_MAPPED.  Measured on GB300 (a Grace host): the 2^20-tile
+ * scale-factor permute moves 336-338 GB/s of link traffic, host to host,
+ * where the copy engines move 340 GB/s in both directions at once and
+ * lc_layout_copy_host 320. */
 int lc_layout_copy_mapped(const void *src_host, const lc_tile_layout *src_layout, void *dst_host,
                           const lc_tile_layout *dst_layout, int32_t elem_bytes, int64_t n_tiles,
                           lc_stream_t stream);
-
 
 /* Staging bytes lc_layout_copy_host needs for this copy (three slots of a
  * chunk of about 48 MiB of source tiles -- at least one tile, at most 1024
