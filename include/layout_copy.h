@@ -253,7 +253,8 @@ int lc_layout_copy_host(const void *src_host, const lc_tile_layout *src_layout,
  * takes only kernel classes that move words with plain loads and stores (the
  * warp shuffle and warp permutes, the tile transpose's direct form, the
  * shared-memory transpose, the staged and vector copies): no TMA tensor map
- * is built over host memory.  Asynchronous on `stream`; the caller keeps
+ * is built over host memory.  When both buffers are device memory the call
+ * is lc_layout_copy's.  Asynchronous on `stream`; the caller keeps
  * both buffers alive and unmodified (src) until the stream has run the copy.
  * It allocates nothing and needs no staging memory, so callers that cannot
  * allocate device memory and hold page-locked buffers can use it in place

@@ -139,6 +139,16 @@ uintptr_t device_view(const void *base, int64_t lo, int64_t hi) {
 extern "C" int lc_layout_copy_mapped(const void *src_host, const lc_tile_layout *src_layout, void *dst_host,
                                      const lc_tile_layout *dst_layout, int32_t elem_bytes, int64_t n_tiles,
                                      lc_stream_t stream) {
+    {  // two device buffers: the ordinary copy, TMA classes included
+        cudaPointerAttributes as{}, ad{};
+        const bool devs = src_host && dst_host && cudaPointerGetAttributes(&as, src_host) == cudaSuccess &&
+                          cudaPointerGetAttributes(&ad, dst_host) == cudaSuccess &&
+                          as.type == cudaMemoryTypeDevice && ad.type == cudaMemoryTypeDevice;
+        cudaGetLastError();
+        if (devs)
+            return lc_layout_copy_ex(src_host, src_layout, dst_host, dst_layout, elem_bytes, n_tiles, LC_KERNEL_AUTO,
+                                     stream);
+    }
     lc::Plan p;
     lc::PtrInfo ptr;
     ptr.src = reinterpret_cast<uintptr_t>(src_host);

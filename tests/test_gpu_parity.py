@@ -664,6 +664,11 @@ def test_mapped_host_buffers_edges():
     want = dst_h.numpy().copy()
     oracle.copy(src_d.cpu().numpy(), src_l, want, dst_l, 4, 1)
     _assert_same_bytes(dst_h.numpy(), want, "device to mapped")
+    # two device buffers: the ordinary copy (TMA classes allowed)
+    dst_d = torch.full((64 * 48 * 4,), workloads.SENTINEL, dtype=torch.uint8, device="cuda")
+    assert _lib_call_mapped(src_d.data_ptr(), src_l, dst_d.data_ptr(), dst_l, 4) == 0
+    torch.cuda.synchronize()
+    _assert_same_bytes(dst_d.cpu().numpy(), want, "device to device through the mapped entry")
     # pageable host memory is refused before anything is launched
     a = torch.zeros(64 * 48 * 4, dtype=torch.uint8)
     b = torch.zeros(64 * 48 * 4, dtype=torch.uint8).pin_memory()
