@@ -705,3 +705,28 @@ def test_gmem_smem_plan_refusals(M):
     assert code(T((8,), (1,)), T((8,), (1,)), 4, 32, (3, 4, 6)) == S["LC_ERR_BAD_STRIDE"]  # not one-to-one
     assert code(T((8,), (1,)), T((8,), (1,)), 16, 32, (2, 2, 7)) == S["LC_ERR_BAD_STRIDE"]  # splits an element
     assert code(T((1 << 16, 1 << 15), (1 << 15, 1)), T((1 << 16, 1 << 15), (1 << 15, 1)), 1, 32) == S["LC_ERR_SHAPE"]
+
+
+def test_mapped_copy_refusals_need_no_gpu(M):
+    """lc_layout_copy_mapped refuses before launching anything: null
+    pointers, layouts that do not pair, and memory the device cannot
+    address (plain pageable host memory) -- each with its own status."""
+    import ctypes
+    import numpy as np
+    lib = M._lib.lib()
+    a = np.zeros(64 * 48 * 4, np.uint8)
+    b = np.zeros(64 * 48 * 4, np.uint8)
+    sl = M.TileLayout((64, 48), (48, 1)).to_c()
+    dl = M.TileLayout((64, 48), (1, 64)).to_c()
+    bad = M.TileLayout((64, 47), (48, 1)).to_c()
+
+    def call(src, s, dst, d, w=4):
+        return lib.lc_layout_copy_mapped(ctypes.c_void_p(src), ctypes.byref(s), ctypes.c_void_p(dst),
+                                         ctypes.byref(d), w, 1, ctypes.c_void_p(0))
+    names = M._lib.STATUS_NAMES
+    assert names[call(0, sl, b.ctypes.data, dl)] == "LC_ERR_NULL"
+    assert names[call(a.ctypes.data, sl, 0, dl)] == "LC_ERR_NULL"
+    assert names[call(a.ctypes.data, bad, b.ctypes.data, dl)] == "LC_ERR_EXTENT_MISMATCH"
+    assert names[call(a.ctypes.data, sl, b.ctypes.data, dl, 3)] == "LC_ERR_ELEM_BYTES"
+    assert names[call(a.ctypes.data, sl, b.ctypes.data, dl)] == "LC_ERR_NOT_MAPPED"
+    assert lib.lc_status_string(18).decode() == "a byte range is not memory the device can address"
