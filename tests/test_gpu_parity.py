@@ -349,7 +349,7 @@ def test_random_layouts(seed):
         run_case(src, dst, w, n_tiles, kernel="vec_copy", seed=i)
 
 
-@pytest.mark.parametrize("seed", range(4))
+@pytest.mark.parametrize("seed", range(8))
 def test_tile_transpose_fuzz(seed):
     """Seeded transposes through the three forms of the tile class: the
     direct form (1- and 2-byte words, whole V x V blocks), the swizzled ring
@@ -645,6 +645,16 @@ def test_mapped_host_buffers_workloads(cfg, w):
     ones) against the oracle, sentinel bytes after the destination."""
     c = workloads.config(cfg, w, scale="small")
     run_mapped_case(c["src"], c["dst"], c["elem_bytes"], c["n_tiles"], seed=cfg + (w or 0))
+
+
+@pytest.mark.parametrize("seed", range(2))
+def test_mapped_host_buffers_random_layouts(seed):
+    """Seeded random layout pairs (ranks 1-4, gaps, broadcasts, tiles) between
+    pinned host buffers through lc_layout_copy_mapped, against the oracle."""
+    rng = random.Random(5000 + seed)
+    for i in range(40):
+        src, dst, w, n_tiles = _random_layout_pair(rng)
+        run_mapped_case(src, dst, w, n_tiles, seed=i)
 
 
 def test_mapped_host_buffers_edges():
