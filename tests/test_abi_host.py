@@ -730,3 +730,35 @@ def test_mapped_copy_refusals_need_no_gpu(M):
     assert names[call(a.ctypes.data, sl, b.ctypes.data, dl, 3)] == "LC_ERR_ELEM_BYTES"
     assert names[call(a.ctypes.data, sl, b.ctypes.data, dl)] == "LC_ERR_NOT_MAPPED"
     assert lib.lc_status_string(18).decode() == "a byte range is not memory the device can address"
+
+
+def test_plan_tile_forms_at_their_size_boundaries(M):
+    """The tile transpose's size table at its edges (bytes a side, whole
+    blocks, destination rows of whole 16-byte chunks): 1-byte words direct up
+    to 96 MiB, 2-byte words up to 64 MiB, then the ring up to 256 MiB, then
+    TMA stores (2-byte words not with destination rows a multiple of 32 KiB
+    apart); 8- and 16-byte words TMA stores up to 256 MiB, the ring above;
+    4-byte words TMA stores at every size."""
+    def form(rows, cols, w):
+        p = M.plan(dict(shape=(rows, cols), stride=(cols, 1)), dict(shape=(rows, cols), stride=(1, rows)), w, 1,
+                   "tile_transpose")
+        return p["tile_form"]
+    MiB = 1 << 20
+    # 1-byte words: 96 MiB = 8192 x 12288
+    assert form(8192, 12288, 1) == 1 and 8192 * 12288 == 96 * MiB
+    assert form(8192, 12288 + 16, 1) == 0
+    assert form(16384, 16384, 1) == 0 and 16384 * 16384 == 256 * MiB
+    assert form(16384, 16384 + 16, 1) == 2
+    # 2-byte words: 64 MiB = 4096 x 8192 words
+    assert form(4096, 8192, 2) == 1 and 4096 * 8192 * 2 == 64 * MiB
+    assert form(4096, 8192 + 8, 2) == 0
+    assert form(8192, 16384, 2) == 0 and 8192 * 16384 * 2 == 256 * MiB
+    assert form(8192 + 8, 16384, 2) == 2                      # rows 16400 bytes apart
+    assert form(16384, 8192 + 8, 2) == 0                      # rows 32 KiB apart
+    # 8- and 16-byte words: 256 MiB
+    assert form(4096, 8192, 8) == 2 and 4096 * 8192 * 8 == 256 * MiB
+    assert form(4096, 8192 + 2, 8) == 0
+    assert form(4096, 4096, 16) == 2 and 4096 * 4096 * 16 == 256 * MiB
+    assert form(4096, 4096 + 1, 16) == 0
+    # 4-byte words at both ends
+    assert form(64, 64, 4) == 2 and form(16384, 16384, 4) == 2
