@@ -358,7 +358,7 @@ void plan_vec(Plan *p, const PtrInfo &ptr) {
 }
 
 constexpr int64_t kStageTarget = 4 * 1024;  // bytes of units one warp stages at once
-constexpr int64_t kStagedAutoBytes = 32 * 1024;  // single tiles up to this size take the staged copy
+constexpr int64_t kSmallAutoBytes = 32 * 1024;  // single tiles up to this size skip the warp classes
 
 // Warp permute: the smallest innermost (logical-order) mode suffix that is a
 // dense block on both sides and a whole number of warp lanes (32 * P words,
@@ -753,13 +753,22 @@ int make_plan_core(const lc_tile_layout *src, const lc_tile_layout *dst, int32_t
     const bool run = sl.n > 0 && sl.m[sl.n - 1].s == 1 && sl.m[sl.n - 1].d == 1;
     bool has_x = false, has_y = false;
     for (int i = 0; i < sl.n; ++i) { has_x |= sl.m[i].d == 1; has_y |= sl.m[i].s == 1; }
-    // A single small tile is one CTA's work: the staged copy spreads it over
-    // 256 threads where the warp classes give it one warp (the page's 32 x 32
-    // fp32 transpose: 3.8 against 5.4 us per copy replayed from a graph).
-    if (n_tiles == 1 && total * w <= kStagedAutoBytes && !run) {
-        p.w = w;  // the staged copy plans from the caller's layouts and word size
-        p.fused = 1;
-        p.kernel = LC_KERNEL_SMEM_STAGED;
+    // A single small tile is a few CTAs' work at most: the warp classes would
+    // give it one or two warps and the staged copy one CTA.  Measured per copy
+    // replayed from a graph (32 KiB and less): the shared-memory transpose is
+    // fastest for words of 4 bytes and more (the page's 32 x 32 fp32
+    // transpose: 1.9 us, staged 2.6, tile 2.2), the tile transpose for 1- and
+    // 2-byte words (a 128 x 256 byte transpose: 2.1 us, shared-memory
+    // transpose 3.5, staged 40), the vector copy where neither of those
+    // plans (a 37 x 55 2-byte transpose: 2.0 us, shared-memory transpose 2.8).
+    if (n_tiles == 1 && total * w <= kSmallAutoBytes && !run) {
+        if (has_x && has_y) {
+            Plan q = p;
+            if (w >= 4 && plan_smem(&q)) { q.kernel = LC_KERNEL_SMEM_TRANSPOSE; *out = q; return LC_OK; }
+            q = p;
+            if (plan_tile(&q, ptr)) { q.kernel = LC_KERNEL_TILE_TRANSPOSE; *out = q; return LC_OK; }
+        }
+        p.kernel = LC_KERNEL_VEC_COPY;
         *out = p;
         return LC_OK;
     }

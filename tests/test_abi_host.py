@@ -73,7 +73,7 @@ def test_plan_scale_factor_transpose(M):
 
 def test_plan_workloads(M):
     import workloads
-    expect = {1: "smem_staged", 3: "tile_transpose", 5: "tma_copy"}
+    expect = {1: "smem_transpose", 3: "tile_transpose", 5: "tma_copy"}
     for cfg, kname in expect.items():
         c = workloads.config(cfg)
         assert M.plan(c["src"], c["dst"], c["elem_bytes"], c["n_tiles"])["kernel_name"] == kname
@@ -411,9 +411,7 @@ def test_layout_conversion_cache(M):
     for i in range(M._LAYOUT_CACHE_MAX + 10):  # overflow clears the cache
         assert M._c_layout({"shape": (i + 1,), "stride": (1,)}).shape[0] == i + 1
     assert M._c_layout(d).offset == 5
-    assert M.plan(M.TileLayout((32, 32)), M.TileLayout((32, 32), (1, 32)), 4)["kernel_name"] == "smem_staged"
-    # one tile past the staged copy's automatic size takes a warp or tile class
-    assert M.plan(M.TileLayout((96, 96)), M.TileLayout((96, 96), (1, 96)), 4)["kernel_name"] != "smem_staged"
+    assert M.plan(M.TileLayout((32, 32)), M.TileLayout((32, 32), (1, 32)), 4)["kernel_name"] == "smem_transpose"
 
 
 def test_fastdiv_host_mirror():
@@ -527,13 +525,32 @@ def test_tma_copy_plans(M):
 
 def test_unaligned_transposes_plan_the_smem_transpose(M):
     T = M.TileLayout
-    for w in (1, 2, 4, 8):  # single tiles past the staged copy's automatic size
+    for w in (1, 2, 4, 8):  # single tiles past the 32 KiB small-tile rule
         p = M.plan(T((137, 555), (555, 1)), T((137, 555), (1, 137)), w, 1)
         assert p["kernel_name"] == "smem_transpose", w
-    # aligned ones keep the TMA path; small single tiles take the staged copy
+    # aligned ones keep the TMA path
     assert M.plan(T((128, 128), (128, 1)), T((128, 128), (1, 128)), 4, 1)["kernel_name"] == "tile_transpose"
-    assert M.plan(T((64, 64), (64, 1)), T((64, 64), (1, 64)), 4, 1)["kernel_name"] == "smem_staged"
-    assert M.plan(T((37, 55), (55, 1)), T((37, 55), (1, 37)), 2, 1)["kernel_name"] == "smem_staged"
+
+
+def test_small_single_tiles_plan_by_word_size(M):
+    """Single tiles of at most 32 KiB: the shared-memory transpose for words
+    of 4 bytes and more, the tile transpose for narrower words, the vector
+    copy where neither plans; never the warp classes or the staged copy."""
+    T = M.TileLayout
+    tr = lambda r, c: (T((r, c), (c, 1)), T((r, c), (1, r)))
+    cases = [(tr(32, 32), 4, "smem_transpose"), (tr(64, 64), 4, "smem_transpose"),
+             (tr(90, 90), 4, "smem_transpose"), (tr(64, 64), 8, "smem_transpose"),
+             (tr(32, 32), 16, "smem_transpose"), (tr(128, 128), 2, "tile_transpose"),
+             (tr(128, 256), 1, "tile_transpose"), (tr(37, 55), 2, "vec_copy"),
+             ((T((8, 16, 32), (512, 32, 1)), T((8, 16, 32), (16, 1, 128))), 4, "smem_transpose")]
+    for (s, d), w, name in cases:
+        assert M.plan(s, d, w, 1)["kernel_name"] == name, (s, w)
+    # a layout with no contiguous mode on either side: the vector copy
+    assert M.plan(T((16, 16), (32, 2)), T((16, 16), (3, 48)), 4, 1)["kernel_name"] == "vec_copy"
+    # past 32 KiB the general rules apply again
+    assert M.plan(*tr(96, 96), 4, 1)["kernel_name"] not in ("smem_staged", "vec_copy")
+    # the staged copy still plans when forced
+    assert M.plan(*tr(32, 32), 4, 1, kernel="smem_staged")["kernel_name"] == "smem_staged"
 
 
 def test_warp_unit_plan_matches_the_page_and_the_oracle(M):

@@ -97,7 +97,7 @@ SMALL = [(1, None), (2, None), (3, None), (4, 1), (4, 2), (4, 4), (4, 8), (4, 16
 def test_workload_small_auto(cfg, w):
     c = workloads.config(cfg, w, scale="small")
     name = run_case(c["src"], c["dst"], c["elem_bytes"], c["n_tiles"], seed=cfg)
-    expect = {1: "smem_staged", 2: "warp_shuffle", 3: "tile_transpose", 4: "tile_transpose",
+    expect = {1: "smem_transpose", 2: "warp_shuffle", 3: "tile_transpose", 4: "tile_transpose",
               5: "tma_copy", 6: "smem_transpose"}[cfg]
     assert name == expect
 
@@ -148,7 +148,7 @@ def _shuffle_cases(w):
 def test_warp_shuffle_shapes(w):
     for i, (src_l, dst_l, nt) in enumerate(_shuffle_cases(w)):
         assert lc().plan(src_l, dst_l, w, nt, "warp_shuffle")["kernel_name"] == "warp_shuffle", (src_l, dst_l)
-        if nt > 1:  # (single small tiles plan the staged copy)
+        if nt > 1:  # (single tiles of 32 KiB and less take the small-tile rule)
             assert lc().plan(src_l, dst_l, w, nt)["kernel_name"] == "warp_shuffle", (src_l, dst_l)
         run_case(src_l, dst_l, w, nt, kernel="warp_shuffle", seed=100 * w + i)
         run_case(src_l, dst_l, w, nt, seed=200 * w + i)  # the automatic choice
@@ -248,9 +248,10 @@ def test_smem_transpose_any_alignment(w):
     sh = (3, 5, 33, 31)
     run_case(L(sh, row_major(sh)), L(sh, permuted(sh, (1, 0, 3, 2))), w, kernel="smem_transpose", seed=9)
     # misaligned base pointers: the automatic choice takes one of the
-    # transpose classes (the staged copy while the single tile is small)
+    # transpose classes (or, for a small single tile of narrow words that
+    # the tile transpose cannot take, the vector copy)
     assert run_case(L((64, 96), (96, 1)), L((64, 96), (1, 64)), w, src_shift=w if w < 16 else 0,
-                    dst_shift=0) in ("smem_transpose", "tile_transpose", "smem_staged")
+                    dst_shift=0) in ("smem_transpose", "tile_transpose", "vec_copy")
 
 
 @pytest.mark.parametrize("w", [1, 2, 4, 8, 16])
