@@ -293,12 +293,13 @@ int64_t lc_host_staging_bytes(const lc_tile_layout *src_layout,
  * CUDA makes them synchronous with the host, and the result is the same.
  * Set-up: the first call on a device, with that device current, looks up
  * the array's device address (loading the library's code onto the device if
- * needed) before it checks anything else, so any call completes it; make
- * that first call before any stream capture.  The address is kept for the
- * life of the process: do not call this entry point on a device after
- * cudaDeviceReset on it.  Every call shares the array and it keeps the
- * previous call's bytes (nothing in it needs to start at zero); calls that
- * overlap on the GPU, e.g. on two streams, race on it -- serialise them.
+ * needed) before it checks anything else, so any call completes it; that
+ * first call must not itself run inside a stream capture.  The address is
+ * kept for the life of the process: do not call this entry point on a
+ * device after cudaDeviceReset on it.  Every call shares the array and it
+ * keeps the previous call's bytes (nothing in it needs to start at zero);
+ * calls that overlap on the GPU, e.g. on two streams, race on it --
+ * serialise them.
  * Errors: as lc_layout_copy_host; LC_ERR_STAGING when even one tile's
  * source and destination spans (each rounded up to 256 bytes) exceed
  * LC_STATIC_STAGING_BYTES, or when the whole copy must fit at once (one

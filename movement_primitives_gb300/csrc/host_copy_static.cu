@@ -13,9 +13,9 @@
 // array's device address with cudaGetSymbolAddress (it may load this module
 // onto the device) and keeps it for that device; it does so before checking
 // anything else, so any call, even one that is refused, completes the set-up.
-// Make that first call before any stream capture.  The address is kept for
-// the life of the process: after cudaDeviceReset on a device, this entry
-// point must not be called on that device again.  The array is shared by
+// That first call must not itself run inside a stream capture.  The address
+// is kept for the life of the process: after cudaDeviceReset on a device,
+// this entry point must not be called on that device again.  The array is shared by
 // every call and keeps the previous call's bytes; nothing in it needs to
 // start at zero, because every chunk's source span is uploaded before the
 // permute reads it and the permute writes the whole destination image (a
