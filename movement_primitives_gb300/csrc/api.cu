@@ -177,10 +177,12 @@ extern "C" int lc_layout_copy(const void *src, const lc_tile_layout *src_layout,
 
 extern "C" int lc_last_device_error(lc_stream_t stream, uint64_t *detail) {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return LC_ERR_CUDA;
-    unsigned long long words[3] = {0, 0, 0};
-    if (lc::take_module_error(&words[0]) != cudaSuccess || lc::take_error_tile(&words[1]) != cudaSuccess ||
-        lc::take_error_tma_copy(&words[2]) != cudaSuccess)
-        return LC_ERR_CUDA;
+    unsigned long long words[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    cudaError_t (*const take[8])(unsigned long long *) = {
+        lc::take_module_error, lc::take_error_tile, lc::take_error_tma_copy, lc::take_error_warp1,
+        lc::take_error_warp2,  lc::take_error_warp4, lc::take_error_warp8, lc::take_error_warp16};
+    for (int i = 0; i < 8; ++i)
+        if (take[i](&words[i]) != cudaSuccess) return LC_ERR_CUDA;
     unsigned long long v = 0;
     for (unsigned long long w : words)
         if (!v && w) v = w;

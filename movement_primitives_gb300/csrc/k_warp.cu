@@ -31,6 +31,12 @@ int launch_warp(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t st
         a.unit.src_stride[i] = static_cast<int32_t>(wp.unit.m[i].s);
         a.unit.dst_stride[i] = static_cast<int32_t>(wp.unit.m[i].d);
     }
+    int64_t suffix = 1;  // the device's nesting test (lc_device::warp_unit_offsets)
+    a.nested = 1;
+    for (int i = wp.unit.n - 1; i >= 0; --i) {
+        suffix *= wp.unit.m[i].e;
+        a.nested &= (suffix % 32 == 0 || 32 % suffix == 0) ? 1 : 0;
+    }
     a.unit.P = wp.P;
     a.unit.k = wp.k;
     a.unit.shift = wp.shift;
@@ -49,9 +55,17 @@ int launch_warp(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t st
     if (a.narrow)
         for (int i = 0; i < wp.batch.n; ++i) a.bfd[i] = make_fastdiv(static_cast<uint32_t>(wp.batch.m[i].e));
     a.n_units = wp.n_units;
-    a.units_per_stage = lmin(wp.n_units, std::max<int64_t>(1, LC_WARP_SLOT / (wp.U * p.w)));
+    a.timeout_ns = wait_limit_ns();
+    // Bulk-copy prefetch for contiguous units past 8 words a lane, up to one
+    // slot: measured on batches of 32 x 32 transposes, 67 -> 91 % of the
+    // copy peak (4-byte words), 41 -> 67 (2), 28 -> 41 (1); units of 8 words
+    // and less lose with it (4 x 32 fp32 units 98.6 -> 92.4 %), and 8 KiB
+    // units (two slots of them leave one CTA per SM) gain nothing.
+    a.async = LC_WARP_ASYNC && a.contig && wp.P > 8 && a.unit_bytes <= LC_WARP_ASYNC_SLOT;
+    const int64_t slot = a.async ? LC_WARP_ASYNC_SLOT : LC_WARP_SLOT;
+    a.units_per_stage = lmin(wp.n_units, std::max<int64_t>(1, slot / (wp.U * p.w)));
     a.stage_bytes = static_cast<uint32_t>((a.units_per_stage * a.unit_bytes + 127) / 128 * 128);
-    if (a.stage_bytes > static_cast<uint32_t>(kWarpSlotMax)) return LC_ERR_UNSUPPORTED;
+    if (a.stage_bytes > static_cast<uint32_t>(a.async ? kWarpSlotMax / 2 : kWarpSlotMax)) return LC_ERR_UNSUPPORTED;
     switch (p.w) {
         case 1: return launch_warp_width1(wp.P, a, stream);
         case 2: return launch_warp_width2(wp.P, a, stream);

@@ -37,7 +37,14 @@ int launch_loop(const LoopPlan &lp, const uint8_t *src, uint8_t *dst, int64_t *t
 // (tile transpose -> shared-memory transpose, tensor copy -> vector copy).
 int launch_plan(const Plan &p, const uint8_t *src, uint8_t *dst, cudaStream_t stream, bool fallback);
 
+// Error words of the modules whose kernels wait on barriers (each
+// translation unit holds its own), read and cleared by lc_last_device_error.
 cudaError_t take_error_tile(unsigned long long *v);
 cudaError_t take_error_tma_copy(unsigned long long *v);
+cudaError_t take_error_warp1(unsigned long long *v);
+cudaError_t take_error_warp2(unsigned long long *v);
+cudaError_t take_error_warp4(unsigned long long *v);
+cudaError_t take_error_warp8(unsigned long long *v);
+cudaError_t take_error_warp16(unsigned long long *v);
 
 }  // namespace lc

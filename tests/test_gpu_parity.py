@@ -305,6 +305,25 @@ def test_warp_permute_units_with_gaps_and_tiles():
                  kernel="warp_permute", seed=w)
 
 
+@pytest.mark.parametrize("w", [1, 2, 4, 8, 16])
+def test_warp_permute_large_nested_units(w):
+    """Units of 16 and 32 words a lane whose radix nests 32 (offsets formed
+    by shuffles as they are used): 999 tiles packed back to back (an odd
+    last group), and tiles with chunk-sized gaps between them (units found
+    by division), against the oracle."""
+    for i, sh in enumerate([(16, 32), (32, 32), (8, 4, 32), (32, 16)]):
+        perm = tuple(reversed(range(len(sh))))
+        src_l, dst_l = L(sh, row_major(sh)), L(sh, permuted(sh, perm))
+        assert lc().plan(src_l, dst_l, w, 999, "warp_permute")["kernel_name"] == "warp_permute"
+        run_case(src_l, dst_l, w, n_tiles=999, kernel="warp_permute", seed=40 * w + i)
+        n = 1
+        for e in sh:
+            n *= e
+        v = 16 // w  # words per 16-byte chunk: units start on chunks
+        gap_s, gap_d = L(sh, row_major(sh), 2 * v, n + 5 * v), L(sh, permuted(sh, perm), v, n + 3 * v)
+        run_case(gap_s, gap_d, w, n_tiles=7, kernel="warp_permute", seed=41 * w + i)
+
+
 def test_axis_permutes_auto():
     rng = random.Random(5)
     for _ in range(25):
