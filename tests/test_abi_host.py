@@ -532,6 +532,28 @@ def test_unaligned_transposes_plan_the_smem_transpose(M):
     assert M.plan(T((128, 128), (128, 1)), T((128, 128), (1, 128)), 4, 1)["kernel_name"] == "tile_transpose"
 
 
+def test_batched_small_planes_plan(M):
+    """Batches of small transposed planes: the warp permute for units up to
+    32 words a lane, except 16-byte words past 8 a lane (their words alone
+    take 128 registers); planes of 4-byte words and wider of at most 16 KiB
+    that the warp permute does not take go to the shared-memory transpose,
+    larger ones and narrower words to the TMA tile."""
+    T = M.TileLayout
+    tr = lambda r, c: (T((r, c), (c, 1)), T((r, c), (1, r)))
+    cases = [((32, 32), 4, "warp_permute"), ((32, 32), 2, "warp_permute"), ((32, 32), 1, "warp_permute"),
+             ((32, 32), 8, "warp_permute"), ((128, 8), 4, "warp_permute"),
+             # (16, 16) 16-byte units: no conflict-free swizzle, so not the warp permute
+             ((16, 16), 16, "smem_transpose"), ((32, 32), 16, "smem_transpose"), ((64, 32), 4, "smem_transpose"), ((64, 64), 4, "smem_transpose"),
+             ((32, 64), 2, "tile_transpose"), ((64, 128), 4, "tile_transpose")]
+    for (r, c), w, name in cases:
+        p = M.plan(*tr(r, c), w, 4096)
+        assert p["kernel_name"] == name, ((r, c), w, p["kernel_name"])
+        if name == "warp_permute":
+            assert p["P"] <= 32 and not (w == 16 and p["P"] > 8)
+    # forced, the warp permute still takes 16-byte units of 32 words a lane
+    assert M.plan(*tr(32, 32), 16, 4096, kernel="warp_permute")["P"] == 32
+
+
 def test_small_single_tiles_plan_by_word_size(M):
     """Single tiles of at most 32 KiB: the shared-memory transpose for words
     of 4 bytes and more, the tile transpose for narrower words, the vector
