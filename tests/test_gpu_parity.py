@@ -324,6 +324,21 @@ def test_warp_permute_large_nested_units(w):
         run_case(gap_s, gap_d, w, n_tiles=7, kernel="warp_permute", seed=41 * w + i)
 
 
+@pytest.mark.parametrize("w", [1, 2, 4])
+def test_warp_permute_prefetch_cycles_slots(w):
+    """Enough 32 x 32 units that every warp of the bulk-prefetch form takes
+    about three groups (4 KiB each): its two slots alternate and each slot's
+    barrier completes more than one phase; the whole batch against the
+    oracle."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    warps = sms * 3 * 8  # 3 CTAs of 8 warps a SM at most
+    units_per_group = 4096 // (1024 * w)
+    n_tiles = 3 * warps * units_per_group + 5  # and a ragged last group
+    sh = (32, 32)
+    src_l, dst_l = L(sh, row_major(sh)), L(sh, permuted(sh, (1, 0)))
+    assert run_case(src_l, dst_l, w, n_tiles=n_tiles, seed=70 + w) == "warp_permute"
+
+
 def test_axis_permutes_auto():
     rng = random.Random(5)
     for _ in range(25):
