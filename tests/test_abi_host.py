@@ -532,6 +532,58 @@ def test_unaligned_transposes_plan_the_smem_transpose(M):
     assert M.plan(T((128, 128), (128, 1)), T((128, 128), (1, 128)), 4, 1)["kernel_name"] == "tile_transpose"
 
 
+def _unit_point(modes, flat):
+    """(source, destination) word offsets of logical index `flat` of a unit
+    whose modes (extent, src_stride, dst_stride) are listed outermost first."""
+    so = do = 0
+    for e, ss, ds in reversed(modes):
+        so += (flat % e) * ss
+        do += (flat % e) * ds
+        flat //= e
+    return so, do
+
+
+def test_warp_unit_lane_digits_split_where_32_nests(M):
+    """The identity behind the warp permute's offsets without stored
+    tables: when every suffix product of the unit's extents divides 32 or is
+    a multiple of it, the logical index lane + 32 j has disjoint lane and j
+    digits, so its offset on either side is the offset of lane plus that of
+    32 j, for every lane and every j < P; where 32 does not nest (48 = 3 x 16
+    words after a 16) some pair breaks it."""
+    T = M.TileLayout
+
+    def nests(modes):
+        suffix = 1
+        for e, _, _ in reversed(modes):
+            suffix *= e
+            if suffix % 32 and 32 % suffix:
+                return False
+        return True
+
+    cases = [((32, 32), (1, 0), True), ((16, 32), (1, 0), True), ((8, 4, 32), (2, 1, 0), True),
+             ((128, 8), (1, 0), True), ((4, 32), (1, 0), True), ((6, 48), (1, 0), False),
+             ((2, 3, 16), (2, 1, 0), False)]
+    for sh, perm, expect in cases:
+        r = len(sh)
+        st = [1] * r
+        for i in range(r - 2, -1, -1):
+            st[i] = st[i + 1] * sh[i + 1]
+        psh = [sh[q] for q in perm]
+        pst = [1] * r
+        for i in range(r - 2, -1, -1):
+            pst[i] = pst[i + 1] * psh[i + 1]
+        dst = [0] * r
+        for j, q in enumerate(perm):
+            dst[q] = pst[j]
+        _, info = M.warp_unit_plan(T(sh, tuple(st)), T(sh, tuple(dst)), 4)
+        modes, P = info["modes"], info["P"]
+        assert nests(modes) == expect, sh
+        split = all(_unit_point(modes, lane + 32 * j) ==
+                    tuple(a + b for a, b in zip(_unit_point(modes, lane), _unit_point(modes, 32 * j)))
+                    for lane in range(32) for j in range(P))
+        assert split == expect, sh
+
+
 def test_batched_small_planes_plan(M):
     """Batches of small transposed planes: the warp permute for units up to
     32 words a lane, except 16-byte words past 8 a lane (their words alone
